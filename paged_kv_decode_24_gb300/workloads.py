@@ -1,0 +1,187 @@
+"""Seeded synthetic inputs for paged-KV decode attention.
+
+This module only draws numbers and lays them out; it holds none of the
+attention arithmetic.  Both the CUDA path and the float64 oracle consume the
+arrays it returns, so the two sides always see the same fp16 bytes.
+
+Workloads (head layouts of LLaMA-2-7B, 32x128 MHA, and LLaMA-3-8B, 32/8x128
+GQA; 16-token pages):
+
+  1  tiny GQA-2:  B=2, Hq=4, Hkv=2, D=64, L={37,100}, 32-page pool permuted,
+                  q/K/V uniform in [-1, 1], no split
+  2  long single sequence, MHA: B=1, 32/32, D=128, L=4096, 512-page pool
+                  permuted, N(0,1)*0.5, 16 splits
+  3  xLLM-style batch, MHA: B=48, 32/32, D=128, L_b = {5,13,27,51}[b%4] +
+                  U{0..512}, N(0, 0.5), pages scattered
+  4  GQA-4 large batch: B=160, 32/8, D=128, L_b ~ U{128..2048}, N(0, 0.5)
+  5  skewed Flash-Decoding mix: B=256, 32/8, D=128, 255 x U{16..128} and one
+                  32768-token sequence (last), N(0, 0.5)
+
+Conventions (the plainest readings of the workload descriptions):
+  * "N(0, s)" means standard deviation s; draws are float32, rounded to fp16.
+  * Integer "uniform in [a, b]" is inclusive at both ends.
+  * When the pool size is not given it is the pages needed plus 25 % slack,
+    rounded up.  Pages come from a seeded permutation of the pool and are
+    consumed in sequence order.
+  * seq_lens include the token being decoded: the decode step appends k_new /
+    v_new at position L_b - 1 and then attends positions 0 .. L_b - 1.
+  * Pool rows that no sequence owns hold random values of the same law unless
+    ``poison`` is set, in which case they hold fp16 NaN so that any read of an
+    unowned row shows up in the output.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+SEED_BASE = 24000
+PAGE_SIZE = 16
+
+CONFIG_NAMES = {
+    1: "tiny paged decode, B=2, GQA 4/2, D=64, L={37,100}, S=16",
+    2: "LLaMA-2-7B heads, B=1, MHA 32/32, D=128, L=4096, S=16, split 16",
+    3: "xLLM-style batch, B=48, MHA 32/32, D=128, L={5,13,27,51}+U[0,512], S=16",
+    4: "LLaMA-3-8B heads, B=160, GQA 32/8, D=128, L~U[128,2048], S=16",
+    5: "skewed mix, B=256, GQA 32/8, D=128, 255xU[16,128] + 1x32768, S=16",
+}
+
+
+@dataclasses.dataclass
+class Workload:
+    """One decode step's inputs.  Arrays are host numpy arrays."""
+
+    name: str
+    config: int
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_pages: int
+    max_pages_per_seq: int
+    forced_splits: int          # 0 = let the planner choose
+    scale: float
+    seq_lens: np.ndarray        # int32 [B], includes the new token
+    block_table: np.ndarray     # int32 [B][max_pages_per_seq], -1 pad
+    q: np.ndarray               # fp16 [B][Hq][D]
+    k_new: np.ndarray           # fp16 [B][Hkv][D]
+    v_new: np.ndarray           # fp16 [B][Hkv][D]
+    k_pages: np.ndarray         # fp16 [P][Hkv][S][D]
+    v_pages: np.ndarray         # fp16 [P][Hkv][S][D]
+
+    @property
+    def group_size(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    def kv_bytes(self) -> int:
+        """K and V bytes the step must read: sum(L) * Hkv * D * 2 tensors * 2 B."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 4
+
+
+def _draw(rng: np.random.Generator, shape, dist) -> np.ndarray:
+    kind, param = dist
+    n = int(np.prod(shape))
+    if kind == "uniform":
+        x = rng.random(n, dtype=np.float32) * np.float32(2.0 * param) - np.float32(param)
+    elif kind == "normal":
+        x = rng.standard_normal(n, dtype=np.float32) * np.float32(param)
+    else:
+        raise ValueError(kind)
+    return x.astype(np.float16).reshape(shape)
+
+
+def _lengths(cfg: int, rng: np.random.Generator) -> np.ndarray:
+    if cfg == 1:
+        return np.array([37, 100], np.int32)
+    if cfg == 2:
+        return np.array([4096], np.int32)
+    if cfg == 3:
+        prompt = np.array([5, 13, 27, 51], np.int32)[np.arange(48) % 4]
+        return (prompt + rng.integers(0, 512, size=48, endpoint=True)).astype(np.int32)
+    if cfg == 4:
+        return rng.integers(128, 2048, size=160, endpoint=True).astype(np.int32)
+    if cfg == 5:
+        short = rng.integers(16, 128, size=255, endpoint=True)
+        return np.concatenate([short, [32768]]).astype(np.int32)
+    raise ValueError(f"unknown config {cfg}")
+
+
+_SHAPES = {
+    # cfg: (Hq, Hkv, D, pool pages or None, distribution, forced splits)
+    1: (4, 2, 64, 32, ("uniform", 1.0), 1),
+    2: (32, 32, 128, 512, ("normal", 0.5), 16),
+    3: (32, 32, 128, None, ("normal", 0.5), 0),
+    4: (32, 8, 128, None, ("normal", 0.5), 0),
+    5: (32, 8, 128, None, ("normal", 0.5), 0),
+}
+
+
+def layout(seq_lens: np.ndarray, num_pages: int, page_size: int, rng: np.random.Generator,
+           max_pages_per_seq: int | None = None) -> np.ndarray:
+    """Block table from a seeded permutation of the pool, consumed in sequence order."""
+    pages_needed = [(int(l) + page_size - 1) // page_size for l in seq_lens]
+    width = max(max(pages_needed, default=0), 1) if max_pages_per_seq is None else max_pages_per_seq
+    if sum(pages_needed) > num_pages:
+        raise ValueError("pool too small")
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((len(seq_lens), width), -1, np.int32)
+    cursor = 0
+    for b, n in enumerate(pages_needed):
+        bt[b, :n] = perm[cursor:cursor + n]
+        cursor += n
+    return bt
+
+
+def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE_SIZE,
+                num_pages=None, dist=("normal", 0.5), seed=0, forced_splits=0,
+                scale=None, poison=False, max_pages_per_seq=None, name="custom",
+                config=0) -> Workload:
+    """Any shape: used by the tests for ragged, empty and edge cases."""
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, np.int32)
+    B = len(seq_lens)
+    needed = sum((int(l) + page_size - 1) // page_size for l in seq_lens)
+    if num_pages is None:
+        num_pages = max(1, math.ceil(needed * 1.25))
+    bt = layout(seq_lens, num_pages, page_size, rng, max_pages_per_seq)
+    q = _draw(rng, (B, num_q_heads, head_dim), dist)
+    k_new = _draw(rng, (B, num_kv_heads, head_dim), dist)
+    v_new = _draw(rng, (B, num_kv_heads, head_dim), dist)
+    pool_shape = (num_pages, num_kv_heads, page_size, head_dim)
+    k_pages = _draw(rng, pool_shape, dist)
+    v_pages = _draw(rng, pool_shape, dist)
+    if poison:
+        owned = np.zeros((num_pages, page_size), bool)
+        for b, L in enumerate(seq_lens):
+            for t in range(int(L)):
+                owned[bt[b, t // page_size], t % page_size] = True
+        k_pages[~owned] = np.float16(np.nan)
+        v_pages[~owned] = np.float16(np.nan)
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    return Workload(name=name, config=config, batch=B, num_q_heads=num_q_heads,
+                    num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size,
+                    num_pages=num_pages, max_pages_per_seq=bt.shape[1],
+                    forced_splits=forced_splits, scale=float(scale), seq_lens=seq_lens,
+                    block_table=bt, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages,
+                    v_pages=v_pages)
+
+
+def make_config(cfg: int, seed: int | None = None, poison: bool = False) -> Workload:
+    """The five benchmark workloads, seeded with 24000 + cfg by default."""
+    if cfg not in _SHAPES:
+        raise ValueError(f"unknown config {cfg}")
+    seed = SEED_BASE + cfg if seed is None else seed
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, pool, dist, splits = _SHAPES[cfg]
+    seq_lens = _lengths(cfg, rng)
+    # The remaining draws come from a second stream so that the lengths above
+    # do not shift when the pool size changes.
+    sub_seed = int(rng.integers(0, 2**31 - 1))
+    w = make_custom(seq_lens=seq_lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                    page_size=PAGE_SIZE, num_pages=pool, dist=dist, seed=sub_seed,
+                    forced_splits=splits, poison=poison, name=CONFIG_NAMES[cfg], config=cfg)
+    return w
