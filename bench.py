@@ -1,0 +1,548 @@
+"""Benchmark: decode attention over a paged KV cache on one GB300 (or N replicas).
+
+One step is one layer's decode attention over one batch:
+    pa_kv_append -> pa_decode_attention (split kernel + log-sum-exp combine),
+and once per 32-layer model step pa_plan (host) -> pa_plan_upload, inside the
+timed region: the plan depends only on seq_lens, which every layer shares.  Inputs are synthetic and
+seeded, with the shapes of the five workloads in
+paged_kv_decode_24_gb300/workloads.py.  The default is workload 2 (LLaMA-2-7B
+heads, one 4096-token sequence, 16 splits).
+
+The JSON line reports:
+  value         KV-read GB/s of the whole job (K and V bytes of every attended
+                token / device time per step), all ranks together
+  ms_per_step   device time per step (CUDA events, max over ranks)
+  roofline      the decode call (split + combine kernels) against the
+                measured HBM copy bandwidth
+  e2e           the same metric with host buffers: per-step inputs copied
+                from pinned host memory and the output read back
+  cpu_baseline  the float64 oracle on this host's cores, on a bounded sample
+
+Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
+in total), so L2 never holds the pages a step reads.
+
+--impl reference times the float64 CPU oracle (the only reference this
+method has) on the same workload, metric and unit.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/step and KV-read GB/s as % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
+                    help="per-layer KV caches; fewer only to shrink profiler captures")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+
+def oracle_sample(w, budget_s):
+    """Run the float64 oracle's attention on whole sequences (every head)
+    until about ``budget_s`` seconds pass.  Returns (seconds, KV bytes
+    covered, description).  The oracle's append is left out: it copies whole
+    pools functionally, which says nothing about the method."""
+    import oracle
+    order = list(np.argsort(-w.seq_lens, kind="stable"))   # longest first, cycling
+    t0 = time.perf_counter()
+    kv = 0
+    seqs = 0
+    i = 0
+    while True:
+        b = int(order[i % len(order)])
+        i += 1
+        sub_bt = w.block_table[b:b + 1]
+        sub_l = w.seq_lens[b:b + 1]
+        oracle.decode_attention(w.q[b:b + 1], w.k_pages, w.v_pages, sub_bt, sub_l, w.scale)
+        kv += int(sub_l[0]) * w.num_kv_heads * w.head_dim * 4
+        seqs += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s and seqs >= 1:
+            break
+    return dt, kv, f"{seqs} whole sequences (all heads), longest first"
+
+
+def oracle_worker(args):
+    from paged_kv_decode_24_gb300 import workloads
+    w = workloads.make_config(args.config)
+    dt, kv, desc = oracle_sample(w, args.cpu_seconds)
+    print(json.dumps({"seconds": dt, "kv_bytes": kv, "sample": desc}))
+
+
+def run_oracle_subprocess(cfg, seconds):
+    """The oracle in a fresh single-threaded process (started by exec, so no
+    CUDA state is shared)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", "--config",
+                        str(cfg), "--cpu-seconds", str(seconds)], capture_output=True, text=True,
+                       env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    gbs = res["kv_bytes"] / res["seconds"] / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"config {cfg}: {res['sample']}, {res['seconds']:.1f} s of float64 numpy"}
+
+
+# ---------------------------------------------------------------------------
+# device helpers
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_24_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(cfg):
+    """DRAM bytes per launch of the split kernel from a committed ncu capture,
+    only while the kernel sources still hash to what was profiled."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("configs", {}).get(str(cfg))
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+MODEL_LAYERS = 32   # LLaMA-2-7B and LLaMA-3-8B both have 32 decoder layers
+
+
+def run_ours(args):
+    LAYERS = args.layers
+    import torch
+
+    from paged_kv_decode_24_gb300 import accounting, binding, workloads
+    from paged_kv_decode_24_gb300 import build as _build
+
+    world, rank, local = dist_setup(args)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds)   # before any CUDA call
+
+    _build.ensure_built()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+    stream = torch.cuda.Stream(device=dev)
+
+    w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank)
+    shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                               w.max_pages_per_seq, w.num_pages)
+    kv_bytes = w.kv_bytes()
+    dec_bytes = accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                        w.page_size)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    lens_host = np.ascontiguousarray(w.seq_lens)
+
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q = to_dev(w.q)
+    k_new = to_dev(w.k_new)
+    v_new = to_dev(w.v_new)
+    bt = to_dev(w.block_table)
+    sl = to_dev(w.seq_lens)
+    kp0 = to_dev(w.k_pages)
+    vp0 = to_dev(w.v_pages)
+    # One KV cache per layer, as in the model: every layer's pages are distinct
+    # memory, so a layer's reads never hit what the previous layers left in L2.
+    pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(LAYERS - 1)]
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # The plan is made once per model decode step (it depends only on seq_lens,
+    # shared by all layers) into pinned host memory, double-buffered so the
+    # host never rewrites a buffer whose upload is still in flight.
+    plan0 = binding.Plan(shape, lens_host, num_sms, w.forced_splits)
+    staging = [torch.empty(int(plan0.c.blob_bytes), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    staged_evt = [torch.cuda.Event(), torch.cuda.Event()]
+    workspace = binding.alloc_workspace(plan0, dev)
+    struct0 = plan0.structure()
+
+    def plan_step(m, strm):
+        slot = m % 2
+        staged_evt[slot].synchronize()
+        plan = binding.Plan(shape, lens_host, num_sms, w.forced_splits, host_buffer=staging[slot])
+        if plan.structure() != struct0:
+            raise RuntimeError("plan structure changed; captured graphs would be stale")
+        binding.upload(plan, workspace, stream=strm)
+        staged_evt[slot].record(strm)
+        return plan
+
+    with torch.cuda.stream(stream):
+        plan_step(0, stream)
+        # warm-up calls (set kernel attributes) before capture
+        binding.append(shape, k_new, v_new, kp0, vp0, bt, sl, status, stream=stream)
+        binding.decode(shape, plan0, q, kp0, vp0, bt, sl, w.scale, out, workspace, status,
+                       stream=stream)
+    stream.synchronize()
+
+    g_app, g_dec = [], []
+    for l in range(LAYERS):
+        kp, vp = pools[l]
+        ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=stream):
+            binding.append(shape, k_new, v_new, kp, vp, bt, sl, status)
+        with torch.cuda.graph(gd, stream=stream):
+            binding.decode(shape, plan0, q, kp, vp, bt, sl, w.scale, out, workspace, status)
+        g_app.append(ga)
+        g_dec.append(gd)
+    launches_per_step = 2 + (1 if plan0.c.num_groups > 0 else 0)
+
+    def step(i, ev=None):
+        l = i % LAYERS
+        if l == 0:
+            plan_step(i // LAYERS, stream)             # a2: plan (host) + upload
+        g_app[l].replay()                              # a1: append
+        if ev is not None:
+            ev[0].record(stream)
+        g_dec[l].replay()                              # a3-a7: split decode + combine
+        if ev is not None:
+            ev[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+
+    uuid = None
+    try:
+        u = str(props.uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(K):
+            step(i, evs[i])
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+
+    total_ms = start.elapsed_time(end)
+    dec_ms = np.array([a.elapsed_time(b) for a, b in evs])
+    ms_per_step = max_over_ranks(total_ms / K, world, dev)
+    dec_mean_ms = float(dec_ms.mean())
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+
+    # ---- end to end: every layer step copies q, k_new, v_new in from pinned
+    # host memory (plus seq_lens and the block table once per model step) and
+    # reads the output back.
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hq, hk, hv, hbt, hsl = pin(w.q), pin(w.k_new), pin(w.v_new), pin(w.block_table), pin(w.seq_lens)
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        nb = lambda t: t.numel() * t.element_size()
+        h2d_total = [0]
+
+        def e2e_step(i):
+            if i % LAYERS == 0:
+                bt.copy_(hbt, non_blocking=True)
+                sl.copy_(hsl, non_blocking=True)
+                h2d_total[0] += nb(hbt) + nb(hsl) + int(plan0.c.blob_bytes)
+            q.copy_(hq, non_blocking=True)
+            k_new.copy_(hk, non_blocking=True)
+            v_new.copy_(hv, non_blocking=True)
+            h2d_total[0] += nb(hq) + nb(hk) + nb(hv)
+            step(i)
+            hout.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(max(3, min(args.warmup, LAYERS))):
+                e2e_step(i)
+        stream.synchronize()
+        Ke = K
+        h2d_total[0] = 0
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            s2.record(stream)
+            for i in range(Ke):
+                e2e_step(i)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / Ke, world, dev)
+        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 5),
+               "h2d_bytes_per_step": int(round(h2d_total[0] / Ke)),
+               "d2h_bytes_per_step": int(nb(hout))}
+
+    peak, peak_src = read_peaks()
+    achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "accumulate": "f32",
+        "data": "synthetic (seeded; shapes and value laws of the workload)",
+        "config": {
+            "workload": w.name,
+            "config_id": args.config,
+            "batch": w.batch,
+            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}",
+            "head_dim": w.head_dim,
+            "page_size": w.page_size,
+            "sum_seq_len": int(w.seq_lens.sum()),
+            "kv_read_bytes_per_step": kv_bytes,
+            "splits": int(plan0.c.max_splits),
+            "work_items": int(plan0.c.num_work_items),
+            "step": "one layer: pa_kv_append + pa_decode_attention (split + combine); "
+                    f"pa_plan + pa_plan_upload once per {LAYERS}-layer model step, inside the timing",
+            "launch": "each layer's append and decode replayed as CUDA graphs",
+            "l2": f"{LAYERS} per-layer KV caches ({LAYERS * 2 * w.k_pages.nbytes / 2**30:.1f} GiB) "
+                  f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "hbm_frac_step": round(value / world / peak, 4),
+        "roofline": {
+            "kernel": "pa_decode_attention = split_decode_kernel + combine_kernel (timed together)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peak_src == "measured"
+                           else "fallback 6800 GB/s (of fallback)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic_for(args.config),
+            "algorithmic_bytes_per_launch": dec_bytes,
+            "us_per_launch": round(dec_mean_ms * 1e3, 3),
+            "us_per_launch_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 3),
+                                      round(float(np.percentile(dec_ms, 90)) * 1e3, 3)],
+        },
+        "plan_host_us": None,
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    # host cost of pa_plan alone (reported, not part of the device timing)
+    t0 = time.perf_counter()
+    for _ in range(20):
+        binding.Plan(shape, lens_host, num_sms, w.forced_splits)
+    res["plan_host_us"] = round((time.perf_counter() - t0) / 20 * 1e6, 2)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from paged_kv_decode_24_gb300 import workloads
+    w = workloads.make_config(args.config)
+    per_step = max(0.2, 120.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step / 4)
+    total_s = 0.0
+    total_kv = 0
+    desc = ""
+    for _ in range(args.steps):
+        dt, kv, desc = oracle_sample(w, per_step)
+        total_s += dt
+        total_kv += kv
+    value = total_kv / total_s / 1e9
+    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else (len(os.sched_getaffinity(0))
+                                                                      if hasattr(os, "sched_getaffinity") else os.cpu_count())
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; shapes and value laws of the workload)",
+        "config": {"workload": w.name, "config_id": args.config},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {desc}, about {per_step:.2f} s"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res))
+
+
+def main():
+    args = parse()
+    if args.oracle_worker:
+        oracle_worker(args)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

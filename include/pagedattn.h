@@ -1,0 +1,218 @@
+/*
+ * libpagedattn -- decode-phase attention over a paged KV cache (GB300, sm_103a).
+ *
+ * The operation: during decode every sequence of the batch adds one token.
+ * Its keys/values are appended to the sequence's KV cache, and each query
+ * head attends over all cached tokens:
+ *
+ *     out[b][h] = softmax(scale * K_b q[b][h]) V_b
+ *
+ * K_b and V_b are the sequence's cached rows of KV head h / G (G = Hq / Hkv,
+ * consecutive query heads share a KV head).  They are gathered through the
+ * sequence's block table of fixed-size pages.
+ *
+ * Sources (web pages, by title and section):
+ *  - "Eine LLM-Inferenz-Engine von Grund auf mit C++ und CUDA bauen",
+ *    section 1.1: the KV cache, prefill vs. one-token-at-a-time decode.
+ *    Section 3.4: long-context attention reads contiguous blocks and merges
+ *    without atomics.
+ *  - swiftLLM, feature list: PagedAttention (block-table paging) and paged
+ *    attention v2 (Flash-Decoding: split the sequence, merge with
+ *    log-sum-exp).
+ *  - MonadKai/xLLM, introduction: KV cache with GQA; online-normaliser
+ *    softmax.
+ *
+ * Conventions shared by every call:
+ *  - Types: q, K, V, k_new, v_new and out are IEEE fp16.  Accumulation is
+ *    fp32.  Indices are int32.
+ *  - Layouts, all dense row-major:
+ *      q, out           [batch][num_q_heads][head_dim]
+ *      k_new, v_new     [batch][num_kv_heads][head_dim]
+ *      k_pages, v_pages [num_pages][num_kv_heads][page_size][head_dim]
+ *                       (each (page, kv head) slice is one contiguous run of
+ *                       page_size * head_dim halves)
+ *      block_table      [batch][max_pages_per_seq]; entry j is the physical
+ *                       page holding tokens j*S .. j*S+S-1 of the sequence
+ *      seq_lens         [batch]; counts the token being decoded
+ *  - Logical token t of sequence b sits in page block_table[b][t / S], slot
+ *    t % S.
+ *  - Supported shapes: head_dim 64 or 128, page_size 16, G = Hq / Hkv in
+ *    {1, 2, 4, 8}.  Anything else returns PA_ERR_UNSUPPORTED.
+ *  - Pointers named "device" are CUDA device pointers; "host" pointers are
+ *    ordinary host memory.  Device buffers must be 16-byte aligned.  The
+ *    caller owns every buffer.  The library allocates no device memory.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every device call is asynchronous and stream-ordered.  It returns after
+ *    launching.
+ *  - Errors: bad arguments are detected on the host before any launch and
+ *    return a non-zero pa_status_t.  A launch failure returns PA_ERR_CUDA.
+ *    Problems seen only on the device do not trap.  The kernel skips the
+ *    access and ORs a PA_DEV_* bit into *dev_status (device int32, caller
+ *    zeroes it; read it after the stream is synchronised).  Such problems
+ *    are a block-table entry outside [0, num_pages), a seq_len outside
+ *    [0, max_pages_per_seq * S], or a workspace not holding the plan.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* null pointer, misaligned buffer, bad size, bad seq_len */
+  PA_ERR_UNSUPPORTED = 2,  /* head_dim / page_size / group size not built */
+  PA_ERR_WORKSPACE = 3,    /* workspace smaller than the plan needs */
+  PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  PA_ERR_DEVICE_OOB = 5,   /* (reported through dev_status, see below) */
+  PA_ERR_TIMEOUT = 6,      /* (reported through dev_status, see below) */
+  PA_ERR_NO_MEMORY = 7,    /* host allocation in pa_plan failed */
+  PA_ERR_PLAN = 8          /* plan does not match the shape */
+} pa_status_t;
+
+/* Bits ORed into *dev_status by the kernels. */
+#define PA_DEV_BAD_PAGE 0x1       /* block-table entry outside [0, num_pages): page skipped */
+#define PA_DEV_BAD_SEQ_LEN 0x2    /* seq_len < 0 or > max_pages_per_seq * page_size: clamped */
+#define PA_DEV_PLAN_MISMATCH 0x4  /* workspace does not hold this plan, or seq_lens differ from it */
+#define PA_DEV_TIMEOUT 0x8        /* a bounded wait on a page copy gave up: output not written */
+
+typedef struct {
+  int32_t batch;             /* B, >= 0 */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv, divides Hq */
+  int32_t head_dim;          /* D: 64 or 128 */
+  int32_t page_size;         /* S: 16 */
+  int32_t max_pages_per_seq; /* row length of block_table */
+  int32_t num_pages;         /* P: pages in each pool */
+} pa_shape_t;
+
+/*
+ * A plan: how one decode call splits the batch into warp tasks.
+ *
+ * Each task is one (sequence, KV head, page range).  A sequence is cut into
+ * several page-aligned ranges (Flash-Decoding splits) when that balances the
+ * GPU.  pa_plan fills the struct.  host_blob (the task list, owned by the
+ * plan) is released by pa_plan_free.
+ */
+typedef struct {
+  pa_shape_t shape;          /* the shape the plan was made for */
+  int32_t num_work_items;    /* warp tasks: one per (sequence, KV head, split) */
+  int32_t num_groups;        /* (sequence, KV head) pairs with more than one split */
+  int32_t num_split_items;   /* tasks that write partial results */
+  int32_t max_splits;        /* largest split count of any sequence */
+  int32_t chunk_pages;       /* target pages per split chosen by the planner */
+  int32_t num_ctas;          /* grid of the split kernel */
+  int32_t warps_per_cta;
+  int32_t owns_blob;         /* 1 if host_blob was allocated by pa_plan */
+  uint64_t plan_id;          /* stamp written into the workspace by pa_plan_upload */
+  size_t blob_bytes;         /* bytes pa_plan_upload copies into the workspace */
+  size_t workspace_bytes;    /* minimum workspace for pa_decode_attention */
+  void* host_blob;           /* task list in host memory, owned by the plan */
+} pa_plan_t;
+
+/*
+ * Append the new token's K and V (decode-phase cache update; from-scratch
+ * engine article, section 1.1; swiftLLM PagedAttention).
+ *
+ * For every b with seq_lens[b] = L > 0, row k_new[b][h] is copied to
+ * k_pages[block_table[b][(L-1)/S]][h][(L-1)%S], and likewise for V.  The
+ * copy is bit for bit.  Sequences with L == 0 are skipped.
+ * Device: k_new, v_new, k_pages, v_pages, block_table, seq_lens, dev_status.
+ */
+pa_status_t pa_kv_append(const pa_shape_t* shape, const void* k_new, const void* v_new,
+                         void* k_pages, void* v_pages, const int32_t* block_table,
+                         const int32_t* seq_lens, int32_t* dev_status, void* stream);
+
+/*
+ * Plan the split-K decomposition (swiftLLM paged attention v2 /
+ * Flash-Decoding; "Eine LLM-Inferenz-Engine ...", section 3.4 on long
+ * contexts).  Host-only; touches no GPU.
+ *
+ * seq_lens_host: host int32[batch], the lengths the next decode calls will
+ * see.  num_sms: SM count of the target GPU (152 on GB300).
+ * forced_splits > 0 cuts every sequence into min(forced_splits, pages)
+ * near-equal page ranges.  0 lets the planner choose from the total work
+ * and num_sms.
+ * Returns PA_ERR_INVALID_ARG for a bad seq_len, PA_ERR_UNSUPPORTED for an
+ * unsupported shape, and PA_ERR_NO_MEMORY on host allocation failure.  On
+ * success *plan_out owns host memory; release it with pa_plan_free.
+ */
+pa_status_t pa_plan(const pa_shape_t* shape, const int32_t* seq_lens_host, int32_t num_sms,
+                    int32_t forced_splits, pa_plan_t* plan_out);
+
+/*
+ * Same as pa_plan, but the task list is written into caller-owned host
+ * memory (for example pinned memory, so that pa_plan_upload is a true
+ * asynchronous copy and can be captured in a CUDA graph).  The plan does not
+ * own host_buffer; pa_plan_free leaves it alone.  If host_buffer_bytes is
+ * too small, returns PA_ERR_WORKSPACE and sets plan_out->blob_bytes to the
+ * size needed.  The buffer must stay unchanged until every upload that reads
+ * it has completed on its stream.
+ */
+pa_status_t pa_plan_in(const pa_shape_t* shape, const int32_t* seq_lens_host, int32_t num_sms,
+                       int32_t forced_splits, void* host_buffer, size_t host_buffer_bytes,
+                       pa_plan_t* plan_out);
+
+/* Release the plan's host memory (safe on a zeroed or already freed plan). */
+void pa_plan_free(pa_plan_t* plan);
+
+/*
+ * Copy the plan's task list into the head of a device workspace
+ * (cudaMemcpyAsync on stream).  The list starts with a header giving its
+ * task, group and index counts.  pa_decode_attention checks those counts on
+ * the device against the plan it is called with and sets
+ * PA_DEV_PLAN_MISMATCH if they differ.  One upload serves any number of
+ * decode calls that use the same plan and workspace.  A plan of the same
+ * structure uploaded later (the next decode step's plan, for example) also
+ * serves a call or a captured CUDA graph made with the earlier one.
+ * Returns PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
+ */
+pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Decode attention (the operation at the top of this header), computed with
+ * an online softmax normaliser (xLLM introduction, SoftMax: online
+ * normalizer).  Splits follow the plan; their (output, log-sum-exp) partials
+ * are merged by a separate combine kernel (swiftLLM paged attention v2).
+ *
+ * Device: q, k_pages, v_pages, block_table, seq_lens, out [B][Hq][D] fp16,
+ * workspace (holding the uploaded plan), dev_status.
+ * scale: the logit scale, normally 1/sqrt(head_dim).
+ * out receives fp16 rounded to nearest even from the fp32 result.  A
+ * sequence of length 0 gets zeros.
+ * Returns PA_ERR_PLAN if plan->shape differs from *shape, and
+ * PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
+ */
+pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                                const void* k_pages, const void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens, float scale,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream);
+
+/*
+ * Export the physical slot of every logical token, for exact comparison
+ * with the oracle: out_slots[b][t] = block_table[b][t/S]*S + t%S for
+ * t < seq_lens[b], else -1.  A bad page index gives -2 and sets
+ * PA_DEV_BAD_PAGE.  Device: block_table, seq_lens,
+ * out_slots int32 [batch][max_pages_per_seq * page_size].
+ */
+pa_status_t pa_debug_gather_indices(const pa_shape_t* shape, const int32_t* block_table,
+                                    const int32_t* seq_lens, int32_t* out_slots,
+                                    int32_t* dev_status, void* stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status_t status);
+
+/* Library version string. */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,303 @@
+"""ctypes binding of libpagedattn (include/pagedattn.h).
+
+Argument marshalling only.  Torch tensors supply device memory and the
+current CUDA stream; every computation runs in the library's kernels.  There
+is no fallback: if the shared library is missing or a call fails, this module
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libpagedattn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "pagedattn.h")
+
+PA_DEV_BAD_PAGE = 0x1
+PA_DEV_BAD_SEQ_LEN = 0x2
+PA_DEV_PLAN_MISMATCH = 0x4
+PA_DEV_TIMEOUT = 0x8
+
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
+                4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE_OOB", 6: "PA_ERR_TIMEOUT",
+                7: "PA_ERR_NO_MEMORY", 8: "PA_ERR_PLAN"}
+
+
+class PaShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
+
+
+class PaPlan(ctypes.Structure):
+    _fields_ = [("shape", PaShape), ("num_work_items", ctypes.c_int32),
+                ("num_groups", ctypes.c_int32), ("num_split_items", ctypes.c_int32),
+                ("max_splits", ctypes.c_int32), ("chunk_pages", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
+                ("owns_blob", ctypes.c_int32), ("plan_id", ctypes.c_uint64),
+                ("blob_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
+                ("host_blob", ctypes.c_void_p)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn, code, lib):
+        self.code = code
+        msg = lib.pa_status_string(code).decode() if lib is not None else "?"
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}: {msg}")
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "pa_kv_append": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pa_plan": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, ctypes.c_int32, ctypes.c_int32,
+                               ctypes.POINTER(PaPlan)]),
+    "pa_plan_in": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, ctypes.c_int32, ctypes.c_int32, _P,
+                                  ctypes.c_size_t, ctypes.POINTER(PaPlan)]),
+    "pa_plan_free": (None, [ctypes.POINTER(PaPlan)]),
+    "pa_plan_upload": (ctypes.c_int, [ctypes.POINTER(PaPlan), _P, ctypes.c_size_t, _P]),
+    "pa_decode_attention": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan), _P, _P,
+                                           _P, _P, _P, ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                           _P, _P]),
+    "pa_debug_gather_indices": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
+    "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pa_version": (ctypes.c_char_p, []),
+}
+
+
+def declared_functions(header: str = HEADER) -> list[str]:
+    """Names of the functions include/pagedattn.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (once) and attach signatures.  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpagedattn not built ({path} missing); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise PagedAttnError(fn, code, _lib)
+
+
+def make_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+               num_pages) -> PaShape:
+    return PaShape(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
+                   int(max_pages_per_seq), int(num_pages))
+
+
+class Plan:
+    """Owner of a pa_plan_t; frees the host task list when collected.
+
+    With ``host_buffer`` (a host tensor or numpy array, e.g. pinned memory)
+    the task list is written there by pa_plan_in instead of a malloc'ed block.
+    """
+
+    def __init__(self, shape: PaShape, seq_lens_host, num_sms: int, forced_splits: int = 0,
+                 host_buffer=None):
+        lib = load()
+        self.shape = shape
+        self.c = PaPlan()
+        lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        self._lens = lens
+        lp = lens.ctypes.data if lens.size else None
+        if host_buffer is None:
+            code = lib.pa_plan(ctypes.byref(shape), lp, int(num_sms), int(forced_splits),
+                               ctypes.byref(self.c))
+        else:
+            self._buf = host_buffer
+            ptr, nbytes = _host_ptr(host_buffer)
+            code = lib.pa_plan_in(ctypes.byref(shape), lp, int(num_sms), int(forced_splits), ptr,
+                                  nbytes, ctypes.byref(self.c))
+        _check("pa_plan", code)
+
+    def structure(self):
+        c = self.c
+        return (c.num_work_items, c.num_groups, c.num_split_items, c.num_ctas, c.blob_bytes)
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self.c.workspace_bytes)
+
+    def blob(self) -> np.ndarray:
+        """The task list as int32 (host copy, for inspection and tests)."""
+        n = int(self.c.blob_bytes) // 4
+        buf = (ctypes.c_int32 * n).from_address(self.c.host_blob)
+        return np.frombuffer(buf, dtype=np.int32, count=n).copy()
+
+    def free(self):
+        if _lib is not None and getattr(self, "c", None) is not None and self.c.host_blob:
+            _lib.pa_plan_free(ctypes.byref(self.c))
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def _host_ptr(buf):
+    """(address, bytes) of a host numpy array or CPU torch tensor."""
+    if isinstance(buf, np.ndarray):
+        if not buf.flags["C_CONTIGUOUS"]:
+            raise ValueError("host buffer must be contiguous")
+        return ctypes.c_void_p(buf.ctypes.data), buf.nbytes
+    if getattr(buf, "is_cuda", True) or not buf.is_contiguous():
+        raise ValueError("host buffer must be a contiguous CPU tensor or numpy array")
+    return ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size()
+
+
+# --------------------------------------------------------------------------
+# torch-facing wrappers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def shape_of(q, k_pages, block_table) -> PaShape:
+    B, Hq, D = q.shape
+    P, Hkv, S, D2 = k_pages.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_pages differ")
+    return make_shape(B, Hq, Hkv, D, S, block_table.shape[1], P)
+
+
+def append(shape, k_new, v_new, k_pages, v_pages, block_table, seq_lens, status, stream=None):
+    torch = _torch()
+    lib = load()
+    _check("pa_kv_append", lib.pa_kv_append(
+        ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
+        _dev_ptr(v_new, torch.float16, "v_new"), _dev_ptr(k_pages, torch.float16, "k_pages"),
+        _dev_ptr(v_pages, torch.float16, "v_pages"), _dev_ptr(block_table, torch.int32, "block_table"),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(status, torch.int32, "status"),
+        _stream(stream)))
+
+
+def upload(plan: Plan, workspace, stream=None):
+    torch = _torch()
+    lib = load()
+    _check("pa_plan_upload", lib.pa_plan_upload(
+        ctypes.byref(plan.c), _dev_ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
+
+
+def decode(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens, scale, out, workspace,
+           status, stream=None):
+    torch = _torch()
+    lib = load()
+    _check("pa_decode_attention", lib.pa_decode_attention(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def gather_indices(shape, block_table, seq_lens, out_slots, status, stream=None):
+    torch = _torch()
+    lib = load()
+    _check("pa_debug_gather_indices", lib.pa_debug_gather_indices(
+        ctypes.byref(shape), _dev_ptr(block_table, torch.int32, "block_table"),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(out_slots, torch.int32, "out_slots"),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def alloc_workspace(plan: Plan, device="cuda"):
+    """A uint8 device buffer of the plan's workspace size (256-byte aligned by torch)."""
+    torch = _torch()
+    return torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+
+
+class Prepared:
+    """A library call with its ctypes arguments converted once.
+
+    Calling it re-issues the same call (same buffers, same stream) with no
+    per-call Python marshalling; used where host overhead would otherwise
+    dominate a short kernel.  The tensors are kept alive by the object.
+    """
+
+    def __init__(self, name, args, keep):
+        self._fn = getattr(load(), name)
+        self._name = name
+        self._args = tuple(args)
+        self._keep = keep
+
+    def __call__(self):
+        code = self._fn(*self._args)
+        if code != 0:
+            raise PagedAttnError(self._name, code, _lib)
+
+
+def prepare_append(shape, k_new, v_new, k_pages, v_pages, block_table, seq_lens, status,
+                   stream=None) -> Prepared:
+    torch = _torch()
+    args = [ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
+            _dev_ptr(v_new, torch.float16, "v_new"), _dev_ptr(k_pages, torch.float16, "k_pages"),
+            _dev_ptr(v_pages, torch.float16, "v_pages"),
+            _dev_ptr(block_table, torch.int32, "block_table"),
+            _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(status, torch.int32, "status"),
+            _stream(stream)]
+    return Prepared("pa_kv_append", args, (shape, k_new, v_new, k_pages, v_pages, block_table,
+                                           seq_lens, status))
+
+
+def prepare_decode(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens, scale, out,
+                   workspace, status, stream=None) -> Prepared:
+    torch = _torch()
+    args = [ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+            _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+            _dev_ptr(block_table, torch.int32, "block_table"),
+            _dev_ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale),
+            _dev_ptr(out, torch.float16, "out"), _dev_ptr(workspace, torch.uint8, "workspace"),
+            ctypes.c_size_t(workspace.numel()), _dev_ptr(status, torch.int32, "status"),
+            _stream(stream)]
+    return Prepared("pa_decode_attention", args, (shape, plan, q, k_pages, v_pages, block_table,
+                                                  seq_lens, out, workspace, status))
+
+
+def prepare_upload(plan: Plan, workspace, stream=None) -> Prepared:
+    torch = _torch()
+    args = [ctypes.byref(plan.c), _dev_ptr(workspace, torch.uint8, "workspace"),
+            ctypes.c_size_t(workspace.numel()), _stream(stream)]
+    return Prepared("pa_plan_upload", args, (plan, workspace))

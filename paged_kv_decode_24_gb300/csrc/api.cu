@@ -1,0 +1,175 @@
+// C-ABI entry points of libpagedattn: argument checks, then launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "decode_kernel.cuh"
+#include "launch.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+cudaError_t launch_split_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+
+cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
+                         cudaStream_t stream) {
+  if (head_dim == 64) return launch_split_d64(p, group, grid, stream);
+  if (head_dim == 128) return launch_split_d128(p, group, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return p && ((uintptr_t)p % a) == 0; }
+
+bool same_plan_shape(const pa_shape_t& a, const pa_shape_t& b) {
+  return a.batch == b.batch && a.num_q_heads == b.num_q_heads && a.num_kv_heads == b.num_kv_heads &&
+         a.head_dim == b.head_dim && a.page_size == b.page_size &&
+         a.max_pages_per_seq == b.max_pages_per_seq;
+}
+
+pa_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PA_OK;
+  (void)cudaGetLastError();  // clear a sticky launch error so later calls report their own
+  return PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" const char* pa_status_string(pa_status_t status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape (head_dim 64/128, page_size 16, Hq/Hkv in 1,2,4,8)";
+    case PA_ERR_WORKSPACE: return "workspace smaller than the plan requires";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_DEVICE_OOB: return "device detected an out-of-range index";
+    case PA_ERR_TIMEOUT: return "device wait timed out";
+    case PA_ERR_NO_MEMORY: return "host allocation failed";
+    case PA_ERR_PLAN: return "plan does not match the shape";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* pa_version(void) { return "libpagedattn 0.1 (sm_103a)"; }
+
+extern "C" pa_status_t pa_kv_append(const pa_shape_t* shape, const void* k_new, const void* v_new,
+                                    void* k_pages, void* v_pages, const int32_t* block_table,
+                                    const int32_t* seq_lens, int32_t* dev_status, void* stream) {
+  using namespace pa;
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (shape->batch == 0) return PA_OK;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pages, 16) ||
+      !aligned(v_pages, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  AppendParams p{};
+  p.k_new = (const __half*)k_new;
+  p.v_new = (const __half*)v_new;
+  p.k_pages = (__half*)k_pages;
+  p.v_pages = (__half*)v_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.status = dev_status;
+  p.batch = shape->batch;
+  p.num_kv_heads = shape->num_kv_heads;
+  p.head_dim = shape->head_dim;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pages = shape->num_pages;
+  return cuda_status(launch_append(p, (cudaStream_t)stream));
+}
+
+extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (!plan || !plan->host_blob || plan->blob_bytes == 0) return PA_ERR_INVALID_ARG;
+  if (!pa::aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  return pa::cuda_status(cudaMemcpyAsync(workspace, plan->host_blob, plan->blob_bytes,
+                                         cudaMemcpyHostToDevice, (cudaStream_t)stream));
+}
+
+extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan,
+                                           const void* q, const void* k_pages, const void* v_pages,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           float scale, void* out, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream) {
+  using namespace pa;
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
+  if (shape->batch == 0) return PA_OK;
+  if (plan->num_work_items <= 0) return PA_ERR_PLAN;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
+      !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+
+  const int G = shape->num_q_heads / shape->num_kv_heads;
+  const int D = shape->head_dim;
+  const Layout lay = layout(plan->num_work_items, plan->num_groups, plan->num_split_items, G, D);
+  char* ws = (char*)workspace;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  SplitParams p{};
+  p.q = (const __half*)q;
+  p.k_pages = (const __half*)k_pages;
+  p.v_pages = (const __half*)v_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = (__half*)out;
+  p.ws_header = (const int32_t*)ws;
+  p.items = (const int4*)(ws + lay.items_off);
+  p.part_lse = (float*)(ws + lay.lse_off);
+  p.part_o = (float*)(ws + lay.o_off);
+  p.status = dev_status;
+  p.qscale = (float)((double)scale * 1.4426950408889634);  // log2(e)
+  p.batch = shape->batch;
+  p.num_q_heads = shape->num_q_heads;
+  p.num_kv_heads = shape->num_kv_heads;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pages = shape->num_pages;
+  p.num_items = plan->num_work_items;
+  p.num_groups = plan->num_groups;
+  p.num_split_items = plan->num_split_items;
+  st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
+  if (st != PA_OK || plan->num_groups == 0) return st;
+
+  CombineParams c{};
+  c.ws_header = (const int32_t*)ws;
+  c.groups = (const int4*)(ws + lay.groups_off);
+  c.idx = (const int32_t*)(ws + lay.idx_off);
+  c.part_lse = p.part_lse;
+  c.part_o = p.part_o;
+  c.out = (__half*)out;
+  c.status = dev_status;
+  c.group_size = G;
+  c.num_q_heads = shape->num_q_heads;
+  c.num_items = p.num_items;
+  c.num_groups = p.num_groups;
+  c.num_split_items = p.num_split_items;
+  return cuda_status(launch_combine(c, D, plan->num_groups * G, s));
+}
+
+extern "C" pa_status_t pa_debug_gather_indices(const pa_shape_t* shape, const int32_t* block_table,
+                                               const int32_t* seq_lens, int32_t* out_slots,
+                                               int32_t* dev_status, void* stream) {
+  using namespace pa;
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (shape->batch == 0) return PA_OK;
+  if ((int64_t)shape->num_pages * shape->page_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(out_slots, 4) ||
+      !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  return cuda_status(launch_gather(block_table, seq_lens, out_slots, dev_status, shape->batch,
+                                   shape->max_pages_per_seq, shape->num_pages,
+                                   (cudaStream_t)stream));
+}

@@ -1,0 +1,45 @@
+// Kernel parameter blocks and launchers (host <-> device glue, internal).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+struct SplitParams;  // decode_kernel.cuh
+
+struct CombineParams {
+  const int32_t* ws_header;
+  const int4* groups;
+  const int32_t* idx;
+  const float* part_lse;
+  const float* part_o;
+  __half* out;
+  int32_t* status;
+  int32_t group_size;
+  int32_t num_q_heads;
+  int32_t num_items, num_groups, num_split_items;  // must match the workspace header
+};
+
+struct AppendParams {
+  const __half* k_new;
+  const __half* v_new;
+  __half* k_pages;
+  __half* v_pages;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t* status;
+  int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
+};
+
+cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
+                         cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_gather(const int32_t* block_table, const int32_t* seq_lens, int32_t* out,
+                          int32_t* status, int batch, int max_pages, int num_pages,
+                          cudaStream_t stream);
+
+}  // namespace pa

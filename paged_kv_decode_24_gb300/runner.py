@@ -1,0 +1,69 @@
+"""Device-side holder for one decode step's buffers, driving the C ABI.
+
+Moves a host workload into torch CUDA tensors once, then issues
+pa_kv_append / pa_plan / pa_plan_upload / pa_decode_attention through
+``binding``.  It holds no arithmetic of its own.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding
+
+
+class DeviceDecode:
+    def __init__(self, w, device="cuda", num_sms=None):
+        import torch
+        self.torch = torch
+        self.w = w
+        self.device = torch.device(device)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
+        self.q = t(w.q)
+        self.k_new = t(w.k_new)
+        self.v_new = t(w.v_new)
+        self.k_pages = t(w.k_pages)
+        self.v_pages = t(w.v_pages)
+        self.block_table = t(w.block_table)
+        self.seq_lens = t(w.seq_lens)
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.shape = binding.shape_of(self.q, self.k_pages, self.block_table)
+        if num_sms is None:
+            num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.num_sms = int(num_sms)
+        self.plan_obj = None
+        self.workspace = None
+
+    def make_plan(self, forced_splits=None, seq_lens_host=None):
+        fs = self.w.forced_splits if forced_splits is None else forced_splits
+        lens = self.w.seq_lens if seq_lens_host is None else seq_lens_host
+        self.plan_obj = binding.Plan(self.shape, lens, self.num_sms, fs)
+        need = self.plan_obj.workspace_bytes
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = binding.alloc_workspace(self.plan_obj, self.device)
+        binding.upload(self.plan_obj, self.workspace)
+        return self.plan_obj
+
+    def append(self):
+        binding.append(self.shape, self.k_new, self.v_new, self.k_pages, self.v_pages,
+                       self.block_table, self.seq_lens, self.status)
+
+    def decode(self, out=None):
+        if self.plan_obj is None:
+            self.make_plan()
+        binding.decode(self.shape, self.plan_obj, self.q, self.k_pages, self.v_pages,
+                       self.block_table, self.seq_lens, self.w.scale,
+                       self.out if out is None else out, self.workspace, self.status)
+        return self.out if out is None else out
+
+    def gather_slots(self):
+        width = self.shape.max_pages_per_seq * self.shape.page_size
+        slots = self.torch.empty((self.shape.batch, width), dtype=self.torch.int32,
+                                 device=self.device)
+        binding.gather_indices(self.shape, self.block_table, self.seq_lens, slots, self.status)
+        return slots
+
+    def read_status(self) -> int:
+        self.torch.cuda.synchronize(self.device)
+        return int(self.status.item())

@@ -158,8 +158,9 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
         for b, L in enumerate(seq_lens):
             for t in range(int(L)):
                 owned[bt[b, t // page_size], t % page_size] = True
-        k_pages[~owned] = np.float16(np.nan)
-        v_pages[~owned] = np.float16(np.nan)
+        pg, slot = np.nonzero(~owned)
+        k_pages[pg, :, slot, :] = np.float16(np.nan)
+        v_pages[pg, :, slot, :] = np.float16(np.nan)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return Workload(name=name, config=config, batch=B, num_q_heads=num_q_heads,

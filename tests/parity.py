@@ -1,0 +1,31 @@
+"""Shared helpers of the GPU parity tests: the tolerance and the comparison.
+
+Tolerance for fp16 q/K/V with fp32 accumulation and fp16 output, element by
+element over every compared output:
+    max |gpu - oracle|                        <= 2e-3
+    max |gpu - oracle| / max(|oracle|, 1e-3)  <= 1e-2
+Rounding the exact result to fp16 alone costs a relative 2^-11 (4.9e-4).
+The 1e-3 floor keeps near-zero outputs from making the ratio meaningless.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+MAX_ABS = 2e-3
+MAX_REL = 1e-2
+REL_FLOOR = 1e-3
+
+
+def errors(got, want):
+    g = np.asarray(got, np.float64)
+    w = np.asarray(want, np.float64)
+    d = np.abs(g - w)
+    return float(d.max(initial=0.0)), float((d / np.maximum(np.abs(w), REL_FLOOR)).max(initial=0.0))
+
+
+def assert_close(got, want, what=""):
+    assert np.all(np.isfinite(np.asarray(got, np.float64))), f"{what}: non-finite output"
+    ea, er = errors(got, want)
+    assert ea <= MAX_ABS and er <= MAX_REL, f"{what}: max_abs={ea:.3g} max_rel={er:.3g}"
+    return ea, er

@@ -1,0 +1,206 @@
+"""Host-side checks of libpagedattn that need no GPU.
+
+The library loads and exports every function include/pagedattn.h declares.
+pa_plan is pure host code, so its task list can be checked in full here.
+Argument errors are rejected before any CUDA call.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from paged_kv_decode_24_gb300 import binding, workloads
+
+
+def test_exports_every_declared_symbol(lib):
+    names = binding.declared_functions()
+    assert {"pa_kv_append", "pa_plan", "pa_plan_free", "pa_plan_upload", "pa_decode_attention",
+            "pa_debug_gather_indices", "pa_status_string", "pa_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in the header but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.pa_status_string(code)
+    assert b"sm_103a" in lib.pa_version()
+
+
+def _shape(w):
+    return binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                              w.max_pages_per_seq, w.num_pages)
+
+
+def _decode_blob(plan):
+    blob = plan.blob()
+    W, C, nidx = blob[1], blob[2], blob[3]
+    items = blob[16:16 + 4 * W].reshape(W, 4)
+    groups = blob[16 + 4 * W:16 + 4 * W + 4 * C].reshape(C, 4)
+    idx = blob[16 + 4 * W + 4 * C:16 + 4 * W + 4 * C + nidx]
+    return blob, items, groups, idx
+
+
+def check_plan_covers(w, plan):
+    """Every (sequence, kv head) has its pages [0, ceil(L/S)) covered exactly
+    once by page ranges, split tasks appear in their group in page order, and
+    tasks are longest first."""
+    blob, items, groups, idx = _decode_blob(plan)
+    assert blob[0] == 0x564B4150
+    S = w.page_size
+    cover = {}
+    for i, (b, hw, lo, hi) in enumerate(items):
+        hw = int(hw) & 0xFFFFFFFF
+        h = hw & 0xFFFF
+        cover.setdefault((int(b), h), []).append((int(lo), int(hi), i, bool(hw & 0x80000000),
+                                                  bool(hw & 0x40000000)))
+    assert len(cover) == w.batch * w.num_kv_heads
+    for b in range(w.batch):
+        npg = (int(w.seq_lens[b]) + S - 1) // S
+        for h in range(w.num_kv_heads):
+            ranges = sorted(cover[(b, h)])
+            assert ranges[0][0] == 0 and ranges[-1][1] == npg
+            for (lo0, hi0, *_), (lo1, *_r) in zip(ranges, ranges[1:]):
+                assert hi0 == lo1
+            split = len(ranges) > 1
+            assert all(r[3] == split for r in ranges)
+            assert [r[4] for r in ranges] == [False] * (len(ranges) - 1) + [True]
+    sizes = items[:, 3] - items[:, 2]
+    assert np.all(np.diff(sizes) <= 0), "tasks are not longest first"
+    for (b, h, n, off) in groups:
+        assert n > 1
+        members = [int(i) for i in idx[off:off + n]]
+        assert sorted(members) == sorted(r[2] for r in cover[(int(b), int(h))])
+        los = [items[i, 2] for i in members]
+        assert los == sorted(los)
+    assert plan.c.workspace_bytes >= plan.c.blob_bytes
+    return items, groups
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_plan_for_benchmark_workloads(lib, cfg):
+    w = workloads.make_config(cfg)
+    plan = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits)
+    items, groups = check_plan_covers(w, plan)
+    if cfg == 1:
+        assert plan.c.num_groups == 0 and plan.c.num_work_items == w.batch * w.num_kv_heads
+    if cfg == 2:
+        assert plan.c.max_splits == 16 and plan.c.num_work_items == 16 * 32
+        assert np.all(items[:, 3] - items[:, 2] == 16)
+    if cfg == 5:
+        # the 32k sequence is cut, the short ones are not
+        assert plan.c.max_splits > 8
+        long_items = items[items[:, 0] == 255]
+        assert len(long_items) == plan.c.max_splits * w.num_kv_heads
+
+
+@pytest.mark.parametrize("lens", [[0], [0, 0, 3], [1], [16], [17], [4095, 1, 0, 33]])
+@pytest.mark.parametrize("forced", [0, 1, 3, 16])
+def test_plan_ragged_and_empty(lib, lens, forced):
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=8, num_kv_heads=2, head_dim=128, seed=1)
+    plan = binding.Plan(_shape(w), w.seq_lens, 152, forced)
+    check_plan_covers(w, plan)
+
+
+def test_plan_rejects_bad_inputs(lib):
+    w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=2)
+    s = _shape(w)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(s, [10, w.max_pages_per_seq * 16 + 1], 152)
+    assert e.value.code == 1
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(s, [-1, 5], 152)
+    assert e.value.code == 1
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(s, [10, 20], 0)
+    assert e.value.code == 1
+    for bad, code in [(dict(head_dim=96), 2), (dict(page_size=8), 2), (dict(num_q_heads=6), 2),
+                      (dict(num_q_heads=5), 1), (dict(num_kv_heads=0), 1), (dict(num_pages=0), 1)]:
+        kw = dict(batch=2, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
+                  max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages)
+        kw.update(bad)
+        with pytest.raises(binding.PagedAttnError) as e:
+            binding.Plan(binding.make_shape(**kw), [10, 20], 152)
+        assert e.value.code == code, bad
+
+
+def test_plan_free_is_idempotent(lib):
+    w = workloads.make_custom(seq_lens=[5], num_q_heads=1, num_kv_heads=1, head_dim=64, seed=3)
+    plan = binding.Plan(_shape(w), w.seq_lens, 152)
+    plan.free()
+    plan.free()
+    lib.pa_plan_free(None)
+
+
+def test_plan_is_deterministic_but_ids_differ(lib):
+    w = workloads.make_config(4)
+    a = binding.Plan(_shape(w), w.seq_lens, 152)
+    b = binding.Plan(_shape(w), w.seq_lens, 152)
+    ba, bb = a.blob(), b.blob()
+    assert np.array_equal(np.delete(ba, [4, 5]), np.delete(bb, [4, 5]))
+    assert a.c.plan_id != b.c.plan_id
+
+
+def test_plan_in_caller_buffer(lib):
+    w = workloads.make_config(3)
+    s = _shape(w)
+    ref = binding.Plan(s, w.seq_lens, 152)
+    small = np.zeros(16, np.uint8)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(s, w.seq_lens, 152, host_buffer=small)
+    assert e.value.code == 3
+    buf = np.zeros(ref.c.blob_bytes + 64, np.uint8)
+    p = binding.Plan(s, w.seq_lens, 152, host_buffer=buf)
+    assert p.c.owns_blob == 0 and p.c.host_blob == buf.ctypes.data
+    got = buf[:ref.c.blob_bytes].view(np.int32)
+    assert np.array_equal(np.delete(got, [4, 5]), np.delete(ref.blob(), [4, 5]))
+    p.free()   # must not free the caller's buffer
+    assert buf[:4].view(np.int32)[0] == 0x564B4150
+
+
+def test_decode_rejects_before_launch(lib):
+    """Argument errors return before touching CUDA (this host has no GPU)."""
+    w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=4)
+    s = _shape(w)
+    plan = binding.Plan(s, w.seq_lens, 152)
+    fake = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: the calls below fail earlier
+    null = ctypes.c_void_p(0)
+    args = lambda **o: [o.get(k, fake) for k in ("q", "kp", "vp", "bt", "sl")]
+    # null pointer
+    r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), *args(q=null),
+                                ctypes.c_float(0.1), fake, fake, plan.c.workspace_bytes, fake, None)
+    assert r == 1
+    # misaligned q
+    r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), *args(q=ctypes.c_void_p(0x10002)),
+                                ctypes.c_float(0.1), fake, fake, plan.c.workspace_bytes, fake, None)
+    assert r == 1
+    # workspace too small
+    r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), *args(), ctypes.c_float(0.1),
+                                fake, fake, plan.c.workspace_bytes - 1, fake, None)
+    assert r == 3
+    # non-finite scale
+    r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), *args(),
+                                ctypes.c_float(float("nan")), fake, fake, plan.c.workspace_bytes, fake, None)
+    assert r == 1
+    # plan made for another shape
+    s2 = binding.make_shape(2, 4, 2, 64, 16, w.max_pages_per_seq + 1, w.num_pages)
+    r = lib.pa_decode_attention(ctypes.byref(s2), ctypes.byref(plan.c), *args(), ctypes.c_float(0.1),
+                                fake, fake, plan.c.workspace_bytes, fake, None)
+    assert r == 8
+    # upload into a too-small workspace
+    assert lib.pa_plan_upload(ctypes.byref(plan.c), fake, plan.c.workspace_bytes - 1, None) == 3
+    # append with an unsupported head_dim
+    s3 = binding.make_shape(2, 4, 2, 80, 16, 4, 8)
+    assert lib.pa_kv_append(ctypes.byref(s3), fake, fake, fake, fake, fake, fake, fake, None) == 2
+
+
+def test_empty_batch_is_a_no_op(lib):
+    s = binding.make_shape(0, 4, 2, 64, 16, 4, 8)
+    plan = binding.Plan(s, np.zeros(0, np.int32), 152)
+    assert plan.c.num_work_items == 0
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), fake, fake, fake, fake,
+                                   fake, ctypes.c_float(0.1), fake, fake, 1 << 20, fake, None) == 0
+    assert lib.pa_kv_append(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, None) == 0
