@@ -11,10 +11,10 @@ namespace {
 template <int G>
 cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int D = 128;
-  constexpr int NS = stages_for(D);
-  constexpr int smem = kWarpsPerCta * warp_smem(D, G, NS).bytes;
+  constexpr int NSH = half_stages_for(D);
+  constexpr int smem = kWarpsPerCta * warp_smem(D, G, NSH).bytes;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
-  auto kern = split_decode_kernel<D, G, NS>;
+  auto kern = split_decode_kernel<D, G, kWarpsPerCta, NSH>;
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -1,35 +1,41 @@
 // Split decode attention over a paged KV cache.
 //
-// One warp = one task (sequence b, KV head g, page range [pg0, pg1)).  The
-// warp streams its pages through a private ring of NS shared-memory stages.
-// Lane 0 issues one 1-D bulk copy per (page, head) slice of K and of V; each
-// slice is one contiguous run of S*D halves, so one copy moves a whole tile
-// with no address math per row.  Copies complete on an mbarrier.  The warp
-// serves all G query heads of its KV head from that single read of K and V
-// (GQA: MonadKai/xLLM, KV cache with GQA).  It keeps an online softmax
-// (xLLM introduction, SoftMax with an online normalizer): a running max m, a
-// running sum l and a rescaled accumulator per query head.
+// One CTA = one task (sequence b, KV head g, page range [pg0, pg1)).  The
+// CTA's NW warps take the task's pages round-robin (warp w: pages w, w+NW,
+// ...).  Each warp streams its pages through a private ring of NSH
+// shared-memory half-stages: a K tile or a V tile of one page, each one
+// contiguous (page, head) slice of S*D halves.  Lane 0 fills a half-stage
+// with a single 1-D bulk copy that completes on that stage's mbarrier.
+// Separate K and V stages let the V copy of a page land while the page's
+// scores are being computed, without doubling the ring.
+//
+// The warp serves all G query heads of its KV head from that single read of
+// K and V (GQA: MonadKai/xLLM, KV cache with GQA).  It keeps an online softmax
+// per query head (xLLM introduction, SoftMax with an online normalizer):
+// running max m, running sum l, and an accumulator rescaled whenever m grows.
+// At the end the NW warp states (m, l, acc) meet in shared memory and merge
+// with the same log-sum-exp rule the combine kernel uses.  No atomics touch
+// data, and every reduction has a fixed order, so reruns are bit-identical.
+// This follows the from-scratch engine article, section 3.4: shared memory
+// instead of atomicAdd.
 //
 // Lane roles on a page of 16 tokens:
 //   QK: lane = (row group rg = lane/8, chunk c = lane%8).  Lane (rg, c) takes
 //       tokens rg, rg+4, rg+8, rg+12 and, in each row, dims [8c, 8c+8) (and
 //       [64+8c, 64+8c+8) when D = 128).  Eight lanes read one 128-byte run
-//       per shared-memory load, so the loads are conflict-free.  The 4*G
-//       partial dot products are summed over the 8 chunk lanes by a
-//       reduce-scatter (3 shuffle rounds, halving the values each round)
-//       instead of 4*G separate butterflies.
+//       per shared-memory load, conflict-free.  The 4*G partial dot products
+//       are summed over the 8 chunk lanes by a reduce-scatter: 3 shuffle
+//       rounds, halving the values each round.
 //   PV: lane owns output dims [D/32*lane, D/32*(lane+1)) of every head and
-//       walks the 16 rows; the softmax weights come from shared memory as
+//       walks the 16 rows.  The weights are read from shared memory as
 //       broadcasts.
-// All reductions are shuffles or shared memory in a fixed order, with no
-// atomics on data, so a rerun is bit-identical.  This follows the
-// from-scratch engine article, section 3.4: shared memory instead of
-// atomicAdd.
+// The multiply-adds of both products use the packed two-wide FP32 FMA
+// (fma.rn.f32x2), so each instruction does two.
 //
-// A task whose sequence has more than one split writes its normalised
-// output and log2-sum-exp to the workspace.  combine_kernel merges those
-// (swiftLLM, paged attention v2 / Flash-Decoding).  Otherwise the task
-// writes the fp16 output directly.
+// A task whose sequence has more than one split writes its normalised output
+// and log2-sum-exp to the workspace.  combine_kernel merges them (swiftLLM,
+// paged attention v2 / Flash-Decoding).  Otherwise the task writes fp16
+// output directly.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -66,6 +72,20 @@ struct Geometry {
   static constexpr int HEAD_LANES = 8 / G;            // chunk lanes that share one head
 };
 
+// d = a * b + c on two fp32 lanes with one instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 // Sum the N values held by each of the 8 lanes of a row group (lane bits
 // 0..2) so that afterwards lane c holds complete sums.  Each round sends
 // half of the remaining values to the partner lane and keeps the other
@@ -92,56 +112,63 @@ __device__ __forceinline__ void reduce_scatter(float* v, int lane) {
   }
 }
 
-__device__ __forceinline__ void half8_to_float(const uint4& raw, float* f) {
+__device__ __forceinline__ void half8_to_float2x4(const uint4& raw, float2* f) {
   const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 x = __half22float2(h2[e]);
-    f[2 * e] = x.x;
-    f[2 * e + 1] = x.y;
-  }
+  for (int e = 0; e < 4; ++e) f[e] = __half22float2(h2[e]);
 }
 
-template <int D, int G, int NS>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+// Shared memory of one warp (bytes); the CTA holds NW of these.
+template <int D, int G, int NSH>
+struct WarpLayout {
+  static constexpr WarpSmem W = warp_smem(D, G, NSH);
+  static constexpr int TILE = W.tile;
+  static constexpr int RING = W.ring;
+  static constexpr int BAR = W.bar;
+  static constexpr int PAGE = W.page;
+  static constexpr int P = W.p;
+  static constexpr int A = W.a;
+  static constexpr int BYTES = W.bytes;
+};
+
+template <int D, int G, int NW, int NSH>
+__global__ void __launch_bounds__(NW * 32)
     split_decode_kernel(const SplitParams p) {
   using Geo = Geometry<D, G>;
-  constexpr WarpSmem L = warp_smem(D, G, NS);
+  using L = WarpLayout<D, G, NSH>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ int cta_failed;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rg = lane >> 3;
   const int c = lane & 7;
-  unsigned char* ws = smem_raw + warp * L.bytes;
+  unsigned char* ws = smem_raw + warp * L::BYTES;
   const uint32_t ws_u32 = smem_u32(ws);
-  int* page_ids = reinterpret_cast<int*>(ws + L.page_off);
-  float* p_s = reinterpret_cast<float*>(ws + L.p_off);  // [16][G] softmax weights of a page
-  float* a_s = reinterpret_cast<float*>(ws + L.a_off);  // [G] rescale factors of a page
+  int* page_ids = reinterpret_cast<int*>(ws + L::PAGE);
+  float* p_s = reinterpret_cast<float*>(ws + L::P);
+  float* a_s = reinterpret_cast<float*>(ws + L::A);
 
+  if (threadIdx.x == 0) cta_failed = 0;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(ws_u32 + L.bar_off + 16 * s, 1);
-      mbar_init(ws_u32 + L.bar_off + 16 * s + 8, 1);
-    }
+    for (int s = 0; s < NSH; ++s) mbar_init(ws_u32 + L::BAR + 8 * s, 1);
     fence_barrier_init();
   }
-  __syncwarp();
+  __syncthreads();
 
   pdl_launch_dependents();
   pdl_wait_primary();  // everything the previous kernel wrote is visible after this
 
-  const int item_idx = blockIdx.x * kWarpsPerCta + warp;
-  if (item_idx >= p.num_items) return;
-
+  const int item_idx = blockIdx.x;
+  if (item_idx >= p.num_items) return;  // whole CTA
   const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
+  const int4 it = p.items[item_idx];
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
       hdr.w != p.num_split_items) {
-    if (lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+    if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
     return;
   }
-  const int4 it = p.items[item_idx];
   const int b = it.x;
   const uint32_t hw = (uint32_t)it.y;
   const int kvh = (int)(hw & kItemHeadMask);
@@ -150,20 +177,22 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   const int pg0 = it.z, pg1 = it.w;
   if (b < 0 || b >= p.batch || kvh >= p.num_kv_heads || pg0 < 0 || pg1 < pg0 ||
       pg1 > p.max_pages) {
-    if (lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+    if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
     return;
   }
   const int Lmax = p.max_pages * kPageSize;
   int seq_len = p.seq_lens[b];
   if (seq_len < 0 || seq_len > Lmax) {
-    if (lane == 0) set_status(p.status, PA_DEV_BAD_SEQ_LEN);
+    if (threadIdx.x == 0) set_status(p.status, PA_DEV_BAD_SEQ_LEN);
     seq_len = min(max(seq_len, 0), Lmax);
   }
-  if (is_last && seq_len > pg1 * kPageSize && lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+  if (is_last && seq_len > pg1 * kPageSize && threadIdx.x == 0)
+    set_status(p.status, PA_DEV_PLAN_MISMATCH);
   const int npg = pg1 - pg0;
+  const int npk = warp < npg ? (npg - warp + NW - 1) / NW : 0;  // pages of this warp
 
-  // q for the G heads of this KV head, pre-scaled by scale*log2(e).
-  float qf[G][Geo::CH * 8];
+  // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
+  float2 qf[G][Geo::CH * 4];
   {
     const __half* qb = p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
 #pragma unroll
@@ -171,10 +200,11 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 #pragma unroll
       for (int ch = 0; ch < Geo::CH; ++ch) {
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * D + ch * 64 + c * 8));
-        float f[8];
-        half8_to_float(raw, f);
+        float2 f[4];
+        half8_to_float2x4(raw, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qf[h][ch * 8 + e] = f[e] * p.qscale;
+        for (int e = 0; e < 4; ++e)
+          qf[h][ch * 4 + e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
       }
   }
 
@@ -185,18 +215,20 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   const uint64_t policy = l2_evict_first_policy();
 
   // Block-table entries of the task, 32 per window: lane k of the current
-  // window holds entry 32*w + k; the next window is loaded one window ahead
-  // so the copy issue never waits on it.
+  // window holds entry 32*w + k.  The next window is loaded one window ahead.
   int bt_cur = lane < npg ? __ldg(bt_row + lane) : -1;
   int bt_nxt = 32 + lane < npg ? __ldg(bt_row + 32 + lane) : -1;
   int bt_w = 0;
 
-  // Issue page j of the task into stage j % NS.  Warp-collective (the entry
-  // comes by shuffle); lane 0 issues.  j grows by one per call.  A page past
-  // the sequence end or with an invalid index is not copied: its barriers
-  // are released empty and the page is masked.
-  auto issue = [&](int j) {
-    if ((j >> 5) != bt_w) {
+  // Issue half-tile hi of this warp: page k = hi/2 of the warp (task page
+  // j = warp + k*NW), K tile for even hi, V tile for odd hi, into stage
+  // hi % NSH.  Warp-collective (the block-table entry comes by shuffle);
+  // lane 0 issues.  hi grows by one per call.  A page past the sequence end
+  // or with an invalid index is not copied: its barrier is released empty and
+  // the page is masked.
+  auto issue = [&](int hi) {
+    const int j = warp + (hi >> 1) * NW;
+    if ((j >> 5) != bt_w) {  // j grows by at most NW <= 32 between calls
       ++bt_w;
       bt_cur = bt_nxt;
       const int idx = 32 * (bt_w + 1) + lane;
@@ -204,87 +236,87 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     }
     int phys = __shfl_sync(kFull, bt_cur, j & 31);
     if (lane == 0) {
-      const int s = j % NS;
-      const uint32_t kb = ws_u32 + L.bar_off + 16 * s;
+      const int s = hi % NSH;
+      const uint32_t bar = ws_u32 + L::BAR + 8 * s;
       if ((pg0 + j) * kPageSize >= seq_len) {
         phys = -1;
       } else if (phys < 0 || phys >= p.num_pages) {
-        set_status(p.status, PA_DEV_BAD_PAGE);
+        if ((hi & 1) == 0) set_status(p.status, PA_DEV_BAD_PAGE);
         phys = -1;
       }
       page_ids[s] = phys;
       fence_proxy_async_smem();
       if (phys >= 0) {
-        mbar_arrive_expect_tx(kb, L.tile);
-        bulk_g2s(ws_u32 + L.k_off + s * L.tile, kbase + (size_t)phys * page_stride, L.tile, kb,
-                 policy);
-        mbar_arrive_expect_tx(kb + 8, L.tile);
-        bulk_g2s(ws_u32 + L.v_off + s * L.tile, vbase + (size_t)phys * page_stride, L.tile, kb + 8,
-                 policy);
+        const __half* src = ((hi & 1) ? vbase : kbase) + (size_t)phys * page_stride;
+        mbar_arrive_expect_tx(bar, L::TILE);
+        bulk_g2s(ws_u32 + L::RING + s * L::TILE, src, L::TILE, bar, policy);
       } else {
-        mbar_arrive(kb);
-        mbar_arrive(kb + 8);
+        mbar_arrive(bar);
       }
     }
   };
 
-  const int npre = npg < NS ? npg : NS;
-  for (int j = 0; j < npre; ++j) issue(j);
+  const int nhalf = 2 * npk;
+  const int npre = nhalf < NSH ? nhalf : NSH;
+  for (int hi = 0; hi < npre; ++hi) issue(hi);
 
-  // Softmax state of this lane's head (lanes of one head hold equal copies).
-  float m_run = -INFINITY, l_run = 0.f;
+  // Softmax state of this lane's head: m is shared by the lanes of a head,
+  // l_part is this lane's own share of the running sum.
+  float m_run = -INFINITY, l_part = 0.f;
   const int myh = (G == 1) ? 0 : ((c * Geo::NVL) >> 2);
-  float acc[G][Geo::DPL];
+  float2 acc[G][Geo::DPL / 2];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int d = 0; d < Geo::DPL; ++d) acc[h][d] = 0.f;
+    for (int d = 0; d < Geo::DPL / 2; ++d) acc[h][d] = make_float2(0.f, 0.f);
 
-  int jfail = -1;
-  for (int j = 0; j < npg; ++j) {
-    const int s = j % NS;
-    const uint32_t kb = ws_u32 + L.bar_off + 16 * s;
-    const uint32_t par = (uint32_t)(j / NS) & 1u;
-    if (!__all_sync(kFull, mbar_wait_bounded(kb, par))) {
-      jfail = j;
+  bool failed = false;
+  int hfail = 0;
+  for (int k = 0; k < npk; ++k) {
+    const int hk = 2 * k;
+    const int sk = hk % NSH;
+    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sk, (hk / NSH) & 1))) {
+      failed = true;
+      hfail = hk;
       break;
     }
-    const int phys = page_ids[s];
+    const int phys = page_ids[sk];
+    const int j = warp + k * NW;
     const int nvalid = phys < 0 ? 0 : min(kPageSize, seq_len - (pg0 + j) * kPageSize);
 
     if (nvalid > 0) {
       // ---- scores of the page's 16 tokens for the G heads
-      const __half* Ks = reinterpret_cast<const __half*>(ws + L.k_off + s * L.tile);
+      const __half* Ks = reinterpret_cast<const __half*>(ws + L::RING + sk * L::TILE);
       float v[Geo::NV];
-#pragma unroll
-      for (int k = 0; k < Geo::NV; ++k) v[k] = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = rg + 4 * i;
+        float2 a2[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < Geo::CH; ++ch) {
           const uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * D + ch * 64 + c * 8);
-          float kf[8];
-          half8_to_float(raw, kf);
+          float2 kf[4];
+          half8_to_float2x4(raw, kf);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float a = v[h * 4 + i];
+          for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a = fmaf(qf[h][ch * 8 + e], kf[e], a);
-            v[h * 4 + i] = a;
-          }
+            for (int e = 0; e < 4; ++e) a2[h] = ffma2(qf[h][ch * 4 + e], kf[e], a2[h]);
         }
+#pragma unroll
+        for (int h = 0; h < G; ++h) v[h * 4 + i] = a2[h].x + a2[h].y;
       }
       reduce_scatter<Geo::NV, 4>(v, lane);
 
       // ---- online softmax update for this lane's head
       float pmax = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < Geo::NVL; ++k) {
-        const int vi = (Geo::NV >= 8) ? c * Geo::NVL + k : (c >> 1);
+      for (int e = 0; e < Geo::NVL; ++e) {
+        const int vi = (Geo::NV >= 8) ? c * Geo::NVL + e : (c >> 1);
         const int t = rg + 4 * (vi & 3);
-        if (t >= nvalid) v[k] = -INFINITY;
-        pmax = fmaxf(pmax, v[k]);
+        if (t >= nvalid) v[e] = -INFINITY;
+        pmax = fmaxf(pmax, v[e]);
       }
 #pragma unroll
       for (int m = 1; m < Geo::HEAD_LANES; m <<= 1)
@@ -296,27 +328,26 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
       const float alpha = dead ? 1.f : ex2(m_run - m_new);
       float psum = 0.f;
 #pragma unroll
-      for (int k = 0; k < Geo::NVL; ++k) {
-        const int vi = (Geo::NV >= 8) ? c * Geo::NVL + k : (c >> 1);
+      for (int e = 0; e < Geo::NVL; ++e) {
+        const int vi = (Geo::NV >= 8) ? c * Geo::NVL + e : (c >> 1);
         const int t = rg + 4 * (vi & 3);
-        const float pk = dead ? 0.f : ex2(v[k] - m_new);
+        const float pk = dead ? 0.f : ex2(v[e] - m_new);
         p_s[t * G + (vi >> 2)] = pk;
         psum += pk;
       }
-      // G == 1: lanes c and c^1 hold the same value, so bit 0 is not summed.
-#pragma unroll
-      for (int m = (G == 1 ? 2 : 1); m < Geo::HEAD_LANES; m <<= 1)
-        psum += __shfl_xor_sync(kFull, psum, m);
-      psum += __shfl_xor_sync(kFull, psum, 8);
-      psum += __shfl_xor_sync(kFull, psum, 16);
-      l_run = l_run * alpha + psum;
+      l_part = l_part * alpha + psum;
       m_run = m_new;
       if (rg == 0 && (c & (Geo::HEAD_LANES - 1)) == 0) a_s[myh] = alpha;
       __syncwarp();
     }
+    // the K stage is free: refill it with the half-tile NSH ahead
+    if (hk + NSH < nhalf) issue(hk + NSH);
 
-    if (!__all_sync(kFull, mbar_wait_bounded(kb + 8, par))) {
-      jfail = j;
+    const int hv = hk + 1;
+    const int sv = hv % NSH;
+    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sv, (hv / NSH) & 1))) {
+      failed = true;
+      hfail = hv;
       break;
     }
     if (nvalid > 0) {
@@ -332,85 +363,101 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-          for (int d = 0; d < Geo::DPL; ++d) acc[h][d] *= al[h];
+          for (int d = 0; d < Geo::DPL / 2; ++d)
+            acc[h][d] = make_float2(acc[h][d].x * al[h], acc[h][d].y * al[h]);
       }
-      const __half* Vs = reinterpret_cast<const __half*>(ws + L.v_off + s * L.tile);
+      const __half* Vs = reinterpret_cast<const __half*>(ws + L::RING + sv * L::TILE);
 #pragma unroll
       for (int t = 0; t < kPageSize; ++t) {
         if (t < nvalid) {
           float pp[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) pp[h] = p_s[t * G + h];
-          float vf[Geo::DPL];
+          float2 vf[Geo::DPL / 2];
           if constexpr (Geo::DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            vf[0] = a.x;
-            vf[1] = a.y;
-            vf[2] = bb.x;
-            vf[3] = bb.y;
+            vf[0] = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            vf[1] = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
           } else {
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(Vs + t * D + lane * 2));
-            vf[0] = a.x;
-            vf[1] = a.y;
+            vf[0] = __half22float2(*reinterpret_cast<const __half2*>(Vs + t * D + lane * 2));
           }
 #pragma unroll
           for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int d = 0; d < Geo::DPL; ++d) acc[h][d] = fmaf(pp[h], vf[d], acc[h][d]);
+            for (int d = 0; d < Geo::DPL / 2; ++d)
+              acc[h][d] = ffma2(make_float2(pp[h], pp[h]), vf[d], acc[h][d]);
         }
       }
     }
     __syncwarp();
-    if (j + NS < npg) issue(j + NS);
+    if (hv + NSH < nhalf) issue(hv + NSH);
   }
 
-  if (jfail >= 0) {
-    // A copy did not land in time.  Report, let the copies already issued
-    // finish (bounded), and leave without writing.
+  if (failed) {
+    // A copy did not land in time.  Report it and let the copies already
+    // issued finish (bounded).  The CTA writes nothing.
     if (lane == 0) {
       set_status(p.status, PA_DEV_TIMEOUT);
-      const int last = min(npg, jfail + NS);
-      for (int j = jfail; j < last; ++j) {
-        const uint32_t kb = ws_u32 + L.bar_off + 16 * (j % NS);
-        const uint32_t par = (uint32_t)(j / NS) & 1u;
-        mbar_wait_bounded(kb, par, 10000000ull);
-        mbar_wait_bounded(kb + 8, par, 10000000ull);
-      }
+      const int last = min(nhalf, hfail + NSH);
+      for (int h = hfail; h < last; ++h)
+        mbar_wait_bounded(ws_u32 + L::BAR + 8 * (h % NSH), (h / NSH) & 1, 10000000ull);
+      cta_failed = 1;
     }
     __syncwarp();
-    return;
   }
 
-  // ---- epilogue: normalise and write
+  // ---- merge the NW warp states in shared memory (the rings are free now)
+  if (lane == 0 && !failed) {
+#pragma unroll
+    for (int s = 0; s < NSH; ++s) mbar_inval(ws_u32 + L::BAR + 8 * s);
+  }
+  // l: sum this lane's share over the lanes of the head (G == 1: lanes c and
+  // c^1 hold the same values, so bit 0 is not summed).
+#pragma unroll
+  for (int m = (G == 1 ? 2 : 1); m < Geo::HEAD_LANES; m <<= 1)
+    l_part += __shfl_xor_sync(kFull, l_part, m);
+  l_part += __shfl_xor_sync(kFull, l_part, 8);
+  l_part += __shfl_xor_sync(kFull, l_part, 16);
+  __syncthreads();
+  if (cta_failed) return;
+  float* st = reinterpret_cast<float*>(smem_raw);  // [NW][2G + G*D]
+  constexpr int SLOT = 2 * G + G * D;
+  float* mine = st + warp * SLOT;
+  if (rg == 0 && (c & (Geo::HEAD_LANES - 1)) == 0) {
+    mine[myh] = m_run;
+    mine[G + myh] = l_part;
+  }
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const int rep = h * Geo::HEAD_LANES;  // lane (rg 0, c = h*HEAD_LANES) owns head h's state
-    const float lh = __shfl_sync(kFull, l_run, rep);
-    const float mh = __shfl_sync(kFull, m_run, rep);
-    const float inv = lh > 0.f ? 1.f / lh : 0.f;
+    float* o = mine + 2 * G + h * D + lane * Geo::DPL;
+#pragma unroll
+    for (int d = 0; d < Geo::DPL / 2; ++d) {
+      o[2 * d] = acc[h][d].x;
+      o[2 * d + 1] = acc[h][d].y;
+    }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, st[w * SLOT + h]);
+    float Z = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float sc = ex2(st[w * SLOT + h] - M);  // 0 for an empty warp (m = -inf)
+        Z = fmaf(st[w * SLOT + G + h], sc, Z);
+        O = fmaf(st[w * SLOT + 2 * G + h * D + d], sc, O);
+      }
+    }
+    const float r = Z > 0.f ? O / Z : 0.f;
     if (!is_split) {
-      __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + lane * Geo::DPL;
-      if constexpr (Geo::DPL == 4) {
-        const __half2 a = __floats2half2_rn(acc[h][0] * inv, acc[h][1] * inv);
-        const __half2 bb = __floats2half2_rn(acc[h][2] * inv, acc[h][3] * inv);
-        uint2 w;
-        w.x = *reinterpret_cast<const uint32_t*>(&a);
-        w.y = *reinterpret_cast<const uint32_t*>(&bb);
-        *reinterpret_cast<uint2*>(o) = w;
-      } else {
-        *reinterpret_cast<__half2*>(o) = __floats2half2_rn(acc[h][0] * inv, acc[h][1] * inv);
-      }
+      p.out[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] = __float2half_rn(r);
     } else {
-      float* o = p.part_o + ((size_t)item_idx * G + h) * D + lane * Geo::DPL;
-      if constexpr (Geo::DPL == 4) {
-        *reinterpret_cast<float4*>(o) =
-            make_float4(acc[h][0] * inv, acc[h][1] * inv, acc[h][2] * inv, acc[h][3] * inv);
-      } else {
-        *reinterpret_cast<float2*>(o) = make_float2(acc[h][0] * inv, acc[h][1] * inv);
-      }
-      if (lane == 0) p.part_lse[(size_t)item_idx * G + h] = lh > 0.f ? mh + lg2(lh) : -INFINITY;
+      p.part_o[((size_t)item_idx * G + h) * D + d] = r;
+      if (d == 0) p.part_lse[(size_t)item_idx * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
 }

@@ -15,9 +15,9 @@
 namespace pa {
 
 constexpr int kPageSize = 16;        // tokens per page (the only size built)
-constexpr int kWarpsPerCta = 4;      // independent warp tasks per CTA
+constexpr int kWarpsPerCta = 4;      // warps sharing one task's pages
 constexpr int kMaxSplits = 1024;     // per (sequence, KV head); the combine keeps weights in smem
-constexpr int kMinChunkPages = 4;    // auto planner never cuts finer than this
+constexpr int kMinChunkPages = 8;    // auto planner never cuts finer than this
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
@@ -27,38 +27,42 @@ constexpr uint32_t kItemSplit = 0x80000000u;  // writes a partial (o, lse) inste
 constexpr uint32_t kItemLast = 0x40000000u;   // last page range of its sequence
 constexpr uint32_t kItemHeadMask = 0x0000ffffu;
 
-// Page-copy pipeline depth per warp.
-PA_HD constexpr int stages_for(int head_dim) { return head_dim == 64 ? 6 : 3; }
+// Per-warp ring depth in half-stages (one K or V tile of one page each).
+PA_HD constexpr int half_stages_for(int head_dim) { return head_dim == 64 ? 6 : 3; }
 
-// Shared memory of one warp's pipeline; the kernel carves exactly this.
+// Shared memory of one warp of the split-decode kernel; the kernel carves
+// exactly this, and the CTA holds kWarpsPerCta of them.
 struct WarpSmem {
-  int tile, k_off, v_off, bar_off, page_off, p_off, a_off, bytes;
+  int tile, ring, bar, page, p, a, bytes;
 };
 
 PA_HD constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-PA_HD constexpr WarpSmem warp_smem(int head_dim, int group, int stages) {
+PA_HD constexpr WarpSmem warp_smem(int head_dim, int group, int nsh) {
   WarpSmem w{};
-  w.tile = kPageSize * head_dim * 2;
-  w.k_off = 0;
-  w.v_off = stages * w.tile;
-  w.bar_off = 2 * stages * w.tile;
-  w.page_off = w.bar_off + 2 * stages * 8;
-  w.p_off = align_up(w.page_off + stages * 4, 16);
-  w.a_off = w.p_off + kPageSize * group * 4;
-  w.bytes = align_up(w.a_off + (group < 4 ? 4 : group) * 4, 128);
+  w.tile = kPageSize * head_dim * 2;         // one K or V tile of one (page, head)
+  w.ring = 0;                                // nsh tiles
+  w.bar = nsh * w.tile;                      // nsh mbarriers
+  w.page = w.bar + 8 * nsh;                  // nsh physical page ids
+  w.p = align_up(w.page + 4 * nsh, 16);      // [16][group] softmax weights
+  w.a = w.p + kPageSize * group * 4;         // [group] rescale factors
+  w.bytes = align_up(w.a + 4 * (group < 4 ? 4 : group), 128);
   return w;
 }
 
 inline int cta_smem_bytes(int head_dim, int group) {
-  return kWarpsPerCta * warp_smem(head_dim, group, stages_for(head_dim)).bytes;
+  return kWarpsPerCta * warp_smem(head_dim, group, half_stages_for(head_dim)).bytes;
 }
 
-inline int resident_warps_per_sm(int head_dim, int group) {
-  int ctas = (int)(kSmemPerSm / (size_t)(cta_smem_bytes(head_dim, group) + 1024));
-  if (ctas < 1) ctas = 1;
-  if (ctas * kWarpsPerCta > 64) ctas = 64 / kWarpsPerCta;
-  return ctas * kWarpsPerCta;
+// Resident split-decode CTAs per SM, from shared memory and a register
+// estimate per group size (the planner runs on the host without a GPU).
+inline int resident_ctas_per_sm(int head_dim, int group) {
+  int by_smem = (int)(kSmemPerSm / (size_t)(cta_smem_bytes(head_dim, group) + 1024));
+  const int regs = group <= 1 ? 72 : group == 2 ? 80 : group == 4 ? 128 : 256;
+  int by_regs = 65536 / (kWarpsPerCta * 32 * regs);
+  int n = by_smem < by_regs ? by_smem : by_regs;
+  if (n * kWarpsPerCta > 64) n = 64 / kWarpsPerCta;
+  return n < 1 ? 1 : n;
 }
 
 // Workspace = [plan blob | lse partials | o partials].

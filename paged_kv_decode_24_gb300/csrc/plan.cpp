@@ -73,12 +73,12 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   }
 
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
-  // that the task count is about twice the warp slots of the GPU, never
-  // finer than kMinChunkPages.
+  // that the task count is about three times the CTAs the GPU holds at once
+  // (one CTA per task), never finer than kMinChunkPages.
   int32_t chunk = 0;
   if (forced_splits == 0) {
-    const int64_t slots = (int64_t)num_sms * resident_warps_per_sm(D, G);
-    const int64_t target_tasks = 2 * slots;
+    const int64_t slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
+    const int64_t target_tasks = 3 * slots;
     chunk = (int32_t)std::max<int64_t>((total_units + target_tasks - 1) / target_tasks,
                                        kMinChunkPages);
   }
@@ -182,7 +182,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->max_splits = max_splits;
   plan_out->chunk_pages = forced_splits > 0 ? max_size : chunk;
   plan_out->warps_per_cta = kWarpsPerCta;
-  plan_out->num_ctas = (W + kWarpsPerCta - 1) / kWarpsPerCta;
+  plan_out->num_ctas = W;
   plan_out->owns_blob = dst ? 0 : 1;
   plan_out->plan_id = id;
   plan_out->blob_bytes = lay.blob_bytes;
