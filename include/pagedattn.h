@@ -194,6 +194,39 @@ pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, 
                                 void* out, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_status, void* stream);
 
+/* Size of the library-owned scratch array used by pa_decode_attention_static. */
+#define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+/*
+ * pa_decode_attention without a caller workspace: an entry point that
+ * allocates nothing.  It has no counterpart in the pages; it exists for
+ * callers that cannot allocate device memory.  Examples are code embedded in
+ * another runtime that receives only its input and output buffers and must
+ * not call cudaMalloc (the host runtime owns all device memory and its
+ * accounting), and latency-critical loops where a cudaMalloc could stall on
+ * device synchronisation.
+ *
+ * Same arguments and result as pa_decode_attention, minus the workspace.
+ * The task list and the split partials live in one file-scope __device__
+ * array of PA_STATIC_WORKSPACE_BYTES (16 MiB).  Every GPU that loads the
+ * library holds the array until the process exits.  Each call uploads the
+ * plan's task list into it (host_blob must still be valid), then launches
+ * the same kernels.  No cudaMalloc, cudaFree or allocating library routine
+ * is called.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current.  Make that first call
+ *    before any stream capture.
+ *  - A plan whose workspace_bytes exceeds PA_STATIC_WORKSPACE_BYTES is
+ *    rejected with PA_ERR_WORKSPACE before anything is launched.
+ *  - All calls on a device share the array, which keeps the previous call's
+ *    contents.  Nothing in it needs to start at zero.  Calls that overlap on
+ *    the GPU (other streams, other host threads) race on it: serialise them.
+ */
+pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t* plan,
+                                       const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       float scale, void* out, int32_t* dev_status, void* stream);
+
 /*
  * Export the physical slot of every logical token, for exact comparison
  * with the oracle: out_slots[b][t] = block_table[b][t/S]*S + t%S for
