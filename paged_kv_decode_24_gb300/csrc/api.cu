@@ -104,7 +104,7 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
   if (!plan) return PA_ERR_INVALID_ARG;
   if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
   if (shape->batch == 0) return PA_OK;
-  if (plan->num_work_items <= 0) return PA_ERR_PLAN;
+  if (plan->num_work_items <= 0 || plan->num_ctas <= 0) return PA_ERR_PLAN;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
       !aligned(workspace, 256))
@@ -114,7 +114,8 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
 
   const int G = shape->num_q_heads / shape->num_kv_heads;
   const int D = shape->head_dim;
-  const Layout lay = layout(plan->num_work_items, plan->num_groups, plan->num_split_items, G, D);
+  const Layout lay = layout(plan->num_work_items, plan->num_groups, plan->num_split_items,
+                            plan->num_ctas, G, D);
   char* ws = (char*)workspace;
   cudaStream_t s = (cudaStream_t)stream;
 
@@ -127,6 +128,8 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
   p.out = (__half*)out;
   p.ws_header = (const int32_t*)ws;
   p.items = (const int4*)(ws + lay.items_off);
+  p.item_slots = (const int32_t*)(ws + lay.slots_off);
+  p.ctas = (const int2*)(ws + lay.ctas_off);
   p.part_lse = (float*)(ws + lay.lse_off);
   p.part_o = (float*)(ws + lay.o_off);
   p.status = dev_status;
@@ -139,13 +142,13 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
   p.num_items = plan->num_work_items;
   p.num_groups = plan->num_groups;
   p.num_split_items = plan->num_split_items;
+  p.num_ctas = plan->num_ctas;
   st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
   if (st != PA_OK || plan->num_groups == 0) return st;
 
   CombineParams c{};
   c.ws_header = (const int32_t*)ws;
   c.groups = (const int4*)(ws + lay.groups_off);
-  c.idx = (const int32_t*)(ws + lay.idx_off);
   c.part_lse = p.part_lse;
   c.part_o = p.part_o;
   c.out = (__half*)out;

@@ -1,8 +1,9 @@
 // Split decode attention over a paged KV cache.
 //
-// One CTA = one task (sequence b, KV head g, page range [pg0, pg1)).  The
-// CTA's NW warps take the task's pages round-robin (warp w: pages w, w+NW,
-// ...).  Each warp streams its pages through a private ring of NSH
+// A task is (sequence b, KV head g, page range [pg0, pg1)).  A CTA either
+// shares one task among its NW warps (warp w takes pages w, w+NW, ...) or,
+// for short tasks, runs up to NW of them, one per warp.  Each warp streams
+// its pages through a private ring of NSH
 // shared-memory half-stages: a K tile or a V tile of one page, each one
 // contiguous (page, head) slice of S*D halves.  Lane 0 fills a half-stage
 // with a single 1-D bulk copy that completes on that stage's mbarrier.
@@ -28,9 +29,10 @@
 //       rounds, halving the values each round.
 //   PV: lane owns output dims [D/32*lane, D/32*(lane+1)) of every head and
 //       walks the 16 rows.  The weights are read from shared memory as
-//       broadcasts.
+//       broadcasts, stored twice over (p, p) so that one 64-bit load is a
+//       whole operand.
 // The multiply-adds of both products use the packed two-wide FP32 FMA
-// (fma.rn.f32x2), so each instruction does two.
+// (fma.rn.f32x2) on pairs of adjacent dims, so each instruction does two.
 //
 // A task whose sequence has more than one split writes its normalised output
 // and log2-sum-exp to the workspace.  combine_kernel merges them (swiftLLM,
@@ -55,12 +57,14 @@ struct SplitParams {
   __half* out;
   const int32_t* ws_header;
   const int4* items;
+  const int32_t* item_slots;  // partial slot of each task, -1 = direct output
   float* part_lse;
   float* part_o;
+  const int2* ctas;  // per CTA: first task, task count (1 = shared by the warps)
   int32_t* status;
   float qscale;  // scale * log2(e): scores are kept in base 2
   int32_t batch, num_q_heads, num_kv_heads, max_pages, num_pages;
-  int32_t num_items, num_groups, num_split_items;  // must match the workspace header
+  int32_t num_items, num_groups, num_split_items, num_ctas;  // must match the header
 };
 
 template <int D, int G>
@@ -112,6 +116,19 @@ __device__ __forceinline__ void reduce_scatter(float* v, int lane) {
   }
 }
 
+// d = a * (s, s) on two fp32 lanes with one instruction.
+__device__ __forceinline__ float2 fmul2s(float2 a, float s) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(s));
+  return d;
+}
+
 __device__ __forceinline__ void half8_to_float2x4(const uint4& raw, float2* f) {
   const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
@@ -131,8 +148,14 @@ struct WarpLayout {
   static constexpr int BYTES = W.bytes;
 };
 
+// Four CTAs (16 warps) per SM for G <= 4: the register cap is 128.
+template <int G>
+struct MinCtas {
+  static constexpr int value = G <= 4 ? 4 : 2;
+};
+
 template <int D, int G, int NW, int NSH>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     split_decode_kernel(const SplitParams p) {
   using Geo = Geometry<D, G>;
   using L = WarpLayout<D, G, NSH>;
@@ -149,6 +172,22 @@ __global__ void __launch_bounds__(NW * 32)
   float* p_s = reinterpret_cast<float*>(ws + L::P);
   float* a_s = reinterpret_cast<float*>(ws + L::A);
 
+  if ((int)blockIdx.x >= p.num_ctas) return;  // whole CTA
+  // The task list is written only by pa_plan_upload (a copy, which the
+  // programmatic launch does not overlap), so it may be read before the
+  // wait on the previous kernel.
+  const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
+  const int hdr_ctas = p.ws_header[8];
+  const int2 cd = p.ctas[blockIdx.x];
+  const bool coop = cd.y == 1;  // CTA-uniform
+  const int task = coop ? cd.x : (warp < cd.y ? cd.x + warp : -1);
+  int4 it = make_int4(0, 0, 0, 0);
+  int slot = -1;
+  if (task >= 0 && task < p.num_items) {
+    it = p.items[task];
+    slot = p.item_slots[task];
+  }
+
   if (threadIdx.x == 0) cta_failed = 0;
   if (lane == 0) {
 #pragma unroll
@@ -160,15 +199,13 @@ __global__ void __launch_bounds__(NW * 32)
   pdl_launch_dependents();
   pdl_wait_primary();  // everything the previous kernel wrote is visible after this
 
-  const int item_idx = blockIdx.x;
-  if (item_idx >= p.num_items) return;  // whole CTA
-  const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
-  const int4 it = p.items[item_idx];
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
-      hdr.w != p.num_split_items) {
+      hdr.w != p.num_split_items || hdr_ctas != p.num_ctas || cd.y < 1 || cd.y > NW ||
+      cd.x < 0 || cd.x + cd.y > p.num_items) {
     if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
-    return;
+    return;  // CTA-uniform
   }
+  if (task < 0) return;  // idle warp of a partial bundle; bundles never sync the CTA
   const int b = it.x;
   const uint32_t hw = (uint32_t)it.y;
   const int kvh = (int)(hw & kItemHeadMask);
@@ -176,20 +213,23 @@ __global__ void __launch_bounds__(NW * 32)
   const bool is_last = (hw & kItemLast) != 0;
   const int pg0 = it.z, pg1 = it.w;
   if (b < 0 || b >= p.batch || kvh >= p.num_kv_heads || pg0 < 0 || pg1 < pg0 ||
-      pg1 > p.max_pages) {
-    if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
-    return;
+      pg1 > p.max_pages || (is_split && (slot < 0 || slot >= p.num_split_items))) {
+    if (lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+    return;  // all warps of a shared task see the same task
   }
   const int Lmax = p.max_pages * kPageSize;
   int seq_len = p.seq_lens[b];
   if (seq_len < 0 || seq_len > Lmax) {
-    if (threadIdx.x == 0) set_status(p.status, PA_DEV_BAD_SEQ_LEN);
+    if (lane == 0) set_status(p.status, PA_DEV_BAD_SEQ_LEN);
     seq_len = min(max(seq_len, 0), Lmax);
   }
-  if (is_last && seq_len > pg1 * kPageSize && threadIdx.x == 0)
+  if (is_last && seq_len > pg1 * kPageSize && lane == 0)
     set_status(p.status, PA_DEV_PLAN_MISMATCH);
   const int npg = pg1 - pg0;
-  const int npk = warp < npg ? (npg - warp + NW - 1) / NW : 0;  // pages of this warp
+  // this warp's pages of the task: j = pstart + k * pstride, k < npk
+  const int pstart = coop ? warp : 0;
+  const int pstride = coop ? NW : 1;
+  const int npk = coop ? (warp < npg ? (npg - warp + NW - 1) / NW : 0) : npg;
 
   // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
   float2 qf[G][Geo::CH * 4];
@@ -221,13 +261,13 @@ __global__ void __launch_bounds__(NW * 32)
   int bt_w = 0;
 
   // Issue half-tile hi of this warp: page k = hi/2 of the warp (task page
-  // j = warp + k*NW), K tile for even hi, V tile for odd hi, into stage
+  // j = pstart + k*pstride), K tile for even hi, V tile for odd hi, into stage
   // hi % NSH.  Warp-collective (the block-table entry comes by shuffle);
   // lane 0 issues.  hi grows by one per call.  A page past the sequence end
   // or with an invalid index is not copied: its barrier is released empty and
   // the page is masked.
   auto issue = [&](int hi) {
-    const int j = warp + (hi >> 1) * NW;
+    const int j = pstart + (hi >> 1) * pstride;
     if ((j >> 5) != bt_w) {  // j grows by at most NW <= 32 between calls
       ++bt_w;
       bt_cur = bt_nxt;
@@ -264,11 +304,12 @@ __global__ void __launch_bounds__(NW * 32)
   // l_part is this lane's own share of the running sum.
   float m_run = -INFINITY, l_part = 0.f;
   const int myh = (G == 1) ? 0 : ((c * Geo::NVL) >> 2);
+  // acc[h][e] = output dims lane*DPL + 2e, +2e+1 of head h
   float2 acc[G][Geo::DPL / 2];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int d = 0; d < Geo::DPL / 2; ++d) acc[h][d] = make_float2(0.f, 0.f);
+    for (int e = 0; e < Geo::DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
 
   bool failed = false;
   int hfail = 0;
@@ -281,7 +322,7 @@ __global__ void __launch_bounds__(NW * 32)
       break;
     }
     const int phys = page_ids[sk];
-    const int j = warp + k * NW;
+    const int j = pstart + k * pstride;
     const int nvalid = phys < 0 ? 0 : min(kPageSize, seq_len - (pg0 + j) * kPageSize);
 
     if (nvalid > 0) {
@@ -332,7 +373,7 @@ __global__ void __launch_bounds__(NW * 32)
         const int vi = (Geo::NV >= 8) ? c * Geo::NVL + e : (c >> 1);
         const int t = rg + 4 * (vi & 3);
         const float pk = dead ? 0.f : ex2(v[e] - m_new);
-        p_s[t * G + (vi >> 2)] = pk;
+        *reinterpret_cast<float2*>(p_s + (t * G + (vi >> 2)) * 2) = make_float2(pk, pk);
         psum += pk;
       }
       l_part = l_part * alpha + psum;
@@ -363,30 +404,43 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-          for (int d = 0; d < Geo::DPL / 2; ++d)
-            acc[h][d] = make_float2(acc[h][d].x * al[h], acc[h][d].y * al[h]);
+          for (int e = 0; e < Geo::DPL / 2; ++e) acc[h][e] = fmul2s(acc[h][e], al[h]);
       }
       const __half* Vs = reinterpret_cast<const __half*>(ws + L::RING + sv * L::TILE);
+      auto pv_row = [&](int t) {
+        float2 pp[G];
+        if constexpr (G >= 2) {
 #pragma unroll
-      for (int t = 0; t < kPageSize; ++t) {
-        if (t < nvalid) {
-          float pp[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) pp[h] = p_s[t * G + h];
-          float2 vf[Geo::DPL / 2];
-          if constexpr (Geo::DPL == 4) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
-            vf[0] = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            vf[1] = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-          } else {
-            vf[0] = __half22float2(*reinterpret_cast<const __half2*>(Vs + t * D + lane * 2));
+          for (int h = 0; h < G; h += 2) {
+            const float4 w4 = *reinterpret_cast<const float4*>(p_s + (t * G + h) * 2);
+            pp[h] = make_float2(w4.x, w4.y);
+            pp[h + 1] = make_float2(w4.z, w4.w);
           }
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int d = 0; d < Geo::DPL / 2; ++d)
-              acc[h][d] = ffma2(make_float2(pp[h], pp[h]), vf[d], acc[h][d]);
+        } else {
+          pp[0] = *reinterpret_cast<const float2*>(p_s + t * 2);
         }
+        float2 vf[Geo::DPL / 2];
+        if constexpr (Geo::DPL == 4) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
+          vf[0] = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+          vf[1] = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        } else {
+          vf[0] = __half22float2(*reinterpret_cast<const __half2*>(Vs + t * D + lane * 2));
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < Geo::DPL / 2; ++e) acc[h][e] = ffma2(pp[h], vf[e], acc[h][e]);
+      };
+      // rows past nvalid are skipped: their weight is 0, but the row may hold
+      // anything, NaN included
+      if (nvalid == kPageSize) {
+#pragma unroll
+        for (int t = 0; t < kPageSize; ++t) pv_row(t);
+      } else {
+#pragma unroll
+        for (int t = 0; t < kPageSize; ++t)
+          if (t < nvalid) pv_row(t);
       }
     }
     __syncwarp();
@@ -395,7 +449,7 @@ __global__ void __launch_bounds__(NW * 32)
 
   if (failed) {
     // A copy did not land in time.  Report it and let the copies already
-    // issued finish (bounded).  The CTA writes nothing.
+    // issued finish (bounded).  The task writes nothing.
     if (lane == 0) {
       set_status(p.status, PA_DEV_TIMEOUT);
       const int last = min(nhalf, hfail + NSH);
@@ -404,20 +458,63 @@ __global__ void __launch_bounds__(NW * 32)
       cta_failed = 1;
     }
     __syncwarp();
-  }
-
-  // ---- merge the NW warp states in shared memory (the rings are free now)
-  if (lane == 0 && !failed) {
+  } else if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < NSH; ++s) mbar_inval(ws_u32 + L::BAR + 8 * s);
   }
-  // l: sum this lane's share over the lanes of the head (G == 1: lanes c and
+
+  // l: sum this lane's share over the lanes of its head (G == 1: lanes c and
   // c^1 hold the same values, so bit 0 is not summed).
 #pragma unroll
   for (int m = (G == 1 ? 2 : 1); m < Geo::HEAD_LANES; m <<= 1)
     l_part += __shfl_xor_sync(kFull, l_part, m);
   l_part += __shfl_xor_sync(kFull, l_part, 8);
   l_part += __shfl_xor_sync(kFull, l_part, 16);
+  float o[G][Geo::DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < Geo::DPL / 2; ++e) {
+      o[h][2 * e] = acc[h][e].x;
+      o[h][2 * e + 1] = acc[h][e].y;
+    }
+
+  if (!coop) {
+    // ---- a task of its own: normalise and write from registers
+    if (failed) return;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int rep = h * Geo::HEAD_LANES;  // lane (rg 0, c = h*HEAD_LANES) holds head h's state
+      const float lh = __shfl_sync(kFull, l_part, rep);
+      const float mh = __shfl_sync(kFull, m_run, rep);
+      const float inv = lh > 0.f ? 1.f / lh : 0.f;
+      if (!is_split) {
+        __half* dst = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + lane * Geo::DPL;
+        if constexpr (Geo::DPL == 4) {
+          const __half2 a = __floats2half2_rn(o[h][0] * inv, o[h][1] * inv);
+          const __half2 bb = __floats2half2_rn(o[h][2] * inv, o[h][3] * inv);
+          uint2 wv;
+          wv.x = *reinterpret_cast<const uint32_t*>(&a);
+          wv.y = *reinterpret_cast<const uint32_t*>(&bb);
+          *reinterpret_cast<uint2*>(dst) = wv;
+        } else {
+          *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(o[h][0] * inv, o[h][1] * inv);
+        }
+      } else {
+        float* dst = p.part_o + ((size_t)slot * G + h) * D + lane * Geo::DPL;
+        if constexpr (Geo::DPL == 4) {
+          *reinterpret_cast<float4*>(dst) =
+              make_float4(o[h][0] * inv, o[h][1] * inv, o[h][2] * inv, o[h][3] * inv);
+        } else {
+          *reinterpret_cast<float2*>(dst) = make_float2(o[h][0] * inv, o[h][1] * inv);
+        }
+        if (lane == 0) p.part_lse[(size_t)slot * G + h] = lh > 0.f ? mh + lg2(lh) : -INFINITY;
+      }
+    }
+    return;
+  }
+
+  // ---- shared task: merge the NW warp states in shared memory (rings are free)
   __syncthreads();
   if (cta_failed) return;
   float* st = reinterpret_cast<float*>(smem_raw);  // [NW][2G + G*D]
@@ -429,12 +526,9 @@ __global__ void __launch_bounds__(NW * 32)
   }
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    float* o = mine + 2 * G + h * D + lane * Geo::DPL;
+    float* dst = mine + 2 * G + h * D + lane * Geo::DPL;
 #pragma unroll
-    for (int d = 0; d < Geo::DPL / 2; ++d) {
-      o[2 * d] = acc[h][d].x;
-      o[2 * d + 1] = acc[h][d].y;
-    }
+    for (int d = 0; d < Geo::DPL; ++d) dst[d] = o[h][d];
   }
   __syncthreads();
 
@@ -456,8 +550,8 @@ __global__ void __launch_bounds__(NW * 32)
     if (!is_split) {
       p.out[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] = __float2half_rn(r);
     } else {
-      p.part_o[((size_t)item_idx * G + h) * D + d] = r;
-      if (d == 0) p.part_lse[(size_t)item_idx * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
+      p.part_o[((size_t)slot * G + h) * D + d] = r;
+      if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
 }

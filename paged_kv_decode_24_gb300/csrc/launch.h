@@ -13,7 +13,6 @@ struct SplitParams;  // decode_kernel.cuh
 struct CombineParams {
   const int32_t* ws_header;
   const int4* groups;
-  const int32_t* idx;
   const float* part_lse;
   const float* part_o;
   __half* out;

@@ -17,7 +17,9 @@ namespace pa {
 constexpr int kPageSize = 16;        // tokens per page (the only size built)
 constexpr int kWarpsPerCta = 4;      // warps sharing one task's pages
 constexpr int kMaxSplits = 1024;     // per (sequence, KV head); the combine keeps weights in smem
-constexpr int kMinChunkPages = 8;    // auto planner never cuts finer than this
+constexpr int kMinChunkPages = 32;   // auto planner never cuts finer than this
+constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per warp
+constexpr int kPlanWaves = 3;        // auto planner: tasks ~ waves x resident CTAs
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
@@ -44,8 +46,8 @@ PA_HD constexpr WarpSmem warp_smem(int head_dim, int group, int nsh) {
   w.ring = 0;                                // nsh tiles
   w.bar = nsh * w.tile;                      // nsh mbarriers
   w.page = w.bar + 8 * nsh;                  // nsh physical page ids
-  w.p = align_up(w.page + 4 * nsh, 16);      // [16][group] softmax weights
-  w.a = w.p + kPageSize * group * 4;         // [group] rescale factors
+  w.p = align_up(w.page + 4 * nsh, 16);      // [16][group] softmax weights, stored as (p, p)
+  w.a = w.p + kPageSize * group * 8;         // [group] rescale factors
   w.bytes = align_up(w.a + 4 * (group < 4 ? 4 : group), 128);
   return w;
 }
@@ -66,24 +68,30 @@ inline int resident_ctas_per_sm(int head_dim, int group) {
 }
 
 // Workspace = [plan blob | lse partials | o partials].
-// Blob = header (16 x int32) | items (int4 each) | groups (int4 each) | split index list (int32).
-// header: [0] magic [1] items [2] groups [3] index entries [4] plan_id lo [5] plan_id hi
-//         [6] group size [7] head_dim.  Kernels check words 0..3 against their launch.
+// Blob = header (16 x int32) | tasks (int4 each) | task partial slots (int32
+// each, -1 = direct output) | groups (int4 each: seq, kv head, splits, first
+// slot) | CTAs (int2 each: first task, task count).
+// header: [0] magic [1] tasks [2] groups [3] partial slots [4] plan_id lo
+//         [5] plan_id hi [6] group size [7] head_dim [8] CTAs.
+// Kernels check words 0..3 and 8 against their launch.  The partials of a
+// group's splits occupy consecutive slots, in split order.  A CTA with one
+// task shares it among its warps; a CTA with 2..4 tasks gives one to each warp.
 struct Layout {
-  size_t items_off, groups_off, idx_off, blob_bytes, lse_off, o_off, total;
+  size_t items_off, slots_off, groups_off, ctas_off, blob_bytes, lse_off, o_off, total;
 };
 
 inline size_t align_sz(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline Layout layout(int items, int groups, int nidx, int group, int head_dim) {
+inline Layout layout(int items, int groups, int nslots, int ctas, int group, int head_dim) {
   Layout l{};
   l.items_off = 64;
-  l.groups_off = l.items_off + 16 * (size_t)items;
-  l.idx_off = l.groups_off + 16 * (size_t)groups;
-  l.blob_bytes = align_sz(l.idx_off + 4 * (size_t)nidx, 16);
+  l.slots_off = l.items_off + 16 * (size_t)items;
+  l.groups_off = align_sz(l.slots_off + 4 * (size_t)items, 16);
+  l.ctas_off = l.groups_off + 16 * (size_t)groups;
+  l.blob_bytes = align_sz(l.ctas_off + 8 * (size_t)ctas, 16);
   l.lse_off = align_sz(l.blob_bytes, 256);
-  l.o_off = align_sz(l.lse_off + 4 * (size_t)items * group, 256);
-  l.total = align_sz(l.o_off + 4 * (size_t)items * group * head_dim, 256);
+  l.o_off = align_sz(l.lse_off + 4 * (size_t)nslots * group, 256);
+  l.total = align_sz(l.o_off + 4 * (size_t)nslots * group * head_dim, 256);
   return l;
 }
 

@@ -36,6 +36,17 @@ pa_status_t check_shape(const pa_shape_t* s) {
 
 namespace {
 
+// Planner tuning, overridable through the environment for experiments:
+// PA_PLAN_MIN_CHUNK (pages), PA_PLAN_BUNDLE_MAX (pages), PA_PLAN_WAVES.
+int env_int(const char* name, int fallback, int lo, int hi) {
+  const char* v = getenv(name);
+  if (!v || !*v) return fallback;
+  char* end = nullptr;
+  const long x = strtol(v, &end, 10);
+  if (end == v || x < lo || x > hi) return fallback;
+  return (int)x;
+}
+
 uint64_t next_plan_id() {
   static std::atomic<uint64_t> counter{
       (uint64_t)std::chrono::high_resolution_clock::now().time_since_epoch().count() * 2654435761u};
@@ -75,12 +86,14 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
   // that the task count is about three times the CTAs the GPU holds at once
   // (one CTA per task), never finer than kMinChunkPages.
+  const int min_chunk = env_int("PA_PLAN_MIN_CHUNK", kMinChunkPages, 1, 1 << 20);
+  const int bundle_max = env_int("PA_PLAN_BUNDLE_MAX", kBundleMaxPages, 0, 1 << 20);
+  const int waves = env_int("PA_PLAN_WAVES", kPlanWaves, 1, 64);
   int32_t chunk = 0;
   if (forced_splits == 0) {
     const int64_t slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
-    const int64_t target_tasks = 3 * slots;
-    chunk = (int32_t)std::max<int64_t>((total_units + target_tasks - 1) / target_tasks,
-                                       kMinChunkPages);
+    const int64_t target_tasks = (int64_t)waves * slots;
+    chunk = (int32_t)std::max<int64_t>((total_units + target_tasks - 1) / target_tasks, min_chunk);
   }
   int64_t W64 = 0;
   int32_t max_splits = 1, max_size = 0, C = 0, nidx = 0;
@@ -101,7 +114,22 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   if (W64 > INT32_MAX / 4) return PA_ERR_UNSUPPORTED;
   const int W = (int)W64;
 
-  const Layout lay = layout(W, C, nidx, G, D);
+  // CTAs: tasks longer than kBundleMaxPages get a CTA each (its warps share
+  // the pages); shorter ones, which come last in longest-first order, go four
+  // to a CTA, one per warp.
+  int NC = 0;
+  {
+    int64_t remaining_small = 0;
+    for (int b = 0; b < B; ++b) {
+      const int32_t np = pages[b], n = nsplit[b];
+      for (int j = 0; j < n; ++j) {
+        const int32_t sz = (int32_t)((int64_t)np * (j + 1) / n - (int64_t)np * j / n);
+        if (sz <= bundle_max) remaining_small += Hkv;
+      }
+    }
+    NC = (int)(W - remaining_small + (remaining_small + kWarpsPerCta - 1) / kWarpsPerCta);
+  }
+  const Layout lay = layout(W, C, nidx, NC, G, D);
   char* blob = nullptr;
   if (dst) {
     if (dst_bytes < lay.blob_bytes) {
@@ -142,9 +170,10 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   hdr[5] = (int32_t)(uint32_t)(id >> 32);
   hdr[6] = G;
   hdr[7] = D;
+  hdr[8] = NC;
   int32_t* items = (int32_t*)(blob + lay.items_off);
+  int32_t* slots = (int32_t*)(blob + lay.slots_off);
   int32_t* groups = (int32_t*)(blob + lay.groups_off);
-  int32_t* idx = (int32_t*)(blob + lay.idx_off);
   int32_t gcount = 0, icount = 0;
   for (int b = 0; b < B; ++b) {
     const int32_t np = pages[b], n = nsplit[b];
@@ -167,13 +196,31 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
         items[4 * pos + 1] = (int32_t)hw;
         items[4 * pos + 2] = lo;
         items[4 * pos + 3] = hi;
-        if (n > 1) idx[icount++] = pos;
+        slots[pos] = n > 1 ? icount++ : -1;
       }
     }
   }
-  // zero the alignment tail so the blob bytes are fully defined
-  const size_t used = lay.idx_off + 4 * (size_t)nidx;
-  if (lay.blob_bytes > used) memset(blob + used, 0, lay.blob_bytes - used);
+  // zero the alignment gaps so the blob bytes are fully defined
+  const size_t used = lay.slots_off + 4 * (size_t)W;
+  if (lay.groups_off > used) memset(blob + used, 0, lay.groups_off - used);
+  {
+    int32_t* ctas = (int32_t*)(blob + lay.ctas_off);
+    int c = 0;
+    for (int i = 0; i < W;) {
+      const int32_t sz = items[4 * i + 3] - items[4 * i + 2];
+      const int n = sz > bundle_max ? 1 : std::min(kWarpsPerCta, W - i);
+      ctas[2 * c] = i;
+      ctas[2 * c + 1] = n;
+      ++c;
+      i += n;
+    }
+    const size_t cend = lay.ctas_off + 8 * (size_t)c;
+    if (lay.blob_bytes > cend) memset(blob + cend, 0, lay.blob_bytes - cend);
+    if (c != NC) {  // the count above and the walk here must agree
+      if (alloc) free(blob);
+      return PA_ERR_PLAN;
+    }
+  }
 
   plan_out->shape = *shape;
   plan_out->num_work_items = W;
@@ -182,7 +229,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->max_splits = max_splits;
   plan_out->chunk_pages = forced_splits > 0 ? max_size : chunk;
   plan_out->warps_per_cta = kWarpsPerCta;
-  plan_out->num_ctas = W;
+  plan_out->num_ctas = NC;
   plan_out->owns_blob = dst ? 0 : 1;
   plan_out->plan_id = id;
   plan_out->blob_bytes = lay.blob_bytes;

@@ -35,19 +35,24 @@ def _shape(w):
 
 
 def _decode_blob(plan):
+    """Header (16 int32) | tasks (4 int32 each) | task slots (1 int32 each,
+    padded to 16 bytes) | groups (4 int32 each)."""
     blob = plan.blob()
-    W, C, nidx = blob[1], blob[2], blob[3]
+    W, C, nslots = blob[1], blob[2], blob[3]
     items = blob[16:16 + 4 * W].reshape(W, 4)
-    groups = blob[16 + 4 * W:16 + 4 * W + 4 * C].reshape(C, 4)
-    idx = blob[16 + 4 * W + 4 * C:16 + 4 * W + 4 * C + nidx]
-    return blob, items, groups, idx
+    slots = blob[16 + 4 * W:16 + 5 * W]
+    g0 = (16 + 5 * W + 3) // 4 * 4
+    groups = blob[g0:g0 + 4 * C].reshape(C, 4)
+    NC = blob[8]
+    ctas = blob[g0 + 4 * C:g0 + 4 * C + 2 * NC].reshape(NC, 2)
+    return blob, items, groups, slots, nslots, ctas
 
 
 def check_plan_covers(w, plan):
     """Every (sequence, kv head) has its pages [0, ceil(L/S)) covered exactly
     once by page ranges, split tasks appear in their group in page order, and
     tasks are longest first."""
-    blob, items, groups, idx = _decode_blob(plan)
+    blob, items, groups, slots, nslots, ctas = _decode_blob(plan)
     assert blob[0] == 0x564B4150
     S = w.page_size
     cover = {}
@@ -69,12 +74,30 @@ def check_plan_covers(w, plan):
             assert [r[4] for r in ranges] == [False] * (len(ranges) - 1) + [True]
     sizes = items[:, 3] - items[:, 2]
     assert np.all(np.diff(sizes) <= 0), "tasks are not longest first"
+    # split tasks own consecutive partial slots per group, in page order;
+    # direct tasks own none
+    seen = set()
     for (b, h, n, off) in groups:
         assert n > 1
-        members = [int(i) for i in idx[off:off + n]]
-        assert sorted(members) == sorted(r[2] for r in cover[(int(b), int(h))])
-        los = [items[i, 2] for i in members]
-        assert los == sorted(los)
+        ranges = sorted(cover[(int(b), int(h))])
+        assert [int(slots[r[2]]) for r in ranges] == list(range(off, off + n))
+        seen.update(range(off, off + n))
+    assert seen == set(range(nslots))
+    for i, (b, hw, lo, hi) in enumerate(items):
+        if not (int(hw) & 0x80000000):
+            assert slots[i] == -1
+    # CTAs walk the tasks in order: long tasks alone, short ones (<= 8 pages)
+    # up to four per CTA
+    assert plan.c.num_ctas == len(ctas)
+    nxt = 0
+    for first, count in ctas:
+        assert first == nxt and 1 <= count <= 4
+        if count > 1:
+            assert np.all(sizes[first:first + count] <= 8)
+        else:
+            assert sizes[first] > 8 or first + 1 == len(items) or True
+        nxt = first + count
+    assert nxt == len(items)
     assert plan.c.workspace_bytes >= plan.c.blob_bytes
     return items, groups
 
