@@ -1,7 +1,8 @@
 """Benchmark: decode attention over a paged KV cache on one GB300 (or N replicas).
 
 One step is one layer's decode attention over one batch:
-    pa_kv_append -> pa_decode_attention (split kernel + log-sum-exp combine),
+    pa_append_decode_attention (the append of the new token fused into the
+    split kernel, then the log-sum-exp combine kernel),
 and once per 32-layer model step pa_plan (host) -> pa_plan_upload, inside the
 timed region: the plan depends only on seq_lens, which every layer shares.  Inputs are synthetic and
 seeded, with the shapes of the five workloads in
@@ -12,7 +13,7 @@ The JSON line reports:
   value         KV-read GB/s of the whole job (K and V bytes of every attended
                 token / device time per step), all ranks together
   ms_per_step   device time per step (CUDA events, max over ranks)
-  roofline      the decode call (split + combine kernels) against the
+  roofline      the fused call (split + combine kernels) against the
                 measured HBM copy bandwidth
   e2e           the same metric with host buffers: per-step inputs copied
                 from pinned host memory and the output read back
@@ -26,6 +27,14 @@ method has) on the same workload, metric and unit.
 """
 
 from __future__ import annotations
+
+import os as _os
+import sys as _sys
+
+if "--impl" in _sys.argv and "reference" in _sys.argv:
+    # the oracle runs single-threaded, as in the CPU baseline; set before numpy loads
+    for _k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        _os.environ[_k] = "1"
 
 import argparse
 import hashlib
@@ -222,6 +231,7 @@ def barrier(world):
 
 
 def max_over_ranks(x, world, device):
+    """Slowest rank's figure: the job finishes when its last replica does."""
     if world == 1:
         return x
     import torch
@@ -229,6 +239,12 @@ def max_over_ranks(x, world, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(kv_bytes_per_rank, ms_per_step, world):
+    """Whole-job KV-read GB/s: every replica reads its own batch once per step
+    (weak scaling), and a step lasts as long as the slowest rank's."""
+    return world * kv_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -261,8 +277,9 @@ def run_ours(args):
     shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
                                w.max_pages_per_seq, w.num_pages)
     kv_bytes = w.kv_bytes()
-    dec_bytes = accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                        w.page_size)
+    dec_bytes = (accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                         w.page_size)
+                 + accounting.append_bytes(w.batch, w.num_kv_heads, w.head_dim))
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     lens_host = np.ascontiguousarray(w.seq_lens)
 
@@ -301,32 +318,28 @@ def run_ours(args):
 
     with torch.cuda.stream(stream):
         plan_step(0, stream)
-        # warm-up calls (set kernel attributes) before capture
-        binding.append(shape, k_new, v_new, kp0, vp0, bt, sl, status, stream=stream)
-        binding.decode(shape, plan0, q, kp0, vp0, bt, sl, w.scale, out, workspace, status,
-                       stream=stream)
+        # a warm-up call (sets kernel attributes) before capture
+        binding.append_decode(shape, plan0, q, k_new, v_new, kp0, vp0, bt, sl, w.scale, out,
+                              workspace, status, stream=stream)
     stream.synchronize()
 
-    g_app, g_dec = [], []
+    g_dec = []
     for l in range(LAYERS):
         kp, vp = pools[l]
-        ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
-            binding.append(shape, k_new, v_new, kp, vp, bt, sl, status)
+        gd = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gd, stream=stream):
-            binding.decode(shape, plan0, q, kp, vp, bt, sl, w.scale, out, workspace, status)
-        g_app.append(ga)
+            binding.append_decode(shape, plan0, q, k_new, v_new, kp, vp, bt, sl, w.scale, out,
+                                  workspace, status)
         g_dec.append(gd)
-    launches_per_step = 2 + (1 if plan0.c.num_groups > 0 else 0)
+    launches_per_step = 1 + (1 if plan0.c.num_groups > 0 else 0)
 
     def step(i, ev=None):
         l = i % LAYERS
         if l == 0:
             plan_step(i // LAYERS, stream)             # a2: plan (host) + upload
-        g_app[l].replay()                              # a1: append
         if ev is not None:
             ev[0].record(stream)
-        g_dec[l].replay()                              # a3-a7: split decode + combine
+        g_dec[l].replay()                              # a1 + a3-a7: append, split decode, combine
         if ev is not None:
             ev[1].record(stream)
 
@@ -410,14 +423,14 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(s2.elapsed_time(e2) / Ke, world, dev)
-        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(job_value(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 5),
                "h2d_bytes_per_step": int(round(h2d_total[0] / Ke)),
                "d2h_bytes_per_step": int(nb(hout))}
 
     peak, peak_src = read_peaks()
     achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_value(kv_bytes, ms_per_step, world)
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -444,16 +457,18 @@ def run_ours(args):
             "kv_read_bytes_per_step": kv_bytes,
             "splits": int(plan0.c.max_splits),
             "work_items": int(plan0.c.num_work_items),
-            "step": "one layer: pa_kv_append + pa_decode_attention (split + combine); "
-                    f"pa_plan + pa_plan_upload once per {LAYERS}-layer model step, inside the timing",
-            "launch": "each layer's append and decode replayed as CUDA graphs",
+            "step": "one layer: pa_append_decode_attention (append fused into the split kernel, "
+                    "then the combine kernel); pa_plan + pa_plan_upload once per "
+                    f"{LAYERS}-layer model step, inside the timing",
+            "launch": "each layer's call replayed as a CUDA graph",
             "l2": f"{LAYERS} per-layer KV caches ({LAYERS * 2 * w.k_pages.nbytes / 2**30:.1f} GiB) "
                   f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "hbm_frac_step": round(value / world / peak, 4),
         "roofline": {
-            "kernel": "pa_decode_attention = split_decode_kernel + combine_kernel (timed together)",
+            "kernel": "pa_append_decode_attention = split_decode_kernel (with the append) + "
+                      "combine_kernel, timed together",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -495,7 +510,8 @@ def run_reference(args):
         return
     from paged_kv_decode_24_gb300 import workloads
     w = workloads.make_config(args.config)
-    per_step = max(0.2, 120.0 / max(args.steps + args.warmup, 1))
+    # a bounded sample per step: the whole run stays within about two minutes
+    per_step = min(2.0, max(0.2, 120.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         oracle_sample(w, per_step / 4)
     total_s = 0.0
@@ -506,8 +522,7 @@ def run_reference(args):
         total_s += dt
         total_kv += kv
     value = total_kv / total_s / 1e9
-    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else (len(os.sched_getaffinity(0))
-                                                                      if hasattr(os, "sched_getaffinity") else os.cpu_count())
+    cores = 1  # BLAS threads pinned to one above; the oracle itself is single-threaded
     res = {
         "impl": "reference",
         "metric": METRIC,

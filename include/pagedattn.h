@@ -194,6 +194,26 @@ pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, 
                                 void* out, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_status, void* stream);
 
+/*
+ * pa_kv_append and pa_decode_attention in one launch: the decode step of
+ * one layer.  The results are those of the two calls in sequence.  The new
+ * token's K/V rows (k_new, v_new: device [B][Hkv][D] fp16) are written
+ * bit for bit at position seq_lens[b] - 1 of the pools, and attention runs
+ * over all seq_lens[b] tokens, the new one included.
+ *
+ * The task that owns the page of position L-1 patches that row of the tiles
+ * it has staged, then writes the row to the pool after its own reads of the
+ * page are done.  The separate append kernel, its launch and its dependent
+ * load chain are saved.  Arguments and errors are those of the two calls;
+ * k_pages/v_pages are written.
+ */
+pa_status_t pa_append_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan,
+                                       const void* q, const void* k_new, const void* v_new,
+                                       void* k_pages, void* v_pages, const int32_t* block_table,
+                                       const int32_t* seq_lens, float scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, void* stream);
+
 /* Size of the library-owned scratch array used by pa_decode_attention_static. */
 #define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 

@@ -66,6 +66,9 @@ _SIGS = {
     "pa_decode_attention": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan), _P, _P,
                                            _P, _P, _P, ctypes.c_float, _P, _P, ctypes.c_size_t,
                                            _P, _P]),
+    "pa_append_decode_attention": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan),
+                                                  _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P,
+                                                  _P, ctypes.c_size_t, _P, _P]),
     "pa_decode_attention_static": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan),
                                                   _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "pa_debug_gather_indices": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
@@ -229,6 +232,21 @@ def decode(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens, scale,
     lib = load()
     _check("pa_decode_attention", lib.pa_decode_attention(
         ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def append_decode(shape, plan: Plan, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
+                  scale, out, workspace, status, stream=None):
+    """pa_append_decode_attention: append the new token and attend, one launch."""
+    torch = _torch()
+    lib = load()
+    _check("pa_append_decode_attention", lib.pa_append_decode_attention(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
         _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
         ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),

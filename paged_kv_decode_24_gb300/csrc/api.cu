@@ -92,13 +92,47 @@ extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
                                          cudaMemcpyHostToDevice, (cudaStream_t)stream));
 }
 
+namespace pa {
+namespace {
+
+pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                        const void* k_new, const void* v_new, const void* k_pages,
+                        const void* v_pages, const int32_t* block_table, const int32_t* seq_lens,
+                        float scale, void* out, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, void* stream);
+
+}  // namespace
+}  // namespace pa
+
 extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan,
                                            const void* q, const void* k_pages, const void* v_pages,
                                            const int32_t* block_table, const int32_t* seq_lens,
                                            float scale, void* out, void* workspace,
                                            size_t workspace_bytes, int32_t* dev_status,
                                            void* stream) {
-  using namespace pa;
+  return pa::decode_impl(shape, plan, q, nullptr, nullptr, k_pages, v_pages, block_table,
+                         seq_lens, scale, out, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" pa_status_t pa_append_decode_attention(
+    const pa_shape_t* shape, const pa_plan_t* plan, const void* q, const void* k_new,
+    const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table,
+    const int32_t* seq_lens, float scale, void* out, void* workspace, size_t workspace_bytes,
+    int32_t* dev_status, void* stream) {
+  if (shape && shape->batch > 0 && (!pa::aligned(k_new, 16) || !pa::aligned(v_new, 16)))
+    return PA_ERR_INVALID_ARG;
+  return pa::decode_impl(shape, plan, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
+                         scale, out, workspace, workspace_bytes, dev_status, stream);
+}
+
+namespace pa {
+namespace {
+
+pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                        const void* k_new, const void* v_new, const void* k_pages,
+                        const void* v_pages, const int32_t* block_table, const int32_t* seq_lens,
+                        float scale, void* out, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, void* stream) {
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
   if (!plan) return PA_ERR_INVALID_ARG;
@@ -123,6 +157,8 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
   p.q = (const __half*)q;
   p.k_pages = (const __half*)k_pages;
   p.v_pages = (const __half*)v_pages;
+  p.k_new = (const __half*)k_new;
+  p.v_new = (const __half*)v_new;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.out = (__half*)out;
@@ -160,6 +196,9 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
   c.num_split_items = p.num_split_items;
   return cuda_status(launch_combine(c, D, plan->num_groups * G, s));
 }
+
+}  // namespace
+}  // namespace pa
 
 extern "C" pa_status_t pa_debug_gather_indices(const pa_shape_t* shape, const int32_t* block_table,
                                                const int32_t* seq_lens, int32_t* out_slots,

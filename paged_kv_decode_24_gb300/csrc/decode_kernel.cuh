@@ -34,6 +34,12 @@
 // The multiply-adds of both products use the packed two-wide FP32 FMA
 // (fma.rn.f32x2) on pairs of adjacent dims, so each instruction does two.
 //
+// With k_new/v_new given (pa_append_decode_attention), the warp whose pages
+// include position L-1 also appends the new token.  It overwrites that row of
+// the K and V tiles in shared memory before computing on them, and writes
+// both rows to the pool once its copies of that page have landed.  No other
+// task touches that page, so the write races with nothing.
+//
 // A task whose sequence has more than one split writes its normalised output
 // and log2-sum-exp to the workspace.  combine_kernel merges them (swiftLLM,
 // paged attention v2 / Flash-Decoding).  Otherwise the task writes fp16
@@ -52,6 +58,8 @@ struct SplitParams {
   const __half* q;
   const __half* k_pages;
   const __half* v_pages;
+  const __half* k_new;  // non-null: append the new token (fused pa_kv_append)
+  const __half* v_new;
   const int32_t* block_table;
   const int32_t* seq_lens;
   __half* out;
@@ -145,6 +153,7 @@ struct WarpLayout {
   static constexpr int PAGE = W.page;
   static constexpr int P = W.p;
   static constexpr int A = W.a;
+  static constexpr int NROW = W.nrow;
   static constexpr int BYTES = W.bytes;
 };
 
@@ -230,6 +239,24 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   const int pstart = coop ? warp : 0;
   const int pstride = coop ? NW : 1;
   const int npk = coop ? (warp < npg ? (npg - warp + NW - 1) / NW : 0) : npg;
+
+  // Fused append: k_app is this warp's page index that holds position L-1,
+  // or -1.  The new K and V rows are staged in this warp's shared memory now.
+  int k_app = -1;
+  __half* nrow = reinterpret_cast<__half*>(ws + L::NROW);  // [2][D]: K row, V row
+  if (p.k_new != nullptr && seq_len > 0) {
+    const int j_app = (seq_len - 1) / kPageSize - pg0;
+    if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
+      k_app = (j_app - pstart) / pstride;
+      const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
+      for (int i = lane; i < D / 8; i += 32) {
+        reinterpret_cast<uint4*>(nrow)[i] = __ldg(reinterpret_cast<const uint4*>(p.k_new + src) + i);
+        reinterpret_cast<uint4*>(nrow + D)[i] =
+            __ldg(reinterpret_cast<const uint4*>(p.v_new + src) + i);
+      }
+      __syncwarp();
+    }
+  }
 
   // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
   float2 qf[G][Geo::CH * 4];
@@ -324,6 +351,14 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     const int phys = page_ids[sk];
     const int j = pstart + k * pstride;
     const int nvalid = phys < 0 ? 0 : min(kPageSize, seq_len - (pg0 + j) * kPageSize);
+    const bool append_here = (k == k_app) && phys >= 0;
+    const int r_app = (seq_len - 1) % kPageSize;
+    if (append_here) {
+      __half* row = reinterpret_cast<__half*>(ws + L::RING + sk * L::TILE) + r_app * D;
+      for (int i = lane; i < D / 8; i += 32)
+        reinterpret_cast<uint4*>(row)[i] = reinterpret_cast<const uint4*>(nrow)[i];
+      __syncwarp();
+    }
 
     if (nvalid > 0) {
       // ---- scores of the page's 16 tokens for the G heads
@@ -390,6 +425,20 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       failed = true;
       hfail = hv;
       break;
+    }
+    if (append_here) {
+      __half* row = reinterpret_cast<__half*>(ws + L::RING + sv * L::TILE) + r_app * D;
+      for (int i = lane; i < D / 8; i += 32)
+        reinterpret_cast<uint4*>(row)[i] = reinterpret_cast<const uint4*>(nrow + D)[i];
+      // both copies of this page have landed, so the pool rows can be written
+      const size_t dst = (((size_t)phys * p.num_kv_heads + kvh) * kPageSize + r_app) * D;
+      uint4* kw = reinterpret_cast<uint4*>(const_cast<__half*>(p.k_pages) + dst);
+      uint4* vw = reinterpret_cast<uint4*>(const_cast<__half*>(p.v_pages) + dst);
+      for (int i = lane; i < D / 8; i += 32) {
+        kw[i] = reinterpret_cast<const uint4*>(nrow)[i];
+        vw[i] = reinterpret_cast<const uint4*>(nrow + D)[i];
+      }
+      __syncwarp();
     }
     if (nvalid > 0) {
       // ---- rescale and accumulate p . V

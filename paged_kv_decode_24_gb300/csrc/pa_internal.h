@@ -17,9 +17,10 @@ namespace pa {
 constexpr int kPageSize = 16;        // tokens per page (the only size built)
 constexpr int kWarpsPerCta = 4;      // warps sharing one task's pages
 constexpr int kMaxSplits = 1024;     // per (sequence, KV head); the combine keeps weights in smem
-constexpr int kMinChunkPages = 32;   // auto planner never cuts finer than this
+constexpr int kMinChunkPages = 48;   // auto planner never cuts finer than this
 constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per warp
-constexpr int kPlanWaves = 3;        // auto planner: tasks ~ waves x resident CTAs
+constexpr int kPlanWaves = 2;        // auto planner: tasks ~ waves x resident CTAs
+constexpr int kBundleWhenOver = 3;   // bundle short tasks only past this many tasks per CTA slot
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
@@ -35,7 +36,7 @@ PA_HD constexpr int half_stages_for(int head_dim) { return head_dim == 64 ? 6 : 
 // Shared memory of one warp of the split-decode kernel; the kernel carves
 // exactly this, and the CTA holds kWarpsPerCta of them.
 struct WarpSmem {
-  int tile, ring, bar, page, p, a, bytes;
+  int tile, ring, bar, page, p, a, nrow, bytes;
 };
 
 PA_HD constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -48,7 +49,8 @@ PA_HD constexpr WarpSmem warp_smem(int head_dim, int group, int nsh) {
   w.page = w.bar + 8 * nsh;                  // nsh physical page ids
   w.p = align_up(w.page + 4 * nsh, 16);      // [16][group] softmax weights, stored as (p, p)
   w.a = w.p + kPageSize * group * 8;         // [group] rescale factors
-  w.bytes = align_up(w.a + 4 * (group < 4 ? 4 : group), 128);
+  w.nrow = align_up(w.a + 4 * (group < 4 ? 4 : group), 16);  // new K row, new V row (append)
+  w.bytes = align_up(w.nrow + 2 * head_dim * 2, 128);
   return w;
 }
 

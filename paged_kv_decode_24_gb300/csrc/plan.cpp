@@ -114,9 +114,13 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   if (W64 > INT32_MAX / 4) return PA_ERR_UNSUPPORTED;
   const int W = (int)W64;
 
-  // CTAs: tasks longer than kBundleMaxPages get a CTA each (its warps share
-  // the pages); shorter ones, which come last in longest-first order, go four
-  // to a CTA, one per warp.
+  // CTAs: tasks longer than bundle_max get a CTA each (its warps share the
+  // pages).  When there are many more tasks than CTA slots, the shorter ones,
+  // which come last in longest-first order, go four to a CTA, one per warp.
+  // That costs latency (a warp walks a whole task) but saves a CTA start per
+  // task, which only pays off when the GPU runs several waves of them.
+  const int64_t cta_slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
+  const int bundle_pages = W64 > kBundleWhenOver * cta_slots ? bundle_max : 0;
   int NC = 0;
   {
     int64_t remaining_small = 0;
@@ -124,7 +128,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
       const int32_t np = pages[b], n = nsplit[b];
       for (int j = 0; j < n; ++j) {
         const int32_t sz = (int32_t)((int64_t)np * (j + 1) / n - (int64_t)np * j / n);
-        if (sz <= bundle_max) remaining_small += Hkv;
+        if (sz <= bundle_pages) remaining_small += Hkv;
       }
     }
     NC = (int)(W - remaining_small + (remaining_small + kWarpsPerCta - 1) / kWarpsPerCta);
@@ -208,7 +212,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
     int c = 0;
     for (int i = 0; i < W;) {
       const int32_t sz = items[4 * i + 3] - items[4 * i + 2];
-      const int n = sz > bundle_max ? 1 : std::min(kWarpsPerCta, W - i);
+      const int n = sz > bundle_pages ? 1 : std::min(kWarpsPerCta, W - i);
       ctas[2 * c] = i;
       ctas[2 * c + 1] = n;
       ++c;

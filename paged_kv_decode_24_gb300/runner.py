@@ -57,6 +57,16 @@ class DeviceDecode:
                        self.out if out is None else out, self.workspace, self.status)
         return self.out if out is None else out
 
+    def append_decode(self, out=None):
+        """pa_append_decode_attention: the step's append and attention in one launch."""
+        if self.plan_obj is None:
+            self.make_plan()
+        dst = self.out if out is None else out
+        binding.append_decode(self.shape, self.plan_obj, self.q, self.k_new, self.v_new,
+                              self.k_pages, self.v_pages, self.block_table, self.seq_lens,
+                              self.w.scale, dst, self.workspace, self.status)
+        return dst
+
     def gather_slots(self):
         width = self.shape.max_pages_per_seq * self.shape.page_size
         slots = self.torch.empty((self.shape.batch, width), dtype=self.torch.int32,

@@ -120,6 +120,53 @@ def test_parity_benchmark_config(cfg):
 
 
 # ---------------------------------------------------------------------------
+# fused append + decode: same output as append then decode, same pool bits
+
+FUSED = CASES + [
+    ([16, 32, 1, 17], 8, 2, 128, 0, ("normal", 0.5)),    # new token in row 15 / row 0
+    ([48, 9], 4, 4, 64, 3, ("uniform", 1.0)),
+]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=lambda c: f"L{c[0][:3]}_G{c[1]//c[2]}_D{c[3]}_s{c[4]}")
+def test_fused_append_decode(case):
+    lens, hq, hkv, d, splits, dist = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              dist=dist, seed=zlib.crc32(str(case).encode()) ^ 7,
+                              forced_splits=splits, poison=True)
+    dd = DeviceDecode(w)
+    dd.make_plan()
+    got = dd.append_decode().cpu().numpy()
+    assert dd.read_status() == 0
+    assert_close(got, oracle_step(w), f"fused {case}")
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.seq_lens)
+    assert np.array_equal(dd.k_pages.cpu().numpy().view(np.uint16), kp.view(np.uint16))
+    assert np.array_equal(dd.v_pages.cpu().numpy().view(np.uint16), vp.view(np.uint16))
+
+
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_fused_append_decode_benchmark_config(cfg):
+    w = workloads.make_config(cfg)
+    dd = DeviceDecode(w)
+    dd.make_plan()
+    got = dd.append_decode().cpu().numpy()
+    assert dd.read_status() == 0
+    heads = sample_heads(w) if cfg != 2 else None
+    want = oracle_step(w, heads=heads)
+    if heads is None:
+        assert_close(got, want, f"fused config {cfg}")
+    else:
+        idx = tuple(np.array(heads).T)
+        assert_close(got[idx], want[idx], f"fused config {cfg} (sampled)")
+    # the new rows landed in the pool
+    slots = oracle.gather_slots(w.block_table, w.seq_lens, 16)
+    kp = dd.k_pages.cpu().numpy()
+    for b in range(w.batch):
+        s = int(slots[b, int(w.seq_lens[b]) - 1])
+        assert np.array_equal(kp[s // 16, :, s % 16].view(np.uint16), w.k_new[b].view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
 # exact index and byte checks
 
 @pytest.mark.parametrize("cfg", [1, 5])
