@@ -9,12 +9,17 @@ seeded, with the shapes of the five workloads in
 paged_kv_decode_24_gb300/workloads.py.  The default is workload 2 (LLaMA-2-7B
 heads, one 4096-token sequence, 16 splits).
 
+Each model step (32 layer steps) is one CUDA graph: the plan upload, then
+the 32 layers' calls back to back; K layer steps are timed exactly (a shorter
+graph covers K mod 32).
+
 The JSON line reports:
   value         KV-read GB/s of the whole job (K and V bytes of every attended
                 token / device time per step), all ranks together
-  ms_per_step   device time per step (CUDA events, max over ranks)
+  ms_per_step   device time per layer step (CUDA events, max over ranks)
   roofline      the fused call (split + combine kernels) against the
-                measured HBM copy bandwidth
+                measured HBM copy bandwidth: its mean duration over the timed
+                region; us_per_launch_isolated is one call alone (own graph)
   e2e           the same metric with host buffers: per-step inputs copied
                 from pinned host memory and the output read back
   cpu_baseline  the float64 oracle on this host's cores, on a bounded sample
@@ -172,7 +177,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "100"]
+               "-lms", "50"]
         if self.uuid:
             cmd.insert(1, f"--id={self.uuid}")
         try:
@@ -180,12 +185,11 @@ class ClockSampler:
                                          text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.2)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.2)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -299,53 +303,75 @@ def run_ours(args):
 
     # The plan is made once per model decode step (it depends only on seq_lens,
     # shared by all layers) into pinned host memory, double-buffered so the
-    # host never rewrites a buffer whose upload is still in flight.
+    # host never rewrites a buffer whose upload may still be pending.
     plan0 = binding.Plan(shape, lens_host, num_sms, w.forced_splits)
     staging = [torch.empty(int(plan0.c.blob_bytes), dtype=torch.uint8).pin_memory() for _ in range(2)]
     staged_evt = [torch.cuda.Event(), torch.cuda.Event()]
     workspace = binding.alloc_workspace(plan0, dev)
     struct0 = plan0.structure()
+    staged_plans = [binding.Plan(shape, lens_host, num_sms, w.forced_splits, host_buffer=staging[i])
+                    for i in range(2)]
 
-    def plan_step(m, strm):
-        slot = m % 2
+    def replan(slot):
+        """a2 on the host: a fresh plan into the pinned buffer the slot's graph uploads."""
         staged_evt[slot].synchronize()
         plan = binding.Plan(shape, lens_host, num_sms, w.forced_splits, host_buffer=staging[slot])
         if plan.structure() != struct0:
             raise RuntimeError("plan structure changed; captured graphs would be stale")
-        binding.upload(plan, workspace, stream=strm)
-        staged_evt[slot].record(strm)
-        return plan
+        staged_plans[slot] = plan
 
     with torch.cuda.stream(stream):
-        plan_step(0, stream)
+        binding.upload(staged_plans[0], workspace, stream=stream)
         # a warm-up call (sets kernel attributes) before capture
         binding.append_decode(shape, plan0, q, k_new, v_new, kp0, vp0, bt, sl, w.scale, out,
                               workspace, status, stream=stream)
     stream.synchronize()
 
-    g_dec = []
-    for l in range(LAYERS):
-        kp, vp = pools[l]
-        gd = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gd, stream=stream):
-            binding.append_decode(shape, plan0, q, k_new, v_new, kp, vp, bt, sl, w.scale, out,
-                                  workspace, status)
-        g_dec.append(gd)
+    # One graph per model step: the plan upload (a2), then the layers' fused
+    # calls (a1 + a3..a7) back to back, as a serving engine issues them.
+    def capture_model_step(slot, nlayers, host_io=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if host_io is not None:
+                host_io["per_step"](stream)
+            binding.upload(staged_plans[slot], workspace)
+            for l in range(nlayers):
+                kp, vp = pools[l]
+                if host_io is not None:
+                    host_io["per_layer_in"]()
+                binding.append_decode(shape, plan0, q, k_new, v_new, kp, vp, bt, sl, w.scale, out,
+                                      workspace, status)
+                if host_io is not None:
+                    host_io["per_layer_out"]()
+        return g
+
+    K = args.steps
+    full, rem = divmod(K, LAYERS)
+    graphs_full = [capture_model_step(i, LAYERS) for i in range(2)] if full else []
+    graphs_rem = [capture_model_step(i, rem) for i in range(2)] if rem else []
     launches_per_step = 1 + (1 if plan0.c.num_groups > 0 else 0)
 
-    def step(i, ev=None):
-        l = i % LAYERS
-        if l == 0:
-            plan_step(i // LAYERS, stream)             # a2: plan (host) + upload
-        if ev is not None:
-            ev[0].record(stream)
-        g_dec[l].replay()                              # a1 + a3-a7: append, split decode, combine
-        if ev is not None:
-            ev[1].record(stream)
+    def run_steps(nsteps, gfull, grem, m0=0):
+        """nsteps layer-steps as model-step graphs; returns the model steps issued."""
+        nf, nr = divmod(nsteps, LAYERS)
+        m = m0
+        for _ in range(nf):
+            slot = m % 2
+            replan(slot)
+            gfull[slot].replay()
+            staged_evt[slot].record(stream)
+            m += 1
+        if nr:
+            slot = m % 2
+            replan(slot)
+            grem[slot].replay()
+            staged_evt[slot].record(stream)
+            m += 1
+        return m
 
+    warm_full = graphs_full or [capture_model_step(i, LAYERS) for i in range(2)]
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i)
+        run_steps(max(args.warmup, LAYERS), warm_full, graphs_rem or warm_full)
     stream.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x}")
@@ -356,76 +382,105 @@ def run_ours(args):
         uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         pass
+    def sustain(seconds):
+        """Untimed model steps of the same workload for about `seconds`, so the
+        clock samples see the GPU under this load."""
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t0 < seconds:
+                run_steps(4 * LAYERS, warm_full, warm_full)
+                stream.synchronize()
+
     clocks = ClockSampler(uuid)
     clocks.start()
-
-    K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
+    sustain(0.4)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for i in range(K):
-            step(i, evs[i])
+        run_steps(K, graphs_full, graphs_rem)
         end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    sustain(0.4)
     clk = clocks.stop()
-
+    if clk is not None:
+        clk["window"] = "0.4 s of the same workload before and after the timed region, and the region"
     total_ms = start.elapsed_time(end)
-    dec_ms = np.array([a.elapsed_time(b) for a, b in evs])
     ms_per_step = max_over_ranks(total_ms / K, world, dev)
-    dec_mean_ms = float(dec_ms.mean())
+    # the fused call is the only work in a step besides a2's amortised upload,
+    # so its mean launch duration over the timed region is the step time
+    dec_mean_ms = total_ms / K
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x}")
 
+    # ---- one call alone (its own graph, events around it), over the layers'
+    # caches in turn so L2 holds none of its pages: reported beside
+    iso = []
+    n_iso = min(LAYERS, 8)
+    g1 = []
+    for l in range(n_iso):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            binding.append_decode(shape, plan0, q, k_new, v_new, pools[l][0], pools[l][1], bt, sl,
+                                  w.scale, out, workspace, status)
+        g1.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(24):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g1[i % n_iso].replay()
+            b.record(stream)
+            iso.append((a, b))
+    torch.cuda.synchronize()
+    iso_us = float(np.median([a.elapsed_time(b) for a, b in iso[8:]])) * 1e3
+
     # ---- end to end: every layer step copies q, k_new, v_new in from pinned
     # host memory (plus seq_lens and the block table once per model step) and
-    # reads the output back.
+    # reads the output back, all inside the model-step graphs.
     e2e = None
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         hq, hk, hv, hbt, hsl = pin(w.q), pin(w.k_new), pin(w.v_new), pin(w.block_table), pin(w.seq_lens)
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         nb = lambda t: t.numel() * t.element_size()
-        h2d_total = [0]
 
-        def e2e_step(i):
-            if i % LAYERS == 0:
-                bt.copy_(hbt, non_blocking=True)
-                sl.copy_(hsl, non_blocking=True)
-                h2d_total[0] += nb(hbt) + nb(hsl) + int(plan0.c.blob_bytes)
+        def per_step(strm):
+            bt.copy_(hbt, non_blocking=True)
+            sl.copy_(hsl, non_blocking=True)
+
+        def per_layer_in():
             q.copy_(hq, non_blocking=True)
             k_new.copy_(hk, non_blocking=True)
             v_new.copy_(hv, non_blocking=True)
-            h2d_total[0] += nb(hq) + nb(hk) + nb(hv)
-            step(i)
+
+        def per_layer_out():
             hout.copy_(out, non_blocking=True)
 
+        io = {"per_step": per_step, "per_layer_in": per_layer_in, "per_layer_out": per_layer_out}
+        e_full = [capture_model_step(i, LAYERS, io) for i in range(2)] if full else []
+        e_rem = [capture_model_step(i, rem, io) for i in range(2)] if rem else []
         with torch.cuda.stream(stream):
-            for i in range(max(3, min(args.warmup, LAYERS))):
-                e2e_step(i)
+            run_steps(LAYERS, e_full or warm_full, e_rem or warm_full)
         stream.synchronize()
-        Ke = K
-        h2d_total[0] = 0
         s2 = torch.cuda.Event(enable_timing=True)
         e2 = torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             s2.record(stream)
-            for i in range(Ke):
-                e2e_step(i)
+            nmodel = run_steps(K, e_full, e_rem)
             e2.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / Ke, world, dev)
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / K, world, dev)
+        h2d = (K * (nb(hq) + nb(hk) + nb(hv)) + nmodel * (nb(hbt) + nb(hsl) + int(plan0.c.blob_bytes)))
         e2e = {"value": round(job_value(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 5),
-               "h2d_bytes_per_step": int(round(h2d_total[0] / Ke)),
+               "h2d_bytes_per_step": int(round(h2d / K)),
                "d2h_bytes_per_step": int(nb(hout))}
 
     peak, peak_src = read_peaks()
@@ -460,7 +515,8 @@ def run_ours(args):
             "step": "one layer: pa_append_decode_attention (append fused into the split kernel, "
                     "then the combine kernel); pa_plan + pa_plan_upload once per "
                     f"{LAYERS}-layer model step, inside the timing",
-            "launch": "each layer's call replayed as a CUDA graph",
+            "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
+                      "calls back to back, programmatic dependent launch between kernels)",
             "l2": f"{LAYERS} per-layer KV caches ({LAYERS * 2 * w.k_pages.nbytes / 2**30:.1f} GiB) "
                   f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -479,8 +535,7 @@ def run_ours(args):
             "traffic": traffic_for(args.config),
             "algorithmic_bytes_per_launch": dec_bytes,
             "us_per_launch": round(dec_mean_ms * 1e3, 3),
-            "us_per_launch_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 3),
-                                      round(float(np.percentile(dec_ms, 90)) * 1e3, 3)],
+            "us_per_launch_isolated": round(iso_us, 3),
         },
         "plan_host_us": None,
         "cpu_baseline": cpu_base,

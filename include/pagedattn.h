@@ -106,6 +106,7 @@ typedef struct {
   int32_t max_splits;        /* largest split count of any sequence */
   int32_t chunk_pages;       /* target pages per split chosen by the planner */
   int32_t num_ctas;          /* grid of the split kernel */
+  int32_t num_shared_ctas;   /* the first num_shared_ctas CTAs share one task among their warps */
   int32_t warps_per_cta;
   int32_t owns_blob;         /* 1 if host_blob was allocated by pa_plan */
   uint64_t plan_id;          /* stamp written into the workspace by pa_plan_upload */

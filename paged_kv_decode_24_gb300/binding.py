@@ -39,7 +39,8 @@ class PaPlan(ctypes.Structure):
     _fields_ = [("shape", PaShape), ("num_work_items", ctypes.c_int32),
                 ("num_groups", ctypes.c_int32), ("num_split_items", ctypes.c_int32),
                 ("max_splits", ctypes.c_int32), ("chunk_pages", ctypes.c_int32),
-                ("num_ctas", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("num_shared_ctas", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32),
                 ("owns_blob", ctypes.c_int32), ("plan_id", ctypes.c_uint64),
                 ("blob_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("host_blob", ctypes.c_void_p)]

@@ -1,8 +1,13 @@
 // C-ABI entry points of libpagedattn: argument checks, then launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "decode_kernel.cuh"
 #include "launch.h"
@@ -13,11 +18,56 @@ namespace pa {
 cudaError_t launch_split_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
 cudaError_t launch_split_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
 
+cudaError_t launch_split_tc_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+
+// MHA (G = 1) does one multiply-add per K or V element: the CUDA-core kernel
+// keeps up with HBM.  With G >= 2 query heads per KV head the CUDA-core kernel
+// becomes issue-bound (about 900 instructions per page at G = 4), so those
+// groups go to the tensor-core kernel.
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
                          cudaStream_t stream) {
-  if (head_dim == 64) return launch_split_d64(p, group, grid, stream);
-  if (head_dim == 128) return launch_split_d128(p, group, grid, stream);
+  if (group == 1) {
+    if (head_dim == 64) return launch_split_d64(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_d128(p, group, grid, stream);
+  } else {
+    if (head_dim == 64) return launch_split_tc_d64(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_tc_d128(p, group, grid, stream);
+  }
   return cudaErrorInvalidValue;
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// A pool [P][Hkv][16][D] fp16 as a 4-D tensor, innermost first, with boxes of
+// 64 halves x 16 rows and the 128-byte swizzle.
+static bool encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape_t& s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t D = (cuuint64_t)s.head_dim;
+  cuuint64_t dims[4] = {D, (cuuint64_t)kPageSize, (cuuint64_t)s.num_kv_heads,
+                        (cuuint64_t)s.num_pages};
+  cuuint64_t strides[3] = {D * 2, D * 2 * kPageSize, D * 2 * kPageSize * s.num_kv_heads};
+  cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(pool), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 namespace {
@@ -138,7 +188,9 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   if (!plan) return PA_ERR_INVALID_ARG;
   if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
   if (shape->batch == 0) return PA_OK;
-  if (plan->num_work_items <= 0 || plan->num_ctas <= 0) return PA_ERR_PLAN;
+  if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
+      plan->num_shared_ctas > plan->num_ctas)
+    return PA_ERR_PLAN;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
       !aligned(workspace, 256))
@@ -148,8 +200,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
 
   const int G = shape->num_q_heads / shape->num_kv_heads;
   const int D = shape->head_dim;
-  const Layout lay = layout(plan->num_work_items, plan->num_groups, plan->num_split_items,
-                            plan->num_ctas, G, D);
+  const Layout lay = layout(plan->num_work_items, plan->num_groups, plan->num_split_items, G, D);
   char* ws = (char*)workspace;
   cudaStream_t s = (cudaStream_t)stream;
 
@@ -165,7 +216,6 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.ws_header = (const int32_t*)ws;
   p.items = (const int4*)(ws + lay.items_off);
   p.item_slots = (const int32_t*)(ws + lay.slots_off);
-  p.ctas = (const int2*)(ws + lay.ctas_off);
   p.part_lse = (float*)(ws + lay.lse_off);
   p.part_o = (float*)(ws + lay.o_off);
   p.status = dev_status;
@@ -179,6 +229,9 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.num_groups = plan->num_groups;
   p.num_split_items = plan->num_split_items;
   p.num_ctas = plan->num_ctas;
+  p.num_shared = plan->num_shared_ctas;
+  if (!encode_pool_map(&p.tmap_k, k_pages, *shape) || !encode_pool_map(&p.tmap_v, v_pages, *shape))
+    return PA_ERR_CUDA;
   st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
   if (st != PA_OK || plan->num_groups == 0) return st;
 

@@ -34,6 +34,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
   const int4 grp = gi < p.num_groups ? p.groups[gi] : make_int4(0, 0, 0, 0);
 
+  // The next kernel in the stream may become resident now; it waits for this
+  // grid before it touches anything this kernel reads or writes.
+  pdl_launch_dependents();
   pdl_wait_primary();  // partials of the split kernel are visible after this
 
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||

@@ -1,4 +1,4 @@
-// Split-decode kernel instantiations for head_dim 64 (G = 1, 2, 4, 8).
+// CUDA-core split-decode kernel for head_dim 64, MHA (G = 1).
 #include <atomic>
 
 #include "decode_kernel.cuh"
@@ -41,13 +41,7 @@ cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_split_d64(const SplitParams& p, int group, int grid, cudaStream_t stream) {
-  switch (group) {
-    case 1: return launch_g<1>(p, grid, stream);
-    case 2: return launch_g<2>(p, grid, stream);
-    case 4: return launch_g<4>(p, grid, stream);
-    case 8: return launch_g<8>(p, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return group == 1 ? launch_g<1>(p, grid, stream) : cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -1,4 +1,6 @@
-// Split decode attention over a paged KV cache.
+// Split decode attention over a paged KV cache, on CUDA cores.  Used for MHA
+// (G = 1), where one multiply-add per K or V element keeps up with HBM;
+// decode_tc.cuh holds the tensor-core form used for G >= 2.
 //
 // A task is (sequence b, KV head g, page range [pg0, pg1)).  A CTA either
 // shares one task among its NW warps (warp w takes pages w, w+NW, ...) or,
@@ -46,6 +48,7 @@
 // output directly.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -68,11 +71,13 @@ struct SplitParams {
   const int32_t* item_slots;  // partial slot of each task, -1 = direct output
   float* part_lse;
   float* part_o;
-  const int2* ctas;  // per CTA: first task, task count (1 = shared by the warps)
   int32_t* status;
   float qscale;  // scale * log2(e): scores are kept in base 2
   int32_t batch, num_q_heads, num_kv_heads, max_pages, num_pages;
   int32_t num_items, num_groups, num_split_items, num_ctas;  // must match the header
+  int32_t num_shared;  // CTAs [0, num_shared) share a task; the rest run up to NW short tasks
+  CUtensorMap tmap_k;  // pools as 4-D tensors [P][Hkv][16][D] for the TMA tensor copies
+  CUtensorMap tmap_v;
 };
 
 template <int D, int G>
@@ -186,10 +191,12 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   // programmatic launch does not overlap), so it may be read before the
   // wait on the previous kernel.
   const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
-  const int hdr_ctas = p.ws_header[8];
-  const int2 cd = p.ctas[blockIdx.x];
-  const bool coop = cd.y == 1;  // CTA-uniform
-  const int task = coop ? cd.x : (warp < cd.y ? cd.x + warp : -1);
+  const int2 hdr_ctas = *reinterpret_cast<const int2*>(p.ws_header + 8);
+  // CTA -> task(s) by arithmetic: no descriptor load on the startup path
+  const bool coop = (int)blockIdx.x < p.num_shared;  // CTA-uniform
+  const int first = coop ? (int)blockIdx.x : p.num_shared + ((int)blockIdx.x - p.num_shared) * NW;
+  const int count = coop ? 1 : min(NW, p.num_items - first);
+  const int task = coop ? first : (warp < count ? first + warp : -1);
   int4 it = make_int4(0, 0, 0, 0);
   int slot = -1;
   if (task >= 0 && task < p.num_items) {
@@ -209,8 +216,8 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   pdl_wait_primary();  // everything the previous kernel wrote is visible after this
 
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
-      hdr.w != p.num_split_items || hdr_ctas != p.num_ctas || cd.y < 1 || cd.y > NW ||
-      cd.x < 0 || cd.x + cd.y > p.num_items) {
+      hdr.w != p.num_split_items || hdr_ctas.x != p.num_ctas || hdr_ctas.y != p.num_shared ||
+      count < 1 || first < 0 || first + count > p.num_items) {
     if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
     return;  // CTA-uniform
   }

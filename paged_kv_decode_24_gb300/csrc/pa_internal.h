@@ -72,25 +72,25 @@ inline int resident_ctas_per_sm(int head_dim, int group) {
 // Workspace = [plan blob | lse partials | o partials].
 // Blob = header (16 x int32) | tasks (int4 each) | task partial slots (int32
 // each, -1 = direct output) | groups (int4 each: seq, kv head, splits, first
-// slot) | CTAs (int2 each: first task, task count).
+// slot).
 // header: [0] magic [1] tasks [2] groups [3] partial slots [4] plan_id lo
-//         [5] plan_id hi [6] group size [7] head_dim [8] CTAs.
-// Kernels check words 0..3 and 8 against their launch.  The partials of a
-// group's splits occupy consecutive slots, in split order.  A CTA with one
-// task shares it among its warps; a CTA with 2..4 tasks gives one to each warp.
+//         [5] plan_id hi [6] group size [7] head_dim [8] CTAs [9] shared CTAs.
+// Kernels check words 0..3 and 8..9 against their launch.  The partials of a
+// group's splits occupy consecutive slots, in split order.  CTA i < shared
+// CTAs runs task i with all its warps; the CTAs after it run the remaining
+// (short) tasks four at a time, one per warp, in task order.
 struct Layout {
-  size_t items_off, slots_off, groups_off, ctas_off, blob_bytes, lse_off, o_off, total;
+  size_t items_off, slots_off, groups_off, blob_bytes, lse_off, o_off, total;
 };
 
 inline size_t align_sz(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline Layout layout(int items, int groups, int nslots, int ctas, int group, int head_dim) {
+inline Layout layout(int items, int groups, int nslots, int group, int head_dim) {
   Layout l{};
   l.items_off = 64;
   l.slots_off = l.items_off + 16 * (size_t)items;
   l.groups_off = align_sz(l.slots_off + 4 * (size_t)items, 16);
-  l.ctas_off = l.groups_off + 16 * (size_t)groups;
-  l.blob_bytes = align_sz(l.ctas_off + 8 * (size_t)ctas, 16);
+  l.blob_bytes = align_sz(l.groups_off + 16 * (size_t)groups, 16);
   l.lse_off = align_sz(l.blob_bytes, 256);
   l.o_off = align_sz(l.lse_off + 4 * (size_t)nslots * group, 256);
   l.total = align_sz(l.o_off + 4 * (size_t)nslots * group * head_dim, 256);

@@ -121,19 +121,17 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   // task, which only pays off when the GPU runs several waves of them.
   const int64_t cta_slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
   const int bundle_pages = W64 > kBundleWhenOver * cta_slots ? bundle_max : 0;
-  int NC = 0;
-  {
-    int64_t remaining_small = 0;
-    for (int b = 0; b < B; ++b) {
-      const int32_t np = pages[b], n = nsplit[b];
-      for (int j = 0; j < n; ++j) {
-        const int32_t sz = (int32_t)((int64_t)np * (j + 1) / n - (int64_t)np * j / n);
-        if (sz <= bundle_pages) remaining_small += Hkv;
-      }
+  int n_small = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t np = pages[b], n = nsplit[b];
+    for (int j = 0; j < n; ++j) {
+      const int32_t sz = (int32_t)((int64_t)np * (j + 1) / n - (int64_t)np * j / n);
+      if (sz <= bundle_pages) n_small += Hkv;
     }
-    NC = (int)(W - remaining_small + (remaining_small + kWarpsPerCta - 1) / kWarpsPerCta);
   }
-  const Layout lay = layout(W, C, nidx, NC, G, D);
+  const int n_shared = W - n_small;  // longest first: the small tasks are the last ones
+  const int NC = n_shared + (n_small + kWarpsPerCta - 1) / kWarpsPerCta;
+  const Layout lay = layout(W, C, nidx, G, D);
   char* blob = nullptr;
   if (dst) {
     if (dst_bytes < lay.blob_bytes) {
@@ -175,6 +173,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   hdr[6] = G;
   hdr[7] = D;
   hdr[8] = NC;
+  hdr[9] = n_shared;
   int32_t* items = (int32_t*)(blob + lay.items_off);
   int32_t* slots = (int32_t*)(blob + lay.slots_off);
   int32_t* groups = (int32_t*)(blob + lay.groups_off);
@@ -207,24 +206,8 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   // zero the alignment gaps so the blob bytes are fully defined
   const size_t used = lay.slots_off + 4 * (size_t)W;
   if (lay.groups_off > used) memset(blob + used, 0, lay.groups_off - used);
-  {
-    int32_t* ctas = (int32_t*)(blob + lay.ctas_off);
-    int c = 0;
-    for (int i = 0; i < W;) {
-      const int32_t sz = items[4 * i + 3] - items[4 * i + 2];
-      const int n = sz > bundle_pages ? 1 : std::min(kWarpsPerCta, W - i);
-      ctas[2 * c] = i;
-      ctas[2 * c + 1] = n;
-      ++c;
-      i += n;
-    }
-    const size_t cend = lay.ctas_off + 8 * (size_t)c;
-    if (lay.blob_bytes > cend) memset(blob + cend, 0, lay.blob_bytes - cend);
-    if (c != NC) {  // the count above and the walk here must agree
-      if (alloc) free(blob);
-      return PA_ERR_PLAN;
-    }
-  }
+  if (lay.blob_bytes > lay.groups_off + 16 * (size_t)C)
+    memset(blob + lay.groups_off + 16 * (size_t)C, 0, lay.blob_bytes - lay.groups_off - 16 * (size_t)C);
 
   plan_out->shape = *shape;
   plan_out->num_work_items = W;
@@ -234,6 +217,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->chunk_pages = forced_splits > 0 ? max_size : chunk;
   plan_out->warps_per_cta = kWarpsPerCta;
   plan_out->num_ctas = NC;
+  plan_out->num_shared_ctas = n_shared;
   plan_out->owns_blob = dst ? 0 : 1;
   plan_out->plan_id = id;
   plan_out->blob_bytes = lay.blob_bytes;

@@ -43,9 +43,8 @@ def _decode_blob(plan):
     slots = blob[16 + 4 * W:16 + 5 * W]
     g0 = (16 + 5 * W + 3) // 4 * 4
     groups = blob[g0:g0 + 4 * C].reshape(C, 4)
-    NC = blob[8]
-    ctas = blob[g0 + 4 * C:g0 + 4 * C + 2 * NC].reshape(NC, 2)
-    return blob, items, groups, slots, nslots, ctas
+    NC, n_shared = blob[8], blob[9]
+    return blob, items, groups, slots, nslots, (NC, n_shared)
 
 
 def check_plan_covers(w, plan):
@@ -86,18 +85,13 @@ def check_plan_covers(w, plan):
     for i, (b, hw, lo, hi) in enumerate(items):
         if not (int(hw) & 0x80000000):
             assert slots[i] == -1
-    # CTAs walk the tasks in order: long tasks alone, short ones (<= 8 pages)
-    # up to four per CTA
-    assert plan.c.num_ctas == len(ctas)
-    nxt = 0
-    for first, count in ctas:
-        assert first == nxt and 1 <= count <= 4
-        if count > 1:
-            assert np.all(sizes[first:first + count] <= 8)
-        else:
-            assert sizes[first] > 8 or first + 1 == len(items) or True
-        nxt = first + count
-    assert nxt == len(items)
+    # CTAs: the first n_shared tasks get a CTA each; the remaining (short,
+    # <= 8 pages) tasks go four to a CTA
+    NC, n_shared = ctas
+    assert plan.c.num_ctas == NC and plan.c.num_shared_ctas == n_shared
+    assert 0 <= n_shared <= len(items)
+    assert NC == n_shared + (len(items) - n_shared + 3) // 4
+    assert np.all(sizes[n_shared:] <= 8)
     assert plan.c.workspace_bytes >= plan.c.blob_bytes
     return items, groups
 
