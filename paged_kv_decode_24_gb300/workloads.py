@@ -28,6 +28,11 @@ Conventions (the plainest readings of the workload descriptions):
   * Pool rows that no sequence owns hold random values of the same law unless
     ``poison`` is set, in which case they hold fp16 NaN so that any read of an
     unowned row shows up in the output.
+  * With ``kv="int8"`` the cache also comes as INT8 codes with one fp32 scale
+    per (page, kv head, slot) row, drawn directly: codes are N(0, 40) rounded
+    to integers and clipped to [-127, 127], scales uniform in [0.004, 0.012)
+    (about what N(0, 0.5) rows quantise to).  Nothing here quantises; poison
+    sets the scales of unowned rows to NaN.
 """
 
 from __future__ import annotations
@@ -71,6 +76,10 @@ class Workload:
     v_new: np.ndarray           # fp16 [B][Hkv][D]
     k_pages: np.ndarray         # fp16 [P][Hkv][S][D]
     v_pages: np.ndarray         # fp16 [P][Hkv][S][D]
+    k_codes: np.ndarray | None = None    # int8 [P][Hkv][S][D] (kv="int8")
+    v_codes: np.ndarray | None = None
+    k_scales: np.ndarray | None = None   # float32 [P][Hkv][S]
+    v_scales: np.ndarray | None = None
 
     @property
     def group_size(self) -> int:
@@ -79,6 +88,10 @@ class Workload:
     def kv_bytes(self) -> int:
         """K and V bytes the step must read: sum(L) * Hkv * D * 2 tensors * 2 B."""
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 4
+
+    def kv_bytes_int8(self) -> int:
+        """The same for the INT8 cache: sum(L) * Hkv * 2 tensors * (D codes + a 4 B scale)."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * 2 * (self.head_dim + 4)
 
 
 def _draw(rng: np.random.Generator, shape, dist) -> np.ndarray:
@@ -138,7 +151,7 @@ def layout(seq_lens: np.ndarray, num_pages: int, page_size: int, rng: np.random.
 def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE_SIZE,
                 num_pages=None, dist=("normal", 0.5), seed=0, forced_splits=0,
                 scale=None, poison=False, max_pages_per_seq=None, name="custom",
-                config=0) -> Workload:
+                config=0, kv="fp16") -> Workload:
     """Any shape: used by the tests for ragged, empty and edge cases."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
@@ -163,15 +176,32 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
         v_pages[pg, :, slot, :] = np.float16(np.nan)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
+    q8 = {}
+    if kv == "int8":
+        def codes():
+            c = np.rint(rng.standard_normal(pool_shape, dtype=np.float32) * np.float32(40.0))
+            return np.clip(c, -127, 127).astype(np.int8)
+
+        def scales():
+            return (np.float32(0.004) + rng.random(pool_shape[:3], dtype=np.float32)
+                    * np.float32(0.008)).astype(np.float32)
+
+        q8 = dict(k_codes=codes(), v_codes=codes(), k_scales=scales(), v_scales=scales())
+        if poison:
+            q8["k_scales"][pg, :, slot] = np.float32(np.nan)
+            q8["v_scales"][pg, :, slot] = np.float32(np.nan)
+    elif kv != "fp16":
+        raise ValueError(kv)
     return Workload(name=name, config=config, batch=B, num_q_heads=num_q_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size,
                     num_pages=num_pages, max_pages_per_seq=bt.shape[1],
                     forced_splits=forced_splits, scale=float(scale), seq_lens=seq_lens,
                     block_table=bt, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages,
-                    v_pages=v_pages)
+                    v_pages=v_pages, **q8)
 
 
-def make_config(cfg: int, seed: int | None = None, poison: bool = False) -> Workload:
+def make_config(cfg: int, seed: int | None = None, poison: bool = False,
+                kv: str = "fp16") -> Workload:
     """The five benchmark workloads, seeded with 24000 + cfg by default."""
     if cfg not in _SHAPES:
         raise ValueError(f"unknown config {cfg}")
@@ -184,5 +214,6 @@ def make_config(cfg: int, seed: int | None = None, poison: bool = False) -> Work
     sub_seed = int(rng.integers(0, 2**31 - 1))
     w = make_custom(seq_lens=seq_lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                     page_size=PAGE_SIZE, num_pages=pool, dist=dist, seed=sub_seed,
-                    forced_splits=splits, poison=poison, name=CONFIG_NAMES[cfg], config=cfg)
+                    forced_splits=splits, poison=poison, name=CONFIG_NAMES[cfg], config=cfg,
+                    kv=kv)
     return w
