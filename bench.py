@@ -27,6 +27,10 @@ The JSON line reports:
 Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
 in total), so L2 never holds the pages a step reads.
 
+--kv int8 runs the same steps over the INT8 cache (codes with one fp32 scale
+per row) through pa_append_decode_attention_q8; value and roofline then
+count the INT8 rows' bytes (D + 4 per row and tensor).
+
 --impl reference times the float64 CPU oracle (the only reference this
 method has) on the same workload, metric and unit.
 """
@@ -71,6 +75,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
+                    help="KV-cache type: fp16, or INT8 codes with per-row fp32 scales")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
                     help="per-layer KV caches; fewer only to shrink profiler captures")
     return ap.parse_args()
@@ -85,6 +91,8 @@ def oracle_sample(w, budget_s):
     covered, description).  The oracle's append is left out: it copies whole
     pools functionally, which says nothing about the method."""
     import oracle
+    q8 = w.k_codes is not None
+    row = w.head_dim + 4 if q8 else 2 * w.head_dim
     order = list(np.argsort(-w.seq_lens, kind="stable"))   # longest first, cycling
     t0 = time.perf_counter()
     kv = 0
@@ -95,8 +103,12 @@ def oracle_sample(w, budget_s):
         i += 1
         sub_bt = w.block_table[b:b + 1]
         sub_l = w.seq_lens[b:b + 1]
-        oracle.decode_attention(w.q[b:b + 1], w.k_pages, w.v_pages, sub_bt, sub_l, w.scale)
-        kv += int(sub_l[0]) * w.num_kv_heads * w.head_dim * 4
+        if q8:
+            oracle.decode_attention_q8(w.q[b:b + 1], w.k_codes, w.v_codes, w.k_scales,
+                                       w.v_scales, sub_bt, sub_l, w.scale)
+        else:
+            oracle.decode_attention(w.q[b:b + 1], w.k_pages, w.v_pages, sub_bt, sub_l, w.scale)
+        kv += int(sub_l[0]) * w.num_kv_heads * 2 * row
         seqs += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s and seqs >= 1:
@@ -106,12 +118,12 @@ def oracle_sample(w, budget_s):
 
 def oracle_worker(args):
     from paged_kv_decode_24_gb300 import workloads
-    w = workloads.make_config(args.config)
+    w = workloads.make_config(args.config, kv=args.kv)
     dt, kv, desc = oracle_sample(w, args.cpu_seconds)
     print(json.dumps({"seconds": dt, "kv_bytes": kv, "sample": desc}))
 
 
-def run_oracle_subprocess(cfg, seconds):
+def run_oracle_subprocess(cfg, seconds, kv="fp16"):
     """The oracle in a fresh single-threaded process (started by exec, so no
     CUDA state is shared)."""
     env = dict(os.environ)
@@ -119,14 +131,16 @@ def run_oracle_subprocess(cfg, seconds):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", "--config",
-                        str(cfg), "--cpu-seconds", str(seconds)], capture_output=True, text=True,
+                        str(cfg), "--cpu-seconds", str(seconds), "--kv", kv], capture_output=True,
+                       text=True,
                        env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     res = json.loads(r.stdout.strip().splitlines()[-1])
     gbs = res["kv_bytes"] / res["seconds"] / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"config {cfg}: {res['sample']}, {res['seconds']:.1f} s of float64 numpy"}
+            "sample": f"config {cfg} ({kv} cache): {res['sample']}, "
+                      f"{res['seconds']:.1f} s of float64 numpy"}
 
 
 # ---------------------------------------------------------------------------
@@ -152,7 +166,7 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_for(cfg):
+def traffic_for(cfg, kv="fp16"):
     """DRAM bytes per launch of the split kernel from a committed ncu capture,
     only while the kernel sources still hash to what was profiled."""
     try:
@@ -162,7 +176,7 @@ def traffic_for(cfg):
         return None
     if d.get("source_hash") != kernel_source_hash():
         return None
-    ent = d.get("configs", {}).get(str(cfg))
+    ent = d.get("configs", {}).get(str(cfg) if kv == "fp16" else f"{cfg}-{kv}")
     return None if ent is None else ent.get("dram_bytes_per_launch")
 
 
@@ -267,7 +281,7 @@ def run_ours(args):
     world, rank, local = dist_setup(args)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds)   # before any CUDA call
+        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds, args.kv)  # before CUDA
 
     _build.ensure_built()
     binding.load()
@@ -277,13 +291,15 @@ def run_ours(args):
     num_sms = props.multi_processor_count
     stream = torch.cuda.Stream(device=dev)
 
-    w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank)
+    q8 = args.kv == "int8"
+    w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank,
+                              kv=args.kv)
     shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
                                w.max_pages_per_seq, w.num_pages)
-    kv_bytes = w.kv_bytes()
+    kv_bytes = w.kv_bytes_int8() if q8 else w.kv_bytes()
     dec_bytes = (accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                         w.page_size)
-                 + accounting.append_bytes(w.batch, w.num_kv_heads, w.head_dim))
+                                         w.page_size, kv=args.kv)
+                 + accounting.append_bytes(w.batch, w.num_kv_heads, w.head_dim, kv=args.kv))
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     lens_host = np.ascontiguousarray(w.seq_lens)
 
@@ -293,11 +309,20 @@ def run_ours(args):
     v_new = to_dev(w.v_new)
     bt = to_dev(w.block_table)
     sl = to_dev(w.seq_lens)
-    kp0 = to_dev(w.k_pages)
-    vp0 = to_dev(w.v_pages)
+    if q8:
+        cache0 = (to_dev(w.k_codes), to_dev(w.v_codes), to_dev(w.k_scales), to_dev(w.v_scales))
+    else:
+        cache0 = (to_dev(w.k_pages), to_dev(w.v_pages))
     # One KV cache per layer, as in the model: every layer's pages are distinct
     # memory, so a layer's reads never hit what the previous layers left in L2.
-    pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(LAYERS - 1)]
+    pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(LAYERS - 1)]
+    cache_bytes = sum(t.numel() * t.element_size() for t in cache0)
+    step_call = binding.append_decode_q8 if q8 else binding.append_decode
+
+    def layer_call(pool, qq, kn, vn, o, stream=None):
+        """One layer's fused append + decode over that layer's cache."""
+        step_call(shape, plan0, qq, kn, vn, *pool, bt, sl, w.scale, o, workspace, status,
+                  stream=stream)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -323,8 +348,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         binding.upload(staged_plans[0], workspace, stream=stream)
         # a warm-up call (sets kernel attributes) before capture
-        binding.append_decode(shape, plan0, q, k_new, v_new, kp0, vp0, bt, sl, w.scale, out,
-                              workspace, status, stream=stream)
+        layer_call(pools[0], q, k_new, v_new, out, stream=stream)
     stream.synchronize()
 
     # One graph per model step: the plan upload (a2), then the layers' fused
@@ -334,9 +358,7 @@ def run_ours(args):
         with torch.cuda.graph(g, stream=stream):
             binding.upload(staged_plans[slot], workspace)
             for l in range(nlayers):
-                kp, vp = pools[l]
-                binding.append_decode(shape, plan0, q, k_new, v_new, kp, vp, bt, sl, w.scale, out,
-                                      workspace, status)
+                layer_call(pools[l], q, k_new, v_new, out)
         return g
 
     K = args.steps
@@ -418,8 +440,7 @@ def run_ours(args):
     for l in range(n_iso):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            binding.append_decode(shape, plan0, q, k_new, v_new, pools[l][0], pools[l][1], bt, sl,
-                                  w.scale, out, workspace, status)
+            layer_call(pools[l], q, k_new, v_new, out)
         g1.append(g)
     with torch.cuda.stream(stream):
         for i in range(24):
@@ -479,9 +500,7 @@ def run_ours(args):
                     stream.wait_event(ready[l])
                     if l >= 2:
                         stream.wait_event(back[l - 2])  # output set l%2 has been read back
-                    kp, vp = pools[l]
-                    binding.append_decode(shape, plan0, qb[l % 2], kb[l % 2], vb[l % 2], kp, vp, bt,
-                                          sl, w.scale, ob[l % 2], workspace, status)
+                    layer_call(pools[l], qb[l % 2], kb[l % 2], vb[l % 2], ob[l % 2])
                     done.append(torch.cuda.Event())
                     done[l].record(stream)
                     side_out.wait_event(done[l])
@@ -540,10 +559,11 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16",
+        "kv_cache": "int8 codes + fp32 row scales" if q8 else "fp16",
         "accumulate": "f32",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
         "config": {
-            "workload": w.name,
+            "workload": w.name + (", INT8 KV cache (per-row scales)" if q8 else ""),
             "config_id": args.config,
             "batch": w.batch,
             "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}",
@@ -558,14 +578,15 @@ def run_ours(args):
                     f"{LAYERS}-layer model step, inside the timing",
             "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
                       "calls back to back, programmatic dependent launch between kernels)",
-            "l2": f"{LAYERS} per-layer KV caches ({LAYERS * 2 * w.k_pages.nbytes / 2**30:.1f} GiB) "
+            "l2": f"{LAYERS} per-layer KV caches ({LAYERS * cache_bytes / 2**30:.1f} GiB) "
                   f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "hbm_frac_step": round(value / world / peak, 4),
         "roofline": {
-            "kernel": "pa_append_decode_attention = split_decode_kernel (with the append) + "
-                      "combine_kernel, timed together",
+            "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if q8 else
+                       "pa_append_decode_attention = split_decode_kernel") +
+                      " (with the append) + combine_kernel, timed together",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -573,7 +594,7 @@ def run_ours(args):
                            else "fallback 6800 GB/s (of fallback)",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_for(args.config),
+            "traffic": traffic_for(args.config, args.kv),
             "algorithmic_bytes_per_launch": dec_bytes,
             "us_per_launch": round(dec_mean_ms * 1e3, 3),
             "us_per_launch_isolated": round(iso_us, 3),
@@ -605,7 +626,7 @@ def run_reference(args):
     if rank != 0:
         return
     from paged_kv_decode_24_gb300 import workloads
-    w = workloads.make_config(args.config)
+    w = workloads.make_config(args.config, kv=args.kv)
     # a bounded sample per step: the whole run stays within about two minutes
     per_step = min(2.0, max(0.2, 120.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
@@ -633,7 +654,9 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
-        "config": {"workload": w.name, "config_id": args.config},
+        "config": {"workload": w.name + (", INT8 KV cache (per-row scales)"
+                                         if args.kv == "int8" else ""),
+                   "config_id": args.config},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {desc}, about {per_step:.2f} s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

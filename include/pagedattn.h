@@ -215,6 +215,55 @@ pa_status_t pa_append_decode_attention(const pa_shape_t* shape, const pa_plan_t*
                                        void* workspace, size_t workspace_bytes,
                                        int32_t* dev_status, void* stream);
 
+/* ---- INT8 KV cache ---------------------------------------------------
+ *
+ * The same paged cache held as INT8 codes with one fp32 scale per row
+ * (MonadKai/xLLM, introduction: KV-cache quantisation, per-row INT8).  A row
+ * is one token's D-vector of one KV head, and its value is code * scale.
+ *
+ * Layout (device):
+ *   k_codes, v_codes: [num_pages][Hkv][16][D] int8 (a row is D bytes, a
+ *                     (page, head) tile is 16 * D contiguous bytes)
+ *   k_scales, v_scales: [num_pages][Hkv][16] fp32 (16-byte aligned)
+ * A decode reads D + 4 bytes per row and tensor where the fp16 cache reads
+ * 2 D.  The plan, workspace, q, out, block table, seq_lens and status are
+ * those of the fp16 calls, and one plan serves both caches.
+ *
+ * Quantisation of a new row (append): scale = max|x| / 127 and
+ * code = x / scale rounded to nearest, ties to even, clamped to
+ * [-127, 127], both divisions in IEEE fp32 round-to-nearest; an all-zero
+ * row gets scale 0 and zero codes.  Non-finite inputs give unspecified codes.
+ *
+ * Errors are those of the fp16 calls.  Scale pointers that are null or not
+ * 16-byte aligned give PA_ERR_INVALID_ARG.
+ */
+
+/* pa_kv_append into the INT8 cache: quantise k_new/v_new ([B][Hkv][D] fp16)
+ * and write codes and scales at position seq_lens[b] - 1. */
+pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_new, const void* v_new,
+                            void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            int32_t* dev_status, void* stream);
+
+/* pa_decode_attention over the INT8 cache: attention over the dequantised
+ * rows, fp32 accumulation, fp16 output. */
+pa_status_t pa_decode_attention_q8(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                                   const void* k_codes, const void* v_codes,
+                                   const float* k_scales, const float* v_scales,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   float scale, void* out, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream);
+
+/* pa_kv_append_q8 and pa_decode_attention_q8 in one launch, with the same
+ * results as the two calls in sequence. */
+pa_status_t pa_append_decode_attention_q8(const pa_shape_t* shape, const pa_plan_t* plan,
+                                          const void* q, const void* k_new, const void* v_new,
+                                          void* k_codes, void* v_codes, float* k_scales,
+                                          float* v_scales, const int32_t* block_table,
+                                          const int32_t* seq_lens, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* dev_status, void* stream);
+
 /* Size of the library-owned scratch array used by pa_decode_attention_static. */
 #define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 

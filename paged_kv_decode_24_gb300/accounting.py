@@ -25,24 +25,35 @@ def kv_cache_bytes(seq_lens, kv_width: int, bytes_per_element: int, layers: int 
     return int(2 * rounded.sum() * kv_width * bytes_per_element * layers)
 
 
-def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 page_size: int) -> int:
-    """Algorithmic HBM bytes of one decode-attention call (fp16 q/K/V/out).
+def kv_row_bytes(head_dim: int, kv: str = "fp16") -> int:
+    """Bytes of one cached row (one token, one KV head, K or V): D fp16 values,
+    or D int8 codes and one fp32 scale (per-row INT8 cache)."""
+    if kv == "fp16":
+        return 2 * head_dim
+    if kv == "int8":
+        return head_dim + 4
+    raise ValueError(kv)
 
-    K and V of every attended token, q and out, the block-table entries that
-    are read (one int32 per used page) and seq_lens.
+
+def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 page_size: int, kv: str = "fp16") -> int:
+    """Algorithmic HBM bytes of one decode-attention call (fp16 q/out).
+
+    K and V of every attended token (fp16 or INT8 rows), q and out, the
+    block-table entries that are read (one int32 per used page) and seq_lens.
     """
     lens = np.asarray(seq_lens, np.int64)
     B = len(lens)
-    kv = kv_cache_bytes(lens, num_kv_heads * head_dim, 2)
+    kv = int(2 * lens.sum() * num_kv_heads * kv_row_bytes(head_dim, kv))
     q_out = 2 * B * num_q_heads * head_dim * 2
     pages = int(((lens + page_size - 1) // page_size).sum())
     return int(kv + q_out + 4 * pages + 4 * B)
 
 
-def append_bytes(batch: int, num_kv_heads: int, head_dim: int) -> int:
-    """pa_kv_append reads k_new, v_new and writes them once: 2 x 2 x B*Hkv*D fp16."""
-    return 2 * 2 * batch * num_kv_heads * head_dim * 2
+def append_bytes(batch: int, num_kv_heads: int, head_dim: int, kv: str = "fp16") -> int:
+    """The append reads k_new, v_new (fp16) and writes one row of each."""
+    rows = 2 * batch * num_kv_heads
+    return rows * (2 * head_dim + kv_row_bytes(head_dim, kv))
 
 
 def decode_flops(seq_lens, num_q_heads: int, head_dim: int) -> int:

@@ -72,6 +72,15 @@ _SIGS = {
                                                   _P, ctypes.c_size_t, _P, _P]),
     "pa_decode_attention_static": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan),
                                                   _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "pa_kv_append_q8": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P]),
+    "pa_decode_attention_q8": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan), _P,
+                                              _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                              ctypes.c_size_t, _P, _P]),
+    "pa_append_decode_attention_q8": (ctypes.c_int, [ctypes.POINTER(PaShape),
+                                                     ctypes.POINTER(PaPlan), _P, _P, _P, _P, _P,
+                                                     _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                                     ctypes.c_size_t, _P, _P]),
     "pa_debug_gather_indices": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_version": (ctypes.c_char_p, []),
@@ -249,6 +258,54 @@ def append_decode(shape, plan: Plan, q, k_new, v_new, k_pages, v_pages, block_ta
         ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
         _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
         _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def _q8_pools(k_codes, v_codes, k_scales, v_scales):
+    torch = _torch()
+    return (_dev_ptr(k_codes, torch.int8, "k_codes"), _dev_ptr(v_codes, torch.int8, "v_codes"),
+            _dev_ptr(k_scales, torch.float32, "k_scales"),
+            _dev_ptr(v_scales, torch.float32, "v_scales"))
+
+
+def append_q8(shape, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens,
+              status, stream=None):
+    """pa_kv_append_q8: quantise the new rows into the INT8 cache."""
+    torch = _torch()
+    lib = load()
+    _check("pa_kv_append_q8", lib.pa_kv_append_q8(
+        ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
+        _dev_ptr(v_new, torch.float16, "v_new"), *_q8_pools(k_codes, v_codes, k_scales, v_scales),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def decode_q8(shape, plan: Plan, q, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens,
+              scale, out, workspace, status, stream=None):
+    """pa_decode_attention_q8: decode over the INT8 cache."""
+    torch = _torch()
+    lib = load()
+    _check("pa_decode_attention_q8", lib.pa_decode_attention_q8(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        *_q8_pools(k_codes, v_codes, k_scales, v_scales),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def append_decode_q8(shape, plan: Plan, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales,
+                     block_table, seq_lens, scale, out, workspace, status, stream=None):
+    """pa_append_decode_attention_q8: append the new token and attend, one launch."""
+    torch = _torch()
+    lib = load()
+    _check("pa_append_decode_attention_q8", lib.pa_append_decode_attention_q8(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
+        *_q8_pools(k_codes, v_codes, k_scales, v_scales),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
         ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),

@@ -20,6 +20,8 @@ cudaError_t launch_split_d128(const SplitParams& p, int group, int grid, cudaStr
 
 cudaError_t launch_split_tc_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
 cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_q8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
 
 // MHA (G = 1) does one multiply-add per K or V element: the CUDA-core kernel
 // keeps up with HBM.  With G >= 2 query heads per KV head the CUDA-core kernel
@@ -34,6 +36,15 @@ cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid
     if (head_dim == 64) return launch_split_tc_d64(p, group, grid, stream);
     if (head_dim == 128) return launch_split_tc_d128(p, group, grid, stream);
   }
+  return cudaErrorInvalidValue;
+}
+
+// The INT8 cache has one kernel for every group size: its products run on
+// tensor cores, which the padding of G = 1 to 8 heads does not slow down.
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
+                            cudaStream_t stream) {
+  if (head_dim == 64) return launch_split_q8_d64(p, group, grid, stream);
+  if (head_dim == 128) return launch_split_q8_d128(p, group, grid, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -68,6 +79,24 @@ static bool encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape_t
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(pool), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// An INT8 code pool [P][Hkv][16][D] as a 4-D tensor with one box per
+// (page, head) tile: D bytes x 16 rows, 128-byte swizzle for D = 128 and
+// 64-byte swizzle for D = 64 (a row is never wider than its swizzle span).
+static bool encode_code_map(CUtensorMap* map, const void* pool, const pa_shape_t& s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t D = (cuuint64_t)s.head_dim;
+  cuuint64_t dims[4] = {D, (cuuint64_t)kPageSize, (cuuint64_t)s.num_kv_heads,
+                        (cuuint64_t)s.num_pages};
+  cuuint64_t strides[3] = {D, D * kPageSize, D * kPageSize * s.num_kv_heads};
+  cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kPageSize, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(pool), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 namespace {
@@ -133,6 +162,37 @@ extern "C" pa_status_t pa_kv_append(const pa_shape_t* shape, const void* k_new, 
   return cuda_status(launch_append(p, (cudaStream_t)stream));
 }
 
+extern "C" pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_new,
+                                       const void* v_new, void* k_codes, void* v_codes,
+                                       float* k_scales, float* v_scales,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t* dev_status, void* stream) {
+  using namespace pa;
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (shape->batch == 0) return PA_OK;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_codes, 16) ||
+      !aligned(v_codes, 16) || !aligned(k_scales, 16) || !aligned(v_scales, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  AppendQ8Params p{};
+  p.k_new = (const __half*)k_new;
+  p.v_new = (const __half*)v_new;
+  p.k_codes = (int8_t*)k_codes;
+  p.v_codes = (int8_t*)v_codes;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.status = dev_status;
+  p.batch = shape->batch;
+  p.num_kv_heads = shape->num_kv_heads;
+  p.head_dim = shape->head_dim;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pages = shape->num_pages;
+  return cuda_status(launch_append_q8(p, (cudaStream_t)stream));
+}
+
 extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
                                       size_t workspace_bytes, void* stream) {
   if (!plan || !plan->host_blob || plan->blob_bytes == 0) return PA_ERR_INVALID_ARG;
@@ -145,11 +205,21 @@ extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
 namespace pa {
 namespace {
 
+// The cache a decode reads: fp16 pools, or INT8 code pools with their row
+// scales (scales non-null).
+struct KvCache {
+  const void* k;
+  const void* v;
+  const float* k_scales;
+  const float* v_scales;
+  bool int8() const { return k_scales != nullptr; }
+};
+
 pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
-                        const void* k_new, const void* v_new, const void* k_pages,
-                        const void* v_pages, const int32_t* block_table, const int32_t* seq_lens,
-                        float scale, void* out, void* workspace, size_t workspace_bytes,
-                        int32_t* dev_status, void* stream);
+                        const void* k_new, const void* v_new, const KvCache& kv,
+                        const int32_t* block_table, const int32_t* seq_lens, float scale,
+                        void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream);
 
 }  // namespace
 }  // namespace pa
@@ -160,8 +230,9 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
                                            float scale, void* out, void* workspace,
                                            size_t workspace_bytes, int32_t* dev_status,
                                            void* stream) {
-  return pa::decode_impl(shape, plan, q, nullptr, nullptr, k_pages, v_pages, block_table,
-                         seq_lens, scale, out, workspace, workspace_bytes, dev_status, stream);
+  return pa::decode_impl(shape, plan, q, nullptr, nullptr, {k_pages, v_pages, nullptr, nullptr},
+                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                         stream);
 }
 
 extern "C" pa_status_t pa_append_decode_attention(
@@ -171,18 +242,47 @@ extern "C" pa_status_t pa_append_decode_attention(
     int32_t* dev_status, void* stream) {
   if (shape && shape->batch > 0 && (!pa::aligned(k_new, 16) || !pa::aligned(v_new, 16)))
     return PA_ERR_INVALID_ARG;
-  return pa::decode_impl(shape, plan, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
-                         scale, out, workspace, workspace_bytes, dev_status, stream);
+  return pa::decode_impl(shape, plan, q, k_new, v_new, {k_pages, v_pages, nullptr, nullptr},
+                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                         stream);
+}
+
+extern "C" pa_status_t pa_decode_attention_q8(const pa_shape_t* shape, const pa_plan_t* plan,
+                                              const void* q, const void* k_codes,
+                                              const void* v_codes, const float* k_scales,
+                                              const float* v_scales, const int32_t* block_table,
+                                              const int32_t* seq_lens, float scale, void* out,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_status, void* stream) {
+  if (shape && shape->batch > 0 && (!pa::aligned(k_scales, 16) || !pa::aligned(v_scales, 16)))
+    return PA_ERR_INVALID_ARG;
+  return pa::decode_impl(shape, plan, q, nullptr, nullptr, {k_codes, v_codes, k_scales, v_scales},
+                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                         stream);
+}
+
+extern "C" pa_status_t pa_append_decode_attention_q8(
+    const pa_shape_t* shape, const pa_plan_t* plan, const void* q, const void* k_new,
+    const void* v_new, void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+    const int32_t* block_table, const int32_t* seq_lens, float scale, void* out, void* workspace,
+    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (shape && shape->batch > 0 &&
+      (!pa::aligned(k_new, 16) || !pa::aligned(v_new, 16) || !pa::aligned(k_scales, 16) ||
+       !pa::aligned(v_scales, 16)))
+    return PA_ERR_INVALID_ARG;
+  return pa::decode_impl(shape, plan, q, k_new, v_new, {k_codes, v_codes, k_scales, v_scales},
+                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                         stream);
 }
 
 namespace pa {
 namespace {
 
 pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
-                        const void* k_new, const void* v_new, const void* k_pages,
-                        const void* v_pages, const int32_t* block_table, const int32_t* seq_lens,
-                        float scale, void* out, void* workspace, size_t workspace_bytes,
-                        int32_t* dev_status, void* stream) {
+                        const void* k_new, const void* v_new, const KvCache& kv,
+                        const int32_t* block_table, const int32_t* seq_lens, float scale,
+                        void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream) {
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
   if (!plan) return PA_ERR_INVALID_ARG;
@@ -191,7 +291,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
       plan->num_shared_ctas > plan->num_ctas)
     return PA_ERR_PLAN;
-  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+  if (!aligned(q, 16) || !aligned(kv.k, 16) || !aligned(kv.v, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
       !aligned(workspace, 256))
     return PA_ERR_INVALID_ARG;
@@ -206,8 +306,15 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
 
   SplitParams p{};
   p.q = (const __half*)q;
-  p.k_pages = (const __half*)k_pages;
-  p.v_pages = (const __half*)v_pages;
+  if (kv.int8()) {
+    p.k_codes = (const int8_t*)kv.k;
+    p.v_codes = (const int8_t*)kv.v;
+    p.k_scales = kv.k_scales;
+    p.v_scales = kv.v_scales;
+  } else {
+    p.k_pages = (const __half*)kv.k;
+    p.v_pages = (const __half*)kv.v;
+  }
   p.k_new = (const __half*)k_new;
   p.v_new = (const __half*)v_new;
   p.block_table = block_table;
@@ -230,9 +337,15 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.num_split_items = plan->num_split_items;
   p.num_ctas = plan->num_ctas;
   p.num_shared = plan->num_shared_ctas;
-  if (!encode_pool_map(&p.tmap_k, k_pages, *shape) || !encode_pool_map(&p.tmap_v, v_pages, *shape))
-    return PA_ERR_CUDA;
-  st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
+  if (kv.int8()) {
+    if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
+      return PA_ERR_CUDA;
+    st = cuda_status(launch_split_q8(p, D, G, plan->num_ctas, s));
+  } else {
+    if (!encode_pool_map(&p.tmap_k, kv.k, *shape) || !encode_pool_map(&p.tmap_v, kv.v, *shape))
+      return PA_ERR_CUDA;
+    st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
+  }
   if (st != PA_OK || plan->num_groups == 0) return st;
 
   CombineParams c{};

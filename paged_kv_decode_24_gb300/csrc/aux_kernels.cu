@@ -1,11 +1,12 @@
-// Combine (log-sum-exp merge of split partials), KV append and the debug
-// gather-index export.
+// Combine (log-sum-exp merge of split partials), KV append (fp16 and INT8
+// caches) and the debug gather-index export.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "quant_common.cuh"
 
 namespace pa {
 
@@ -151,6 +152,53 @@ __global__ void append_kernel(const AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Append into the INT8 cache: one warp per (sequence, KV head) quantises the
+// new K and V rows (per-row INT8, quant_common.cuh) and writes their codes
+// and scales at position L-1.
+constexpr int kAppendWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_q8_kernel(const AppendQ8Params p) {
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)p.batch * p.num_kv_heads;
+  const int Lmax = p.max_pages * kPageSize;
+  for (long long r = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5); r < total;
+       r += (long long)gridDim.x * kAppendWarps) {
+    const int h = (int)(r % p.num_kv_heads);
+    const int b = (int)(r / p.num_kv_heads);
+    const int L = p.seq_lens[b];
+    if (L < 0 || L > Lmax) {
+      if (h == 0 && lane == 0) set_status(p.status, PA_DEV_BAD_SEQ_LEN);
+      continue;
+    }
+    if (L == 0) continue;
+    const int pos = L - 1;
+    const int page = p.block_table[(size_t)b * p.max_pages + pos / kPageSize];
+    if (page < 0 || page >= p.num_pages) {
+      if (h == 0 && lane == 0) set_status(p.status, PA_DEV_BAD_PAGE);
+      continue;
+    }
+    const size_t row = ((size_t)page * p.num_kv_heads + h) * kPageSize + pos % kPageSize;
+    const size_t src = ((size_t)b * p.num_kv_heads + h) * D;
+    float sk, sv;
+    const uint32_t ck = quantize_row_warp<D>(p.k_new + src, lane, sk);
+    const uint32_t cv = quantize_row_warp<D>(p.v_new + src, lane, sv);
+    if constexpr (PER == 4) {
+      reinterpret_cast<uint32_t*>(p.k_codes + row * D)[lane] = ck;
+      reinterpret_cast<uint32_t*>(p.v_codes + row * D)[lane] = cv;
+    } else {
+      reinterpret_cast<uint16_t*>(p.k_codes + row * D)[lane] = (uint16_t)ck;
+      reinterpret_cast<uint16_t*>(p.v_codes + row * D)[lane] = (uint16_t)cv;
+    }
+    if (lane == 0) {
+      p.k_scales[row] = sk;
+      p.v_scales[row] = sv;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Debug export of the gather map: slot = page * S + t % S, -1 past the end,
 // -2 for an invalid page index.
 __global__ void gather_slots_kernel(const int32_t* block_table, const int32_t* seq_lens,
@@ -209,6 +257,17 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaS
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const long long work = (long long)p.batch * p.num_kv_heads * (p.head_dim / 8);
   append_kernel<<<grid_for(work, 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream) {
+  const long long rows = (long long)p.batch * p.num_kv_heads;
+  long long g = (rows + kAppendWarps - 1) / kAppendWarps;
+  const int grid = (int)(g < 1 ? 1 : g > 152 * 16 ? 152 * 16 : g);
+  if (p.head_dim == 64)
+    append_q8_kernel<64><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  else
+    append_q8_kernel<128><<<grid, kAppendWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,8 +1,7 @@
 // CUDA-core split-decode kernel for head_dim 128, MHA (G = 1).
-#include <atomic>
-
 #include "decode_kernel.cuh"
 #include "launch.h"
+#include "split_launch.cuh"
 
 namespace pa {
 
@@ -14,34 +13,18 @@ cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int NSH = half_stages_for(D);
   constexpr int smem = kWarpsPerCta * warp_smem(D, G, NSH).bytes;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
-  auto kern = split_decode_kernel<D, G, kWarpsPerCta, NSH>;
   static std::atomic<unsigned long long> configured{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit);
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kWarpsPerCta * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  auto kern = split_decode_kernel<D, G, kWarpsPerCta, NSH>;
+  return launch_split_kernel(kern, smem, configured, p, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_split_d128(const SplitParams& p, int group, int grid, cudaStream_t stream) {
-  return group == 1 ? launch_g<1>(p, grid, stream) : cudaErrorInvalidValue;
+  switch (group) {
+    case 1: return launch_g<1>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace pa

@@ -78,6 +78,12 @@ struct SplitParams {
   int32_t num_shared;  // CTAs [0, num_shared) share a task; the rest run up to NW short tasks
   CUtensorMap tmap_k;  // pools as 4-D tensors [P][Hkv][16][D] for the TMA tensor copies
   CUtensorMap tmap_v;
+  // INT8 cache (split_decode_q8_kernel only): codes [P][Hkv][16][D] and
+  // per-row scales [P][Hkv][16]; the fused append writes them.
+  const int8_t* k_codes;
+  const int8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
 };
 
 template <int D, int G>

@@ -111,6 +111,19 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Shared-memory scalar loads by shared-window address (ld.shared, not the
+// generic path a pointer derived from dynamic shared memory would take).
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -33,8 +33,24 @@ struct AppendParams {
   int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
 };
 
+struct AppendQ8Params {
+  const __half* k_new;
+  const __half* v_new;
+  int8_t* k_codes;
+  int8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t* status;
+  int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
+};
+
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
                          cudaStream_t stream);
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const int32_t* block_table, const int32_t* seq_lens, int32_t* out,

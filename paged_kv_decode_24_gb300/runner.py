@@ -1,8 +1,9 @@
 """Device-side holder for one decode step's buffers, driving the C ABI.
 
 Moves a host workload into torch CUDA tensors once, then issues
-pa_kv_append / pa_plan / pa_plan_upload / pa_decode_attention through
-``binding``.  It holds no arithmetic of its own.
+pa_kv_append / pa_plan / pa_plan_upload / pa_decode_attention (and their
+INT8-cache forms when the workload carries one) through ``binding``.  It
+holds no arithmetic of its own.
 """
 
 from __future__ import annotations
@@ -26,6 +27,12 @@ class DeviceDecode:
         self.v_pages = t(w.v_pages)
         self.block_table = t(w.block_table)
         self.seq_lens = t(w.seq_lens)
+        self.q8 = w.k_codes is not None   # the workload also carries an INT8 cache
+        if self.q8:
+            self.k_codes = t(w.k_codes)
+            self.v_codes = t(w.v_codes)
+            self.k_scales = t(w.k_scales)
+            self.v_scales = t(w.v_scales)
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.shape = binding.shape_of(self.q, self.k_pages, self.block_table)
@@ -65,6 +72,30 @@ class DeviceDecode:
         binding.append_decode(self.shape, self.plan_obj, self.q, self.k_new, self.v_new,
                               self.k_pages, self.v_pages, self.block_table, self.seq_lens,
                               self.w.scale, dst, self.workspace, self.status)
+        return dst
+
+    def append_q8(self):
+        binding.append_q8(self.shape, self.k_new, self.v_new, self.k_codes, self.v_codes,
+                          self.k_scales, self.v_scales, self.block_table, self.seq_lens,
+                          self.status)
+
+    def decode_q8(self, out=None):
+        if self.plan_obj is None:
+            self.make_plan()
+        dst = self.out if out is None else out
+        binding.decode_q8(self.shape, self.plan_obj, self.q, self.k_codes, self.v_codes,
+                          self.k_scales, self.v_scales, self.block_table, self.seq_lens,
+                          self.w.scale, dst, self.workspace, self.status)
+        return dst
+
+    def append_decode_q8(self, out=None):
+        if self.plan_obj is None:
+            self.make_plan()
+        dst = self.out if out is None else out
+        binding.append_decode_q8(self.shape, self.plan_obj, self.q, self.k_new, self.v_new,
+                                 self.k_codes, self.v_codes, self.k_scales, self.v_scales,
+                                 self.block_table, self.seq_lens, self.w.scale, dst,
+                                 self.workspace, self.status)
         return dst
 
     def gather_slots(self):

@@ -1,0 +1,195 @@
+"""GPU parity of the INT8-cache path (pa_kv_append_q8, pa_decode_attention_q8,
+pa_append_decode_attention_q8) against the float64 oracle, through the C ABI.
+
+The append's codes and scales are compared bit for bit: both sides decide
+them with correctly rounded fp32 divisions.  Attention outputs use the fp16
+path's tolerance.
+"""
+
+from __future__ import annotations
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_decode_24_gb300 import binding, workloads
+from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.parity import assert_close
+from tests.test_gpu_parity import sample_heads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    return lib
+
+
+def oracle_q8(w, heads=None):
+    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
+                                         w.v_new, w.block_table, w.seq_lens)
+    out = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale,
+                                     heads=heads)
+    return out, (kc, vc, ks, vs)
+
+
+def gpu_q8(w, forced_splits=None, fused=False):
+    dd = DeviceDecode(w)
+    dd.make_plan(forced_splits=forced_splits)
+    if fused:
+        out = dd.append_decode_q8()
+    else:
+        dd.append_q8()
+        out = dd.decode_q8()
+    status = dd.read_status()
+    assert status == 0, f"device status {status:#x}"
+    return out.cpu().numpy(), dd
+
+
+def assert_pools_equal(dd, pools):
+    kc, vc, ks, vs = pools
+    assert np.array_equal(dd.k_codes.cpu().numpy(), kc)
+    assert np.array_equal(dd.v_codes.cpu().numpy(), vc)
+    assert np.array_equal(dd.k_scales.cpu().numpy().view(np.uint32), ks.view(np.uint32))
+    assert np.array_equal(dd.v_scales.cpu().numpy().view(np.uint32), vs.view(np.uint32))
+
+
+CASES = [
+    # (seq_lens, Hq, Hkv, D, forced splits, dist)
+    ([37, 100], 4, 2, 64, 1, ("uniform", 1.0)),
+    ([1, 2, 15, 16, 17, 31, 33, 64], 8, 8, 128, 0, ("normal", 0.5)),     # G = 1
+    ([5, 300, 129, 1000], 32, 8, 128, 0, ("normal", 0.5)),               # G = 4
+    ([777, 50, 1], 16, 2, 128, 3, ("normal", 1.0)),                      # G = 8
+    ([513, 257], 8, 1, 64, 5, ("uniform", 1.0)),                         # G = 8, D = 64
+    ([2000, 3, 640], 4, 4, 64, 0, ("normal", 0.5)),                      # G = 1, D = 64
+    ([96, 97, 1500], 16, 16, 128, 7, ("normal", 0.5)),
+    ([250, 16], 32, 16, 64, 2, ("normal", 0.5)),                         # G = 2, D = 64
+    ([300, 45, 1], 16, 8, 128, 0, ("normal", 0.5)),                      # G = 2
+]
+
+
+def _ids(c):
+    return f"L{c[0][:3]}_G{c[1] // c[2]}_D{c[3]}_s{c[4]}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_q8_parity_full(case):
+    lens, hq, hkv, d, splits, dist = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              dist=dist, seed=zlib.crc32(str(case).encode()) ^ 8,
+                              forced_splits=splits, kv="int8")
+    got, dd = gpu_q8(w)
+    want, pools = oracle_q8(w)
+    assert_close(got, want, f"q8 {case}")
+    assert_pools_equal(dd, pools)
+
+
+@pytest.mark.parametrize("case", CASES + [([16, 32, 1, 17], 8, 2, 128, 0, ("normal", 0.5)),
+                                          ([48, 9], 4, 4, 64, 3, ("uniform", 1.0))], ids=_ids)
+def test_q8_fused_append_decode(case):
+    """One launch gives the output and the pool bits of append then decode.
+    Unowned rows have NaN scales: a read of one would show in the output."""
+    lens, hq, hkv, d, splits, dist = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              dist=dist, seed=zlib.crc32(str(case).encode()) ^ 9,
+                              forced_splits=splits, poison=True, kv="int8")
+    got, dd = gpu_q8(w, fused=True)
+    want, pools = oracle_q8(w)
+    assert_close(got, want, f"q8 fused {case}")
+    # poisoned scales of unowned rows come back untouched (NaN == NaN bitwise)
+    assert_pools_equal(dd, pools)
+
+
+def test_q8_append_ties_and_zero_rows_bit_exact():
+    """New rows built from hand-worked values (exact ratios, half-way cases,
+    an all-zero row): codes and scales match the oracle bit for bit."""
+    D = 128
+    rows = [[127, -2.5, 3.5, 0.5, -0.5, 1.5, -126.5, 0], [63.5, 1.25, -0.75, 0.25],
+            [-254, 3, 5, 7], [-127, 126.625, -0.375, 64.5], [0, 0, 0, 0]]
+    w = workloads.make_custom(seq_lens=[3, 17, 40, 64, 1], num_q_heads=8, num_kv_heads=2,
+                              head_dim=D, seed=41, kv="int8")
+    rng = np.random.default_rng(42)
+    for b, r in enumerate(rows):
+        for h in range(2):
+            x = np.zeros(D, np.float16)
+            x[rng.permutation(D)[:len(r)]] = np.array(r, np.float16)
+            w.k_new[b, h] = x
+            w.v_new[b, h] = -x
+    dd = DeviceDecode(w)
+    dd.append_q8()
+    assert dd.read_status() == 0
+    _, pools = oracle_q8(w, heads=[])
+    assert_pools_equal(dd, pools)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_q8_benchmark_config(cfg):
+    w = workloads.make_config(cfg, kv="int8")
+    got, dd = gpu_q8(w, fused=True)
+    heads = sample_heads(w) if cfg != 2 else None
+    want, _ = oracle_q8(w, heads=heads)
+    if heads is None:
+        assert_close(got, want, f"q8 config {cfg}")
+    else:
+        idx = tuple(np.array(heads).T)
+        assert_close(got[idx], want[idx], f"q8 config {cfg} (sampled)")
+    assert np.all(np.isfinite(got.astype(np.float32)))
+
+
+def test_q8_page_permutation_bit_identical():
+    lens = [37, 400, 5, 129]
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=8, num_kv_heads=2, head_dim=128, seed=43,
+                              kv="int8")
+    ref, _ = gpu_q8(w)
+    w2 = workloads.make_custom(seq_lens=lens, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               seed=43, kv="int8")
+    perm = np.random.default_rng(44).permutation(w.num_pages)
+    for name in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        a = getattr(w2, name)
+        b = np.empty_like(a)
+        b[perm] = a
+        setattr(w2, name, b)
+    w2.block_table = np.where(w.block_table >= 0, perm[np.maximum(w.block_table, 0)],
+                              -1).astype(np.int32)
+    got, _ = gpu_q8(w2)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+
+
+def test_q8_split_matches_unsplit():
+    w = workloads.make_custom(seq_lens=[1500, 700, 33], num_q_heads=16, num_kv_heads=4,
+                              head_dim=128, seed=45, kv="int8")
+    want, _ = oracle_q8(w)
+    for s in (1, 2, 5, 16, 0):
+        got, _ = gpu_q8(w, forced_splits=s)
+        assert_close(got, want, f"q8 splits={s}")
+
+
+def test_q8_zero_length_and_single_token():
+    w = workloads.make_custom(seq_lens=[0, 1, 40, 0], num_q_heads=4, num_kv_heads=4, head_dim=64,
+                              seed=46, kv="int8")
+    got, _ = gpu_q8(w)
+    want, _ = oracle_q8(w)
+    assert np.all(got[0] == 0) and np.all(got[3] == 0)
+    assert_close(got, want, "zero and one token")
+
+
+def test_q8_bad_page_is_flagged_and_skipped():
+    w = workloads.make_custom(seq_lens=[40, 40], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                              seed=47, kv="int8")
+    w.block_table[0, 1] = w.num_pages + 7
+    dd = DeviceDecode(w)
+    dd.make_plan()
+    out = dd.decode_q8().cpu().numpy()
+    assert dd.read_status() & binding.PA_DEV_BAD_PAGE
+    assert np.all(np.isfinite(out.astype(np.float32)))
+    # sequence 1 is untouched by the bad entry (its new token was not appended)
+    kc, vc = w.k_codes, w.v_codes
+    want1 = oracle.decode_attention_q8(w.q, kc, vc, w.k_scales, w.v_scales, w.block_table,
+                                       w.seq_lens, w.scale, heads=[(1, h) for h in range(4)])
+    assert_close(out[1], want1[1], "sequence 1")
