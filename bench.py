@@ -76,10 +76,13 @@ def parse():
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
-                    help="KV-cache type: fp16, or INT8 codes with per-row fp32 scales")
+                    help="KV-cache type: 16-bit elements, or INT8 codes with per-row fp32 scales")
+    ap.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16",
+                    help="element type of q, K, V and out (the INT8 cache takes fp16)")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
                     help="per-layer KV caches; fewer only to shrink profiler captures")
-    return ap.parse_args()
+    args = ap.parse_args()
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -118,12 +121,12 @@ def oracle_sample(w, budget_s):
 
 def oracle_worker(args):
     from paged_kv_decode_24_gb300 import workloads
-    w = workloads.make_config(args.config, kv=args.kv)
+    w = workloads.make_config(args.config, kv=args.kv, dtype=args.dtype)
     dt, kv, desc = oracle_sample(w, args.cpu_seconds)
     print(json.dumps({"seconds": dt, "kv_bytes": kv, "sample": desc}))
 
 
-def run_oracle_subprocess(cfg, seconds, kv="fp16"):
+def run_oracle_subprocess(cfg, seconds, kv="fp16", dtype="fp16"):
     """The oracle in a fresh single-threaded process (started by exec, so no
     CUDA state is shared)."""
     env = dict(os.environ)
@@ -131,15 +134,15 @@ def run_oracle_subprocess(cfg, seconds, kv="fp16"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", "--config",
-                        str(cfg), "--cpu-seconds", str(seconds), "--kv", kv], capture_output=True,
-                       text=True,
+                        str(cfg), "--cpu-seconds", str(seconds), "--kv", kv, "--dtype", dtype],
+                       capture_output=True, text=True,
                        env=env, timeout=600)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     res = json.loads(r.stdout.strip().splitlines()[-1])
     gbs = res["kv_bytes"] / res["seconds"] / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"config {cfg} ({kv} cache): {res['sample']}, "
+            "sample": f"config {cfg} ({kv} cache, {dtype}): {res['sample']}, "
                       f"{res['seconds']:.1f} s of float64 numpy"}
 
 
@@ -166,7 +169,7 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_for(cfg, kv="fp16"):
+def traffic_for(cfg, kv="fp16", dtype="fp16"):
     """DRAM bytes per launch of the split kernel from a committed ncu capture,
     only while the kernel sources still hash to what was profiled."""
     try:
@@ -176,7 +179,8 @@ def traffic_for(cfg, kv="fp16"):
         return None
     if d.get("source_hash") != kernel_source_hash():
         return None
-    ent = d.get("configs", {}).get(str(cfg) if kv == "fp16" else f"{cfg}-{kv}")
+    key = "-".join([str(cfg)] + [x for x in (kv, dtype) if x != "fp16"])   # "4", "4-int8", "4-bf16"
+    ent = d.get("configs", {}).get(key)
     return None if ent is None else ent.get("dram_bytes_per_launch")
 
 
@@ -281,7 +285,8 @@ def run_ours(args):
     world, rank, local = dist_setup(args)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds, args.kv)  # before CUDA
+        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds, args.kv,
+                                         args.dtype)  # before any CUDA call
 
     _build.ensure_built()
     binding.load()
@@ -292,10 +297,12 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
 
     q8 = args.kv == "int8"
+    if q8 and args.dtype != "fp16":
+        raise SystemExit("the INT8 cache takes fp16 q/out")
     w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank,
-                              kv=args.kv)
+                              kv=args.kv, dtype=args.dtype)
     shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
-                               w.max_pages_per_seq, w.num_pages)
+                               w.max_pages_per_seq, w.num_pages, args.dtype)
     kv_bytes = w.kv_bytes_int8() if q8 else w.kv_bytes()
     dec_bytes = (accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.page_size, kv=args.kv)
@@ -304,15 +311,18 @@ def run_ours(args):
     lens_host = np.ascontiguousarray(w.seq_lens)
 
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    q = to_dev(w.q)
-    k_new = to_dev(w.k_new)
-    v_new = to_dev(w.v_new)
+    elem_t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    # bf16 workloads hold bf16-exact float32 values: the cast is exact
+    to_elem = lambda a: to_dev(a).to(elem_t)
+    q = to_elem(w.q)
+    k_new = to_elem(w.k_new)
+    v_new = to_elem(w.v_new)
     bt = to_dev(w.block_table)
     sl = to_dev(w.seq_lens)
     if q8:
         cache0 = (to_dev(w.k_codes), to_dev(w.v_codes), to_dev(w.k_scales), to_dev(w.v_scales))
     else:
-        cache0 = (to_dev(w.k_pages), to_dev(w.v_pages))
+        cache0 = (to_elem(w.k_pages), to_elem(w.v_pages))
     # One KV cache per layer, as in the model: every layer's pages are distinct
     # memory, so a layer's reads never hit what the previous layers left in L2.
     pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(LAYERS - 1)]
@@ -462,7 +472,9 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-        hq, hk, hv, hbt, hsl = pin(w.q), pin(w.k_new), pin(w.v_new), pin(w.block_table), pin(w.seq_lens)
+        pin_e = lambda a: pin(a).to(elem_t).pin_memory()
+        hq, hk, hv = pin_e(w.q), pin_e(w.k_new), pin_e(w.v_new)
+        hbt, hsl = pin(w.block_table), pin(w.seq_lens)
         hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(LAYERS)]
         nb = lambda t: t.numel() * t.element_size()
         side_in = torch.cuda.Stream(device=dev)
@@ -558,12 +570,13 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
-        "kv_cache": "int8 codes + fp32 row scales" if q8 else "fp16",
+        "dtype": "bf16" if args.dtype == "bf16" else "f16",
+        "kv_cache": "int8 codes + fp32 row scales" if q8 else args.dtype,
         "accumulate": "f32",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
         "config": {
-            "workload": w.name + (", INT8 KV cache (per-row scales)" if q8 else ""),
+            "workload": w.name + (", INT8 KV cache (per-row scales)" if q8 else "") +
+                        (", bf16" if args.dtype == "bf16" else ""),
             "config_id": args.config,
             "batch": w.batch,
             "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}",
@@ -594,7 +607,7 @@ def run_ours(args):
                            else "fallback 6800 GB/s (of fallback)",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_for(args.config, args.kv),
+            "traffic": traffic_for(args.config, args.kv, args.dtype),
             "algorithmic_bytes_per_launch": dec_bytes,
             "us_per_launch": round(dec_mean_ms * 1e3, 3),
             "us_per_launch_isolated": round(iso_us, 3),
@@ -626,7 +639,7 @@ def run_reference(args):
     if rank != 0:
         return
     from paged_kv_decode_24_gb300 import workloads
-    w = workloads.make_config(args.config, kv=args.kv)
+    w = workloads.make_config(args.config, kv=args.kv, dtype=args.dtype)
     # a bounded sample per step: the whole run stays within about two minutes
     per_step = min(2.0, max(0.2, 120.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
@@ -655,7 +668,8 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
         "config": {"workload": w.name + (", INT8 KV cache (per-row scales)"
-                                         if args.kv == "int8" else ""),
+                                         if args.kv == "int8" else "") +
+                               (", bf16" if args.dtype == "bf16" else ""),
                    "config_id": args.config},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {desc}, about {per_step:.2f} s"},

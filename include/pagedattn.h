@@ -88,7 +88,13 @@ typedef struct {
   int32_t page_size;         /* S: 16 */
   int32_t max_pages_per_seq; /* row length of block_table */
   int32_t num_pages;         /* P: pages in each pool */
+  int32_t dtype;             /* element type of q, k_new, v_new, the pools and out:
+                                PA_DTYPE_F16 (0, the default of a zeroed struct) or
+                                PA_DTYPE_BF16 (1); the INT8-cache calls take F16 only */
 } pa_shape_t;
+
+#define PA_DTYPE_F16 0
+#define PA_DTYPE_BF16 1
 
 /*
  * A plan: how one decode call splits the batch into warp tasks.

@@ -32,7 +32,12 @@ class PaShape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
-                ("num_pages", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+PA_DTYPE_F16 = 0
+PA_DTYPE_BF16 = 1
+DTYPES = {"fp16": PA_DTYPE_F16, "bf16": PA_DTYPE_BF16}
 
 
 class PaPlan(ctypes.Structure):
@@ -116,9 +121,11 @@ def _check(fn: str, code: int):
 
 
 def make_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
-               num_pages) -> PaShape:
+               num_pages, dtype="fp16") -> PaShape:
+    """pa_shape_t; dtype "fp16" or "bf16" (or the PA_DTYPE_* code)."""
+    code = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     return PaShape(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
-                   int(max_pages_per_seq), int(num_pages))
+                   int(max_pages_per_seq), int(num_pages), code)
 
 
 class Plan:
@@ -210,20 +217,29 @@ def _stream(stream=None):
 
 
 def shape_of(q, k_pages, block_table) -> PaShape:
+    torch = _torch()
     B, Hq, D = q.shape
     P, Hkv, S, D2 = k_pages.shape
     if D2 != D:
         raise ValueError("head_dim of q and k_pages differ")
-    return make_shape(B, Hq, Hkv, D, S, block_table.shape[1], P)
+    dtype = "bf16" if q.dtype == torch.bfloat16 else "fp16"
+    return make_shape(B, Hq, Hkv, D, S, block_table.shape[1], P, dtype)
+
+
+def _elem(shape):
+    """The torch element type of q, the pools, the new rows and out for this shape."""
+    torch = _torch()
+    return torch.bfloat16 if shape.dtype == PA_DTYPE_BF16 else torch.float16
 
 
 def append(shape, k_new, v_new, k_pages, v_pages, block_table, seq_lens, status, stream=None):
     torch = _torch()
     lib = load()
+    et = _elem(shape)
     _check("pa_kv_append", lib.pa_kv_append(
-        ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
-        _dev_ptr(v_new, torch.float16, "v_new"), _dev_ptr(k_pages, torch.float16, "k_pages"),
-        _dev_ptr(v_pages, torch.float16, "v_pages"), _dev_ptr(block_table, torch.int32, "block_table"),
+        ctypes.byref(shape), _dev_ptr(k_new, et, "k_new"),
+        _dev_ptr(v_new, et, "v_new"), _dev_ptr(k_pages, et, "k_pages"),
+        _dev_ptr(v_pages, et, "v_pages"), _dev_ptr(block_table, torch.int32, "block_table"),
         _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(status, torch.int32, "status"),
         _stream(stream)))
 
@@ -240,11 +256,12 @@ def decode(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens, scale,
            status, stream=None):
     torch = _torch()
     lib = load()
+    et = _elem(shape)
     _check("pa_decode_attention", lib.pa_decode_attention(
-        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
-        _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, et, "q"),
+        _dev_ptr(k_pages, et, "k_pages"), _dev_ptr(v_pages, et, "v_pages"),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
-        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        ctypes.c_float(scale), _dev_ptr(out, et, "out"),
         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
@@ -254,12 +271,13 @@ def append_decode(shape, plan: Plan, q, k_new, v_new, k_pages, v_pages, block_ta
     """pa_append_decode_attention: append the new token and attend, one launch."""
     torch = _torch()
     lib = load()
+    et = _elem(shape)
     _check("pa_append_decode_attention", lib.pa_append_decode_attention(
-        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
-        _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
-        _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, et, "q"),
+        _dev_ptr(k_new, et, "k_new"), _dev_ptr(v_new, et, "v_new"),
+        _dev_ptr(k_pages, et, "k_pages"), _dev_ptr(v_pages, et, "v_pages"),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
-        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        ctypes.c_float(scale), _dev_ptr(out, et, "out"),
         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
@@ -320,11 +338,12 @@ def decode_static(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens,
     """pa_decode_attention_static: decode with the library's own scratch array."""
     torch = _torch()
     lib = load()
+    et = _elem(shape)
     _check("pa_decode_attention_static", lib.pa_decode_attention_static(
-        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
-        _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, et, "q"),
+        _dev_ptr(k_pages, et, "k_pages"), _dev_ptr(v_pages, et, "v_pages"),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
-        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        ctypes.c_float(scale), _dev_ptr(out, et, "out"),
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
 
@@ -366,9 +385,10 @@ class Prepared:
 def prepare_append(shape, k_new, v_new, k_pages, v_pages, block_table, seq_lens, status,
                    stream=None) -> Prepared:
     torch = _torch()
-    args = [ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
-            _dev_ptr(v_new, torch.float16, "v_new"), _dev_ptr(k_pages, torch.float16, "k_pages"),
-            _dev_ptr(v_pages, torch.float16, "v_pages"),
+    et = _elem(shape)
+    args = [ctypes.byref(shape), _dev_ptr(k_new, et, "k_new"),
+            _dev_ptr(v_new, et, "v_new"), _dev_ptr(k_pages, et, "k_pages"),
+            _dev_ptr(v_pages, et, "v_pages"),
             _dev_ptr(block_table, torch.int32, "block_table"),
             _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(status, torch.int32, "status"),
             _stream(stream)]
@@ -379,11 +399,12 @@ def prepare_append(shape, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
 def prepare_decode(shape, plan: Plan, q, k_pages, v_pages, block_table, seq_lens, scale, out,
                    workspace, status, stream=None) -> Prepared:
     torch = _torch()
-    args = [ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
-            _dev_ptr(k_pages, torch.float16, "k_pages"), _dev_ptr(v_pages, torch.float16, "v_pages"),
+    et = _elem(shape)
+    args = [ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, et, "q"),
+            _dev_ptr(k_pages, et, "k_pages"), _dev_ptr(v_pages, et, "v_pages"),
             _dev_ptr(block_table, torch.int32, "block_table"),
             _dev_ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale),
-            _dev_ptr(out, torch.float16, "out"), _dev_ptr(workspace, torch.uint8, "workspace"),
+            _dev_ptr(out, et, "out"), _dev_ptr(workspace, torch.uint8, "workspace"),
             ctypes.c_size_t(workspace.numel()), _dev_ptr(status, torch.int32, "status"),
             _stream(stream)]
     return Prepared("pa_decode_attention", args, (shape, plan, q, k_pages, v_pages, block_table,

@@ -15,11 +15,14 @@
 
 namespace pa {
 
-cudaError_t launch_split_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
-cudaError_t launch_split_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
-
-cudaError_t launch_split_tc_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
-cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_d64(const SplitParams& p, int group, int dtype, int grid,
+                             cudaStream_t stream);
+cudaError_t launch_split_d128(const SplitParams& p, int group, int dtype, int grid,
+                              cudaStream_t stream);
+cudaError_t launch_split_tc_d64(const SplitParams& p, int group, int dtype, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int dtype, int grid,
+                                 cudaStream_t stream);
 cudaError_t launch_split_q8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
 cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
 
@@ -27,14 +30,14 @@ cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int grid, cuda
 // keeps up with HBM.  With G >= 2 query heads per KV head the CUDA-core kernel
 // becomes issue-bound (about 900 instructions per page at G = 4), so those
 // groups go to the tensor-core kernel.
-cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
+cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream) {
   if (group == 1) {
-    if (head_dim == 64) return launch_split_d64(p, group, grid, stream);
-    if (head_dim == 128) return launch_split_d128(p, group, grid, stream);
+    if (head_dim == 64) return launch_split_d64(p, group, dtype, grid, stream);
+    if (head_dim == 128) return launch_split_d128(p, group, dtype, grid, stream);
   } else {
-    if (head_dim == 64) return launch_split_tc_d64(p, group, grid, stream);
-    if (head_dim == 128) return launch_split_tc_d128(p, group, grid, stream);
+    if (head_dim == 64) return launch_split_tc_d64(p, group, dtype, grid, stream);
+    if (head_dim == 128) return launch_split_tc_d128(p, group, dtype, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -65,8 +68,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A pool [P][Hkv][16][D] fp16 as a 4-D tensor, innermost first, with boxes of
-// 64 halves x 16 rows and the 128-byte swizzle.
+// A pool [P][Hkv][16][D] of 16-bit elements as a 4-D tensor, innermost
+// first, with boxes of 64 elements x 16 rows and the 128-byte swizzle.
 static bool encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape_t& s) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
@@ -76,7 +79,9 @@ static bool encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape_t
   cuuint64_t strides[3] = {D * 2, D * 2 * kPageSize, D * 2 * kPageSize * s.num_kv_heads};
   cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(pool), dims, strides, box,
+  const CUtensorMapDataType ty = s.dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(map, ty, 4, const_cast<void*>(pool), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -122,7 +127,9 @@ extern "C" const char* pa_status_string(pa_status_t status) {
   switch (status) {
     case PA_OK: return "ok";
     case PA_ERR_INVALID_ARG: return "invalid argument";
-    case PA_ERR_UNSUPPORTED: return "unsupported shape (head_dim 64/128, page_size 16, Hq/Hkv in 1,2,4,8)";
+    case PA_ERR_UNSUPPORTED:
+      return "unsupported shape (head_dim 64/128, page_size 16, Hq/Hkv in 1,2,4,8, "
+             "dtype f16/bf16; INT8 cache f16 only)";
     case PA_ERR_WORKSPACE: return "workspace smaller than the plan requires";
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_DEVICE_OOB: return "device detected an out-of-range index";
@@ -170,6 +177,7 @@ extern "C" pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_ne
   using namespace pa;
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
+  if (shape->dtype != PA_DTYPE_F16) return PA_ERR_UNSUPPORTED;
   if (shape->batch == 0) return PA_OK;
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_codes, 16) ||
       !aligned(v_codes, 16) || !aligned(k_scales, 16) || !aligned(v_scales, 16) ||
@@ -297,6 +305,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
     return PA_ERR_INVALID_ARG;
   if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  if (kv.int8() && shape->dtype != PA_DTYPE_F16) return PA_ERR_UNSUPPORTED;
 
   const int G = shape->num_q_heads / shape->num_kv_heads;
   const int D = shape->head_dim;
@@ -305,21 +314,21 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   cudaStream_t s = (cudaStream_t)stream;
 
   SplitParams p{};
-  p.q = (const __half*)q;
+  p.q = q;
   if (kv.int8()) {
     p.k_codes = (const int8_t*)kv.k;
     p.v_codes = (const int8_t*)kv.v;
     p.k_scales = kv.k_scales;
     p.v_scales = kv.v_scales;
   } else {
-    p.k_pages = (const __half*)kv.k;
-    p.v_pages = (const __half*)kv.v;
+    p.k_pages = kv.k;
+    p.v_pages = kv.v;
   }
-  p.k_new = (const __half*)k_new;
-  p.v_new = (const __half*)v_new;
+  p.k_new = k_new;
+  p.v_new = v_new;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
-  p.out = (__half*)out;
+  p.out = out;
   p.ws_header = (const int32_t*)ws;
   p.items = (const int4*)(ws + lay.items_off);
   p.item_slots = (const int32_t*)(ws + lay.slots_off);
@@ -344,7 +353,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   } else {
     if (!encode_pool_map(&p.tmap_k, kv.k, *shape) || !encode_pool_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;
-    st = cuda_status(launch_split(p, D, G, plan->num_ctas, s));
+    st = cuda_status(launch_split(p, D, G, shape->dtype, plan->num_ctas, s));
   }
   if (st != PA_OK || plan->num_groups == 0) return st;
 
@@ -353,14 +362,14 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   c.groups = (const int4*)(ws + lay.groups_off);
   c.part_lse = p.part_lse;
   c.part_o = p.part_o;
-  c.out = (__half*)out;
+  c.out = out;
   c.status = dev_status;
   c.group_size = G;
   c.num_q_heads = shape->num_q_heads;
   c.num_items = p.num_items;
   c.num_groups = p.num_groups;
   c.num_split_items = p.num_split_items;
-  return cuda_status(launch_combine(c, D, plan->num_groups * G, s));
+  return cuda_status(launch_combine(c, D, shape->dtype, plan->num_groups * G, s));
 }
 
 }  // namespace

@@ -5,6 +5,7 @@
 #include <math.h>
 
 #include "device_common.cuh"
+#include "elem.cuh"
 #include "launch.h"
 #include "quant_common.cuh"
 
@@ -23,7 +24,7 @@ namespace pa {
 // kernel; after it, one round of loads brings every partial a warp needs.
 constexpr int kCombineWarps = 8;
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
   constexpr int DPL = D / 32;
   __shared__ float sm_m[kCombineWarps], sm_z[kCombineWarps];
@@ -114,8 +115,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
       }
     }
     const float r = Z > 0.f ? O / Z : 0.f;
-    p.out[((size_t)grp.x * p.num_q_heads + (size_t)grp.y * G + j) * D + threadIdx.x] =
-        __float2half_rn(r);
+    static_cast<T*>(p.out)[((size_t)grp.x * p.num_q_heads + (size_t)grp.y * G + j) * D +
+                           threadIdx.x] = Elem<T>::from_f(r);
   }
 }
 
@@ -239,7 +240,8 @@ static int grid_for(long long work, int threads) {
   return (int)g;
 }
 
-cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,
+                           cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kCombineWarps * 32);
@@ -250,8 +252,12 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+  if (dtype == PA_DTYPE_BF16) {
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, p);
+  }
+  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, combine_kernel<__half, 64>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<__half, 128>, p);
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {

@@ -1,4 +1,4 @@
-// CUDA-core split-decode kernel for head_dim 64, MHA (G = 1).
+// CUDA-core split-decode kernel for head_dim 64, MHA (G = 1), fp16 and bf16.
 #include "decode_kernel.cuh"
 #include "launch.h"
 #include "split_launch.cuh"
@@ -7,24 +7,30 @@ namespace pa {
 
 namespace {
 
-template <int G>
+template <typename T, int G>
 cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int D = 64;
   constexpr int NSH = half_stages_for(D);
   constexpr int smem = kWarpsPerCta * warp_smem(D, G, NSH).bytes;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
   static std::atomic<unsigned long long> configured{0};
-  auto kern = split_decode_kernel<D, G, kWarpsPerCta, NSH>;
+  auto kern = split_decode_kernel<T, D, G, kWarpsPerCta, NSH>;
   return launch_split_kernel(kern, smem, configured, p, grid, stream);
+}
+
+template <typename T>
+cudaError_t launch_t(const SplitParams& p, int group, int grid, cudaStream_t stream) {
+  switch (group) {
+    case 1: return launch_g<T, 1>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_split_d64(const SplitParams& p, int group, int grid, cudaStream_t stream) {
-  switch (group) {
-    case 1: return launch_g<1>(p, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_split_d64(const SplitParams& p, int group, int dtype, int grid, cudaStream_t stream) {
+  if (dtype == PA_DTYPE_BF16) return launch_t<__nv_bfloat16>(p, group, grid, stream);
+  return launch_t<__half>(p, group, grid, stream);
 }
 
 }  // namespace pa

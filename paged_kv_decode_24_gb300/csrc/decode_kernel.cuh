@@ -53,19 +53,22 @@
 #include <math.h>
 
 #include "device_common.cuh"
+#include "elem.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
+// Element pointers (q, pools, new rows, out) hold the kernel's element type
+// (fp16 or bf16; fp16 for the INT8-cache kernel's q, new rows and out).
 struct SplitParams {
-  const __half* q;
-  const __half* k_pages;
-  const __half* v_pages;
-  const __half* k_new;  // non-null: append the new token (fused pa_kv_append)
-  const __half* v_new;
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const void* k_new;  // non-null: append the new token (fused pa_kv_append)
+  const void* v_new;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  __half* out;
+  void* out;
   const int32_t* ws_header;
   const int4* items;
   const int32_t* item_slots;  // partial slot of each task, -1 = direct output
@@ -148,12 +151,6 @@ __device__ __forceinline__ float2 fmul2s(float2 a, float s) {
   return d;
 }
 
-__device__ __forceinline__ void half8_to_float2x4(const uint4& raw, float2* f) {
-  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) f[e] = __half22float2(h2[e]);
-}
-
 // Shared memory of one warp (bytes); the CTA holds NW of these.
 template <int D, int G, int NSH>
 struct WarpLayout {
@@ -174,7 +171,7 @@ struct MinCtas {
   static constexpr int value = G <= 4 ? 4 : 2;
 };
 
-template <int D, int G, int NW, int NSH>
+template <typename T, int D, int G, int NW, int NSH>
 __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     split_decode_kernel(const SplitParams p) {
   using Geo = Geometry<D, G>;
@@ -256,16 +253,17 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   // Fused append: k_app is this warp's page index that holds position L-1,
   // or -1.  The new K and V rows are staged in this warp's shared memory now.
   int k_app = -1;
-  __half* nrow = reinterpret_cast<__half*>(ws + L::NROW);  // [2][D]: K row, V row
+  T* nrow = reinterpret_cast<T*>(ws + L::NROW);  // [2][D]: K row, V row
   if (p.k_new != nullptr && seq_len > 0) {
     const int j_app = (seq_len - 1) / kPageSize - pg0;
     if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
       k_app = (j_app - pstart) / pstride;
       const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
       for (int i = lane; i < D / 8; i += 32) {
-        reinterpret_cast<uint4*>(nrow)[i] = __ldg(reinterpret_cast<const uint4*>(p.k_new + src) + i);
+        reinterpret_cast<uint4*>(nrow)[i] =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
         reinterpret_cast<uint4*>(nrow + D)[i] =
-            __ldg(reinterpret_cast<const uint4*>(p.v_new + src) + i);
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
       }
       __syncwarp();
     }
@@ -274,14 +272,14 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
   float2 qf[G][Geo::CH * 4];
   {
-    const __half* qb = p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
+    const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int ch = 0; ch < Geo::CH; ++ch) {
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * D + ch * 64 + c * 8));
         float2 f[4];
-        half8_to_float2x4(raw, f);
+        elem8_to_float2x4<T>(raw, f);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           qf[h][ch * 4 + e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
@@ -290,8 +288,8 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages + pg0;
   const size_t page_stride = (size_t)p.num_kv_heads * kPageSize * D;  // halves
-  const __half* kbase = p.k_pages + (size_t)kvh * kPageSize * D;
-  const __half* vbase = p.v_pages + (size_t)kvh * kPageSize * D;
+  const T* kbase = static_cast<const T*>(p.k_pages) + (size_t)kvh * kPageSize * D;
+  const T* vbase = static_cast<const T*>(p.v_pages) + (size_t)kvh * kPageSize * D;
   const uint64_t policy = l2_evict_first_policy();
 
   // Block-table entries of the task, 32 per window: lane k of the current
@@ -327,7 +325,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       page_ids[s] = phys;
       fence_proxy_async_smem();
       if (phys >= 0) {
-        const __half* src = ((hi & 1) ? vbase : kbase) + (size_t)phys * page_stride;
+        const T* src = ((hi & 1) ? vbase : kbase) + (size_t)phys * page_stride;
         mbar_arrive_expect_tx(bar, L::TILE);
         bulk_g2s(ws_u32 + L::RING + s * L::TILE, src, L::TILE, bar, policy);
       } else {
@@ -367,7 +365,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     const bool append_here = (k == k_app) && phys >= 0;
     const int r_app = (seq_len - 1) % kPageSize;
     if (append_here) {
-      __half* row = reinterpret_cast<__half*>(ws + L::RING + sk * L::TILE) + r_app * D;
+      T* row = reinterpret_cast<T*>(ws + L::RING + sk * L::TILE) + r_app * D;
       for (int i = lane; i < D / 8; i += 32)
         reinterpret_cast<uint4*>(row)[i] = reinterpret_cast<const uint4*>(nrow)[i];
       __syncwarp();
@@ -375,7 +373,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 
     if (nvalid > 0) {
       // ---- scores of the page's 16 tokens for the G heads
-      const __half* Ks = reinterpret_cast<const __half*>(ws + L::RING + sk * L::TILE);
+      const T* Ks = reinterpret_cast<const T*>(ws + L::RING + sk * L::TILE);
       float v[Geo::NV];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -387,7 +385,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
         for (int ch = 0; ch < Geo::CH; ++ch) {
           const uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * D + ch * 64 + c * 8);
           float2 kf[4];
-          half8_to_float2x4(raw, kf);
+          elem8_to_float2x4<T>(raw, kf);
 #pragma unroll
           for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -440,13 +438,13 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       break;
     }
     if (append_here) {
-      __half* row = reinterpret_cast<__half*>(ws + L::RING + sv * L::TILE) + r_app * D;
+      T* row = reinterpret_cast<T*>(ws + L::RING + sv * L::TILE) + r_app * D;
       for (int i = lane; i < D / 8; i += 32)
         reinterpret_cast<uint4*>(row)[i] = reinterpret_cast<const uint4*>(nrow + D)[i];
       // both copies of this page have landed, so the pool rows can be written
       const size_t dst = (((size_t)phys * p.num_kv_heads + kvh) * kPageSize + r_app) * D;
-      uint4* kw = reinterpret_cast<uint4*>(const_cast<__half*>(p.k_pages) + dst);
-      uint4* vw = reinterpret_cast<uint4*>(const_cast<__half*>(p.v_pages) + dst);
+      uint4* kw = reinterpret_cast<uint4*>(static_cast<T*>(const_cast<void*>(p.k_pages)) + dst);
+      uint4* vw = reinterpret_cast<uint4*>(static_cast<T*>(const_cast<void*>(p.v_pages)) + dst);
       for (int i = lane; i < D / 8; i += 32) {
         kw[i] = reinterpret_cast<const uint4*>(nrow)[i];
         vw[i] = reinterpret_cast<const uint4*>(nrow + D)[i];
@@ -468,7 +466,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 #pragma unroll
           for (int e = 0; e < Geo::DPL / 2; ++e) acc[h][e] = fmul2s(acc[h][e], al[h]);
       }
-      const __half* Vs = reinterpret_cast<const __half*>(ws + L::RING + sv * L::TILE);
+      const T* Vs = reinterpret_cast<const T*>(ws + L::RING + sv * L::TILE);
       auto pv_row = [&](int t) {
         float2 pp[G];
         if constexpr (G >= 2) {
@@ -484,10 +482,10 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
         float2 vf[Geo::DPL / 2];
         if constexpr (Geo::DPL == 4) {
           const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
-          vf[0] = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-          vf[1] = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+          vf[0] = Elem<T>::to_f2(raw.x);
+          vf[1] = Elem<T>::to_f2(raw.y);
         } else {
-          vf[0] = __half22float2(*reinterpret_cast<const __half2*>(Vs + t * D + lane * 2));
+          vf[0] = Elem<T>::to_f2(*reinterpret_cast<const uint32_t*>(Vs + t * D + lane * 2));
         }
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -551,16 +549,15 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       const float mh = __shfl_sync(kFull, m_run, rep);
       const float inv = lh > 0.f ? 1.f / lh : 0.f;
       if (!is_split) {
-        __half* dst = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + lane * Geo::DPL;
+        T* dst = static_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D +
+                 lane * Geo::DPL;
         if constexpr (Geo::DPL == 4) {
-          const __half2 a = __floats2half2_rn(o[h][0] * inv, o[h][1] * inv);
-          const __half2 bb = __floats2half2_rn(o[h][2] * inv, o[h][3] * inv);
           uint2 wv;
-          wv.x = *reinterpret_cast<const uint32_t*>(&a);
-          wv.y = *reinterpret_cast<const uint32_t*>(&bb);
+          wv.x = Elem<T>::from_f2(o[h][0] * inv, o[h][1] * inv);
+          wv.y = Elem<T>::from_f2(o[h][2] * inv, o[h][3] * inv);
           *reinterpret_cast<uint2*>(dst) = wv;
         } else {
-          *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(o[h][0] * inv, o[h][1] * inv);
+          *reinterpret_cast<uint32_t*>(dst) = Elem<T>::from_f2(o[h][0] * inv, o[h][1] * inv);
         }
       } else {
         float* dst = p.part_o + ((size_t)slot * G + h) * D + lane * Geo::DPL;
@@ -610,7 +607,8 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     }
     const float r = Z > 0.f ? O / Z : 0.f;
     if (!is_split) {
-      p.out[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] = __float2half_rn(r);
+      static_cast<T*>(p.out)[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] =
+          Elem<T>::from_f(r);
     } else {
       p.part_o[((size_t)slot * G + h) * D + d] = r;
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;

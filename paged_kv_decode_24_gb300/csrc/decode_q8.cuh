@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
       k_app = (j_app - pstart) / pstride;
       const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
       float sk, sv;
-      const uint32_t ck = quantize_row_warp<D>(p.k_new + src, lane, sk);
-      const uint32_t cv = quantize_row_warp<D>(p.v_new + src, lane, sv);
+      const uint32_t ck = quantize_row_warp<D>(static_cast<const __half*>(p.k_new) + src, lane, sk);
+      const uint32_t cv = quantize_row_warp<D>(static_cast<const __half*>(p.v_new) + src, lane, sv);
       if constexpr (D == 128) {
         reinterpret_cast<uint32_t*>(nrow)[lane] = ck;
         reinterpret_cast<uint32_t*>(nrow + D)[lane] = cv;
@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
   uint32_t qb[KSTEPS][2];
   float cb0, cb1;
   {
-    const __half* qrow = p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
+    const __half* qrow =
+        static_cast<const __half*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       if (g < G) {
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
     __syncwarp();
     if (!is_split) {
-      __half* dst = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
+      __half* dst = static_cast<__half*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
       for (int i = lane * 2; i < G * D; i += 64)
         *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(stage[i], stage[i + 1]);
     } else {
@@ -588,7 +589,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
     const float r = Z > 0.f ? O / Z : 0.f;
     if (!is_split) {
-      p.out[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] = __float2half_rn(r);
+      static_cast<__half*>(p.out)[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] =
+          __float2half_rn(r);
     } else {
       p.part_o[((size_t)slot * G + h) * D + d] = r;
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;

@@ -33,6 +33,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "decode_kernel.cuh"
 #include "device_common.cuh"
 #include "pa_internal.h"
@@ -63,14 +65,24 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// D += A . B for one m16n8k16 tile, fp16 inputs, fp32 accumulators.
+// D += A . B for one m16n8k16 tile, fp32 accumulators; A and B both fp16
+// (T = __half) or both bf16 (T = __nv_bfloat16).
+template <typename T = __half>
 __device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (std::is_same<T, __half>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -103,7 +115,7 @@ struct TcLayout {
   static constexpr int BYTES = FLAG + 16 + 1024;      // + slack to align the base to 1024
 };
 
-template <int D, int G, int NW, int NSH>
+template <typename T, int D, int G, int NW, int NSH>
 __global__ void __launch_bounds__(NW * 32, 4)
     split_decode_tc_kernel(const __grid_constant__ SplitParams p) {
   static_assert(G <= 8, "the mma tile holds at most 8 query heads");
@@ -122,7 +134,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
   unsigned char* extra = base + L::RINGS + warp * L::EXTRA;
   const uint32_t bars = smem_u32(extra) + L::BARS;
   int* page_ids = reinterpret_cast<int*>(extra + L::PAGES);
-  __half* nrow = reinterpret_cast<__half*>(extra + L::NROW);
+  T* nrow = reinterpret_cast<T*>(extra + L::NROW);
   int* cta_failed = reinterpret_cast<int*>(base + L::FLAG);
 
   if ((int)blockIdx.x >= p.num_ctas) return;  // whole CTA
@@ -196,9 +208,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
       k_app = (j_app - pstart) / pstride;
       const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
       for (int i = lane; i < D / 8; i += 32) {
-        reinterpret_cast<uint4*>(nrow)[i] = __ldg(reinterpret_cast<const uint4*>(p.k_new + src) + i);
+        reinterpret_cast<uint4*>(nrow)[i] =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
         reinterpret_cast<uint4*>(nrow + D)[i] =
-            __ldg(reinterpret_cast<const uint4*>(p.v_new + src) + i);
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
       }
       __syncwarp();
     }
@@ -208,7 +221,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
   // rows = dims.  Heads past G are zero.
   uint32_t qb[KSTEPS][2];
   {
-    const __half* qrow = p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
+    const T* qrow =
+        static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       if (g < G) {
@@ -315,7 +329,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
         const int chunk = (kk & 3) * 2 + (lane >> 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(ktile + (kk >> 2) * 2048 + swz(kr, chunk), a0, a1, a2, a3);
-        mma_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        mma_16816<T>(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
       float s0 = c[0] * qs, s1 = c[1] * qs, s2 = c[2] * qs, s3 = c[3] * qs;
       if (g >= nvalid) s0 = s1 = -INFINITY;
@@ -340,12 +354,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
       m_run[0] = nA;
       m_run[1] = nB;
       rescale = __any_sync(kFull, al0 != 1.f || al1 != 1.f);
-      // ---- P^T into B fragments, hi and lo fp16 parts
-      const uint32_t h01 = pack_half2(p0, p1);  // token g: heads 2t, 2t+1
-      const uint32_t h23 = pack_half2(p2, p3);  // token g+8
-      const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
-      const uint32_t l01 = pack_half2(p0 - f01.x, p1 - f01.y);
-      const uint32_t l23 = pack_half2(p2 - f23.x, p3 - f23.y);
+      // ---- P^T into B fragments, hi and lo parts in the element type
+      const uint32_t h01 = Elem<T>::from_f2(p0, p1);  // token g: heads 2t, 2t+1
+      const uint32_t h23 = Elem<T>::from_f2(p2, p3);  // token g+8
+      const float2 f01 = Elem<T>::to_f2(h01), f23 = Elem<T>::to_f2(h23);
+      const uint32_t l01 = Elem<T>::from_f2(p0 - f01.x, p1 - f01.y);
+      const uint32_t l23 = Elem<T>::from_f2(p2 - f23.x, p3 - f23.y);
       pb_hi0 = __byte_perm(__shfl_sync(kFull, h01, src1), __shfl_sync(kFull, h01, src2), perm);
       pb_hi1 = __byte_perm(__shfl_sync(kFull, h23, src1), __shfl_sync(kFull, h23, src2), perm);
       pb_lo0 = __byte_perm(__shfl_sync(kFull, l01, src1), __shfl_sync(kFull, l01, src2), perm);
@@ -371,8 +385,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
       }
       // both copies of this page have landed, so the pool rows can be written
       const size_t dst = (((size_t)phys * p.num_kv_heads + kvh) * kPageSize + r_app) * D;
-      uint4* kw = reinterpret_cast<uint4*>(const_cast<__half*>(p.k_pages) + dst);
-      uint4* vw = reinterpret_cast<uint4*>(const_cast<__half*>(p.v_pages) + dst);
+      uint4* kw = reinterpret_cast<uint4*>(static_cast<T*>(const_cast<void*>(p.k_pages)) + dst);
+      uint4* vw = reinterpret_cast<uint4*>(static_cast<T*>(const_cast<void*>(p.v_pages)) + dst);
       for (int i = lane; i < D / 8; i += 32) {
         kw[i] = reinterpret_cast<const uint4*>(nrow)[i];
         vw[i] = reinterpret_cast<const uint4*>(nrow + D)[i];
@@ -407,8 +421,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
           a2 &= mk8;
           a3 &= mk8;
         }
-        mma_16816(o[mt], a0, a1, a2, a3, pb_hi0, pb_hi1);
-        mma_16816(o[mt], a0, a1, a2, a3, pb_lo0, pb_lo1);
+        mma_16816<T>(o[mt], a0, a1, a2, a3, pb_hi0, pb_hi1);
+        mma_16816<T>(o[mt], a0, a1, a2, a3, pb_lo0, pb_lo1);
       }
     }
     __syncwarp();
@@ -466,9 +480,9 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
     __syncwarp();
     if (!is_split) {
-      __half* dst = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
+      T* dst = static_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
       for (int i = lane * 2; i < G * D; i += 64)
-        *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(stage[i], stage[i + 1]);
+        *reinterpret_cast<uint32_t*>(dst + i) = Elem<T>::from_f2(stage[i], stage[i + 1]);
     } else {
       float* dst = p.part_o + (size_t)slot * G * D;
       for (int i = lane * 4; i < G * D; i += 128)
@@ -523,7 +537,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
     }
     const float r = Z > 0.f ? O / Z : 0.f;
     if (!is_split) {
-      p.out[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] = __float2half_rn(r);
+      static_cast<T*>(p.out)[((size_t)b * p.num_q_heads + (size_t)kvh * G + h) * D + d] =
+          Elem<T>::from_f(r);
     } else {
       p.part_o[((size_t)slot * G + h) * D + d] = r;
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;

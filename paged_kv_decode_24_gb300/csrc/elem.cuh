@@ -1,0 +1,51 @@
+// The 16-bit element types of q, K, V and out: fp16 and bf16.  Kernels take
+// the type as a template parameter and convert through Elem<T>; every
+// product accumulates in fp32 and the output is rounded to nearest even.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace pa {
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__half> {
+  // two packed elements (low first) -> fp32 pair
+  static __device__ __forceinline__ float2 to_f2(uint32_t v) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  }
+  // fp32 pair -> two packed elements, each rounded to nearest even
+  static __device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 to_f2(uint32_t v) {
+    // a bf16 is the top half of an fp32: widening is a shift
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  }
+  static __device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Eight packed elements (one 16-byte load) -> four fp32 pairs.
+template <typename T>
+__device__ __forceinline__ void elem8_to_float2x4(const uint4& raw, float2* f) {
+  f[0] = Elem<T>::to_f2(raw.x);
+  f[1] = Elem<T>::to_f2(raw.y);
+  f[2] = Elem<T>::to_f2(raw.z);
+  f[3] = Elem<T>::to_f2(raw.w);
+}
+
+}  // namespace pa

@@ -1,4 +1,6 @@
 // Kernel parameter blocks and launchers (host <-> device glue, internal).
+// Append and combine work for both 16-bit element types: the append copies
+// rows bit for bit, and the combine's output type is chosen at launch.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -15,7 +17,7 @@ struct CombineParams {
   const int4* groups;
   const float* part_lse;
   const float* part_o;
-  __half* out;
+  void* out;  // fp16 or bf16, as the launch's dtype
   int32_t* status;
   int32_t group_size;
   int32_t num_q_heads;
@@ -46,12 +48,13 @@ struct AppendQ8Params {
   int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
 };
 
-cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int grid,
+cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
 cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
                             cudaStream_t stream);
 cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int head_dim, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const int32_t* block_table, const int32_t* seq_lens, int32_t* out,
                           int32_t* status, int batch, int max_pages, int num_pages,

@@ -30,6 +30,7 @@ pa_status_t check_shape(const pa_shape_t* s) {
   if (s->head_dim != 64 && s->head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (s->page_size != kPageSize) return PA_ERR_UNSUPPORTED;
   if (s->num_kv_heads > (int)kItemHeadMask) return PA_ERR_UNSUPPORTED;
+  if (s->dtype != PA_DTYPE_F16 && s->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
   if ((int64_t)s->max_pages_per_seq * s->page_size > INT32_MAX) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }

@@ -19,12 +19,22 @@ class DeviceDecode:
         self.torch = torch
         self.w = w
         self.device = torch.device(device)
-        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
-        self.q = t(w.q)
-        self.k_new = t(w.k_new)
-        self.v_new = t(w.v_new)
-        self.k_pages = t(w.k_pages)
-        self.v_pages = t(w.v_pages)
+        elem = torch.bfloat16 if getattr(w, "dtype", "fp16") == "bf16" else None
+
+        def t(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
+
+        def te(a):
+            # element arrays; bf16 workloads hold bf16-exact float32 values, so
+            # the cast is exact
+            x = t(a)
+            return x.to(elem) if elem is not None else x
+
+        self.q = te(w.q)
+        self.k_new = te(w.k_new)
+        self.v_new = te(w.v_new)
+        self.k_pages = te(w.k_pages)
+        self.v_pages = te(w.v_pages)
         self.block_table = t(w.block_table)
         self.seq_lens = t(w.seq_lens)
         self.q8 = w.k_codes is not None   # the workload also carries an INT8 cache

@@ -18,7 +18,10 @@ GQA; 16-token pages):
                   32768-token sequence (last), N(0, 0.5)
 
 Conventions (the plainest readings of the workload descriptions):
-  * "N(0, s)" means standard deviation s; draws are float32, rounded to fp16.
+  * "N(0, s)" means standard deviation s; draws are float32, rounded to fp16
+    (or, with ``dtype="bf16"``, rounded to nearest-even bf16 and kept as
+    float32 arrays whose values are exactly those bf16 numbers; numpy has no
+    bf16 type).  Both element types see the same draws.
   * Integer "uniform in [a, b]" is inclusive at both ends.
   * When the pool size is not given it is the pages needed plus 25 % slack,
     rounded up.  Pages come from a seeded permutation of the pool and are
@@ -76,6 +79,7 @@ class Workload:
     v_new: np.ndarray           # fp16 [B][Hkv][D]
     k_pages: np.ndarray         # fp16 [P][Hkv][S][D]
     v_pages: np.ndarray         # fp16 [P][Hkv][S][D]
+    dtype: str = "fp16"                  # element type of q/K/V/out ("fp16" or "bf16")
     k_codes: np.ndarray | None = None    # int8 [P][Hkv][S][D] (kv="int8")
     v_codes: np.ndarray | None = None
     k_scales: np.ndarray | None = None   # float32 [P][Hkv][S]
@@ -94,7 +98,14 @@ class Workload:
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * 2 * (self.head_dim + 4)
 
 
-def _draw(rng: np.random.Generator, shape, dist) -> np.ndarray:
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 -> nearest-even bf16 value, returned as float32 (finite inputs)."""
+    bits = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    bits = (bits + (np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1)))) & np.uint32(0xFFFF0000)
+    return bits.view(np.float32)
+
+
+def _draw(rng: np.random.Generator, shape, dist, dtype="fp16") -> np.ndarray:
     kind, param = dist
     n = int(np.prod(shape))
     if kind == "uniform":
@@ -103,6 +114,10 @@ def _draw(rng: np.random.Generator, shape, dist) -> np.ndarray:
         x = rng.standard_normal(n, dtype=np.float32) * np.float32(param)
     else:
         raise ValueError(kind)
+    if dtype == "bf16":
+        return round_bf16(x).reshape(shape)
+    if dtype != "fp16":
+        raise ValueError(dtype)
     return x.astype(np.float16).reshape(shape)
 
 
@@ -151,7 +166,7 @@ def layout(seq_lens: np.ndarray, num_pages: int, page_size: int, rng: np.random.
 def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE_SIZE,
                 num_pages=None, dist=("normal", 0.5), seed=0, forced_splits=0,
                 scale=None, poison=False, max_pages_per_seq=None, name="custom",
-                config=0, kv="fp16") -> Workload:
+                config=0, kv="fp16", dtype="fp16") -> Workload:
     """Any shape: used by the tests for ragged, empty and edge cases."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
@@ -160,20 +175,20 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
     if num_pages is None:
         num_pages = max(1, math.ceil(needed * 1.25))
     bt = layout(seq_lens, num_pages, page_size, rng, max_pages_per_seq)
-    q = _draw(rng, (B, num_q_heads, head_dim), dist)
-    k_new = _draw(rng, (B, num_kv_heads, head_dim), dist)
-    v_new = _draw(rng, (B, num_kv_heads, head_dim), dist)
+    q = _draw(rng, (B, num_q_heads, head_dim), dist, dtype)
+    k_new = _draw(rng, (B, num_kv_heads, head_dim), dist, dtype)
+    v_new = _draw(rng, (B, num_kv_heads, head_dim), dist, dtype)
     pool_shape = (num_pages, num_kv_heads, page_size, head_dim)
-    k_pages = _draw(rng, pool_shape, dist)
-    v_pages = _draw(rng, pool_shape, dist)
+    k_pages = _draw(rng, pool_shape, dist, dtype)
+    v_pages = _draw(rng, pool_shape, dist, dtype)
     if poison:
         owned = np.zeros((num_pages, page_size), bool)
         for b, L in enumerate(seq_lens):
             for t in range(int(L)):
                 owned[bt[b, t // page_size], t % page_size] = True
         pg, slot = np.nonzero(~owned)
-        k_pages[pg, :, slot, :] = np.float16(np.nan)
-        v_pages[pg, :, slot, :] = np.float16(np.nan)
+        k_pages[pg, :, slot, :] = np.nan
+        v_pages[pg, :, slot, :] = np.nan
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     q8 = {}
@@ -197,11 +212,11 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
                     num_pages=num_pages, max_pages_per_seq=bt.shape[1],
                     forced_splits=forced_splits, scale=float(scale), seq_lens=seq_lens,
                     block_table=bt, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages,
-                    v_pages=v_pages, **q8)
+                    v_pages=v_pages, dtype=dtype, **q8)
 
 
 def make_config(cfg: int, seed: int | None = None, poison: bool = False,
-                kv: str = "fp16") -> Workload:
+                kv: str = "fp16", dtype: str = "fp16") -> Workload:
     """The five benchmark workloads, seeded with 24000 + cfg by default."""
     if cfg not in _SHAPES:
         raise ValueError(f"unknown config {cfg}")
@@ -215,5 +230,5 @@ def make_config(cfg: int, seed: int | None = None, poison: bool = False,
     w = make_custom(seq_lens=seq_lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                     page_size=PAGE_SIZE, num_pages=pool, dist=dist, seed=sub_seed,
                     forced_splits=splits, poison=poison, name=CONFIG_NAMES[cfg], config=cfg,
-                    kv=kv)
+                    kv=kv, dtype=dtype)
     return w

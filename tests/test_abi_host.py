@@ -143,6 +143,26 @@ def test_plan_rejects_bad_inputs(lib):
         assert e.value.code == code, bad
 
 
+def test_dtype_is_checked(lib):
+    """fp16 and bf16 plan; any other dtype is unsupported; the INT8-cache calls
+    take fp16 only (all refused before any CUDA call)."""
+    kw = dict(batch=2, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
+              max_pages_per_seq=4, num_pages=8)
+    for dt in ("fp16", "bf16"):
+        binding.Plan(binding.make_shape(**kw, dtype=dt), [10, 20], 152)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(binding.make_shape(**kw, dtype=2), [10, 20], 152)
+    assert e.value.code == 2
+    s = binding.make_shape(**kw, dtype="bf16")
+    plan = binding.Plan(s, [10, 20], 152)
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.pa_kv_append_q8(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, fake,
+                               fake, None) == 2
+    assert lib.pa_decode_attention_q8(ctypes.byref(s), ctypes.byref(plan.c), fake, fake, fake,
+                                      fake, fake, fake, fake, ctypes.c_float(0.1), fake, fake,
+                                      plan.c.workspace_bytes, fake, None) == 2
+
+
 def test_plan_free_is_idempotent(lib):
     w = workloads.make_custom(seq_lens=[5], num_q_heads=1, num_kv_heads=1, head_dim=64, seed=3)
     plan = binding.Plan(_shape(w), w.seq_lens, 152)
