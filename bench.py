@@ -77,6 +77,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
                     help="KV-cache type: 16-bit elements, or INT8 codes with per-row fp32 scales")
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the decode step; swap: KV block swap-out + swap-in "
+                         "(pa_copy_blocks) of a quarter of the workload's sequences")
     ap.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16",
                     help="element type of q, K, V and out (the INT8 cache takes fp16)")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
@@ -679,6 +682,138 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+# ---------------------------------------------------------------------------
+# KV swap: pa_copy_blocks between the device pools and pinned host pools
+
+SWAP_METRIC = "KV swap GB/s (pa_copy_blocks: swap-out to pinned host memory + swap-in)"
+
+
+def swap_selection(w):
+    """Every fourth sequence's pages, and the host slots they go to."""
+    pages = []
+    for b in range(0, w.batch, 4):
+        n = -(-int(w.seq_lens[b]) // w.page_size)
+        pages.extend(int(x) for x in w.block_table[b, :n])
+    return np.array(pages, np.int32)
+
+
+def run_swap(args):
+    import torch
+
+    from paged_kv_decode_24_gb300 import binding, workloads
+    from paged_kv_decode_24_gb300 import build as _build
+
+    world, rank, local = dist_setup(args)
+    w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank)
+    pages = swap_selection(w)
+    n = len(pages)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        blk = np.zeros((n,) + w.k_pages.shape[1:], np.float16)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 2.0:
+            pairs = np.stack([pages, np.arange(n)], 1)
+            blk = oracle.copy_blocks(blk, w.k_pages, pairs)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu_base = {"value": round(reps * n * blk[0].nbytes / dt / 1e9, 3), "unit": "GB/s",
+                    "cores": 1, "kind": "oracle",
+                    "sample": f"oracle.copy_blocks of {n} K pages into a host array, "
+                              f"{reps} times in {dt:.1f} s"}
+    _build.ensure_built()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    kd = torch.from_numpy(w.k_pages).to(dev)
+    vd = torch.from_numpy(w.v_pages).to(dev)
+    hk = torch.empty((n,) + tuple(kd.shape[1:]), dtype=kd.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([pages, np.arange(n, dtype=np.int32)], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), pages], 1)).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    block_bytes = kd[0].numel() * kd.element_size()
+    step_bytes = 4 * n * block_bytes   # K and V, out and back in
+
+    def step():
+        binding.copy_blocks(hk, kd, out_pairs, status, stream=stream)
+        binding.copy_blocks(hv, vd, out_pairs, status, stream=stream)
+        binding.copy_blocks(kd, hk, in_pairs, status, stream=stream)
+        binding.copy_blocks(vd, hv, in_pairs, status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    # the link as one large copy engine transfer each way, for the peak
+    big_h = torch.empty(n * block_bytes, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(n * block_bytes, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            big_d.copy_(big_h, non_blocking=True)
+            big_h.copy_(big_d, non_blocking=True)
+        ev[0].record(stream)
+        big_d.copy_(big_h, non_blocking=True)
+        ev[1].record(stream)
+        big_h.copy_(big_d, non_blocking=True)
+        ev[2].record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = big_d.numel() / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+    d2h_gbs = big_d.numel() / (ev[1].elapsed_time(ev[2]) * 1e-3) / 1e9
+    peak = 2.0 / (1.0 / h2d_gbs + 1.0 / d2h_gbs)   # the same bytes each way
+    clocks = ClockSampler()
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = args.steps
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(K):
+            step()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+    if not (torch.equal(kd.cpu(), torch.from_numpy(w.k_pages)) and
+            torch.equal(vd.cpu(), torch.from_numpy(w.v_pages))):
+        raise RuntimeError("pools changed across swap round trips")
+    ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    res = {
+        "metric": SWAP_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; the workload's pools)",
+        "config": {"workload": w.name + ": every 4th sequence swapped out and back in",
+                   "config_id": args.config, "pages": n, "block_bytes": block_bytes,
+                   "step": "4 pa_copy_blocks (K and V out to pinned host memory, then back)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "host link", "achieved": round(value / world, 1),
+                     "peak": round(peak, 1), "unit": "GB/s", "frac": round(value / world / peak, 4),
+                     "peak_source": f"measured in this run: one {n * block_bytes / 2**20:.0f} MiB "
+                                    f"cudaMemcpyAsync each way ({h2d_gbs:.0f} GB/s in, "
+                                    f"{d2h_gbs:.0f} GB/s out), harmonic mean",
+                     "traffic": None},
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": 2 * n * block_bytes,
+                "d2h_bytes_per_step": 2 * n * block_bytes,
+                "note": "the step itself moves host buffers"},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.oracle_worker:
@@ -688,6 +823,8 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "swap":
+        run_swap(args)
     else:
         run_ours(args)
 

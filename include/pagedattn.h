@@ -303,6 +303,66 @@ pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t*
                                        const int32_t* block_table, const int32_t* seq_lens,
                                        float scale, void* out, int32_t* dev_status, void* stream);
 
+/* ---- KV blocks: how many, which are free, and moving them ------------
+ *
+ * swiftLLM's engine (architecture section) profiles the number of GPU
+ * blocks, allocates the KV cache and a KV swap space, and swaps blocks in
+ * and out before each step's compute.  A block is one page: 16 tokens of
+ * every KV head of a pool.
+ */
+
+#define PA_KV_16BIT 0 /* fp16 or bf16 pools */
+#define PA_KV_INT8 1  /* INT8 code pools plus fp32 row scales */
+
+/* Pages of num_layers layers' K and V pools (kv_kind: PA_KV_16BIT or
+ * PA_KV_INT8) that fit in free_bytes - reserve_bytes:
+ *   floor((free - reserve) / (2 * Hkv * page_size * row_bytes * num_layers)),
+ * row_bytes = 2 * head_dim (16-bit) or head_dim + 4 (INT8 codes + scale).
+ * Host only.  Returns 0 when free <= reserve and -1 on a bad argument. */
+int64_t pa_profile_num_blocks(const pa_shape_t* shape, int32_t num_layers, int32_t kv_kind,
+                              size_t free_bytes, size_t reserve_bytes);
+
+/* Free list of num_blocks pages (host, thread-safe).  Pages come out of a
+ * LIFO stack: a fresh allocator hands out 0, 1, 2, ...; a freed page is the
+ * next one handed out. */
+typedef struct pa_block_allocator pa_block_allocator_t;
+pa_status_t pa_block_allocator_create(int32_t num_blocks, pa_block_allocator_t** out);
+void pa_block_allocator_destroy(pa_block_allocator_t* allocator);
+int32_t pa_block_num_free(pa_block_allocator_t* allocator);  /* -1 for a null allocator */
+
+/* Take n pages into blocks_out[0..n), all or nothing: PA_ERR_NO_MEMORY when
+ * fewer than n are free (nothing taken). */
+pa_status_t pa_block_alloc(pa_block_allocator_t* allocator, int32_t n, int32_t* blocks_out);
+
+/* Return n pages.  A page out of range, not handed out, or listed twice
+ * gives PA_ERR_INVALID_ARG, and then nothing is freed. */
+pa_status_t pa_block_free(pa_block_allocator_t* allocator, const int32_t* blocks, int32_t n);
+
+/* Grow one sequence's block-table row (host, max_pages entries) from old_len
+ * to new_len tokens: entries [ceil(old_len/S), ceil(new_len/S)) get fresh
+ * pages, S = page_size.  PA_ERR_NO_MEMORY (nothing taken) when the pool is
+ * short; PA_ERR_INVALID_ARG when new_len < old_len or the row is too short. */
+pa_status_t pa_block_table_grow(pa_block_allocator_t* allocator, int32_t* row, int32_t max_pages,
+                                int32_t page_size, int32_t old_len, int32_t new_len);
+
+/* Copy whole blocks between two pools of blocks of block_bytes bytes each:
+ * for i < n, block pairs[2i+1] of dst_pool becomes block pairs[2i] of
+ * src_pool, byte for byte.  One kernel moves them all.  Either pool may be
+ * device memory or page-locked host memory mapped into the device's address
+ * space (cudaHostAlloc), so one call is a swap-in (host to device), a
+ * swap-out (device to host) or a block copy within the GPU.
+ *
+ * pairs: device (or mapped) int32 [n][2] = (src block, dst block), 8-byte
+ * aligned.  Pools 16-byte aligned; block_bytes a positive multiple of 16
+ * (a 16-bit pool's block is Hkv * 16 * D * 2 bytes; an INT8 code pool's
+ * Hkv * 16 * D; a scale pool's Hkv * 16 * 4).  No block may be both read
+ * and written by one call, and destinations must be distinct.  A pair with
+ * an index outside [0, src_blocks) or [0, dst_blocks) is skipped and sets
+ * PA_DEV_BAD_PAGE in *dev_status.  n = 0 launches nothing. */
+pa_status_t pa_copy_blocks(void* dst_pool, int32_t dst_blocks, const void* src_pool,
+                           int32_t src_blocks, size_t block_bytes, const int32_t* pairs,
+                           int32_t n, int32_t* dev_status, void* stream);
+
 /*
  * Export the physical slot of every logical token, for exact comparison
  * with the oracle: out_slots[b][t] = block_table[b][t/S]*S + t%S for

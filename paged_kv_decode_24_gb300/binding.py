@@ -86,6 +86,17 @@ _SIGS = {
                                                      ctypes.POINTER(PaPlan), _P, _P, _P, _P, _P,
                                                      _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                                      ctypes.c_size_t, _P, _P]),
+    "pa_profile_num_blocks": (ctypes.c_int64, [ctypes.POINTER(PaShape), ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_size_t, ctypes.c_size_t]),
+    "pa_block_allocator_create": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(_P)]),
+    "pa_block_allocator_destroy": (None, [_P]),
+    "pa_block_num_free": (ctypes.c_int32, [_P]),
+    "pa_block_alloc": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
+    "pa_block_free": (ctypes.c_int, [_P, _P, ctypes.c_int32]),
+    "pa_block_table_grow": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32]),
+    "pa_copy_blocks": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_size_t, _P,
+                                      ctypes.c_int32, _P, _P]),
     "pa_debug_gather_indices": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_version": (ctypes.c_char_p, []),
@@ -353,6 +364,89 @@ def gather_indices(shape, block_table, seq_lens, out_slots, status, stream=None)
     _check("pa_debug_gather_indices", lib.pa_debug_gather_indices(
         ctypes.byref(shape), _dev_ptr(block_table, torch.int32, "block_table"),
         _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(out_slots, torch.int32, "out_slots"),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# KV blocks: page counts, the free list, block copies
+
+PA_KV_16BIT = 0
+PA_KV_INT8 = 1
+
+
+def profile_num_blocks(shape, num_layers, kv_kind, free_bytes, reserve_bytes=0) -> int:
+    """pa_profile_num_blocks: pages of num_layers layers' K and V that fit."""
+    n = load().pa_profile_num_blocks(ctypes.byref(shape), int(num_layers), int(kv_kind),
+                                     int(free_bytes), int(reserve_bytes))
+    if n < 0:
+        raise PagedAttnError("pa_profile_num_blocks", 1, _lib)
+    return int(n)
+
+
+class BlockAllocator:
+    """Owner of a pa_block_allocator_t (host free list of pages)."""
+
+    def __init__(self, num_blocks: int):
+        lib = load()
+        self._h = ctypes.c_void_p()
+        _check("pa_block_allocator_create",
+               lib.pa_block_allocator_create(int(num_blocks), ctypes.byref(self._h)))
+
+    def num_free(self) -> int:
+        return int(load().pa_block_num_free(self._h))
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.empty(max(int(n), 0), np.int32)
+        _check("pa_block_alloc", load().pa_block_alloc(self._h, int(n),
+                                                       out.ctypes.data if n else None))
+        return out
+
+    def free(self, blocks):
+        b = np.ascontiguousarray(np.asarray(blocks, np.int32))
+        _check("pa_block_free", load().pa_block_free(self._h, b.ctypes.data if b.size else None,
+                                                     int(b.size)))
+
+    def grow(self, row: np.ndarray, page_size: int, old_len: int, new_len: int):
+        """pa_block_table_grow on a contiguous int32 numpy row, in place."""
+        if row.dtype != np.int32 or not row.flags["C_CONTIGUOUS"]:
+            raise ValueError("row must be a contiguous int32 array")
+        _check("pa_block_table_grow", load().pa_block_table_grow(
+            self._h, row.ctypes.data, int(row.size), int(page_size), int(old_len), int(new_len)))
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.pa_block_allocator_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _pool_ptr(t, name):
+    """A pool for pa_copy_blocks: a CUDA tensor or a pinned host tensor."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous torch tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be on a CUDA device or in pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def copy_blocks(dst_pool, src_pool, pairs, status, stream=None):
+    """pa_copy_blocks: dst_pool[d] = src_pool[s] for every (s, d) row of the
+    device int32 [n, 2] tensor pairs.  Pools are [blocks, ...] tensors of the
+    same block shape and dtype, on the device or in pinned host memory."""
+    torch = _torch()
+    if dst_pool.dtype != src_pool.dtype or tuple(dst_pool.shape[1:]) != tuple(src_pool.shape[1:]):
+        raise ValueError("pools differ in block shape or dtype")
+    block_bytes = int(np.prod(dst_pool.shape[1:])) * dst_pool.element_size()
+    n = int(pairs.shape[0])
+    _check("pa_copy_blocks", load().pa_copy_blocks(
+        _pool_ptr(dst_pool, "dst_pool"), int(dst_pool.shape[0]), _pool_ptr(src_pool, "src_pool"),
+        int(src_pool.shape[0]), block_bytes, _dev_ptr(pairs, torch.int32, "pairs"), n,
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
 

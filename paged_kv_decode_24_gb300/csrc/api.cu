@@ -375,6 +375,28 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
 }  // namespace
 }  // namespace pa
 
+extern "C" pa_status_t pa_copy_blocks(void* dst_pool, int32_t dst_blocks, const void* src_pool,
+                                      int32_t src_blocks, size_t block_bytes, const int32_t* pairs,
+                                      int32_t n, int32_t* dev_status, void* stream) {
+  using namespace pa;
+  if (n < 0 || dst_blocks < 0 || src_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (block_bytes == 0 || block_bytes % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (n == 0) return PA_OK;
+  if (!aligned(dst_pool, 16) || !aligned(src_pool, 16) || !aligned(pairs, 8) ||
+      !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  CopyBlocksParams p{};
+  p.dst = dst_pool;
+  p.src = src_pool;
+  p.pairs = reinterpret_cast<const int2*>(pairs);
+  p.block_bytes = (int64_t)block_bytes;
+  p.n = n;
+  p.src_blocks = src_blocks;
+  p.dst_blocks = dst_blocks;
+  p.status = dev_status;
+  return cuda_status(launch_copy_blocks(p, (cudaStream_t)stream));
+}
+
 extern "C" pa_status_t pa_debug_gather_indices(const pa_shape_t* shape, const int32_t* block_table,
                                                const int32_t* seq_lens, int32_t* out_slots,
                                                int32_t* dev_status, void* stream) {

@@ -200,6 +200,37 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_q8_kernel(const Appe
 }
 
 // ---------------------------------------------------------------------------
+// Block copy (KV swap in/out, copy within a pool): CTA i takes pairs i, i +
+// grid, ...; its threads move a block in 16-byte words, four loads in flight
+// per thread before the four stores.  Either side may be mapped host memory.
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyBlocksParams p) {
+  const int64_t words = p.block_bytes / 16;
+  for (int i = blockIdx.x; i < p.n; i += gridDim.x) {
+    const int2 pr = p.pairs[i];
+    if (pr.x < 0 || pr.x >= p.src_blocks || pr.y < 0 || pr.y >= p.dst_blocks) {
+      if (threadIdx.x == 0) set_status(p.status, PA_DEV_BAD_PAGE);
+      continue;  // CTA-uniform
+    }
+    const uint4* s = reinterpret_cast<const uint4*>(static_cast<const char*>(p.src) +
+                                                     (size_t)pr.x * (size_t)p.block_bytes);
+    uint4* d = reinterpret_cast<uint4*>(static_cast<char*>(p.dst) +
+                                        (size_t)pr.y * (size_t)p.block_bytes);
+    int64_t w = threadIdx.x;
+    for (; w + 3 * kCopyThreads < words; w += 4 * kCopyThreads) {
+      const uint4 a = s[w], b = s[w + kCopyThreads], c = s[w + 2 * kCopyThreads],
+                  e = s[w + 3 * kCopyThreads];
+      d[w] = a;
+      d[w + kCopyThreads] = b;
+      d[w + 2 * kCopyThreads] = c;
+      d[w + 3 * kCopyThreads] = e;
+    }
+    for (; w < words; w += kCopyThreads) d[w] = s[w];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Debug export of the gather map: slot = page * S + t % S, -1 past the end,
 // -2 for an invalid page index.
 __global__ void gather_slots_kernel(const int32_t* block_table, const int32_t* seq_lens,
@@ -274,6 +305,12 @@ cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream) {
     append_q8_kernel<64><<<grid, kAppendWarps * 32, 0, stream>>>(p);
   else
     append_q8_kernel<128><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream) {
+  const int grid = p.n < 152 * 8 ? p.n : 152 * 8;
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,16 @@ struct AppendQ8Params {
   int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
 };
 
+struct CopyBlocksParams {
+  void* dst;
+  const void* src;
+  const int2* pairs;  // (src block, dst block)
+  int64_t block_bytes;
+  int32_t n, src_blocks, dst_blocks;
+  int32_t* status;
+};
+
+cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream);
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
 cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
