@@ -80,6 +80,8 @@ class Workload:
     k_pages: np.ndarray         # fp16 [P][Hkv][S][D]
     v_pages: np.ndarray         # fp16 [P][Hkv][S][D]
     dtype: str = "fp16"                  # element type of q/K/V/out ("fp16" or "bf16")
+    q_lens: np.ndarray | None = None     # int32 [B]: query tokens per sequence (multi-token);
+                                         # q, k_new, v_new then have sum(q_lens) rows
     k_codes: np.ndarray | None = None    # int8 [P][Hkv][S][D] (kv="int8")
     v_codes: np.ndarray | None = None
     k_scales: np.ndarray | None = None   # float32 [P][Hkv][S]
@@ -166,8 +168,10 @@ def layout(seq_lens: np.ndarray, num_pages: int, page_size: int, rng: np.random.
 def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE_SIZE,
                 num_pages=None, dist=("normal", 0.5), seed=0, forced_splits=0,
                 scale=None, poison=False, max_pages_per_seq=None, name="custom",
-                config=0, kv="fp16", dtype="fp16") -> Workload:
-    """Any shape: used by the tests for ragged, empty and edge cases."""
+                config=0, kv="fp16", dtype="fp16", q_lens=None) -> Workload:
+    """Any shape: used by the tests for ragged, empty and edge cases.  With
+    ``q_lens`` the step has q_lens[b] query tokens per sequence (the newest
+    ones, q_lens[b] <= seq_lens[b]), packed sequence after sequence."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
     B = len(seq_lens)
@@ -175,9 +179,15 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
     if num_pages is None:
         num_pages = max(1, math.ceil(needed * 1.25))
     bt = layout(seq_lens, num_pages, page_size, rng, max_pages_per_seq)
-    q = _draw(rng, (B, num_q_heads, head_dim), dist, dtype)
-    k_new = _draw(rng, (B, num_kv_heads, head_dim), dist, dtype)
-    v_new = _draw(rng, (B, num_kv_heads, head_dim), dist, dtype)
+    rows = B
+    if q_lens is not None:
+        q_lens = np.asarray(q_lens, np.int32)
+        if len(q_lens) != B or np.any(q_lens < 0) or np.any(q_lens > seq_lens):
+            raise ValueError("need 0 <= q_lens[b] <= seq_lens[b]")
+        rows = int(q_lens.sum())
+    q = _draw(rng, (rows, num_q_heads, head_dim), dist, dtype)
+    k_new = _draw(rng, (rows, num_kv_heads, head_dim), dist, dtype)
+    v_new = _draw(rng, (rows, num_kv_heads, head_dim), dist, dtype)
     pool_shape = (num_pages, num_kv_heads, page_size, head_dim)
     k_pages = _draw(rng, pool_shape, dist, dtype)
     v_pages = _draw(rng, pool_shape, dist, dtype)
@@ -212,7 +222,7 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
                     num_pages=num_pages, max_pages_per_seq=bt.shape[1],
                     forced_splits=forced_splits, scale=float(scale), seq_lens=seq_lens,
                     block_table=bt, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages,
-                    v_pages=v_pages, dtype=dtype, **q8)
+                    v_pages=v_pages, dtype=dtype, q_lens=q_lens, **q8)
 
 
 def make_config(cfg: int, seed: int | None = None, poison: bool = False,
