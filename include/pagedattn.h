@@ -303,6 +303,62 @@ pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t*
                                        const int32_t* block_table, const int32_t* seq_lens,
                                        float scale, void* out, int32_t* dev_status, void* stream);
 
+/* ---- Several query tokens per sequence (chunked prefill, piggybacked
+ * prefill and decode) ------------------------------------------------------
+ *
+ * The from-scratch engine article (section 4) names processing several
+ * prompt tokens at once with a FlashAttention-style fused kernel as the next
+ * step after decode; swiftLLM's feature list has piggybacked prefill and
+ * decode and Flash Attention over PagedAttention.
+ *
+ * Sequence b has L = seq_lens[b] cached tokens, the newest q_lens[b] of
+ * which are this step's queries: query i sits at position
+ * L - q_lens[b] + i and attends positions 0 .. that position (causal):
+ *   out[r][h] = softmax(scale * K[0..p] q[r][h]) V[0..p],  p = L - q_lens[b] + i.
+ * q, out: device [T][Hq][D], and k_new, v_new: [T][Hkv][D], packed by
+ * sequence (row r = cu[b] + i, cu = prefix sums of q_lens, T = cu[B]), in
+ * the shape's dtype.  A decode token is q_lens[b] = 1.
+ */
+typedef struct {
+  pa_shape_t shape;     /* the shape the plan was made for */
+  int32_t num_tiles;    /* CTAs: 64 query rows (tokens x heads of one KV head) each */
+  int32_t total_q;      /* T */
+  int32_t owns_blob;    /* 1: host_blob is released by pa_prefill_plan_free */
+  int32_t reserved;
+  uint64_t plan_id;
+  size_t blob_bytes;    /* bytes pa_prefill_plan_upload copies */
+  size_t workspace_bytes;
+  void* host_blob;
+} pa_prefill_plan_t;
+
+/* Host: the tile list (longest work first) and the row offsets cu.
+ * q_lens_host[b] must satisfy 0 <= q_lens[b] <= seq_lens[b]. */
+pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* seq_lens_host,
+                            const int32_t* q_lens_host, pa_prefill_plan_t* plan_out);
+void pa_prefill_plan_free(pa_prefill_plan_t* plan);
+pa_status_t pa_prefill_plan_upload(const pa_prefill_plan_t* plan, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Write the T new rows: row cu[b] + i of k_new/v_new goes to position
+ * seq_lens[b] - q_lens[b] + i of sequence b, bit for bit.  Needs the plan in
+ * the workspace (for cu). */
+pa_status_t pa_kv_append_tokens(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
+                                const void* k_new, const void* v_new, void* k_pages,
+                                void* v_pages, const int32_t* block_table,
+                                const int32_t* seq_lens, const void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* The attention above, for every query row of the plan, on tensor cores
+ * (FlashAttention-style: one CTA per 64 query rows of one KV head streams
+ * the causal part of the sequence's pages once).  Errors as
+ * pa_decode_attention's; device seq_lens shorter than the plan's q_lens
+ * set PA_DEV_PLAN_MISMATCH. */
+pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
+                                 const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* seq_lens, float scale,
+                                 void* out, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* stream);
+
 /* ---- KV blocks: how many, which are free, and moving them ------------
  *
  * swiftLLM's engine (architecture section) profiles the number of GPU

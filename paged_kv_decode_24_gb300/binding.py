@@ -51,6 +51,13 @@ class PaPlan(ctypes.Structure):
                 ("host_blob", ctypes.c_void_p)]
 
 
+class PaPrefillPlan(ctypes.Structure):
+    _fields_ = [("shape", PaShape), ("num_tiles", ctypes.c_int32), ("total_q", ctypes.c_int32),
+                ("owns_blob", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("plan_id", ctypes.c_uint64), ("blob_bytes", ctypes.c_size_t),
+                ("workspace_bytes", ctypes.c_size_t), ("host_blob", ctypes.c_void_p)]
+
+
 class PagedAttnError(RuntimeError):
     def __init__(self, fn, code, lib):
         self.code = code
@@ -97,6 +104,16 @@ _SIGS = {
                                            ctypes.c_int32]),
     "pa_copy_blocks": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_size_t, _P,
                                       ctypes.c_int32, _P, _P]),
+    "pa_prefill_plan": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P,
+                                       ctypes.POINTER(PaPrefillPlan)]),
+    "pa_prefill_plan_free": (None, [ctypes.POINTER(PaPrefillPlan)]),
+    "pa_prefill_plan_upload": (ctypes.c_int, [ctypes.POINTER(PaPrefillPlan), _P, ctypes.c_size_t,
+                                              _P]),
+    "pa_kv_append_tokens": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPrefillPlan),
+                                           _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "pa_prefill_attention": (ctypes.c_int, [ctypes.POINTER(PaShape),
+                                            ctypes.POINTER(PaPrefillPlan), _P, _P, _P, _P, _P,
+                                            ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "pa_debug_gather_indices": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_version": (ctypes.c_char_p, []),
@@ -365,6 +382,76 @@ def gather_indices(shape, block_table, seq_lens, out_slots, status, stream=None)
         ctypes.byref(shape), _dev_ptr(block_table, torch.int32, "block_table"),
         _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(out_slots, torch.int32, "out_slots"),
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# several query tokens per sequence
+
+class PrefillPlan:
+    """Owner of a pa_prefill_plan_t (tile list and row offsets, host side)."""
+
+    def __init__(self, shape: PaShape, seq_lens_host, q_lens_host):
+        lib = load()
+        self.shape = shape
+        self.c = PaPrefillPlan()
+        self._lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        self._qlens = np.ascontiguousarray(np.asarray(q_lens_host, dtype=np.int32))
+        lp = self._lens.ctypes.data if self._lens.size else None
+        qp = self._qlens.ctypes.data if self._qlens.size else None
+        _check("pa_prefill_plan", lib.pa_prefill_plan(ctypes.byref(shape), lp, qp,
+                                                      ctypes.byref(self.c)))
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self.c.workspace_bytes)
+
+    def blob(self) -> np.ndarray:
+        n = int(self.c.blob_bytes) // 4
+        buf = (ctypes.c_int32 * n).from_address(self.c.host_blob)
+        return np.frombuffer(buf, dtype=np.int32, count=n).copy()
+
+    def free(self):
+        if _lib is not None and getattr(self, "c", None) is not None and self.c.host_blob:
+            _lib.pa_prefill_plan_free(ctypes.byref(self.c))
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def prefill_upload(plan: PrefillPlan, workspace, stream=None):
+    torch = _torch()
+    _check("pa_prefill_plan_upload", load().pa_prefill_plan_upload(
+        ctypes.byref(plan.c), _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
+
+
+def append_tokens(shape, plan: PrefillPlan, k_new, v_new, k_pages, v_pages, block_table,
+                  seq_lens, workspace, status, stream=None):
+    """pa_kv_append_tokens: the step's new rows into their pages."""
+    torch = _torch()
+    et = _elem(shape)
+    _check("pa_kv_append_tokens", load().pa_kv_append_tokens(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(k_new, et, "k_new"),
+        _dev_ptr(v_new, et, "v_new"), _dev_ptr(k_pages, et, "k_pages"),
+        _dev_ptr(v_pages, et, "v_pages"), _dev_ptr(block_table, torch.int32, "block_table"),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens"), _dev_ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def prefill(shape, plan: PrefillPlan, q, k_pages, v_pages, block_table, seq_lens, scale, out,
+            workspace, status, stream=None):
+    """pa_prefill_attention: every query row of the plan."""
+    torch = _torch()
+    et = _elem(shape)
+    _check("pa_prefill_attention", load().pa_prefill_attention(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, et, "q"),
+        _dev_ptr(k_pages, et, "k_pages"), _dev_ptr(v_pages, et, "v_pages"),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, et, "out"), _dev_ptr(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
 
 # --------------------------------------------------------------------------

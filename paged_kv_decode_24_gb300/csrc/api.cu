@@ -12,6 +12,7 @@
 #include "decode_kernel.cuh"
 #include "launch.h"
 #include "pa_internal.h"
+#include "prefill.cuh"
 
 namespace pa {
 
@@ -374,6 +375,107 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
 
 }  // namespace
 }  // namespace pa
+
+// ---- several query tokens per sequence
+
+extern "C" pa_status_t pa_prefill_plan_upload(const pa_prefill_plan_t* plan, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
+  if (!plan || !plan->host_blob || plan->blob_bytes == 0) return PA_ERR_INVALID_ARG;
+  if (!pa::aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  return pa::cuda_status(cudaMemcpyAsync(workspace, plan->host_blob, plan->blob_bytes,
+                                         cudaMemcpyHostToDevice, (cudaStream_t)stream));
+}
+
+namespace pa {
+namespace {
+
+pa_status_t check_prefill_call(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
+                               const void* workspace, size_t workspace_bytes) {
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
+  if (plan->num_tiles < 0 || plan->total_q < 0) return PA_ERR_PLAN;
+  if (plan->total_q > 0 && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status_t pa_kv_append_tokens(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
+                                           const void* k_new, const void* v_new, void* k_pages,
+                                           void* v_pages, const int32_t* block_table,
+                                           const int32_t* seq_lens, const void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream) {
+  using namespace pa;
+  pa_status_t st = check_prefill_call(shape, plan, workspace, workspace_bytes);
+  if (st != PA_OK) return st;
+  if (shape->batch == 0 || plan->total_q == 0) return PA_OK;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pages, 16) ||
+      !aligned(v_pages, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  AppendTokensParams p{};
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.cu = (const int32_t*)((const char*)workspace + prefill_layout(plan->num_tiles, shape->batch).cu_off);
+  p.status = dev_status;
+  p.batch = shape->batch;
+  p.total_q = plan->total_q;
+  p.num_kv_heads = shape->num_kv_heads;
+  p.head_dim = shape->head_dim;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pages = shape->num_pages;
+  return cuda_status(launch_append_tokens(p, (cudaStream_t)stream));
+}
+
+extern "C" pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
+                                            const void* q, const void* k_pages,
+                                            const void* v_pages, const int32_t* block_table,
+                                            const int32_t* seq_lens, float scale, void* out,
+                                            void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, void* stream) {
+  using namespace pa;
+  pa_status_t st = check_prefill_call(shape, plan, workspace, workspace_bytes);
+  if (st != PA_OK) return st;
+  if (shape->batch == 0 || plan->num_tiles == 0) return PA_OK;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4))
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  PrefillParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.ws = (const int32_t*)workspace;
+  p.cu = (const int32_t*)((const char*)workspace +
+                          prefill_layout(plan->num_tiles, shape->batch).cu_off);
+  p.status = dev_status;
+  p.qscale = (float)((double)scale * 1.4426950408889634);  // log2(e)
+  p.batch = shape->batch;
+  p.num_q_heads = shape->num_q_heads;
+  p.num_kv_heads = shape->num_kv_heads;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pages = shape->num_pages;
+  p.num_tiles = plan->num_tiles;
+  p.total_q = plan->total_q;
+  if (!encode_pool_map(&p.tmap_k, k_pages, *shape) || !encode_pool_map(&p.tmap_v, v_pages, *shape))
+    return PA_ERR_CUDA;
+  const int G = shape->num_q_heads / shape->num_kv_heads;
+  cudaError_t e = shape->head_dim == 64
+                      ? launch_prefill_d64(p, G, shape->dtype, (cudaStream_t)stream)
+                      : launch_prefill_d128(p, G, shape->dtype, (cudaStream_t)stream);
+  return cuda_status(e);
+}
 
 extern "C" pa_status_t pa_copy_blocks(void* dst_pool, int32_t dst_blocks, const void* src_pool,
                                       int32_t src_blocks, size_t block_bytes, const int32_t* pairs,

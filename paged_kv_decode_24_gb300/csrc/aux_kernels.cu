@@ -231,6 +231,46 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyBlo
 }
 
 // ---------------------------------------------------------------------------
+// Append of several rows per sequence (multi-token step): one thread per
+// 16-byte chunk of a (row, KV head); a row finds its sequence by binary
+// search in cu.
+__global__ void append_tokens_kernel(const AppendTokensParams p) {
+  const int chunks = p.head_dim / 8;
+  const long long total = (long long)p.total_q * p.num_kv_heads * chunks;
+  const int Lmax = p.max_pages * kPageSize;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int ch = (int)(i % chunks);
+    const int h = (int)((i / chunks) % p.num_kv_heads);
+    const int r = (int)(i / chunks / p.num_kv_heads);
+    int lo = 0, hi = p.batch;  // largest b with cu[b] <= r
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cu[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int b = lo, n = p.cu[b + 1] - p.cu[b];
+    const int L = p.seq_lens[b];
+    if (L < n || L > Lmax) {
+      if (ch == 0 && h == 0) set_status(p.status, L > Lmax ? PA_DEV_BAD_SEQ_LEN : PA_DEV_PLAN_MISMATCH);
+      continue;
+    }
+    const int pos = L - n + (r - p.cu[b]);
+    const int page = p.block_table[(size_t)b * p.max_pages + pos / kPageSize];
+    if (page < 0 || page >= p.num_pages) {
+      if (ch == 0 && h == 0) set_status(p.status, PA_DEV_BAD_PAGE);
+      continue;
+    }
+    const size_t dst =
+        (((size_t)page * p.num_kv_heads + h) * kPageSize + pos % kPageSize) * p.head_dim + ch * 8;
+    const size_t src = ((size_t)r * p.num_kv_heads + h) * p.head_dim + ch * 8;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_pages) + dst) =
+        *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_new) + src);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_pages) + dst) =
+        *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v_new) + src);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Debug export of the gather map: slot = page * S + t % S, -1 past the end,
 // -2 for an invalid page index.
 __global__ void gather_slots_kernel(const int32_t* block_table, const int32_t* seq_lens,
@@ -311,6 +351,12 @@ cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream) {
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream) {
   const int grid = p.n < 152 * 8 ? p.n : 152 * 8;
   copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_tokens(const AppendTokensParams& p, cudaStream_t stream) {
+  const long long work = (long long)p.total_q * p.num_kv_heads * (p.head_dim / 8);
+  append_tokens_kernel<<<grid_for(work, 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,27 @@ struct CopyBlocksParams {
 };
 
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream);
+
+// Append of several rows per sequence: row cu[b] + i goes to position
+// seq_lens[b] - (cu[b+1] - cu[b]) + i.  Rows are 16-bit elements, copied
+// bit for bit.
+struct AppendTokensParams {
+  const void* k_new;
+  const void* v_new;
+  void* k_pages;
+  void* v_pages;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* cu;  // [B+1], in the uploaded multi-token plan
+  int32_t* status;
+  int32_t batch, total_q, num_kv_heads, head_dim, max_pages, num_pages;
+};
+
+cudaError_t launch_append_tokens(const AppendTokensParams& p, cudaStream_t stream);
+
+struct PrefillParams;  // prefill.cuh
+cudaError_t launch_prefill_d64(const PrefillParams& p, int group, int dtype, cudaStream_t stream);
+cudaError_t launch_prefill_d128(const PrefillParams& p, int group, int dtype, cudaStream_t stream);
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
 cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,

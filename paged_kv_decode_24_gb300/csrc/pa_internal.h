@@ -101,6 +101,25 @@ inline Layout layout(int items, int groups, int nslots, int group, int head_dim)
   return l;
 }
 
+// Multi-token attention: a tile is kPrefillRows query rows (tokens x heads
+// of one KV head).  Blob = header (16 x int32: [0] magic [1] tiles [2] B
+// [3] T [4,5] plan_id [6] G [7] D) | tiles (int4: sequence, KV head, first
+// token, tokens) | cu (int32 [B+1], row offsets of the sequences).
+constexpr int kPrefillRows = 64;
+constexpr uint32_t kPrefillMagic = 0x564b4650u;  // "PFKV"
+
+struct PrefillLayout {
+  size_t tiles_off, cu_off, blob_bytes;
+};
+
+inline PrefillLayout prefill_layout(int tiles, int batch) {
+  PrefillLayout l{};
+  l.tiles_off = 64;
+  l.cu_off = l.tiles_off + 16 * (size_t)tiles;
+  l.blob_bytes = align_sz(l.cu_off + 4 * ((size_t)batch + 1), 256);
+  return l;
+}
+
 // Validation shared by every entry point.
 pa_status_t check_shape(const pa_shape_t* s);
 

@@ -1,23 +1,22 @@
-// Host-side launch of one split-decode kernel instance (shared by the
-// per-head_dim translation units).
+// Host-side launch of one kernel instance with programmatic dependent launch
+// (shared by the per-head_dim translation units).
 #pragma once
 
 #include <cuda_runtime.h>
 
 #include <atomic>
 
-#include "decode_kernel.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
-// Launch `kern` on `grid` CTAs of kWarpsPerCta warps with `smem` bytes of
-// dynamic shared memory, allowing programmatic dependent launch after the
+// Launch `kern(params)` on `grid` CTAs of `threads` threads with `smem` bytes
+// of dynamic shared memory, allowing programmatic dependent launch after the
 // previous kernel in the stream.  The shared-memory limit is raised once per
 // device; `configured` is the instance's own bit set of configured devices.
-template <typename Kernel>
-cudaError_t launch_split_kernel(Kernel kern, int smem, std::atomic<unsigned long long>& configured,
-                                const SplitParams& p, int grid, cudaStream_t stream) {
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel kern, int smem, std::atomic<unsigned long long>& configured,
+                       const Params& params, int grid, int threads, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -29,7 +28,7 @@ cudaError_t launch_split_kernel(Kernel kern, int smem, std::atomic<unsigned long
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kWarpsPerCta * 32);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -37,7 +36,14 @@ cudaError_t launch_split_kernel(Kernel kern, int smem, std::atomic<unsigned long
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern, params);
+}
+
+// A split-decode kernel: CTAs of kWarpsPerCta warps.
+template <typename Kernel, typename Params>
+cudaError_t launch_split_kernel(Kernel kern, int smem, std::atomic<unsigned long long>& configured,
+                                const Params& p, int grid, cudaStream_t stream) {
+  return launch_pdl(kern, smem, configured, p, grid, kWarpsPerCta * 32, stream);
 }
 
 }  // namespace pa

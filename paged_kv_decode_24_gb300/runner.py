@@ -46,6 +46,7 @@ class DeviceDecode:
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.shape = binding.shape_of(self.q, self.k_pages, self.block_table)
+        self.shape.batch = len(w.seq_lens)   # q may hold several rows per sequence
         if num_sms is None:
             num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.num_sms = int(num_sms)
@@ -106,6 +107,27 @@ class DeviceDecode:
                                  self.k_codes, self.v_codes, self.k_scales, self.v_scales,
                                  self.block_table, self.seq_lens, self.w.scale, dst,
                                  self.workspace, self.status)
+        return dst
+
+    # ---- several query tokens per sequence (workloads made with q_lens)
+
+    def make_prefill_plan(self, seq_lens_host=None):
+        lens = self.w.seq_lens if seq_lens_host is None else seq_lens_host
+        self.pf_plan = binding.PrefillPlan(self.shape, lens, self.w.q_lens)
+        self.pf_ws = binding.alloc_workspace(self.pf_plan, self.device)
+        binding.prefill_upload(self.pf_plan, self.pf_ws)
+        return self.pf_plan
+
+    def append_tokens(self):
+        binding.append_tokens(self.shape, self.pf_plan, self.k_new, self.v_new, self.k_pages,
+                              self.v_pages, self.block_table, self.seq_lens, self.pf_ws,
+                              self.status)
+
+    def prefill(self, out=None):
+        dst = self.out if out is None else out
+        binding.prefill(self.shape, self.pf_plan, self.q, self.k_pages, self.v_pages,
+                        self.block_table, self.seq_lens, self.w.scale, dst, self.pf_ws,
+                        self.status)
         return dst
 
     def gather_slots(self):

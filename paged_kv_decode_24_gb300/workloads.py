@@ -242,3 +242,34 @@ def make_config(cfg: int, seed: int | None = None, poison: bool = False,
                     forced_splits=splits, poison=poison, name=CONFIG_NAMES[cfg], config=cfg,
                     kv=kv, dtype=dtype)
     return w
+
+
+PREFILL_NAMES = {
+    1: "chunked prefill, LLaMA-3-8B heads: B=16, GQA 32/8, D=128, L~U[1024,4096], last 512 "
+       "tokens queried",
+    2: "piggybacked prefill + decode, LLaMA-3-8B heads: 8 prefill chunks of 256 at L~U[256,2048] "
+       "and 56 decode tokens at L~U[128,2048], GQA 32/8, D=128",
+}
+
+
+def make_prefill_config(cfg: int, seed: int | None = None, dtype: str = "fp16") -> Workload:
+    """Multi-token workloads (several query tokens per sequence), seeded
+    with 24100 + cfg by default.  Query tokens are the newest of their
+    sequence; values N(0, 0.5) as in the decode workloads."""
+    seed = SEED_BASE + 100 + cfg if seed is None else seed
+    rng = np.random.default_rng(seed)
+    if cfg == 1:
+        lens = rng.integers(1024, 4096, size=16, endpoint=True).astype(np.int32)
+        q_lens = np.full(16, 512, np.int32)
+    elif cfg == 2:
+        pre = rng.integers(256, 2048, size=8, endpoint=True)
+        dec = rng.integers(128, 2048, size=56, endpoint=True)
+        lens = np.concatenate([pre, dec]).astype(np.int32)
+        q_lens = np.concatenate([np.full(8, 256), np.ones(56)]).astype(np.int32)
+    else:
+        raise ValueError(f"unknown multi-token workload {cfg}")
+    sub_seed = int(rng.integers(0, 2**31 - 1))
+    return make_custom(seq_lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                       dist=("normal", 0.5), seed=sub_seed, q_lens=q_lens,
+                       name=PREFILL_NAMES[cfg], config=cfg, dtype=dtype)
+

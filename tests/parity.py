@@ -10,6 +10,13 @@ The 1e-3 floor keeps near-zero outputs from making the ratio meaningless.
 For bf16 q/K/V/out, rounding the output alone costs up to half an ulp, a
 relative 2^-8 (3.9e-3): the absolute bound is 8e-3 (twice that at |out| = 1),
 and the relative bound and its floor are the fp16 ones.
+
+The multi-token kernel rounds the softmax weights p once to the element
+type before P.V, as FlashAttention does (the decode kernels keep p as hi +
+lo).  That error is at most half an ulp of p times the attended |V|, so it
+scales with |V| (about 0.5 in the workloads), not with |out|: for that path
+the relative bound is taken against max(|oracle|, 0.25).  The absolute
+bounds stay.
 """
 
 from __future__ import annotations
@@ -20,18 +27,19 @@ MAX_ABS = 2e-3
 MAX_REL = 1e-2
 REL_FLOOR = 1e-3
 BF16_MAX_ABS = 8e-3
+P_ROUNDED_REL_FLOOR = 0.25
 
 
-def errors(got, want):
+def errors(got, want, rel_floor=REL_FLOOR):
     g = np.asarray(got, np.float64)
     w = np.asarray(want, np.float64)
     d = np.abs(g - w)
-    return float(d.max(initial=0.0)), float((d / np.maximum(np.abs(w), REL_FLOOR)).max(initial=0.0))
+    return float(d.max(initial=0.0)), float((d / np.maximum(np.abs(w), rel_floor)).max(initial=0.0))
 
 
-def assert_close(got, want, what="", dtype="fp16"):
+def assert_close(got, want, what="", dtype="fp16", rel_floor=REL_FLOOR):
     assert np.all(np.isfinite(np.asarray(got, np.float64))), f"{what}: non-finite output"
-    ea, er = errors(got, want)
+    ea, er = errors(got, want, rel_floor)
     max_abs = BF16_MAX_ABS if dtype == "bf16" else MAX_ABS
     assert ea <= max_abs and er <= MAX_REL, f"{what}: max_abs={ea:.3g} max_rel={er:.3g}"
     return ea, er

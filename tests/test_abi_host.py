@@ -241,3 +241,31 @@ def test_empty_batch_is_a_no_op(lib):
     assert lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), fake, fake, fake, fake,
                                    fake, ctypes.c_float(0.1), fake, fake, 1 << 20, fake, None) == 0
     assert lib.pa_kv_append(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, None) == 0
+
+
+def test_prefill_plan_tiles_cover_every_row_once(lib):
+    lens = [37, 100, 5, 640, 0]
+    qls = [37, 5, 0, 640, 0]
+    for hq, hkv in ((4, 2), (8, 8), (32, 4)):
+        s = binding.make_shape(len(lens), hq, hkv, 64, 16, 40, 100)
+        plan = binding.PrefillPlan(s, lens, qls)
+        blob = plan.blob()
+        assert blob[0] == 0x564B4650 and blob[1] == plan.c.num_tiles and blob[3] == sum(qls)
+        n = int(blob[1])
+        tiles = blob[16:16 + 4 * n].reshape(n, 4)
+        cu = blob[16 + 4 * n:16 + 4 * n + len(lens) + 1]
+        assert cu.tolist() == np.concatenate([[0], np.cumsum(qls)]).tolist()
+        G = hq // hkv
+        seen = set()
+        for b, g, tok0, ntok in tiles:
+            assert 1 <= ntok <= 64 // G and tok0 + ntok <= qls[b]
+            for i in range(tok0, tok0 + ntok):
+                seen.add((int(b), int(g), i))
+        assert seen == {(b, g, i) for b in range(len(lens)) for g in range(hkv)
+                        for i in range(qls[b])}
+        work = [(lens[b] - qls[b] + tok0 + ntok) * ntok for b, g, tok0, ntok in tiles]
+        assert all(x >= y for x, y in zip(work, work[1:]))
+    s = binding.make_shape(2, 4, 2, 64, 16, 8, 20)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.PrefillPlan(s, [10, 20], [11, 1])      # more queries than cached tokens
+    assert e.value.code == 1

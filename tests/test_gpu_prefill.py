@@ -1,0 +1,135 @@
+"""GPU parity of the multi-token path (pa_kv_append_tokens and
+pa_prefill_attention) against the float64 oracle, through the C ABI.
+"""
+
+from __future__ import annotations
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_decode_24_gb300 import binding, workloads
+from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.parity import P_ROUNDED_REL_FLOOR, assert_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    return lib
+
+
+def close(got, want, what, dtype="fp16"):
+    return assert_close(got, want, what, dtype=dtype, rel_floor=P_ROUNDED_REL_FLOOR)
+
+
+def oracle_step(w, rows=None):
+    kp, vp = oracle.kv_append_tokens(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                     w.seq_lens, w.q_lens)
+    return oracle.prefill_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.q_lens, w.scale,
+                                    rows=rows), (kp, vp)
+
+
+def gpu_step(w):
+    dd = DeviceDecode(w)
+    dd.make_prefill_plan()
+    dd.append_tokens()
+    out = dd.prefill()
+    status = dd.read_status()
+    assert status == 0, f"device status {status:#x}"
+    return out.float().cpu().numpy(), dd
+
+
+CASES = [
+    # (seq_lens, q_lens, Hq, Hkv, D)
+    ([37, 100], [37, 5], 4, 2, 64),
+    ([1, 2, 15, 16, 17, 31, 33, 64], [1, 2, 15, 16, 1, 8, 33, 20], 8, 8, 128),   # G = 1
+    ([300, 129, 1000], [64, 129, 200], 32, 8, 128),                              # G = 4
+    ([777, 50], [100, 50], 16, 2, 128),                                          # G = 8
+    ([513, 257], [70, 257], 8, 1, 64),                                           # G = 8, D = 64
+    ([2000, 3, 640], [1, 3, 640], 4, 4, 64),                                     # G = 1, D = 64
+    ([96, 300, 5], [96, 0, 5], 16, 8, 128),                                      # G = 2, empty
+]
+
+
+def _ids(c):
+    return f"L{c[0][:3]}_q{c[1][:3]}_G{c[2] // c[3]}_D{c[4]}"
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_prefill_parity_full(case, dtype):
+    lens, qls, hq, hkv, d = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              seed=zlib.crc32(str(case).encode()) ^ 32, q_lens=qls, dtype=dtype)
+    got, dd = gpu_step(w)
+    want, (kp, _) = oracle_step(w)
+    close(got, want, f"prefill {case} {dtype}", dtype=dtype)
+    assert np.array_equal(dd.k_pages.float().cpu().numpy(), kp.astype(np.float32))
+
+
+def test_prefill_poisoned_pool_never_read():
+    """Rows no sequence owns hold NaN: a read past a query's span would show."""
+    w = workloads.make_custom(seq_lens=[1, 17, 250, 33], num_q_heads=8, num_kv_heads=2,
+                              head_dim=128, seed=91, q_lens=[1, 9, 70, 33], poison=True)
+    got, _ = gpu_step(w)
+    want, _ = oracle_step(w)
+    close(got, want, "prefill poison")
+
+
+def test_prefill_with_one_query_equals_decode():
+    w = workloads.make_custom(seq_lens=[5, 300, 129, 1000], num_q_heads=32, num_kv_heads=8,
+                              head_dim=128, seed=92, q_lens=[1, 1, 1, 1])
+    got, _ = gpu_step(w)
+    want = oracle.decode_attention(w.q, *oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new,
+                                                          w.block_table, w.seq_lens),
+                                   w.block_table, w.seq_lens, w.scale)
+    close(got, want, "prefill as decode")
+
+
+def test_prefill_reruns_are_bit_identical():
+    w = workloads.make_custom(seq_lens=[700, 1500], num_q_heads=16, num_kv_heads=4, head_dim=128,
+                              seed=93, q_lens=[300, 77])
+    _, dd = gpu_step(w)
+    a = dd.prefill().clone()
+    b = dd.prefill().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_prefill_bad_page_and_short_seq_len_are_flagged():
+    w = workloads.make_custom(seq_lens=[40, 40], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                              seed=94, q_lens=[10, 10])
+    w.block_table[0, 1] = w.num_pages + 7
+    dd = DeviceDecode(w)
+    dd.make_prefill_plan()
+    out = dd.prefill().float().cpu().numpy()
+    assert dd.read_status() & binding.PA_DEV_BAD_PAGE
+    assert np.all(np.isfinite(out))
+    w2 = workloads.make_custom(seq_lens=[40, 40], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                               seed=95, q_lens=[10, 10])
+    dd2 = DeviceDecode(w2)
+    dd2.make_prefill_plan()
+    dd2.seq_lens[1] = 5          # fewer cached tokens than the plan's queries
+    dd2.prefill()
+    assert dd2.read_status() & binding.PA_DEV_PLAN_MISMATCH
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_prefill_benchmark_workload(cfg):
+    w = workloads.make_prefill_config(cfg)
+    got, _ = gpu_step(w)
+    rng = np.random.default_rng(96)
+    rows = sorted({(int(r), int(h)) for r, h in zip(rng.integers(0, w.q.shape[0], 64),
+                                                     rng.integers(0, w.num_q_heads, 64))}
+                  | {(0, 0), (w.q.shape[0] - 1, w.num_q_heads - 1)})
+    want, _ = oracle_step(w, rows=rows)
+    idx = tuple(np.array(rows).T)
+    close(got[idx], want[idx], f"prefill workload {cfg} (sampled)")
