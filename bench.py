@@ -77,9 +77,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
                     help="KV-cache type: 16-bit elements, or INT8 codes with per-row fp32 scales")
-    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                     help="decode: the decode step; swap: KV block swap-out + swap-in "
-                         "(pa_copy_blocks) of a quarter of the workload's sequences")
+                         "(pa_copy_blocks) of a quarter of the workload's sequences; prefill: "
+                         "several query tokens per sequence (--config 1 or 2 picks the "
+                         "multi-token workload)")
     ap.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16",
                     help="element type of q, K, V and out (the INT8 cache takes fp16)")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
@@ -814,6 +816,158 @@ def run_swap(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# several query tokens per sequence: pa_kv_append_tokens + pa_prefill_attention
+
+PREFILL_METRIC = "multi-token attention TFLOP/s (causal; pa_kv_append_tokens + pa_prefill_attention)"
+PREFILL_LAYERS = 4
+
+
+def prefill_flops(w):
+    """4 D FLOPs (q.k and p.v) per query head, query token and key it sees."""
+    n = 0
+    for L, qn in zip(w.seq_lens.astype(np.int64), w.q_lens.astype(np.int64)):
+        n += int(qn * (L - qn) + qn * (qn + 1) // 2)   # sum over queries of (position + 1)
+    return 4 * w.head_dim * w.num_q_heads * n
+
+
+def run_prefill(args):
+    import torch
+
+    from paged_kv_decode_24_gb300 import binding, workloads
+    from paged_kv_decode_24_gb300 import build as _build
+
+    if args.config not in (1, 2):
+        raise SystemExit("--op prefill takes --config 1 or 2")
+    world, rank, local = dist_setup(args)
+    w = workloads.make_prefill_config(args.config, seed=workloads.SEED_BASE + 100 + args.config +
+                                      1000 * rank, dtype=args.dtype)
+    flops = prefill_flops(w)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        done = 0
+        rng = np.random.default_rng(0)
+        while time.perf_counter() - t0 < 3.0:
+            r = int(rng.integers(0, w.q.shape[0]))
+            oracle.prefill_attention(w.q, w.k_pages, w.v_pages, w.block_table, w.seq_lens,
+                                     w.q_lens, w.scale,
+                                     rows=[(r, h) for h in range(w.num_q_heads)])
+            b = int(np.searchsorted(np.cumsum(w.q_lens), r, side="right"))
+            pos = int(w.seq_lens[b]) - int(w.q_lens[b]) + (r - int(np.cumsum(w.q_lens)[b] - w.q_lens[b]))
+            done += 4 * w.head_dim * w.num_q_heads * (pos + 1)
+        dt = time.perf_counter() - t0
+        cpu_base = {"value": round(done / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                    "kind": "oracle",
+                    "sample": f"float64 oracle rows (all heads of random query tokens), {dt:.1f} s"}
+    _build.ensure_built()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    elem_t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    to_elem = lambda a: to_dev(a).to(elem_t)
+    shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                               w.max_pages_per_seq, w.num_pages, args.dtype)
+    q, kn, vn = to_elem(w.q), to_elem(w.k_new), to_elem(w.v_new)
+    bt, sl = to_dev(w.block_table), to_dev(w.seq_lens)
+    cache0 = (to_elem(w.k_pages), to_elem(w.v_pages))
+    pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(PREFILL_LAYERS - 1)]
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan = binding.PrefillPlan(shape, w.seq_lens, w.q_lens)
+    ws = binding.alloc_workspace(plan, dev)
+    with torch.cuda.stream(stream):
+        binding.prefill_upload(plan, ws, stream=stream)
+        binding.append_tokens(shape, plan, kn, vn, *pools[0], bt, sl, ws, status, stream=stream)
+        binding.prefill(shape, plan, q, *pools[0], bt, sl, w.scale, out, ws, status, stream=stream)
+    stream.synchronize()
+
+    def capture(nl):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(nl):
+                binding.append_tokens(shape, plan, kn, vn, *pools[l], bt, sl, ws, status)
+                binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status)
+        return g
+
+    K = args.steps
+    full, rem = divmod(K, PREFILL_LAYERS)
+    g_full = capture(PREFILL_LAYERS)
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // PREFILL_LAYERS)):
+            g_full.replay()
+    stream.synchronize()
+    # the split of a step: attention alone, in its own events
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for l in range(PREFILL_LAYERS):
+            binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status,
+                            stream=stream)
+        ev[1].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = ev[0].elapsed_time(ev[1]) / PREFILL_LAYERS
+    clocks = ClockSampler()
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+    ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
+    value = world * flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_src = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, peak_src = 1900.0, "fallback"
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    rows = int(w.q.shape[0])
+    res = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.dtype == "bf16" else "f16",
+        "data": "synthetic (seeded; shapes and value laws of the workload)",
+        "config": {"workload": w.name, "config_id": args.config, "query_rows": rows,
+                   "flops_per_step": flops, "tiles": int(plan.c.num_tiles),
+                   "step": "one layer: pa_kv_append_tokens + pa_prefill_attention",
+                   "launch": f"CUDA graph of {PREFILL_LAYERS} layers' calls over "
+                             f"{PREFILL_LAYERS} per-layer KV caches",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "prefill_kernel (mma.sync m16n8k16)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": "MEASURED_PEAKS.json bf16_tflops (of measured; fp16 has "
+                                    "the same dense rate)" if peak_src == "measured"
+                                    else "fallback 1900 TFLOP/s (of fallback)",
+                     "traffic": None, "us_per_launch": round(attn_ms * 1e3, 3)},
+        "cpu_baseline": cpu_base,
+        "e2e": None,
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.oracle_worker:
@@ -825,6 +979,8 @@ def main():
         run_reference(args)
     elif args.op == "swap":
         run_swap(args)
+    elif args.op == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 
