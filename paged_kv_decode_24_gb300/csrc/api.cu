@@ -13,6 +13,7 @@
 #include "launch.h"
 #include "pa_internal.h"
 #include "prefill.cuh"
+#include "prefill_tc5.cuh"
 
 namespace pa {
 
@@ -447,6 +448,7 @@ extern "C" pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_pr
   pa_status_t st = check_prefill_call(shape, plan, workspace, workspace_bytes);
   if (st != PA_OK) return st;
   if (shape->batch == 0 || plan->num_tiles == 0) return PA_OK;
+  if (!plan->host_blob) return PA_ERR_PLAN;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4))
     return PA_ERR_INVALID_ARG;
@@ -471,9 +473,17 @@ extern "C" pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_pr
   if (!encode_pool_map(&p.tmap_k, k_pages, *shape) || !encode_pool_map(&p.tmap_v, v_pages, *shape))
     return PA_ERR_CUDA;
   const int G = shape->num_q_heads / shape->num_kv_heads;
-  cudaError_t e = shape->head_dim == 64
-                      ? launch_prefill_d64(p, G, shape->dtype, (cudaStream_t)stream)
-                      : launch_prefill_d128(p, G, shape->dtype, (cudaStream_t)stream);
+  const int rows = ((const int32_t*)plan->host_blob)[8];  // the kernel the tiles were cut for
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (rows == kPrefillRowsTc5)
+    e = shape->head_dim == 64 ? launch_prefill_tc5_d64(p, G, shape->dtype, s)
+                              : launch_prefill_tc5_d128(p, G, shape->dtype, s);
+  else if (rows == kPrefillRows)
+    e = shape->head_dim == 64 ? launch_prefill_d64(p, G, shape->dtype, s)
+                              : launch_prefill_d128(p, G, shape->dtype, s);
+  else
+    return PA_ERR_PLAN;
   return cuda_status(e);
 }
 

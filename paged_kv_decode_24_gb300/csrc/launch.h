@@ -79,6 +79,10 @@ cudaError_t launch_append_tokens(const AppendTokensParams& p, cudaStream_t strea
 struct PrefillParams;  // prefill.cuh
 cudaError_t launch_prefill_d64(const PrefillParams& p, int group, int dtype, cudaStream_t stream);
 cudaError_t launch_prefill_d128(const PrefillParams& p, int group, int dtype, cudaStream_t stream);
+cudaError_t launch_prefill_tc5_d64(const PrefillParams& p, int group, int dtype,
+                                   cudaStream_t stream);
+cudaError_t launch_prefill_tc5_d128(const PrefillParams& p, int group, int dtype,
+                                    cudaStream_t stream);
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
 cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,

@@ -101,11 +101,13 @@ inline Layout layout(int items, int groups, int nslots, int group, int head_dim)
   return l;
 }
 
-// Multi-token attention: a tile is kPrefillRows query rows (tokens x heads
-// of one KV head).  Blob = header (16 x int32: [0] magic [1] tiles [2] B
-// [3] T [4,5] plan_id [6] G [7] D) | tiles (int4: sequence, KV head, first
-// token, tokens) | cu (int32 [B+1], row offsets of the sequences).
+// Multi-token attention: a tile is a number of query rows (tokens x heads of
+// one KV head): 128 for the tcgen05 kernel (one TMEM lane per row), 64 for
+// the mma.sync kernel.  Blob = header (16 x int32: [0] magic [1] tiles [2] B
+// [3] T [4,5] plan_id [6] G [7] D [8] rows per tile) | tiles (int4:
+// sequence, KV head, first token, tokens) | cu (int32 [B+1], row offsets).
 constexpr int kPrefillRows = 64;
+constexpr int kPrefillRowsTc5 = 128;
 constexpr uint32_t kPrefillMagic = 0x564b4650u;  // "PFKV"
 
 struct PrefillLayout {

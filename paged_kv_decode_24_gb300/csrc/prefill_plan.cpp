@@ -19,6 +19,13 @@ namespace {
 
 std::atomic<uint64_t> g_prefill_ids{1};
 
+// Rows per tile: the tcgen05 kernel's 128 unless PA_PREFILL_ROWS=64 asks
+// for the mma.sync kernel.
+int prefill_rows() {
+  const char* v = getenv("PA_PREFILL_ROWS");
+  return (v && atoi(v) == kPrefillRows) ? kPrefillRows : kPrefillRowsTc5;
+}
+
 struct Tile {
   int32_t b, g, tok0, ntok;
   int64_t work;
@@ -36,7 +43,8 @@ extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* s
   if (st != PA_OK) return st;
   const int B = shape->batch, Hkv = shape->num_kv_heads, D = shape->head_dim;
   const int G = shape->num_q_heads / Hkv;
-  const int tok_per_tile = kPrefillRows / G;
+  const int rows = prefill_rows();
+  const int tok_per_tile = rows / G;
   if (B > 0 && (!seq_lens_host || !q_lens_host)) return PA_ERR_INVALID_ARG;
 
   std::vector<int32_t> cu((size_t)B + 1, 0);
@@ -68,6 +76,7 @@ extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* s
   blob[5] = (int32_t)(id >> 32);
   blob[6] = G;
   blob[7] = D;
+  blob[8] = rows;
   int32_t* t = blob + lay.tiles_off / 4;
   for (size_t i = 0; i < tiles.size(); ++i) {
     t[4 * i + 0] = tiles[i].b;

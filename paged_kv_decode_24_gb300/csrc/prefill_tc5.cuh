@@ -1,0 +1,507 @@
+// Multi-token attention on the fifth-generation tensor cores (tcgen05):
+// the same operation and tiles as prefill.cuh, with 128-row MMAs issued by
+// one thread from shared-memory descriptors into tensor memory (TMEM).
+//
+// A CTA of 4 warps owns 128 query rows of one (sequence, KV head): 128 / G
+// query tokens times the G heads of the KV head.  Thread r of the CTA owns
+// row r, which is TMEM lane r, so a row's softmax needs no shuffles.
+// Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
+// TMA copies write and the MMA descriptors read):
+//   Q   [D/64 boxes][128 rows][128 B]         A operand of S, K-major
+//   NS stages of 32 tokens (two pages), each
+//     K [D/64 boxes][32 tokens][128 B]        B operand of S, K-major
+//     V [D/64 boxes][32 tokens][128 B]        B operand of P.V, MN-major
+//   P   2 x [128 rows][64 B], 64-byte swizzle  A operand of P.V, K-major
+// TMEM: two S buffers of 32 columns and O of D columns.
+//
+// Per stage kt (thread 0 issues, all threads compute):
+//   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 32)       committed to s_done
+//   row softmax of S(kt) in registers (tcgen05.ld), lazy rescaling
+//   P(kt) to shared memory, once P.V(kt-1) has finished reading it
+//   O += P V       (2 MMAs, M = 128, N = D, K = 32)    committed to pv_done
+// S(kt+1) is issued before the softmax of kt, and P is double-buffered, so
+// the tensor core works while the threads compute.  A stage is refilled once
+// P.V has read it.
+// Every wait is bounded; on failure the CTA waits (bounded) for its copies
+// and MMAs, frees its TMEM and writes nothing.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+
+#include "decode_tc.cuh"
+#include "elem.cuh"
+#include "prefill.cuh"
+
+namespace pa {
+
+namespace tc5 {
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets, the fixed version bits and the swizzle mode (2: 128-byte, 4:
+// 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle = 2) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)swizzle << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the
+// element type, major-ness of A and B, N and M.
+template <typename T>
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, bool b_mn_major) {
+  const uint32_t ty = std::is_same<T, __half>::value ? 0u : 1u;
+  return (1u << 4) | (ty << 7) | (ty << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc5
+
+constexpr int kTc5Rows = 128;   // query rows per CTA (one TMEM lane each)
+constexpr int kTc5Tokens = 32;  // keys per stage (two pages)
+constexpr int kTc5Stages = 3;
+
+template <int D>
+struct Tc5Layout {
+  static constexpr int BOXES = D / 64;
+  static constexpr int Q = 0;                                   // BOXES x 16 KB
+  static constexpr int QBOX = kTc5Rows * 128;
+  static constexpr int KVBOX = kTc5Tokens * 128;                // 4 KB per box
+  static constexpr int STAGE0 = Q + BOXES * QBOX;
+  static constexpr int STAGE = 2 * BOXES * KVBOX;               // K boxes, then V boxes
+  static constexpr int P = STAGE0 + kTc5Stages * STAGE;        // 2 x 8 KB
+  static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
+  // full[NS], s_done[2], s_free[2], pv_done[2], p_ready, drain
+  static constexpr int BARS = P + 2 * PBUF;
+  static constexpr int TMEM_SLOT = align_up(BARS + 8 * (kTc5Stages + 8), 16);
+  static constexpr int FLAG = TMEM_SLOT + 16;
+  static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
+  static constexpr uint32_t TMEM_COLS = 256;                    // S0, S1 (32 each), O (D)
+};
+
+// 160 threads: warps 0-3 own the 128 rows (softmax, output), warp 4 issues
+// the copies and the MMAs.  They meet only on mbarriers.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_constant__ PrefillParams p) {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  using L = Tc5Layout<D>;
+  constexpr int NS = kTc5Stages;
+  constexpr int BN = kTc5Tokens;
+  constexpr int TOKS = kTc5Rows / G;
+  extern __shared__ unsigned char smem_dyn[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(base);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const bool mma_warp = warp == 4;
+  const uint32_t full = sbase + L::BARS;        // NS barriers: the stage's copies landed
+  const uint32_t s_done = full + 8 * NS;        // 2: S(kt) computed
+  const uint32_t s_free = s_done + 16;          // 2: S(kt) read by the 4 row warps
+  const uint32_t pv_done = s_free + 16;         // 2: P.V(kt) computed
+  const uint32_t p_ready = pv_done + 16;        // P(kt) written, O rescaled, by the 4 row warps
+  const uint32_t drain = p_ready + 8;           // every MMA issued has finished (failure path)
+  int* cta_flag = reinterpret_cast<int*>(base + L::FLAG);
+
+  if ((int)blockIdx.x >= p.num_tiles) return;  // whole CTA
+  const int4 hdr = *reinterpret_cast<const int4*>(p.ws);
+  const int4 tile = reinterpret_cast<const int4*>(p.ws + 16)[blockIdx.x];
+  if (tid == 0) {
+    *cta_flag = 0;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+    for (int s = 0; s < NS; ++s) mbar_init(full + 8 * s, 1);
+    mbar_init(s_done, 1);
+    mbar_init(s_done + 8, 1);
+    mbar_init(s_free, 4);
+    mbar_init(s_free + 8, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(pv_done + 8, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (mma_warp) {  // TMEM for this CTA, freed by this warp at the end
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     sbase + L::TMEM_SLOT),
+                 "r"(L::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc5::fence_before();
+  __syncthreads();
+  tc5::fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::TMEM_SLOT);
+  const uint32_t t_s0 = tmem, t_o = tmem + 2 * BN;       // columns: S0, S1, O
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
+
+  pdl_launch_dependents();
+  pdl_wait_primary();
+
+  const int b = tile.x, g = tile.y, tok0 = tile.z, ntok = tile.w;
+  bool bad = hdr.x != (int)kPrefillMagic || hdr.y != p.num_tiles || hdr.z != p.batch ||
+             hdr.w != p.total_q || b < 0 || b >= p.batch || g < 0 || g >= p.num_kv_heads ||
+             tok0 < 0 || ntok < 1 || ntok > TOKS;
+  int cu0 = 0, qn = 0, Lseq = 0;
+  if (!bad) {
+    cu0 = p.cu[b];
+    qn = p.cu[b + 1] - cu0;
+    Lseq = p.seq_lens[b];
+    if (cu0 < 0 || qn < tok0 + ntok || p.cu[b + 1] > p.total_q || Lseq < qn ||
+        Lseq > p.max_pages * kPageSize) {
+      if (tid == 0)
+        set_status(p.status, Lseq > p.max_pages * kPageSize ? PA_DEV_BAD_SEQ_LEN : PA_DEV_PLAN_MISMATCH);
+      bad = true;
+    }
+  } else if (tid == 0) {
+    set_status(p.status, PA_DEV_PLAN_MISMATCH);
+  }
+  const int pos0 = Lseq - qn + tok0;
+  const int span = pos0 + ntok;
+  const int nkt = bad ? 0 : (span + BN - 1) / BN;
+  const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
+
+  // ---- Q tile into shared memory (row = thread of warps 0-3), zero past ntok
+  const int row = tid & 127;
+  const int tt = row / G;                 // query token of this row within the tile
+  const bool ok = !bad && !mma_warp && tt < ntok;
+  const int qpos = pos0 + tt;             // its position
+  const size_t qrow = ((size_t)(cu0 + tok0 + tt) * p.num_q_heads + (size_t)g * G + row % G) * D;
+  if (!mma_warp) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      const int bx = c >> 3, ch = c & 7;
+      *reinterpret_cast<uint4*>(base + L::Q + bx * L::QBOX + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
+  }
+  __syncthreads();
+
+  if (mma_warp) {
+    // ================= copies and MMAs (lane 0) =================
+    if (lane == 0 && nkt > 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      auto issue = [&](int kt) {
+        const int s = kt % NS;
+        int phys[2];
+        int nvalid = 0;
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * kt + u;
+          int ph = -1;
+          if (j * kPageSize < span) {
+            ph = __ldg(bt_row + j);
+            if (ph < 0 || ph >= p.num_pages) {
+              set_status(p.status, PA_DEV_BAD_PAGE);
+              ph = -1;
+            }
+          }
+          phys[u] = ph;
+          nvalid += ph >= 0;
+        }
+        const uint32_t bar = full + 8 * s;
+        if (nvalid == 0) {
+          mbar_arrive(bar);
+          return;
+        }
+        mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * 2 * D * kPageSize * 2));
+        const uint32_t st = sbase + L::STAGE0 + s * L::STAGE;
+        for (int u = 0; u < 2; ++u) {
+          if (phys[u] < 0) continue;
+          for (int bx = 0; bx < L::BOXES; ++bx) {
+            tma_load_4d(st + bx * L::KVBOX + u * 2048, &p.tmap_k, bx * 64, 0, g, phys[u], bar, policy);
+            tma_load_4d(st + (L::BOXES + bx) * L::KVBOX + u * 2048, &p.tmap_v, bx * 64, 0, g,
+                        phys[u], bar, policy);
+          }
+        }
+      };
+      const uint32_t idesc_s = tc5::instr_desc<T>(128, BN, false);
+      const uint32_t idesc_o = tc5::instr_desc<T>(128, D, true);
+      auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T into S buffer kt & 1
+        if (!mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1))) return false;
+        tc5::fence_after();
+        const uint32_t kst = sbase + L::STAGE0 + (kt % NS) * L::STAGE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t a = tc5::smem_desc(sbase + L::Q + (k >> 2) * L::QBOX + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
+          tc5::mma(t_s0 + (uint32_t)((kt & 1) * BN), a, bd, idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc5::commit(s_done + 8 * (kt & 1));
+        return true;
+      };
+      int issued = 0;
+      for (; issued < nkt && issued < NS; ++issued) issue(issued);
+      bool good = issue_s(0);
+      for (int kt = 0; kt < nkt && good; ++kt) {
+        if (kt + 1 < nkt) {
+          // S buffer (kt+1) & 1 last held S(kt-1): wait until the row warps read it
+          if (kt >= 1) good = mbar_wait_bounded(s_free + 8 * ((kt + 1) & 1), (uint32_t)(((kt - 1) >> 1) & 1));
+          good = good && issue_s(kt + 1);
+          if (!good) break;
+        }
+        good = mbar_wait_bounded(p_ready, (uint32_t)(kt & 1));
+        if (!good) break;
+        tc5::fence_after();
+        const uint32_t vst = sbase + L::STAGE0 + (kt % NS) * L::STAGE + L::BOXES * L::KVBOX;
+        const uint32_t pst = sbase + L::P + (kt & 1) * L::PBUF;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t a = tc5::smem_desc(pst + k * 32, 16, 512, 4);  // 64-byte swizzle
+          const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
+          tc5::mma(t_o, a, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
+        }
+        tc5::commit(pv_done + 8 * (kt & 1));
+        // the stage of kt-1 is free once P.V(kt-1) has read it (issued an
+        // iteration ago, so normally done by now)
+        if (kt >= 1 && issued < nkt && issued == kt - 1 + NS) {
+          good = mbar_wait_bounded(pv_done + 8 * ((kt - 1) & 1), (uint32_t)(((kt - 1) >> 1) & 1));
+          if (!good) break;
+          issue(issued++);
+        }
+      }
+      if (!good) {
+        set_status(p.status, PA_DEV_TIMEOUT);
+        *cta_flag = 1;
+        // every MMA issued must finish before TMEM is freed: one more commit
+        // covers them all
+        tc5::commit(drain);
+        mbar_wait_bounded(drain, 0u, 10000000ull);
+      }
+      for (int kt = issued - NS < 0 ? 0 : issued - NS; kt < issued; ++kt)  // copies in flight
+        mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1), 10000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ================= rows: softmax and output (warps 0-3) =================
+    float m_run = -INFINITY, l_run = 0.f;
+    bool good = true;
+    // block-table entries of the stage, loaded one stage ahead (page checks
+    // mask the tokens of a page that was not copied)
+    int nph0 = nkt > 0 ? __ldg(bt_row) : -1;
+    int nph1 = nkt > 0 && kPageSize < span ? __ldg(bt_row + 1) : -1;
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int ph0 = nph0, ph1 = nph1;
+      if (kt + 1 < nkt) {
+        nph0 = __ldg(bt_row + 2 * kt + 2);
+        nph1 = (2 * kt + 3) * kPageSize < span ? __ldg(bt_row + 2 * kt + 3) : -1;
+      }
+      good = __all_sync(kFull, mbar_wait_bounded(s_done + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1)));
+      if (!good) break;
+      tc5::fence_after();
+      float sv[BN];
+      tc5::ld16(t_s0 + (uint32_t)((kt & 1) * BN) + lane_off, sv);
+      tc5::ld16(t_s0 + (uint32_t)((kt & 1) * BN) + 16 + lane_off, sv + 16);
+      tc5::wait_ld();
+      tc5::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free + 8 * (kt & 1));
+
+      // ---- mask, row max (lazy), weights
+      const int kv0 = BN * kt;
+      const bool pg0 = ph0 >= 0 && ph0 < p.num_pages;
+      const bool pg1 = ph1 >= 0 && ph1 < p.num_pages;
+      // visible iff the page was copied and the key is not after the query;
+      // a stage every lane of the warp sees whole skips the per-key test
+      const int lim = ok ? qpos - kv0 : -1;  // last visible column of the stage
+      if (!__all_sync(kFull, pg0 && pg1 && lim >= BN - 1)) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const bool vis = (c < 16 ? pg0 : pg1) && c <= lim;
+          sv[c] = vis ? sv[c] : -INFINITY;
+        }
+      }
+      // row max of the raw scores (the scale is positive), tree-reduced
+      float mx;
+      {
+        float t[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) t[c] = fmaxf(sv[c], sv[c + BN / 2]);
+#pragma unroll
+        for (int w = BN / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) t[c] = fmaxf(t[c], t[c + w]);
+        mx = t[0] * p.qscale;  // in scaled (log2) units
+      }
+      float al = 1.f;
+      bool resc = false;
+      if (mx > m_run + kLazyLog2Prefill) {
+        al = ex2(m_run - mx);  // 0 when the row had no weight yet
+        resc = m_run != -INFINITY;
+        m_run = mx;
+      }
+      // p = 2^(s * scale - m): one FFMA and one ex2 per key
+      uint32_t pk[BN / 2];
+      float ps;
+      {
+        float t[BN / 2];
+        // a row with no weight yet has only masked (-inf) scores: 2^-inf = 0
+        const float nm = m_run == -INFINITY ? -INFINITY : -m_run;
+        const float qs = p.qscale;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float a0 = ex2(fmaf(sv[c], qs, nm));
+          const float a1 = ex2(fmaf(sv[c + 1], qs, nm));
+          t[c / 2] = a0 + a1;
+          pk[c / 2] = Elem<T>::from_f2(a0, a1);
+        }
+#pragma unroll
+        for (int w = BN / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) t[c] += t[c + w];
+        ps = t[0];
+      }
+      l_run = l_run * al + ps;
+
+      // ---- P buffer kt & 1 is free once P.V(kt-2) is done; O may be
+      // rescaled only once P.V(kt-1) is done
+      const bool any_resc = __any_sync(kFull, resc);
+      if (kt >= 2) {
+        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (kt & 1), (uint32_t)(((kt - 2) >> 1) & 1)));
+        if (!good) break;
+      }
+      if (any_resc && kt >= 1) {
+        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((kt - 1) & 1),
+                                                   (uint32_t)(((kt - 1) >> 1) & 1)));
+        if (!good) break;
+      }
+      tc5::fence_after();
+      if (any_resc && kt >= 1) {  // rare: rescale this warp's O rows in TMEM
+        const float f = resc ? al : 1.f;
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          tc5::ld16(t_o + (uint32_t)c + lane_off, ov);
+          tc5::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] *= f;
+          tc5::st16(t_o + (uint32_t)c + lane_off, ov);
+        }
+        tc5::wait_st();
+      }
+      // ---- P(kt) row into its buffer (K-major, 64-byte swizzle: 16-byte
+      // chunk c of row r at chunk c ^ ((r / 2) % 4)); V rows past the span
+      // (which may hold anything) become zeros
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(base + L::P + (kt & 1) * L::PBUF + row * 64 +
+                                  ((ch ^ ((row >> 1) & 3)) << 4)) = v;
+      }
+      if (kv0 + BN > span) {
+        const int first_bad = span - kv0;  // tokens [first_bad, BN) of this stage
+        unsigned char* vsm = base + L::STAGE0 + (kt % NS) * L::STAGE + L::BOXES * L::KVBOX;
+        for (int i = row; i < L::BOXES * BN * 8; i += 128) {  // 16-byte chunks
+          const int bx = i / (BN * 8), r = (i / 8) % BN, ch = i % 8;
+          if (r >= first_bad)
+            *reinterpret_cast<uint4*>(vsm + bx * L::KVBOX + r * 128 + (ch << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc5::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready);
+    }
+    if (nkt > 0 && good) {
+      good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
+                                                 (uint32_t)(((nkt - 1) >> 1) & 1)));
+      if (good) {
+        tc5::fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        T* out = static_cast<T*>(p.out) + qrow;
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          tc5::ld16(t_o + (uint32_t)c + lane_off, ov);
+          tc5::wait_ld();
+          if (ok) {
+            uint4 w0, w1;
+            w0.x = Elem<T>::from_f2(ov[0] * inv, ov[1] * inv);
+            w0.y = Elem<T>::from_f2(ov[2] * inv, ov[3] * inv);
+            w0.z = Elem<T>::from_f2(ov[4] * inv, ov[5] * inv);
+            w0.w = Elem<T>::from_f2(ov[6] * inv, ov[7] * inv);
+            w1.x = Elem<T>::from_f2(ov[8] * inv, ov[9] * inv);
+            w1.y = Elem<T>::from_f2(ov[10] * inv, ov[11] * inv);
+            w1.z = Elem<T>::from_f2(ov[12] * inv, ov[13] * inv);
+            w1.w = Elem<T>::from_f2(ov[14] * inv, ov[15] * inv);
+            reinterpret_cast<uint4*>(out + c)[0] = w0;
+            reinterpret_cast<uint4*>(out + c)[1] = w1;
+          }
+        }
+      }
+    }
+    if (!good && lane == 0) set_status(p.status, PA_DEV_TIMEOUT);
+  }
+
+  // ---- free TMEM once every warp is done with it
+  tc5::fence_before();
+  __syncthreads();
+  if (mma_warp) {
+    tc5::fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(L::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace pa

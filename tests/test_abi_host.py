@@ -258,7 +258,7 @@ def test_prefill_plan_tiles_cover_every_row_once(lib):
         G = hq // hkv
         seen = set()
         for b, g, tok0, ntok in tiles:
-            assert 1 <= ntok <= 64 // G and tok0 + ntok <= qls[b]
+            assert 1 <= ntok <= int(blob[8]) // G and tok0 + ntok <= qls[b]
             for i in range(tok0, tok0 + ntok):
                 seen.add((int(b), int(g), i))
         assert seen == {(b, g, i) for b in range(len(lens)) for g in range(hkv)
