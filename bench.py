@@ -164,10 +164,21 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources the split-decode kernels and their launches are built from: the
+# kernels, the device helpers, the planner that sets the grid, and the C-ABI
+# that fills the launch parameters.
+DECODE_SOURCES = ("api.cu", "device_common.cuh", "elem.cuh", "quant_common.cuh",
+                  "split_launch.cuh", "pa_internal.h", "launch.h", "plan.cpp")
+
+
 def kernel_source_hash():
+    """Hash of the split-decode sources, stamped on the committed DRAM-traffic
+    capture so that a changed kernel reports no stale traffic."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_24_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if not (name.startswith("decode") or name in DECODE_SOURCES):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "decode_kernel.cuh"
@@ -120,6 +121,26 @@ pa_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return PA_OK;
   (void)cudaGetLastError();  // clear a sticky launch error so later calls report their own
   return PA_ERR_CUDA;
+}
+
+// CTAs in the split kernel's first wave on the current device: its SMs (read
+// once per device) times the CTAs one SM holds (the planner's estimate).
+int first_wave_ctas(int head_dim, int group) {
+  static std::atomic<int> sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  int n = sms[dev & 63].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    sms[dev & 63].store(n, std::memory_order_relaxed);
+  }
+  return n * resident_ctas_per_sm(head_dim, group);
 }
 
 }  // namespace
@@ -348,6 +369,13 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.num_split_items = plan->num_split_items;
   p.num_ctas = plan->num_ctas;
   p.num_shared = plan->num_shared_ctas;
+  // Only the first wave's CTAs can start before the previous kernel ends, so
+  // only they prefetch.  PA_L2_PREFETCH_PAGES (0..32) and PA_L2_PREFETCH_CTAS
+  // override both for experiments; read once per process.
+  static const int pf_pages = env_int("PA_L2_PREFETCH_PAGES", kL2PrefetchPages, 0, 32);
+  static const int pf_ctas = env_int("PA_L2_PREFETCH_CTAS", -1, 0, INT32_MAX);
+  p.pf_pages = pf_pages;
+  p.pf_ctas = pf_ctas >= 0 ? pf_ctas : first_wave_ctas(D, G);
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;

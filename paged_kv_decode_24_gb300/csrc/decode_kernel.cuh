@@ -87,7 +87,30 @@ struct SplitParams {
   const int8_t* v_codes;
   const float* k_scales;
   const float* v_scales;
+  // L2 prefetch before the wait on the previous kernel: CTAs [0, pf_ctas)
+  // prefetch the first pf_pages (<= 32) pages of each warp's share.
+  int32_t pf_pages, pf_ctas;
 };
+
+// Before the wait on the previous kernel, lane k of a warp may prefetch page
+// k of the warp's share of task `it` (page j = warp + k * NW of a shared
+// task, j = k of a warp's own task) into L2.  Returns that page's physical
+// index, or -1.  The prefetch is only a hint: the previous kernel may still
+// rewrite the block table, so the entry is read through L2 (ld.global.cg
+// leaves no stale line in L1 for the reads after the wait), every index is
+// bounded to its buffer, and nothing depends on the prefetched bytes.
+template <int NW>
+__device__ __forceinline__ int prefetch_page_of_lane(const SplitParams& p, int4 it, bool coop,
+                                                     int warp, int lane) {
+  if (lane >= p.pf_pages) return -1;
+  const int b = it.x, kvh = (int)((uint32_t)it.y & kItemHeadMask), pg0 = it.z, pg1 = it.w;
+  if (b < 0 || b >= p.batch || kvh >= p.num_kv_heads || pg0 < 0 || pg1 < pg0 || pg1 > p.max_pages)
+    return -1;
+  const int j = coop ? warp + lane * NW : lane;
+  if (j >= pg1 - pg0) return -1;
+  const int phys = __ldcg(p.block_table + (size_t)b * p.max_pages + pg0 + j);
+  return (phys >= 0 && phys < p.num_pages) ? phys : -1;
+}
 
 template <int D, int G>
 struct Geometry {
@@ -207,6 +230,15 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     slot = p.item_slots[task];
   }
 
+  if (task >= 0 && task < p.num_items && (int)blockIdx.x < p.pf_ctas) {
+    const int phys = prefetch_page_of_lane<NW>(p, it, coop, warp, lane);
+    if (phys >= 0) {
+      const size_t off = ((size_t)phys * p.num_kv_heads + ((uint32_t)it.y & kItemHeadMask)) *
+                         (kPageSize * D);
+      prefetch_l2_bulk(static_cast<const T*>(p.k_pages) + off, L::TILE);
+      prefetch_l2_bulk(static_cast<const T*>(p.v_pages) + off, L::TILE);
+    }
+  }
   if (threadIdx.x == 0) cta_failed = 0;
   if (lane == 0) {
 #pragma unroll

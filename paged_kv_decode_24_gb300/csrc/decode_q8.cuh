@@ -148,6 +148,17 @@ __global__ void __launch_bounds__(NW * 32, 4)
     it = p.items[task];
     slot = p.item_slots[task];
   }
+  if (task >= 0 && task < p.num_items && (int)blockIdx.x < p.pf_ctas) {
+    const int phys = prefetch_page_of_lane<NW>(p, it, coop, warp, lane);
+    if (phys >= 0) {
+      const size_t row0 = ((size_t)phys * p.num_kv_heads + ((uint32_t)it.y & kItemHeadMask)) *
+                          kPageSize;
+      prefetch_l2_bulk(p.k_codes + row0 * D, kPageSize * D);
+      prefetch_l2_bulk(p.v_codes + row0 * D, kPageSize * D);
+      prefetch_l2_bulk(p.k_scales + row0, kPageSize * 4);
+      prefetch_l2_bulk(p.v_scales + row0, kPageSize * 4);
+    }
+  }
   if (threadIdx.x == 0) {
     *cta_failed = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");

@@ -84,6 +84,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Ask L2 to fetch [src, src + bytes): src 16-byte aligned, bytes a multiple
+// of 16.  Nothing tracks or waits for its completion.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 policy for data read exactly once per call (the KV pages).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;

@@ -3,6 +3,7 @@
 
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "pagedattn.h"
 
@@ -20,10 +21,22 @@ constexpr int kMaxSplits = 1024;     // per (sequence, KV head); the combine kee
 constexpr int kMinChunkPages = 48;   // auto planner never cuts finer than this
 constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per warp
 constexpr int kPlanWaves = 2;        // auto planner: tasks ~ waves x resident CTAs
+constexpr int kL2PrefetchPages = 2;  // pages per warp asked of L2 before the wait on the previous kernel
 constexpr int kBundleWhenOver = 3;   // bundle short tasks only past this many tasks per CTA slot
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
+
+// Integer tuning knob from the environment, for experiments: `fallback`
+// unless the variable holds an integer in [lo, hi].
+inline int env_int(const char* name, int fallback, int lo, int hi) {
+  const char* v = getenv(name);
+  if (!v || !*v) return fallback;
+  char* end = nullptr;
+  const long x = strtol(v, &end, 10);
+  if (end == v || x < lo || x > hi) return fallback;
+  return (int)x;
+}
 
 // Item flags live in the top bits of the kv_head word.
 constexpr uint32_t kItemSplit = 0x80000000u;  // writes a partial (o, lse) instead of out

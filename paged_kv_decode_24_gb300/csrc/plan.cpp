@@ -37,17 +37,6 @@ pa_status_t check_shape(const pa_shape_t* s) {
 
 namespace {
 
-// Planner tuning, overridable through the environment for experiments:
-// PA_PLAN_MIN_CHUNK (pages), PA_PLAN_BUNDLE_MAX (pages), PA_PLAN_WAVES.
-int env_int(const char* name, int fallback, int lo, int hi) {
-  const char* v = getenv(name);
-  if (!v || !*v) return fallback;
-  char* end = nullptr;
-  const long x = strtol(v, &end, 10);
-  if (end == v || x < lo || x > hi) return fallback;
-  return (int)x;
-}
-
 uint64_t next_plan_id() {
   static std::atomic<uint64_t> counter{
       (uint64_t)std::chrono::high_resolution_clock::now().time_since_epoch().count() * 2654435761u};
@@ -87,6 +76,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
   // that the task count is about three times the CTAs the GPU holds at once
   // (one CTA per task), never finer than kMinChunkPages.
+  // Overridable for experiments: PA_PLAN_MIN_CHUNK, PA_PLAN_BUNDLE_MAX (pages), PA_PLAN_WAVES.
   const int min_chunk = env_int("PA_PLAN_MIN_CHUNK", kMinChunkPages, 1, 1 << 20);
   const int bundle_max = env_int("PA_PLAN_BUNDLE_MAX", kBundleMaxPages, 0, 1 << 20);
   const int waves = env_int("PA_PLAN_WAVES", kPlanWaves, 1, 64);
