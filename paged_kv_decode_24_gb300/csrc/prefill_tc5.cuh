@@ -2,26 +2,29 @@
 // the same operation and tiles as prefill.cuh, with 128-row MMAs issued by
 // one thread from shared-memory descriptors into tensor memory (TMEM).
 //
-// A CTA of 4 warps owns 128 query rows of one (sequence, KV head): 128 / G
-// query tokens times the G heads of the KV head.  Thread r of the CTA owns
-// row r, which is TMEM lane r, so a row's softmax needs no shuffles.
+// A CTA owns 128 query rows of one (sequence, KV head): 128 / G query tokens
+// times the G heads of the KV head.  Thread r of warps 0-3 owns row r, which
+// is TMEM lane r, so a row's softmax needs no shuffles.  Warp 4 issues the
+// MMAs and warp 5 the copies; the six warps meet only on mbarriers.
 // Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
 // TMA copies write and the MMA descriptors read):
 //   Q   [D/64 boxes][128 rows][128 B]         A operand of S, K-major
-//   NS stages of 32 tokens (two pages), each
+//   a ring of NK key stages of 32 tokens (two pages), each
 //     K [D/64 boxes][32 tokens][128 B]        B operand of S, K-major
+//   a ring of NV value stages of 32 tokens, each
 //     V [D/64 boxes][32 tokens][128 B]        B operand of P.V, MN-major
 //   P   2 x [128 rows][64 B], 64-byte swizzle  A operand of P.V, K-major
 // TMEM: two S buffers of 32 columns and O of D columns.
 //
-// Per stage kt (thread 0 issues, all threads compute):
+// Per stage kt:
 //   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 32)       committed to s_done
 //   row softmax of S(kt) in registers (tcgen05.ld), lazy rescaling
-//   P(kt) to shared memory, once P.V(kt-1) has finished reading it
+//   P(kt) to shared memory, once P.V(kt-2) has finished reading its buffer
 //   O += P V       (2 MMAs, M = 128, N = D, K = 32)    committed to pv_done
 // S(kt+1) is issued before the softmax of kt, and P is double-buffered, so
-// the tensor core works while the threads compute.  A stage is refilled once
-// P.V has read it.
+// the tensor core works while the threads compute.  Keys and values have
+// rings of their own: a key stage is refilled as soon as S has read it, a
+// value stage once P.V has, so copies run several stages ahead of the MMAs.
 // Every wait is bounded; on failure the CTA waits (bounded) for its copies
 // and MMAs, frees its TMEM and writes nothing.
 #pragma once
@@ -109,40 +112,53 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// L2 policy for the keys and values: the other tiles of the sequence read
+// them again.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace tc5
 
-constexpr int kTc5Rows = 128;   // query rows per CTA (one TMEM lane each)
-constexpr int kTc5Tokens = 32;  // keys per stage (two pages)
-constexpr int kTc5Stages = 3;
+constexpr int kTc5Rows = 128;    // query rows per CTA (one TMEM lane each)
+constexpr int kTc5Tokens = 32;   // keys per stage (two pages)
+constexpr int kTc5Threads = 192; // row warps 0-3, MMA warp 4, copy warp 5
 
+// Two CTAs share an SM (shared memory ~105 KB and 256 TMEM columns each).
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
+  static constexpr int NK = D == 128 ? 4 : 6;                   // key stages
+  static constexpr int NV = D == 128 ? 3 : 5;                   // value stages
   static constexpr int Q = 0;                                   // BOXES x 16 KB
   static constexpr int QBOX = kTc5Rows * 128;
   static constexpr int KVBOX = kTc5Tokens * 128;                // 4 KB per box
-  static constexpr int STAGE0 = Q + BOXES * QBOX;
-  static constexpr int STAGE = 2 * BOXES * KVBOX;               // K boxes, then V boxes
-  static constexpr int P = STAGE0 + kTc5Stages * STAGE;        // 2 x 8 KB
+  static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
+  static constexpr int K0 = Q + BOXES * QBOX;
+  static constexpr int V0 = K0 + NK * STAGE;
+  static constexpr int P = V0 + NV * STAGE;                     // 2 x 8 KB
   static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
-  // full[NS], s_done[2], s_free[2], pv_done[2], p_ready, drain
+  // k_full[NK], k_free[NK], v_full[NV], v_free[NV], s_done[2], s_free[2],
+  // pv_done[2], p_ready, drain
   static constexpr int BARS = P + 2 * PBUF;
-  static constexpr int TMEM_SLOT = align_up(BARS + 8 * (kTc5Stages + 8), 16);
+  static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 8), 16);
   static constexpr int FLAG = TMEM_SLOT + 16;
   static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
   static constexpr uint32_t TMEM_COLS = 256;                    // S0, S1 (32 each), O (D)
 };
 
-// 160 threads: warps 0-3 own the 128 rows (softmax, output), warp 4 issues
-// the copies and the MMAs.  They meet only on mbarriers.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kTc5Threads, 1)
+    prefill_tc5_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   using L = Tc5Layout<D>;
-  constexpr int NS = kTc5Stages;
+  constexpr int NK = L::NK;
+  constexpr int NV = L::NV;
   constexpr int BN = kTc5Tokens;
   constexpr int TOKS = kTc5Rows / G;
   extern __shared__ unsigned char smem_dyn[];
@@ -153,8 +169,13 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool mma_warp = warp == 4;
-  const uint32_t full = sbase + L::BARS;        // NS barriers: the stage's copies landed
-  const uint32_t s_done = full + 8 * NS;        // 2: S(kt) computed
+  const bool copy_warp = warp == 5;
+  const bool row_warp = warp < 4;
+  const uint32_t k_full = sbase + L::BARS;      // NK: a key stage's copies landed
+  const uint32_t k_free = k_full + 8 * NK;      // NK: S has read a key stage
+  const uint32_t v_full = k_free + 8 * NK;      // NV: a value stage's copies landed
+  const uint32_t v_free = v_full + 8 * NV;      // NV: P.V has read a value stage
+  const uint32_t s_done = v_free + 8 * NV;      // 2: S(kt) computed
   const uint32_t s_free = s_done + 16;          // 2: S(kt) read by the 4 row warps
   const uint32_t pv_done = s_free + 16;         // 2: P.V(kt) computed
   const uint32_t p_ready = pv_done + 16;        // P(kt) written, O rescaled, by the 4 row warps
@@ -168,7 +189,14 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
     *cta_flag = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
-    for (int s = 0; s < NS; ++s) mbar_init(full + 8 * s, 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_free + 8 * s, 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_free + 8 * s, 1);
+    }
     mbar_init(s_done, 1);
     mbar_init(s_done + 8, 1);
     mbar_init(s_free, 4);
@@ -222,10 +250,10 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
   // ---- Q tile into shared memory (row = thread of warps 0-3), zero past ntok
   const int row = tid & 127;
   const int tt = row / G;                 // query token of this row within the tile
-  const bool ok = !bad && !mma_warp && tt < ntok;
+  const bool ok = !bad && row_warp && tt < ntok;
   const int qpos = pos0 + tt;             // its position
   const size_t qrow = ((size_t)(cu0 + tok0 + tt) * p.num_q_heads + (size_t)g * G + row % G) * D;
-  if (!mma_warp) {
+  if (row_warp) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow);
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
@@ -237,12 +265,17 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
   }
   __syncthreads();
 
-  if (mma_warp) {
-    // ================= copies and MMAs (lane 0) =================
+  if (copy_warp) {
+    // ================= copies (lane 0) =================
+    // Stage kt holds pages 2kt and 2kt+1 of the sequence; a page past the
+    // span or with an invalid index is not copied (its rows are masked, and
+    // the row warps zero its value rows before P.V reads them).
     if (lane == 0 && nkt > 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      auto issue = [&](int kt) {
-        const int s = kt % NS;
+      const uint64_t policy = tc5::l2_evict_normal_policy();
+      const uint32_t kv_bytes = (uint32_t)(D * kPageSize * 2);
+      int nk = 0, nv = 0;  // key and value stages issued
+      bool good = true;
+      for (int kt = 0; kt < nkt && good; ++kt) {
         int phys[2];
         int nvalid = 0;
         for (int u = 0; u < 2; ++u) {
@@ -258,39 +291,71 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
           phys[u] = ph;
           nvalid += ph >= 0;
         }
-        const uint32_t bar = full + 8 * s;
+        // keys: the slot is free once S(kt - NK) has been computed
+        const int sk = kt % NK;
+        good = kt < NK || mbar_wait_bounded(k_free + 8 * sk, (uint32_t)((kt / NK - 1) & 1));
+        if (!good) break;
+        const uint32_t kbar = k_full + 8 * sk;
         if (nvalid == 0) {
-          mbar_arrive(bar);
-          return;
+          mbar_arrive(kbar);
+        } else {
+          mbar_arrive_expect_tx(kbar, (uint32_t)nvalid * kv_bytes);
+          for (int u = 0; u < 2; ++u)
+            if (phys[u] >= 0)
+              for (int bx = 0; bx < L::BOXES; ++bx)
+                tma_load_4d(sbase + L::K0 + sk * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_k,
+                            bx * 64, 0, g, phys[u], kbar, policy);
         }
-        mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * 2 * D * kPageSize * 2));
-        const uint32_t st = sbase + L::STAGE0 + s * L::STAGE;
-        for (int u = 0; u < 2; ++u) {
-          if (phys[u] < 0) continue;
-          for (int bx = 0; bx < L::BOXES; ++bx) {
-            tma_load_4d(st + bx * L::KVBOX + u * 2048, &p.tmap_k, bx * 64, 0, g, phys[u], bar, policy);
-            tma_load_4d(st + (L::BOXES + bx) * L::KVBOX + u * 2048, &p.tmap_v, bx * 64, 0, g,
-                        phys[u], bar, policy);
-          }
+        ++nk;
+        // values: the slot is free once P.V(kt - NV) has been computed
+        const int sv = kt % NV;
+        good = kt < NV || mbar_wait_bounded(v_free + 8 * sv, (uint32_t)((kt / NV - 1) & 1));
+        if (!good) break;
+        const uint32_t vbar = v_full + 8 * sv;
+        if (nvalid == 0) {
+          mbar_arrive(vbar);
+        } else {
+          mbar_arrive_expect_tx(vbar, (uint32_t)nvalid * kv_bytes);
+          for (int u = 0; u < 2; ++u)
+            if (phys[u] >= 0)
+              for (int bx = 0; bx < L::BOXES; ++bx)
+                tma_load_4d(sbase + L::V0 + sv * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_v,
+                            bx * 64, 0, g, phys[u], vbar, policy);
         }
-      };
+        ++nv;
+      }
+      if (!good) {
+        set_status(p.status, PA_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int*>(cta_flag) = 1;
+      }
+      // copies in flight land before the CTA exits: the last stage issued
+      // into each slot (on success all of them have been consumed already)
+      for (int k = nk - NK < 0 ? 0 : nk - NK; k < nk; ++k)
+        mbar_wait_bounded(k_full + 8 * (k % NK), (uint32_t)((k / NK) & 1), 10000000ull);
+      for (int k = nv - NV < 0 ? 0 : nv - NV; k < nv; ++k)
+        mbar_wait_bounded(v_full + 8 * (k % NV), (uint32_t)((k / NV) & 1), 10000000ull);
+    }
+    __syncwarp();
+  } else if (mma_warp) {
+    // ================= MMAs (lane 0) =================
+    if (lane == 0 && nkt > 0) {
       const uint32_t idesc_s = tc5::instr_desc<T>(128, BN, false);
       const uint32_t idesc_o = tc5::instr_desc<T>(128, D, true);
       auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T into S buffer kt & 1
-        if (!mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1))) return false;
+        const int sk = kt % NK;
+        if (!mbar_wait_bounded(k_full + 8 * sk, (uint32_t)((kt / NK) & 1))) return false;
         tc5::fence_after();
-        const uint32_t kst = sbase + L::STAGE0 + (kt % NS) * L::STAGE;
+        const uint32_t kst = sbase + L::K0 + sk * L::STAGE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t a = tc5::smem_desc(sbase + L::Q + (k >> 2) * L::QBOX + (k & 3) * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
           tc5::mma(t_s0 + (uint32_t)((kt & 1) * BN), a, bd, idesc_s, k > 0 ? 1u : 0u);
         }
+        tc5::commit(k_free + 8 * sk);
         tc5::commit(s_done + 8 * (kt & 1));
         return true;
       };
-      int issued = 0;
-      for (; issued < nkt && issued < NS; ++issued) issue(issued);
       bool good = issue_s(0);
       for (int kt = 0; kt < nkt && good; ++kt) {
         if (kt + 1 < nkt) {
@@ -299,10 +364,12 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
           good = good && issue_s(kt + 1);
           if (!good) break;
         }
-        good = mbar_wait_bounded(p_ready, (uint32_t)(kt & 1));
+        const int sv = kt % NV;
+        good = mbar_wait_bounded(p_ready, (uint32_t)(kt & 1)) &&
+               mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1));
         if (!good) break;
         tc5::fence_after();
-        const uint32_t vst = sbase + L::STAGE0 + (kt % NS) * L::STAGE + L::BOXES * L::KVBOX;
+        const uint32_t vst = sbase + L::V0 + sv * L::STAGE;
         const uint32_t pst = sbase + L::P + (kt & 1) * L::PBUF;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
@@ -310,25 +377,17 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
           const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
           tc5::mma(t_o, a, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
         }
+        tc5::commit(v_free + 8 * sv);
         tc5::commit(pv_done + 8 * (kt & 1));
-        // the stage of kt-1 is free once P.V(kt-1) has read it (issued an
-        // iteration ago, so normally done by now)
-        if (kt >= 1 && issued < nkt && issued == kt - 1 + NS) {
-          good = mbar_wait_bounded(pv_done + 8 * ((kt - 1) & 1), (uint32_t)(((kt - 1) >> 1) & 1));
-          if (!good) break;
-          issue(issued++);
-        }
       }
       if (!good) {
         set_status(p.status, PA_DEV_TIMEOUT);
-        *cta_flag = 1;
-        // every MMA issued must finish before TMEM is freed: one more commit
-        // covers them all
-        tc5::commit(drain);
-        mbar_wait_bounded(drain, 0u, 10000000ull);
+        *reinterpret_cast<volatile int*>(cta_flag) = 1;
       }
-      for (int kt = issued - NS < 0 ? 0 : issued - NS; kt < issued; ++kt)  // copies in flight
-        mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1), 10000000ull);
+      // every MMA issued finishes before TMEM is freed: one more commit
+      // covers them all
+      tc5::commit(drain);
+      mbar_wait_bounded(drain, 0u, 10000000ull);
     }
     __syncwarp();
   } else {
@@ -448,8 +507,12 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
                                   ((ch ^ ((row >> 1) & 3)) << 4)) = v;
       }
       if (kv0 + BN > span) {
+        // after the stage's value copies have landed, which would overwrite
+        const int sv = kt % NV;
+        good = __all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1)));
+        if (!good) break;
         const int first_bad = span - kv0;  // tokens [first_bad, BN) of this stage
-        unsigned char* vsm = base + L::STAGE0 + (kt % NS) * L::STAGE + L::BOXES * L::KVBOX;
+        unsigned char* vsm = base + L::V0 + sv * L::STAGE;
         for (int i = row; i < L::BOXES * BN * 8; i += 128) {  // 16-byte chunks
           const int bx = i / (BN * 8), r = (i / 8) % BN, ch = i % 8;
           if (r >= first_bad)
@@ -465,6 +528,9 @@ __global__ void __launch_bounds__(160, 1) prefill_tc5_kernel(const __grid_consta
     if (nkt > 0 && good) {
       good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
                                                  (uint32_t)(((nkt - 1) >> 1) & 1)));
+      // a copy or MMA warp that gave up leaves O incomplete: write nothing
+      good = good && *reinterpret_cast<volatile int*>(cta_flag) == 0;
+      good = __all_sync(kFull, good);
       if (good) {
         tc5::fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

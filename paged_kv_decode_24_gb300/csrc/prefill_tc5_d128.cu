@@ -14,7 +14,7 @@ cudaError_t launch_g(const PrefillParams& p, cudaStream_t stream) {
   static_assert(smem <= kMaxCtaSmem, "prefill CTA does not fit in shared memory");
   static std::atomic<unsigned long long> configured{0};
   auto kern = prefill_tc5_kernel<T, D, G>;
-  return launch_pdl(kern, smem, configured, p, p.num_tiles, 160, stream);
+  return launch_pdl(kern, smem, configured, p, p.num_tiles, kTc5Threads, stream);
 }
 
 template <typename T>
