@@ -6,15 +6,18 @@
 // times the G heads of the KV head.  Thread r of warps 0-3 owns row r, which
 // is TMEM lane r, so a row's softmax needs no shuffles.  Warp 4 issues the
 // MMAs and warp 5 the copies; the six warps meet only on mbarriers.
+// Q sits in TMEM (row r in lane r), where the S MMAs read it as their A
+// operand: from shared memory, re-reading the 128 x D tile for every 32 keys
+// would take more shared-memory bandwidth than the tensor core's math.
 // Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
 // TMA copies write and the MMA descriptors read):
-//   Q   [D/64 boxes][128 rows][128 B]         A operand of S, K-major
 //   a ring of NK key stages of 32 tokens (two pages), each
 //     K [D/64 boxes][32 tokens][128 B]        B operand of S, K-major
 //   a ring of NV value stages of 32 tokens, each
 //     V [D/64 boxes][32 tokens][128 B]        B operand of P.V, MN-major
 //   P   2 x [128 rows][64 B], 64-byte swizzle  A operand of P.V, K-major
-// TMEM: two S buffers of 32 columns and O of D columns.
+// TMEM: two S buffers of 32 columns, O of D columns, Q of D/2 columns (two
+// 16-bit elements per 32-bit column).
 //
 // Per stage kt:
 //   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 32)       committed to s_done
@@ -72,6 +75,17 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
       : "memory");
 }
 
+// The same with A (M x K, K-major) read from TMEM: row m in lane m, two
+// 16-bit elements per 32-bit column.
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -97,6 +111,15 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float* v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 __device__ __forceinline__ void st16(uint32_t taddr, const float* v) {
@@ -129,17 +152,15 @@ constexpr int kTc5Rows = 128;    // query rows per CTA (one TMEM lane each)
 constexpr int kTc5Tokens = 32;   // keys per stage (two pages)
 constexpr int kTc5Threads = 192; // row warps 0-3, MMA warp 4, copy warp 5
 
-// Two CTAs share an SM (shared memory ~105 KB and 256 TMEM columns each).
+// Two CTAs share an SM (256 TMEM columns each).
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
-  static constexpr int NK = D == 128 ? 4 : 6;                   // key stages
-  static constexpr int NV = D == 128 ? 3 : 5;                   // value stages
-  static constexpr int Q = 0;                                   // BOXES x 16 KB
-  static constexpr int QBOX = kTc5Rows * 128;
+  static constexpr int NK = D == 128 ? 5 : 8;                   // key stages
+  static constexpr int NV = D == 128 ? 4 : 6;                   // value stages
   static constexpr int KVBOX = kTc5Tokens * 128;                // 4 KB per box
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
-  static constexpr int K0 = Q + BOXES * QBOX;
+  static constexpr int K0 = 0;
   static constexpr int V0 = K0 + NK * STAGE;
   static constexpr int P = V0 + NV * STAGE;                     // 2 x 8 KB
   static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
@@ -149,7 +170,7 @@ struct Tc5Layout {
   static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 8), 16);
   static constexpr int FLAG = TMEM_SLOT + 16;
   static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
-  static constexpr uint32_t TMEM_COLS = 256;                    // S0, S1 (32 each), O (D)
+  static constexpr uint32_t TMEM_COLS = 256;                    // S0, S1 (32 each), O (D), Q (D/2)
 };
 
 template <typename T, int D, int G>
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::TMEM_SLOT);
-  const uint32_t t_s0 = tmem, t_o = tmem + 2 * BN;       // columns: S0, S1, O
+  const uint32_t t_s0 = tmem, t_o = tmem + 2 * BN, t_q = t_o + D;  // columns: S0, S1, O, Q
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
 
   pdl_launch_dependents();
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
   const int nkt = bad ? 0 : (span + BN - 1) / BN;
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
 
-  // ---- Q tile into shared memory (row = thread of warps 0-3), zero past ntok
+  // ---- Q tile into TMEM (row = thread of warps 0-3), zero past ntok
   const int row = tid & 127;
   const int tt = row / G;                 // query token of this row within the tile
   const bool ok = !bad && row_warp && tt < ntok;
@@ -256,14 +277,23 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
   if (row_warp) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow);
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-      const int bx = c >> 3, ch = c & 7;
-      *reinterpret_cast<uint4*>(base + L::Q + bx * L::QBOX + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
+    for (int c = 0; c < D / 32; ++c) {  // 16 columns = 32 elements per store
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = ok ? __ldg(src + 4 * c + i) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+      tc5::st16u(t_q + (uint32_t)(16 * c) + lane_off, w);
     }
-    fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
+    tc5::wait_st();
   }
+  tc5::fence_before();
   __syncthreads();
+  tc5::fence_after();
 
   if (copy_warp) {
     // ================= copies (lane 0) =================
@@ -348,9 +378,9 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
         const uint32_t kst = sbase + L::K0 + sk * L::STAGE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t a = tc5::smem_desc(sbase + L::Q + (k >> 2) * L::QBOX + (k & 3) * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
-          tc5::mma(t_s0 + (uint32_t)((kt & 1) * BN), a, bd, idesc_s, k > 0 ? 1u : 0u);
+          tc5::mma_tmem_a(t_s0 + (uint32_t)((kt & 1) * BN), t_q + (uint32_t)(8 * k), bd, idesc_s,
+                          k > 0 ? 1u : 0u);
         }
         tc5::commit(k_free + 8 * sk);
         tc5::commit(s_done + 8 * (kt & 1));
