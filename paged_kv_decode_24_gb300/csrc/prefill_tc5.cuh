@@ -7,27 +7,28 @@
 // is TMEM lane r, so a row's softmax needs no shuffles.  Warp 4 issues the
 // MMAs and warp 5 the copies; the six warps meet only on mbarriers.
 // Q sits in TMEM (row r in lane r), where the S MMAs read it as their A
-// operand: from shared memory, re-reading the 128 x D tile for every 32 keys
-// would take more shared-memory bandwidth than the tensor core's math.
+// operand, so the 128 x D tile is not re-read from shared memory per stage.
 // Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
 // TMA copies write and the MMA descriptors read):
-//   a ring of NK key stages of 32 tokens (two pages), each
-//     K [D/64 boxes][32 tokens][128 B]        B operand of S, K-major
-//   a ring of NV value stages of 32 tokens, each
-//     V [D/64 boxes][32 tokens][128 B]        B operand of P.V, MN-major
-//   P   2 x [128 rows][64 B], 64-byte swizzle  A operand of P.V, K-major
-// TMEM: two S buffers of 32 columns, O of D columns, Q of D/2 columns (two
-// 16-bit elements per 32-bit column).
+//   a ring of NK key stages of 64 tokens (four pages), each
+//     K [D/64 boxes][64 tokens][128 B]        B operand of S, K-major
+//   a ring of NV value stages of 64 tokens, each
+//     V [D/64 boxes][64 tokens][128 B]        B operand of P.V, MN-major
+//   P   2 x [128 rows][128 B]                 A operand of P.V, K-major
+// TMEM: S of 64 columns, O of D columns, Q of D/2 columns (two 16-bit
+// elements per 32-bit column).
 //
 // Per stage kt:
-//   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 32)       committed to s_done
-//   row softmax of S(kt) in registers (tcgen05.ld), lazy rescaling
+//   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 64)       committed to s_done
+//   the row threads load S(kt) into registers and release its columns;
+//   S(kt+1) is issued at once and runs while they compute
+//   row softmax of S(kt) in registers, lazy rescaling
 //   P(kt) to shared memory, once P.V(kt-2) has finished reading its buffer
-//   O += P V       (2 MMAs, M = 128, N = D, K = 32)    committed to pv_done
-// S(kt+1) is issued before the softmax of kt, and P is double-buffered, so
-// the tensor core works while the threads compute.  Keys and values have
-// rings of their own: a key stage is refilled as soon as S has read it, a
-// value stage once P.V has, so copies run several stages ahead of the MMAs.
+//   O += P V       (4 MMAs, M = 128, N = D, K = 64)    committed to pv_done
+// Keys and values have rings of their own: a key stage is refilled as soon
+// as S has read it, a value stage once P.V has.  Sixty-four keys per stage
+// spread each stage's fixed costs (waits, fences, TMEM loads) over twice the
+// keys of a two-page stage.
 // Every wait is bounded; on failure the CTA waits (bounded) for its copies
 // and MMAs, frees its TMEM and writes nothing.
 #pragma once
@@ -148,33 +149,34 @@ __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.
 
 }  // namespace tc5
 
-constexpr int kTc5Rows = 128;    // query rows per CTA (one TMEM lane each)
-constexpr int kTc5Tokens = 32;   // keys per stage (two pages)
-constexpr int kTc5Threads = 192; // row warps 0-3, MMA warp 4, copy warp 5
+constexpr int kTc5Rows = 128;                        // query rows per CTA (one TMEM lane each)
+constexpr int kTc5Tokens = 64;                       // keys per stage
+constexpr int kTc5Pages = kTc5Tokens / kPageSize;    // pages per stage
+constexpr int kTc5Threads = 192;                     // row warps 0-3, MMA warp 4, copy warp 5
 
-// Two CTAs share an SM (256 TMEM columns each).
+// Two CTAs share an SM (~97 KB of shared memory and 256 TMEM columns each).
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
-  static constexpr int NK = D == 128 ? 5 : 8;                   // key stages
-  static constexpr int NV = D == 128 ? 4 : 6;                   // value stages
-  static constexpr int KVBOX = kTc5Tokens * 128;                // 4 KB per box
+  static constexpr int NK = D == 128 ? 2 : 4;                   // key stages
+  static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
+  static constexpr int KVBOX = kTc5Tokens * 128;                // 8 KB per box
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
   static constexpr int K0 = 0;
   static constexpr int V0 = K0 + NK * STAGE;
-  static constexpr int P = V0 + NV * STAGE;                     // 2 x 8 KB
+  static constexpr int P = V0 + NV * STAGE;                     // 2 x 16 KB
   static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
-  // k_full[NK], k_free[NK], v_full[NV], v_free[NV], s_done[2], s_free[2],
-  // pv_done[2], p_ready, drain
+  // k_full[NK], k_free[NK], v_full[NV], v_free[NV], s_done, s_free,
+  // pv_done[2], p_ready[2], drain
   static constexpr int BARS = P + 2 * PBUF;
-  static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 8), 16);
+  static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 7), 16);
   static constexpr int FLAG = TMEM_SLOT + 16;
   static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
-  static constexpr uint32_t TMEM_COLS = 256;                    // S0, S1 (32 each), O (D), Q (D/2)
+  static constexpr uint32_t TMEM_COLS = 256;                    // S (64), O (D), Q (D/2)
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kTc5Threads, 1)
+__global__ void __launch_bounds__(kTc5Threads, 2)
     prefill_tc5_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   using L = Tc5Layout<D>;
@@ -196,11 +198,13 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
   const uint32_t k_free = k_full + 8 * NK;      // NK: S has read a key stage
   const uint32_t v_full = k_free + 8 * NK;      // NV: a value stage's copies landed
   const uint32_t v_free = v_full + 8 * NV;      // NV: P.V has read a value stage
-  const uint32_t s_done = v_free + 8 * NV;      // 2: S(kt) computed
-  const uint32_t s_free = s_done + 16;          // 2: S(kt) read by the 4 row warps
-  const uint32_t pv_done = s_free + 16;         // 2: P.V(kt) computed
-  const uint32_t p_ready = pv_done + 16;        // P(kt) written, O rescaled, by the 4 row warps
-  const uint32_t drain = p_ready + 8;           // every MMA issued has finished (failure path)
+  const uint32_t s_done = v_free + 8 * NV;      // S(kt) computed
+  const uint32_t s_free = s_done + 8;           // S(kt) loaded by the 4 row warps
+  const uint32_t pv_done = s_free + 8;          // 2: P.V(kt) computed
+  // 2: P(kt) written and O rescaled by the 4 row warps.  Two phases of one
+  // barrier could complete before the MMA warp looks at the first.
+  const uint32_t p_ready = pv_done + 16;
+  const uint32_t drain = p_ready + 16;          // every MMA issued has finished
   int* cta_flag = reinterpret_cast<int*>(base + L::FLAG);
 
   if ((int)blockIdx.x >= p.num_tiles) return;  // whole CTA
@@ -219,12 +223,11 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
       mbar_init(v_free + 8 * s, 1);
     }
     mbar_init(s_done, 1);
-    mbar_init(s_done + 8, 1);
     mbar_init(s_free, 4);
-    mbar_init(s_free + 8, 4);
     mbar_init(pv_done, 1);
     mbar_init(pv_done + 8, 1);
     mbar_init(p_ready, 4);
+    mbar_init(p_ready + 8, 4);
     mbar_init(drain, 1);
     fence_barrier_init();
   }
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::TMEM_SLOT);
-  const uint32_t t_s0 = tmem, t_o = tmem + 2 * BN, t_q = t_o + D;  // columns: S0, S1, O, Q
+  const uint32_t t_s = tmem, t_o = tmem + BN, t_q = t_o + D;  // columns: S, O, Q
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
 
   pdl_launch_dependents();
@@ -297,8 +300,8 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
 
   if (copy_warp) {
     // ================= copies (lane 0) =================
-    // Stage kt holds pages 2kt and 2kt+1 of the sequence; a page past the
-    // span or with an invalid index is not copied (its rows are masked, and
+    // Stage kt holds pages 4kt .. 4kt+3 of the sequence; a page past the
+    // span or with an invalid index is not copied (its keys are masked, and
     // the row warps zero its value rows before P.V reads them).
     if (lane == 0 && nkt > 0) {
       const uint64_t policy = tc5::l2_evict_normal_policy();
@@ -306,10 +309,11 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
       int nk = 0, nv = 0;  // key and value stages issued
       bool good = true;
       for (int kt = 0; kt < nkt && good; ++kt) {
-        int phys[2];
+        int phys[kTc5Pages];
         int nvalid = 0;
-        for (int u = 0; u < 2; ++u) {
-          const int j = 2 * kt + u;
+#pragma unroll
+        for (int u = 0; u < kTc5Pages; ++u) {
+          const int j = kTc5Pages * kt + u;
           int ph = -1;
           if (j * kPageSize < span) {
             ph = __ldg(bt_row + j);
@@ -330,7 +334,8 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
           mbar_arrive(kbar);
         } else {
           mbar_arrive_expect_tx(kbar, (uint32_t)nvalid * kv_bytes);
-          for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int u = 0; u < kTc5Pages; ++u)
             if (phys[u] >= 0)
               for (int bx = 0; bx < L::BOXES; ++bx)
                 tma_load_4d(sbase + L::K0 + sk * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_k,
@@ -346,7 +351,8 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
           mbar_arrive(vbar);
         } else {
           mbar_arrive_expect_tx(vbar, (uint32_t)nvalid * kv_bytes);
-          for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int u = 0; u < kTc5Pages; ++u)
             if (phys[u] >= 0)
               for (int bx = 0; bx < L::BOXES; ++bx)
                 tma_load_4d(sbase + L::V0 + sv * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_v,
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
     if (lane == 0 && nkt > 0) {
       const uint32_t idesc_s = tc5::instr_desc<T>(128, BN, false);
       const uint32_t idesc_o = tc5::instr_desc<T>(128, D, true);
-      auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T into S buffer kt & 1
+      auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T
         const int sk = kt % NK;
         if (!mbar_wait_bounded(k_full + 8 * sk, (uint32_t)((kt / NK) & 1))) return false;
         tc5::fence_after();
@@ -379,23 +385,21 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
-          tc5::mma_tmem_a(t_s0 + (uint32_t)((kt & 1) * BN), t_q + (uint32_t)(8 * k), bd, idesc_s,
-                          k > 0 ? 1u : 0u);
+          tc5::mma_tmem_a(t_s, t_q + (uint32_t)(8 * k), bd, idesc_s, k > 0 ? 1u : 0u);
         }
         tc5::commit(k_free + 8 * sk);
-        tc5::commit(s_done + 8 * (kt & 1));
+        tc5::commit(s_done);
         return true;
       };
       bool good = issue_s(0);
       for (int kt = 0; kt < nkt && good; ++kt) {
         if (kt + 1 < nkt) {
-          // S buffer (kt+1) & 1 last held S(kt-1): wait until the row warps read it
-          if (kt >= 1) good = mbar_wait_bounded(s_free + 8 * ((kt + 1) & 1), (uint32_t)(((kt - 1) >> 1) & 1));
-          good = good && issue_s(kt + 1);
+          // the S columns are free once the row warps have loaded S(kt)
+          good = mbar_wait_bounded(s_free, (uint32_t)(kt & 1)) && issue_s(kt + 1);
           if (!good) break;
         }
         const int sv = kt % NV;
-        good = mbar_wait_bounded(p_ready, (uint32_t)(kt & 1)) &&
+        good = mbar_wait_bounded(p_ready + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1)) &&
                mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1));
         if (!good) break;
         tc5::fence_after();
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
         const uint32_t pst = sbase + L::P + (kt & 1) * L::PBUF;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = tc5::smem_desc(pst + k * 32, 16, 512, 4);  // 64-byte swizzle
+          const uint64_t a = tc5::smem_desc(pst + k * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
           tc5::mma(t_o, a, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
         }
@@ -425,37 +429,45 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool good = true;
     // block-table entries of the stage, loaded one stage ahead (page checks
-    // mask the tokens of a page that was not copied)
-    int nph0 = nkt > 0 ? __ldg(bt_row) : -1;
-    int nph1 = nkt > 0 && kPageSize < span ? __ldg(bt_row + 1) : -1;
+    // mask the keys of a page that was not copied)
+    int nph[kTc5Pages];
+#pragma unroll
+    for (int u = 0; u < kTc5Pages; ++u) nph[u] = nkt > 0 && u * kPageSize < span ? __ldg(bt_row + u) : -1;
     for (int kt = 0; kt < nkt; ++kt) {
-      const int ph0 = nph0, ph1 = nph1;
-      if (kt + 1 < nkt) {
-        nph0 = __ldg(bt_row + 2 * kt + 2);
-        nph1 = (2 * kt + 3) * kPageSize < span ? __ldg(bt_row + 2 * kt + 3) : -1;
+      bool pgv[kTc5Pages];
+      bool all_pages = true;
+#pragma unroll
+      for (int u = 0; u < kTc5Pages; ++u) {
+        pgv[u] = nph[u] >= 0 && nph[u] < p.num_pages;
+        all_pages = all_pages && pgv[u];
       }
-      good = __all_sync(kFull, mbar_wait_bounded(s_done + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1)));
+      if (kt + 1 < nkt) {
+#pragma unroll
+        for (int u = 0; u < kTc5Pages; ++u) {
+          const int j = kTc5Pages * (kt + 1) + u;
+          nph[u] = j * kPageSize < span ? __ldg(bt_row + j) : -1;
+        }
+      }
+      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1)));
       if (!good) break;
       tc5::fence_after();
       float sv[BN];
-      tc5::ld16(t_s0 + (uint32_t)((kt & 1) * BN) + lane_off, sv);
-      tc5::ld16(t_s0 + (uint32_t)((kt & 1) * BN) + 16 + lane_off, sv + 16);
+#pragma unroll
+      for (int c = 0; c < BN; c += 16) tc5::ld16(t_s + (uint32_t)c + lane_off, sv + c);
       tc5::wait_ld();
       tc5::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free + 8 * (kt & 1));
+      if (lane == 0) mbar_arrive(s_free);
 
       // ---- mask, row max (lazy), weights
       const int kv0 = BN * kt;
-      const bool pg0 = ph0 >= 0 && ph0 < p.num_pages;
-      const bool pg1 = ph1 >= 0 && ph1 < p.num_pages;
       // visible iff the page was copied and the key is not after the query;
       // a stage every lane of the warp sees whole skips the per-key test
       const int lim = ok ? qpos - kv0 : -1;  // last visible column of the stage
-      if (!__all_sync(kFull, pg0 && pg1 && lim >= BN - 1)) {
+      if (!__all_sync(kFull, all_pages && lim >= BN - 1)) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
-          const bool vis = (c < 16 ? pg0 : pg1) && c <= lim;
+          const bool vis = pgv[c / kPageSize] && c <= lim;
           sv[c] = vis ? sv[c] : -INFINITY;
         }
       }
@@ -527,22 +539,22 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
         }
         tc5::wait_st();
       }
-      // ---- P(kt) row into its buffer (K-major, 64-byte swizzle: 16-byte
-      // chunk c of row r at chunk c ^ ((r / 2) % 4)); V rows past the span
+      // ---- P(kt) row into its buffer (K-major, 128-byte swizzle: 16-byte
+      // chunk c of row r at chunk c ^ (r % 8)); value rows past the span
       // (which may hold anything) become zeros
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {
         const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(base + L::P + (kt & 1) * L::PBUF + row * 64 +
-                                  ((ch ^ ((row >> 1) & 3)) << 4)) = v;
+        *reinterpret_cast<uint4*>(base + L::P + (kt & 1) * L::PBUF + row * 128 +
+                                  ((ch ^ (row & 7)) << 4)) = v;
       }
       if (kv0 + BN > span) {
         // after the stage's value copies have landed, which would overwrite
-        const int sv = kt % NV;
-        good = __all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1)));
+        const int sv_slot = kt % NV;
+        good = __all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1)));
         if (!good) break;
         const int first_bad = span - kv0;  // tokens [first_bad, BN) of this stage
-        unsigned char* vsm = base + L::V0 + sv * L::STAGE;
+        unsigned char* vsm = base + L::V0 + sv_slot * L::STAGE;
         for (int i = row; i < L::BOXES * BN * 8; i += 128) {  // 16-byte chunks
           const int bx = i / (BN * 8), r = (i / 8) % BN, ch = i % 8;
           if (r >= first_bad)
@@ -553,7 +565,7 @@ __global__ void __launch_bounds__(kTc5Threads, 1)
       fence_proxy_async_smem();
       tc5::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
+      if (lane == 0) mbar_arrive(p_ready + 8 * (kt & 1));
     }
     if (nkt > 0 && good) {
       good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
