@@ -14,7 +14,7 @@
 //     K [D/64 boxes][64 tokens][128 B]        B operand of S, K-major
 //   a ring of NV value stages of 64 tokens, each
 //     V [D/64 boxes][64 tokens][128 B]        B operand of P.V, MN-major
-//   P   2 x [128 rows][128 B]                 A operand of P.V, K-major
+//   P   NP x [128 rows][128 B]                A operand of P.V, K-major
 // TMEM: S of 64 columns, O of D columns, Q of D/2 columns (two 16-bit
 // elements per 32-bit column).
 //
@@ -23,7 +23,7 @@
 //   the row threads load S(kt) into registers and release its columns;
 //   S(kt+1) is issued at once and runs while they compute
 //   row softmax of S(kt) in registers, lazy rescaling
-//   P(kt) to shared memory, once P.V(kt-2) has finished reading its buffer
+//   P(kt) to shared memory, once P.V(kt-NP) has finished reading its buffer
 //   O += P V       (4 MMAs, M = 128, N = D, K = 64)    committed to pv_done
 // Keys and values have rings of their own: a key stage is refilled as soon
 // as S has read it, a value stage once P.V has.  Sixty-four keys per stage
@@ -144,6 +144,23 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   return p;
 }
 
+}  // namespace tc5
+
+// d = a + b on two fp32 lanes with one instruction.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+namespace tc5 {
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -158,17 +175,18 @@ constexpr int kTc5Threads = 192;                     // row warps 0-3, MMA warp 
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
-  static constexpr int NK = D == 128 ? 2 : 4;                   // key stages
+  static constexpr int NK = D == 128 ? 3 : 4;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
+  static constexpr int NP = D == 128 ? 1 : 2;                   // P buffers
   static constexpr int KVBOX = kTc5Tokens * 128;                // 8 KB per box
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
   static constexpr int K0 = 0;
   static constexpr int V0 = K0 + NK * STAGE;
-  static constexpr int P = V0 + NV * STAGE;                     // 2 x 16 KB
+  static constexpr int P = V0 + NV * STAGE;                     // NP x 16 KB
   static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
   // k_full[NK], k_free[NK], v_full[NV], v_free[NV], s_done, s_free,
   // pv_done[2], p_ready[2], drain
-  static constexpr int BARS = P + 2 * PBUF;
+  static constexpr int BARS = P + NP * PBUF;
   static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 7), 16);
   static constexpr int FLAG = TMEM_SLOT + 16;
   static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         if (!good) break;
         tc5::fence_after();
         const uint32_t vst = sbase + L::V0 + sv * L::STAGE;
-        const uint32_t pst = sbase + L::P + (kt & 1) * L::PBUF;
+        const uint32_t pst = sbase + L::P + (kt % L::NP) * L::PBUF;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t a = tc5::smem_desc(pst + k * 32, 16, 1024);
@@ -490,34 +508,39 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         resc = m_run != -INFINITY;
         m_run = mx;
       }
-      // p = 2^(s * scale - m): one FFMA and one ex2 per key
+      // p = 2^(s * scale - m): one ex2 per key, the arguments and the row
+      // sum on packed pairs (fma.rn.f32x2, add.rn.f32x2)
       uint32_t pk[BN / 2];
       float ps;
       {
-        float t[BN / 2];
+        float2 t[BN / 4];
         // a row with no weight yet has only masked (-inf) scores: 2^-inf = 0
         const float nm = m_run == -INFINITY ? -INFINITY : -m_run;
-        const float qs = p.qscale;
+        const float2 qs2 = make_float2(p.qscale, p.qscale), nm2 = make_float2(nm, nm);
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float a0 = ex2(fmaf(sv[c], qs, nm));
-          const float a1 = ex2(fmaf(sv[c + 1], qs, nm));
-          t[c / 2] = a0 + a1;
-          pk[c / 2] = Elem<T>::from_f2(a0, a1);
+        for (int c = 0; c < BN; c += 4) {
+          const float2 x0 = ffma2(make_float2(sv[c], sv[c + 1]), qs2, nm2);
+          const float2 x1 = ffma2(make_float2(sv[c + 2], sv[c + 3]), qs2, nm2);
+          const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));
+          const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
+          t[c / 4] = fadd2(a0, a1);
+          pk[c / 2] = Elem<T>::from_f2(a0.x, a0.y);
+          pk[c / 2 + 1] = Elem<T>::from_f2(a1.x, a1.y);
         }
 #pragma unroll
-        for (int w = BN / 4; w >= 1; w >>= 1)
+        for (int w = BN / 8; w >= 1; w >>= 1)
 #pragma unroll
-          for (int c = 0; c < w; ++c) t[c] += t[c + w];
-        ps = t[0];
+          for (int c = 0; c < w; ++c) t[c] = fadd2(t[c], t[c + w]);
+        ps = t[0].x + t[0].y;
       }
       l_run = l_run * al + ps;
 
-      // ---- P buffer kt & 1 is free once P.V(kt-2) is done; O may be
+      // ---- P buffer kt % NP is free once P.V(kt-NP) is done; O may be
       // rescaled only once P.V(kt-1) is done
       const bool any_resc = __any_sync(kFull, resc);
-      if (kt >= 2) {
-        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (kt & 1), (uint32_t)(((kt - 2) >> 1) & 1)));
+      if (kt >= L::NP) {
+        const int k2 = kt - L::NP;
+        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1)));
         if (!good) break;
       }
       if (any_resc && kt >= 1) {
@@ -545,7 +568,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {
         const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(base + L::P + (kt & 1) * L::PBUF + row * 128 +
+        *reinterpret_cast<uint4*>(base + L::P + (kt % L::NP) * L::PBUF + row * 128 +
                                   ((ch ^ (row & 7)) << 4)) = v;
       }
       if (kv0 + BN > span) {
