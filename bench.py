@@ -960,7 +960,9 @@ def run_prefill(args):
                    "launch": f"CUDA graph of {PREFILL_LAYERS} layers' calls over "
                              f"{PREFILL_LAYERS} per-layer KV caches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "prefill_kernel (mma.sync m16n8k16)", "bound": "tensor",
+        "roofline": {"kernel": ("prefill_kernel (mma.sync m16n8k16, 64-row tiles)"
+                               if os.environ.get("PA_PREFILL_ROWS") == "64" else
+                               "prefill_tc5_kernel (tcgen05, 128-row tiles)"), "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (of measured; fp16 has "
