@@ -5,7 +5,8 @@
 // A CTA owns 128 query rows of one (sequence, KV head): 128 / G query tokens
 // times the G heads of the KV head.  Thread r of warps 0-3 owns row r, which
 // is TMEM lane r, so a row's softmax needs no shuffles.  Warp 4 issues the
-// MMAs and warp 5 the copies; the six warps meet only on mbarriers.
+// MMAs, warp 5 the key copies and warp 6 the value copies; the warps meet
+// only on mbarriers.
 // Q sits in TMEM (row r in lane r), where the S MMAs read it as their A
 // operand, so the 128 x D tile is not re-read from shared memory per stage.
 // Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
@@ -169,7 +170,7 @@ __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.
 constexpr int kTc5Rows = 128;                        // query rows per CTA (one TMEM lane each)
 constexpr int kTc5Tokens = 64;                       // keys per stage
 constexpr int kTc5Pages = kTc5Tokens / kPageSize;    // pages per stage
-constexpr int kTc5Threads = 192;                     // row warps 0-3, MMA warp 4, copy warp 5
+constexpr int kTc5Threads = 224;  // row warps 0-3, MMA warp 4, key copies 5, value copies 6
 
 // Two CTAs share an SM (~97 KB of shared memory and 256 TMEM columns each).
 template <int D>
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool mma_warp = warp == 4;
-  const bool copy_warp = warp == 5;
+  const bool copy_warp = warp == 5 || warp == 6;
   const bool row_warp = warp < 4;
   const uint32_t k_full = sbase + L::BARS;      // NK: a key stage's copies landed
   const uint32_t k_free = k_full + 8 * NK;      // NK: S has read a key stage
@@ -317,16 +318,28 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   tc5::fence_after();
 
   if (copy_warp) {
-    // ================= copies (lane 0) =================
+    // ================= copies (lane 0 of warp 5: keys, of warp 6: values) =================
     // Stage kt holds pages 4kt .. 4kt+3 of the sequence; a page past the
     // span or with an invalid index is not copied (its keys are masked, and
-    // the row warps zero its value rows before P.V reads them).
+    // the row warps zero its value rows before P.V reads them).  Each ring
+    // runs as far ahead as its own slots allow: a key slot is free once S
+    // has read it, a value slot once P.V has.  (With one warp for both, the
+    // keys would wait behind the value ring, which frees a stage later.)
     if (lane == 0 && nkt > 0) {
+      const bool keys = warp == 5;
+      const int NR = keys ? NK : NV;
+      const uint32_t ring = sbase + (keys ? L::K0 : L::V0);
+      const uint32_t full_bar = keys ? k_full : v_full;
+      const uint32_t free_bar = keys ? k_free : v_free;
+      const CUtensorMap* map = keys ? &p.tmap_k : &p.tmap_v;
       const uint64_t policy = tc5::l2_evict_normal_policy();
       const uint32_t kv_bytes = (uint32_t)(D * kPageSize * 2);
-      int nk = 0, nv = 0;  // key and value stages issued
+      int n = 0;  // stages issued
       bool good = true;
-      for (int kt = 0; kt < nkt && good; ++kt) {
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int slot = kt % NR;
+        good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1));
+        if (!good) break;
         int phys[kTc5Pages];
         int nvalid = 0;
 #pragma unroll
@@ -336,47 +349,26 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
           if (j * kPageSize < span) {
             ph = __ldg(bt_row + j);
             if (ph < 0 || ph >= p.num_pages) {
-              set_status(p.status, PA_DEV_BAD_PAGE);
+              if (keys) set_status(p.status, PA_DEV_BAD_PAGE);
               ph = -1;
             }
           }
           phys[u] = ph;
           nvalid += ph >= 0;
         }
-        // keys: the slot is free once S(kt - NK) has been computed
-        const int sk = kt % NK;
-        good = kt < NK || mbar_wait_bounded(k_free + 8 * sk, (uint32_t)((kt / NK - 1) & 1));
-        if (!good) break;
-        const uint32_t kbar = k_full + 8 * sk;
+        const uint32_t bar = full_bar + 8 * slot;
         if (nvalid == 0) {
-          mbar_arrive(kbar);
+          mbar_arrive(bar);
         } else {
-          mbar_arrive_expect_tx(kbar, (uint32_t)nvalid * kv_bytes);
+          mbar_arrive_expect_tx(bar, (uint32_t)nvalid * kv_bytes);
 #pragma unroll
           for (int u = 0; u < kTc5Pages; ++u)
             if (phys[u] >= 0)
               for (int bx = 0; bx < L::BOXES; ++bx)
-                tma_load_4d(sbase + L::K0 + sk * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_k,
-                            bx * 64, 0, g, phys[u], kbar, policy);
+                tma_load_4d(ring + slot * L::STAGE + bx * L::KVBOX + u * 2048, map, bx * 64, 0,
+                            g, phys[u], bar, policy);
         }
-        ++nk;
-        // values: the slot is free once P.V(kt - NV) has been computed
-        const int sv = kt % NV;
-        good = kt < NV || mbar_wait_bounded(v_free + 8 * sv, (uint32_t)((kt / NV - 1) & 1));
-        if (!good) break;
-        const uint32_t vbar = v_full + 8 * sv;
-        if (nvalid == 0) {
-          mbar_arrive(vbar);
-        } else {
-          mbar_arrive_expect_tx(vbar, (uint32_t)nvalid * kv_bytes);
-#pragma unroll
-          for (int u = 0; u < kTc5Pages; ++u)
-            if (phys[u] >= 0)
-              for (int bx = 0; bx < L::BOXES; ++bx)
-                tma_load_4d(sbase + L::V0 + sv * L::STAGE + bx * L::KVBOX + u * 2048, &p.tmap_v,
-                            bx * 64, 0, g, phys[u], vbar, policy);
-        }
-        ++nv;
+        ++n;
       }
       if (!good) {
         set_status(p.status, PA_DEV_TIMEOUT);
@@ -384,10 +376,8 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       }
       // copies in flight land before the CTA exits: the last stage issued
       // into each slot (on success all of them have been consumed already)
-      for (int k = nk - NK < 0 ? 0 : nk - NK; k < nk; ++k)
-        mbar_wait_bounded(k_full + 8 * (k % NK), (uint32_t)((k / NK) & 1), 10000000ull);
-      for (int k = nv - NV < 0 ? 0 : nv - NV; k < nv; ++k)
-        mbar_wait_bounded(v_full + 8 * (k % NV), (uint32_t)((k / NV) & 1), 10000000ull);
+      for (int k = n - NR < 0 ? 0 : n - NR; k < n; ++k)
+        mbar_wait_bounded(full_bar + 8 * (k % NR), (uint32_t)((k / NR) & 1), 10000000ull);
     }
     __syncwarp();
   } else if (mma_warp) {
