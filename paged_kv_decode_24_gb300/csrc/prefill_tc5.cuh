@@ -172,11 +172,11 @@ constexpr int kTc5Tokens = 64;                       // keys per stage
 constexpr int kTc5Pages = kTc5Tokens / kPageSize;    // pages per stage
 constexpr int kTc5Threads = 224;  // row warps 0-3, MMA warp 4, key copies 5, value copies 6
 
-// Two CTAs share an SM (~97 KB of shared memory and 256 TMEM columns each).
+// Two CTAs share an SM (113 KB of shared memory and 256 TMEM columns each).
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
-  static constexpr int NK = D == 128 ? 3 : 4;                   // key stages
+  static constexpr int NK = D == 128 ? 4 : 6;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
   static constexpr int NP = D == 128 ? 1 : 2;                   // P buffers
   static constexpr int KVBOX = kTc5Tokens * 128;                // 8 KB per box
@@ -185,12 +185,19 @@ struct Tc5Layout {
   static constexpr int V0 = K0 + NK * STAGE;
   static constexpr int P = V0 + NV * STAGE;                     // NP x 16 KB
   static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
-  // k_full[NK], k_free[NK], v_full[NV], v_free[NV], s_done, s_free,
-  // pv_done[2], p_ready[2], drain
-  static constexpr int BARS = P + NP * PBUF;
+  static constexpr int BUFS = P + NP * PBUF;                    // the 1024-aligned buffers
+  // SMALL bytes hold the mbarriers (k_full[NK], k_free[NK], v_full[NV],
+  // v_free[NV], s_done, s_free, pv_done[2], p_ready[2], drain), the TMEM
+  // address and a flag.  The buffers start at the first 1024-byte boundary
+  // of the allocation (the 128-byte swizzle needs it); the small area goes
+  // before them when the gap is wide enough, else after them, so BUFS + 1024
+  // bytes always hold both.
+  static constexpr int SMALL = 256;
+  static constexpr int BARS = 0;
   static constexpr int TMEM_SLOT = align_up(BARS + 8 * (2 * NK + 2 * NV + 7), 16);
   static constexpr int FLAG = TMEM_SLOT + 16;
-  static constexpr int BYTES = FLAG + 16 + 1024;                // + slack to align the base
+  static_assert(FLAG + 16 <= SMALL, "barriers overflow their area");
+  static constexpr int BYTES = BUFS + 1024;
   static constexpr uint32_t TMEM_COLS = 256;                    // S (64), O (D), Q (D/2)
 };
 
@@ -203,17 +210,19 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   constexpr int NV = L::NV;
   constexpr int BN = kTc5Tokens;
   constexpr int TOKS = kTc5Rows / G;
-  extern __shared__ unsigned char smem_dyn[];
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  unsigned char* small = base - smem_dyn >= L::SMALL ? smem_dyn : base + L::BUFS;
   const uint32_t sbase = smem_u32(base);
+  const uint32_t ssmall = smem_u32(small);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool mma_warp = warp == 4;
   const bool copy_warp = warp == 5 || warp == 6;
   const bool row_warp = warp < 4;
-  const uint32_t k_full = sbase + L::BARS;      // NK: a key stage's copies landed
+  const uint32_t k_full = ssmall + L::BARS;     // NK: a key stage's copies landed
   const uint32_t k_free = k_full + 8 * NK;      // NK: S has read a key stage
   const uint32_t v_full = k_free + 8 * NK;      // NV: a value stage's copies landed
   const uint32_t v_free = v_full + 8 * NV;      // NV: P.V has read a value stage
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   // barrier could complete before the MMA warp looks at the first.
   const uint32_t p_ready = pv_done + 16;
   const uint32_t drain = p_ready + 16;          // every MMA issued has finished
-  int* cta_flag = reinterpret_cast<int*>(base + L::FLAG);
+  int* cta_flag = reinterpret_cast<int*>(small + L::FLAG);
 
   if ((int)blockIdx.x >= p.num_tiles) return;  // whole CTA
   const int4 hdr = *reinterpret_cast<const int4*>(p.ws);
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   }
   if (mma_warp) {  // TMEM for this CTA, freed by this warp at the end
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     sbase + L::TMEM_SLOT),
+                     ssmall + L::TMEM_SLOT),
                  "r"(L::TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   tc5::fence_before();
   __syncthreads();
   tc5::fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::TMEM_SLOT);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(small + L::TMEM_SLOT);
   const uint32_t t_s = tmem, t_o = tmem + BN, t_q = t_o + D;  // columns: S, O, Q
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
 
