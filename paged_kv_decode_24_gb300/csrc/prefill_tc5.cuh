@@ -445,12 +445,48 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // ================= rows: softmax and output (warps 0-3) =================
     float m_run = -INFINITY, l_run = 0.f;
     bool good = true;
+    // Value rows past the span (which may hold anything) become zeros in the
+    // last stage, after its value copies have landed (they would overwrite).
+    // Each of the 128 row threads takes its share.
+    auto zero_value_tail = [&](int kt) -> bool {
+      const int sv_slot = kt % NV;
+      if (!__all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1))))
+        return false;
+      const int first_bad = span - BN * kt;  // tokens [first_bad, BN) of this stage
+      unsigned char* vsm = base + L::V0 + sv_slot * L::STAGE;
+      for (int i = row; i < L::BOXES * BN * 8; i += 128) {  // 16-byte chunks
+        const int bx = i / (BN * 8), r = (i / 8) % BN, ch = i % 8;
+        if (r >= first_bad)
+          *reinterpret_cast<uint4*>(vsm + bx * L::KVBOX + r * 128 + (ch << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      return true;
+    };
+    // A warp without a query row in the tile (a short tile: fewer than 32 /
+    // G tokens per 32 rows) computes nothing.  It keeps its place in the
+    // barrier counts and zeroes its share of value rows; its P rows feed O
+    // rows that are never written.
+    const bool idle = !__any_sync(kFull, ok);
+    for (int kt = 0; idle && kt < nkt; ++kt) {
+      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1)));
+      if (!good) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      if (BN * kt + BN > span && !zero_value_tail(kt)) {
+        good = false;
+        break;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready + 8 * (kt & 1));
+    }
     // block-table entries of the stage, loaded one stage ahead (page checks
     // mask the keys of a page that was not copied)
     int nph[kTc5Pages];
 #pragma unroll
-    for (int u = 0; u < kTc5Pages; ++u) nph[u] = nkt > 0 && u * kPageSize < span ? __ldg(bt_row + u) : -1;
-    for (int kt = 0; kt < nkt; ++kt) {
+    for (int u = 0; u < kTc5Pages; ++u)
+      nph[u] = !idle && nkt > 0 && u * kPageSize < span ? __ldg(bt_row + u) : -1;
+    for (int kt = 0; !idle && kt < nkt; ++kt) {
       bool pgv[kTc5Pages];
       bool all_pages = true;
 #pragma unroll
@@ -570,26 +606,16 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         *reinterpret_cast<uint4*>(base + L::P + (kt % L::NP) * L::PBUF + row * 128 +
                                   ((ch ^ (row & 7)) << 4)) = v;
       }
-      if (kv0 + BN > span) {
-        // after the stage's value copies have landed, which would overwrite
-        const int sv_slot = kt % NV;
-        good = __all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1)));
-        if (!good) break;
-        const int first_bad = span - kv0;  // tokens [first_bad, BN) of this stage
-        unsigned char* vsm = base + L::V0 + sv_slot * L::STAGE;
-        for (int i = row; i < L::BOXES * BN * 8; i += 128) {  // 16-byte chunks
-          const int bx = i / (BN * 8), r = (i / 8) % BN, ch = i % 8;
-          if (r >= first_bad)
-            *reinterpret_cast<uint4*>(vsm + bx * L::KVBOX + r * 128 + (ch << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
+      if (kv0 + BN > span && !zero_value_tail(kt)) {
+        good = false;
+        break;
       }
       fence_proxy_async_smem();
       tc5::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready + 8 * (kt & 1));
     }
-    if (nkt > 0 && good) {
+    if (!idle && nkt > 0 && good) {
       good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
                                                  (uint32_t)(((nkt - 1) >> 1) & 1)));
       // a copy or MMA warp that gave up leaves O incomplete: write nothing
