@@ -343,27 +343,39 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       const CUtensorMap* map = keys ? &p.tmap_k : &p.tmap_v;
       const uint64_t policy = tc5::l2_evict_normal_policy();
       const uint32_t kv_bytes = (uint32_t)(D * kPageSize * 2);
+      // The block-table entries of stage kt+1 are loaded while the slot of
+      // stage kt is awaited, so their latency is off the copy path.  The
+      // loads are volatile asm, which the compiler keeps in place.
+      int nxt[kTc5Pages];
+      auto load_entries = [&](int kt) {
+#pragma unroll
+        for (int u = 0; u < kTc5Pages; ++u) {
+          const int j = kTc5Pages * kt + u;
+          nxt[u] = -1;
+          if (j * kPageSize < span)
+            asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(nxt[u]) : "l"(bt_row + j));
+        }
+      };
+      load_entries(0);
       int n = 0;  // stages issued
       bool good = true;
       for (int kt = 0; kt < nkt; ++kt) {
+        int phys[kTc5Pages];
+#pragma unroll
+        for (int u = 0; u < kTc5Pages; ++u) phys[u] = nxt[u];
+        if (kt + 1 < nkt) load_entries(kt + 1);
         const int slot = kt % NR;
         good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1));
         if (!good) break;
-        int phys[kTc5Pages];
         int nvalid = 0;
 #pragma unroll
         for (int u = 0; u < kTc5Pages; ++u) {
           const int j = kTc5Pages * kt + u;
-          int ph = -1;
-          if (j * kPageSize < span) {
-            ph = __ldg(bt_row + j);
-            if (ph < 0 || ph >= p.num_pages) {
-              if (keys) set_status(p.status, PA_DEV_BAD_PAGE);
-              ph = -1;
-            }
+          if (j * kPageSize < span && (phys[u] < 0 || phys[u] >= p.num_pages)) {
+            if (keys) set_status(p.status, PA_DEV_BAD_PAGE);
+            phys[u] = -1;
           }
-          phys[u] = ph;
-          nvalid += ph >= 0;
+          nvalid += phys[u] >= 0;
         }
         const uint32_t bar = full_bar + 8 * slot;
         if (nvalid == 0) {
@@ -494,11 +506,13 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         pgv[u] = nph[u] >= 0 && nph[u] < p.num_pages;
         all_pages = all_pages && pgv[u];
       }
-      if (kt + 1 < nkt) {
+      if (kt + 1 < nkt) {  // volatile asm loads stay here, a stage ahead of their use
 #pragma unroll
         for (int u = 0; u < kTc5Pages; ++u) {
           const int j = kTc5Pages * (kt + 1) + u;
-          nph[u] = j * kPageSize < span ? __ldg(bt_row + j) : -1;
+          nph[u] = -1;
+          if (j * kPageSize < span)
+            asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(nph[u]) : "l"(bt_row + j));
         }
       }
       good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1)));
