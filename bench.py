@@ -22,7 +22,10 @@ The JSON line reports:
                 region; us_per_launch_isolated is one call alone (own graph)
   e2e           the same metric with host buffers: per-step inputs copied
                 from pinned host memory and the output read back
-  cpu_baseline  the float64 oracle on this host's cores, on a bounded sample
+  cpu_baseline  the float64 oracle on one host core, on a bounded sample;
+                cpu_baseline_all_cores runs it on every core at once
+  plan_host_us  one pa_plan call on the host (not part of the device timing)
+  append_us     pa_kv_append alone, as its own launch (the step fuses it)
 
 Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
 in total), so L2 never holds the pages a step reads.
@@ -74,6 +77,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-offset", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-stride", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
                     help="KV-cache type: 16-bit elements, or INT8 codes with per-row fp32 scales")
@@ -93,11 +98,13 @@ def parse():
 # ---------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 
-def oracle_sample(w, budget_s):
+def oracle_sample(w, budget_s, offset=0, stride=1):
     """Run the float64 oracle's attention on whole sequences (every head)
-    until about ``budget_s`` seconds pass.  Returns (seconds, KV bytes
-    covered, description).  The oracle's append is left out: it copies whole
-    pools functionally, which says nothing about the method."""
+    until about ``budget_s`` seconds pass, taking sequences offset,
+    offset + stride, ... of the longest-first order (cycling).  Returns
+    (seconds, KV bytes covered, description).  The oracle's append is left
+    out: it copies whole pools functionally, which says nothing about the
+    method."""
     import oracle
     q8 = w.k_codes is not None
     row = w.head_dim + 4 if q8 else 2 * w.head_dim
@@ -105,10 +112,10 @@ def oracle_sample(w, budget_s):
     t0 = time.perf_counter()
     kv = 0
     seqs = 0
-    i = 0
+    i = offset
     while True:
         b = int(order[i % len(order)])
-        i += 1
+        i += stride
         sub_bt = w.block_table[b:b + 1]
         sub_l = w.seq_lens[b:b + 1]
         if q8:
@@ -127,7 +134,7 @@ def oracle_sample(w, budget_s):
 def oracle_worker(args):
     from paged_kv_decode_24_gb300 import workloads
     w = workloads.make_config(args.config, kv=args.kv, dtype=args.dtype)
-    dt, kv, desc = oracle_sample(w, args.cpu_seconds)
+    dt, kv, desc = oracle_sample(w, args.cpu_seconds, args.oracle_offset, args.oracle_stride)
     print(json.dumps({"seconds": dt, "kv_bytes": kv, "sample": desc}))
 
 
@@ -149,6 +156,35 @@ def run_oracle_subprocess(cfg, seconds, kv="fp16", dtype="fp16"):
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"config {cfg} ({kv} cache, {dtype}): {res['sample']}, "
                       f"{res['seconds']:.1f} s of float64 numpy"}
+
+
+def run_oracle_all_cores(cfg, seconds, kv="fp16", dtype="fp16"):
+    """The oracle on every core this process may use: one single-threaded
+    process per core (started by exec, no CUDA state), each on its own share
+    of the sequences (offset i, stride n), all for about ``seconds``.  GB/s =
+    the KV bytes of all of them / the longest one's time."""
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-worker",
+                               "--config", str(cfg), "--cpu-seconds", str(seconds), "--kv", kv,
+                               "--dtype", dtype, "--oracle-offset", str(i),
+                               "--oracle-stride", str(n)],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env)
+             for i in range(n)]
+    res = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=600)
+        if pr.returncode != 0:
+            raise RuntimeError(err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    kvb = sum(r["kv_bytes"] for r in res)
+    dt = max(r["seconds"] for r in res)
+    return {"value": kvb / dt / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"config {cfg} ({kv} cache, {dtype}): {n} single-threaded processes, "
+                      f"sequences dealt round-robin, {dt:.1f} s of float64 numpy each"}
 
 
 # ---------------------------------------------------------------------------
@@ -299,10 +335,11 @@ def run_ours(args):
     from paged_kv_decode_24_gb300 import build as _build
 
     world, rank, local = dist_setup(args)
-    cpu_base = None
+    cpu_base = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds, args.kv,
-                                         args.dtype)  # before any CUDA call
+        # before any CUDA call
+        cpu_base = run_oracle_subprocess(args.config, args.cpu_seconds, args.kv, args.dtype)
+        cpu_all = run_oracle_all_cores(args.config, args.cpu_seconds, args.kv, args.dtype)
 
     _build.ensure_built()
     binding.load()
@@ -571,6 +608,25 @@ def run_ours(args):
                "overlap": "layer l+1's inputs copied in and layer l's output copied out on two "
                           "side streams while layer l computes"}
 
+    # ---- a1 alone: pa_kv_append as its own launch (the step above fuses it
+    # into the split kernel), 32 launches in one graph over the layers' caches
+    app_call = binding.append_q8 if q8 else binding.append
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=stream):
+        for l in range(LAYERS):
+            app_call(shape, k_new, v_new, *pools[l], bt, sl, status)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        ga.replay()
+        ev_a[0].record(stream)
+        for _ in range(4):
+            ga.replay()
+        ev_a[1].record(stream)
+    torch.cuda.synchronize()
+    append_us = ev_a[0].elapsed_time(ev_a[1]) * 1e3 / (4 * LAYERS)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+
     peak, peak_src = read_peaks()
     achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
     value = job_value(kv_bytes, ms_per_step, world)
@@ -629,7 +685,9 @@ def run_ours(args):
             "us_per_launch_isolated": round(iso_us, 3),
         },
         "plan_host_us": None,
+        "append_us": round(append_us, 3),
         "cpu_baseline": cpu_base,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
