@@ -179,6 +179,13 @@ struct Tc5Layout {
   static constexpr int NK = D == 128 ? 4 : 6;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
   static constexpr int NP = D == 128 ? 1 : 2;                   // P buffers
+  // An idle row warp waits for the last stage's value copies without having
+  // waited for P.V of the stage before.  With one value slot that stage's
+  // copy may still be in flight, and the parity wait would then read the
+  // phase before it as complete.  With two or more slots the slot's earlier
+  // phases are always complete.  A single value slot was measured to
+  // corrupt exactly those tiles.
+  static_assert(NV >= 2, "value ring needs two slots");
   static constexpr int KVBOX = kTc5Tokens * 128;                // 8 KB per box
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
   static constexpr int K0 = 0;
