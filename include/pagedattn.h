@@ -321,7 +321,8 @@ pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t*
  */
 typedef struct {
   pa_shape_t shape;     /* the shape the plan was made for */
-  int32_t num_tiles;    /* CTAs: 64 query rows (tokens x heads of one KV head) each */
+  int32_t num_tiles;    /* CTAs: 128 query rows (tokens x heads of one KV head) each
+                           on tcgen05; 64 for the mma.sync form (PA_PREFILL_ROWS=64) */
   int32_t total_q;      /* T */
   int32_t owns_blob;    /* 1: host_blob is released by pa_prefill_plan_free */
   int32_t reserved;
@@ -349,8 +350,9 @@ pa_status_t pa_kv_append_tokens(const pa_shape_t* shape, const pa_prefill_plan_t
                                 size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* The attention above, for every query row of the plan, on tensor cores
- * (FlashAttention-style: one CTA per 64 query rows of one KV head streams
- * the causal part of the sequence's pages once).  Errors as
+ * (FlashAttention-style: one CTA per tile of query rows of one KV head
+ * streams the causal part of the sequence's pages once; tcgen05 MMAs into
+ * tensor memory, or mma.sync when the plan was cut for it).  Errors as
  * pa_decode_attention's; device seq_lens shorter than the plan's q_lens
  * set PA_DEV_PLAN_MISMATCH. */
 pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_prefill_plan_t* plan,
