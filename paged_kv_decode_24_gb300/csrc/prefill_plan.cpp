@@ -1,10 +1,12 @@
 // Host-side tile list of the multi-token attention kernel.
 //
-// A tile is 64 query rows of one (sequence, KV head): 64 / G consecutive
-// query tokens times the G query heads that share the KV head.  Its work is
-// proportional to its rows times the causal length it streams (the
-// position of its last query + 1), and tiles are issued longest first so
-// the tail of the grid holds the short ones.
+// A tile is a block of query rows of one (sequence, KV head): rows / G
+// consecutive query tokens times the G query heads that share the KV head.
+// Its time is set by the causal length it streams (the position of its last
+// query + 1): every stage of keys costs about the same whether the tile has
+// all its rows or a single decode token's G.  Tiles are issued longest
+// stream first (more rows first among equals), so the tail of the grid
+// holds the short ones.
 #include <stdlib.h>
 #include <string.h>
 
@@ -58,11 +60,12 @@ extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* s
     for (int tok0 = 0; tok0 < n; tok0 += tok_per_tile) {
       const int ntok = std::min(tok_per_tile, n - tok0);
       const int64_t span = (int64_t)(L - n + tok0 + ntok);  // keys the tile's last query sees
-      for (int g = 0; g < Hkv; ++g) tiles.push_back({b, g, tok0, ntok, span * ntok});
+      for (int g = 0; g < Hkv; ++g) tiles.push_back({b, g, tok0, ntok, span});
     }
   }
-  std::stable_sort(tiles.begin(), tiles.end(),
-                   [](const Tile& x, const Tile& y) { return x.work > y.work; });
+  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile& x, const Tile& y) {
+    return x.work != y.work ? x.work > y.work : x.ntok > y.ntok;
+  });
   const PrefillLayout lay = prefill_layout((int)tiles.size(), B);
   int32_t* blob = (int32_t*)malloc(lay.blob_bytes);
   if (!blob) return PA_ERR_NO_MEMORY;

@@ -263,8 +263,9 @@ def test_prefill_plan_tiles_cover_every_row_once(lib):
                 seen.add((int(b), int(g), i))
         assert seen == {(b, g, i) for b in range(len(lens)) for g in range(hkv)
                         for i in range(qls[b])}
-        work = [(lens[b] - qls[b] + tok0 + ntok) * ntok for b, g, tok0, ntok in tiles]
-        assert all(x >= y for x, y in zip(work, work[1:]))
+        # longest stream first (a tile's time follows the keys it streams)
+        span = [lens[b] - qls[b] + tok0 + ntok for b, g, tok0, ntok in tiles]
+        assert all(x >= y for x, y in zip(span, span[1:]))
     s = binding.make_shape(2, 4, 2, 64, 16, 8, 20)
     with pytest.raises(binding.PagedAttnError) as e:
         binding.PrefillPlan(s, [10, 20], [11, 1])      # more queries than cached tokens
