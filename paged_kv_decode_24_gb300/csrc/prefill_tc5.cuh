@@ -1,5 +1,5 @@
 // Multi-token attention on the fifth-generation tensor cores (tcgen05):
-// the same operation and tiles as prefill.cuh, with 128-row MMAs issued by
+// the same operation as prefill.cuh, on 128-row tiles, with MMAs issued by
 // one thread from shared-memory descriptors into tensor memory (TMEM).
 //
 // A CTA owns 128 query rows of one (sequence, KV head): 128 / G query tokens
