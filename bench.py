@@ -519,9 +519,10 @@ def run_ours(args):
     # ---- end to end: every layer step's q, k_new and v_new come in from
     # pinned host memory, and every layer step's output goes back to pinned
     # host memory, inside the model-step graphs.  Inputs come in eight layers
-    # per transfer: the first eight before the first layer (with seq_lens,
-    # the block table and the plan), each further eight on a side stream
-    # while the eight before them compute.  A side stream reads each layer's
+    # per transfer (all layers in one when a model step's inputs total at
+    # most 1 MiB): the first chunk before the first layer (with seq_lens, the
+    # block table and the plan), each further chunk on a side stream while
+    # the chunk before it computes.  A side stream reads each layer's
     # output back as soon as that layer is done.  Only the wait for a chunk
     # of inputs joins the kernel chain, once per eight layers, so the other
     # layers keep their programmatic dependent launch; each layer has its own
@@ -551,7 +552,9 @@ def run_ours(args):
                     d_in[base + nq + nk:base + per_layer].view(v_new.shape))
 
         side_in = torch.cuda.Stream(device=dev)
-        CHUNK = 8  # layers whose inputs one transfer brings in
+        # layers whose inputs one transfer brings in: all of them when a model
+        # step's inputs are small (one transfer, no join at all), else eight
+        CHUNK = LAYERS if LAYERS * per_layer * h_in.element_size() <= (1 << 20) else 8
 
         def copy_in(l0, l1):
             d_in[l0 * per_layer:l1 * per_layer].copy_(h_in[l0 * per_layer:l1 * per_layer],
@@ -617,8 +620,8 @@ def run_ours(args):
                "ms_per_step": round(e2e_ms, 5),
                "h2d_bytes_per_step": int(round(h2d_bytes / K)),
                "d2h_bytes_per_step": int(nb(hout[0])),
-               "overlap": "inputs come in eight layers per transfer, each eight while the "
-                          "eight before them compute; a side stream reads each layer's output "
+               "overlap": f"inputs come in {CHUNK} layers per transfer, each chunk while the "
+                          "one before it computes; a side stream reads each layer's output "
                           "back while the next layers compute"}
 
     # ---- a1 alone: pa_kv_append as its own launch (the step above fuses it
