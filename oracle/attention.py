@@ -20,7 +20,7 @@ What it computes, and where the pages define it:
   combine.  ``decode_attention_split`` below writes that merge out only so the
   tests can show that any page-aligned split gives the unsplit answer.
 
-Readings of what the pages leave open (each is stated once more in the design doc):
+Readings of what the pages leave open:
 
 * GQA mapping: query head h reads KV head h // G, G = Hq / Hkv (consecutive
   query heads share a KV head).
