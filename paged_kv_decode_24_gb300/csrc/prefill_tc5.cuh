@@ -375,15 +375,29 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1));
         if (!good) break;
         int nvalid = 0;
+        bool zeroed = false;
 #pragma unroll
         for (int u = 0; u < kTc5Pages; ++u) {
           const int j = kTc5Pages * kt + u;
           if (j * kPageSize < span && (phys[u] < 0 || phys[u] >= p.num_pages)) {
-            if (keys) set_status(p.status, PA_DEV_BAD_PAGE);
+            if (keys) {
+              set_status(p.status, PA_DEV_BAD_PAGE);
+            } else {
+              // a page inside the span that is not copied: its keys are
+              // masked, and its value rows (which may hold anything from
+              // earlier stages) become zeros before P.V reads them
+              for (int bx = 0; bx < L::BOXES; ++bx)
+                for (int c = 0; c < kPageSize * 8; ++c)
+                  *reinterpret_cast<uint4*>(base + L::V0 + slot * L::STAGE + bx * L::KVBOX +
+                                            u * 2048 + c * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+              zeroed = true;
+            }
             phys[u] = -1;
           }
           nvalid += phys[u] >= 0;
         }
+        if (zeroed) fence_proxy_async_smem();  // the tensor core reads them (async proxy)
         const uint32_t bar = full_bar + 8 * slot;
         if (nvalid == 0) {
           mbar_arrive(bar);
