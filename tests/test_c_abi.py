@@ -31,3 +31,25 @@ def test_header_and_host_calls_from_c(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "abi ok" in r.stdout
+
+
+@pytest.mark.gpu
+def test_decode_from_c_on_gpu(lib, tmp_path):
+    """pa_kv_append -> pa_plan -> pa_plan_upload -> pa_decode_attention from a
+    C program: one token per sequence, so each head's output is exactly the
+    new V row of its KV head."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    from paged_kv_decode_24_gb300 import binding
+    libdir = os.path.dirname(binding.LIB_PATH)
+    exe = str(tmp_path / "abi_gpu")
+    r = subprocess.run([nvcc, "-x", "c", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c", "abi_gpu.c"), "-o", exe,
+                        "-L", libdir, "-lpagedattn", "-Xlinker", "-rpath=" + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "decode from C ok" in r.stdout
