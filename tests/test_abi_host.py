@@ -270,3 +270,29 @@ def test_prefill_plan_tiles_cover_every_row_once(lib):
     with pytest.raises(binding.PagedAttnError) as e:
         binding.PrefillPlan(s, [10, 20], [11, 1])      # more queries than cached tokens
     assert e.value.code == 1
+
+
+def test_plans_from_many_host_threads_agree(lib):
+    """pa_plan keeps no shared state but a plan-id counter: plans made at once
+    on several host threads equal the plan made alone (ids aside)."""
+    import threading
+    lens = np.random.default_rng(3).integers(1, 4000, size=160).astype(np.int32)
+    s = binding.make_shape(len(lens), 32, 8, 128, 16, 256, 8192)
+    ref = binding.Plan(s, lens, 152, 0).blob()
+    out, errors = [], []
+
+    def work():
+        try:
+            for _ in range(20):
+                b = binding.Plan(s, lens, 152, 0).blob()
+                b[4:6] = ref[4:6]   # the plan id stamp differs by design
+                out.append(b)
+        except Exception as e:   # surfaced below
+            errors.append(e)
+    threads = [threading.Thread(target=work) for _ in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors
+    assert len(out) == 160 and all(np.array_equal(b, ref) for b in out)
