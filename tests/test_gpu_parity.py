@@ -317,3 +317,18 @@ def test_device_seq_len_out_of_range_is_flagged():
     dd.seq_lens[0] = w.max_pages_per_seq * 16 + 100
     dd.decode()
     assert dd.read_status() & binding.PA_DEV_BAD_SEQ_LEN
+
+
+def test_maximum_split_count():
+    """A request for more splits than the limit is clamped to 1024 page-aligned
+    splits (two pages each here). The combine then merges 1024 partials per
+    head, and the result still matches the unsplit oracle."""
+    w = workloads.make_custom(seq_lens=[32768, 40], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                              seed=29)
+    dd = DeviceDecode(w)
+    dd.append()
+    dd.make_plan(forced_splits=5000)
+    assert int(dd.plan_obj.c.max_splits) == 1024
+    got = dd.decode().cpu().numpy()
+    assert dd.read_status() == 0
+    assert_close(got, oracle_step(w), "1024 splits")
