@@ -133,3 +133,20 @@ def test_prefill_benchmark_workload(cfg):
     want, _ = oracle_step(w, rows=rows)
     idx = tuple(np.array(rows).T)
     close(got[idx], want[idx], f"prefill workload {cfg} (sampled)")
+
+
+def test_prefill_whole_prompt_sampled():
+    """q_lens = seq_lens: a whole 2048-token prompt attends causally over
+    itself (512 tiles across the diagonal); sampled rows against the oracle,
+    the first and last rows of every head among them."""
+    w = workloads.make_custom(seq_lens=[2048, 300], num_q_heads=32, num_kv_heads=8,
+                              head_dim=128, seed=97, q_lens=[2048, 300])
+    got, _ = gpu_step(w)
+    rng = np.random.default_rng(98)
+    rows = {(int(r), int(h)) for r, h in zip(rng.integers(0, w.q.shape[0], 96),
+                                             rng.integers(0, w.num_q_heads, 96))}
+    rows |= {(0, h) for h in range(w.num_q_heads)} | {(2047, h) for h in range(w.num_q_heads)}
+    rows = sorted(rows)
+    want, _ = oracle_step(w, rows=rows)
+    idx = tuple(np.array(rows).T)
+    close(got[idx], want[idx], "whole prompt (sampled)")
