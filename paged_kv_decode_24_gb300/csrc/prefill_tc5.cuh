@@ -329,9 +329,13 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     }
     tc5::wait_st();
   }
-  tc5::fence_before();
-  __syncthreads();
-  tc5::fence_after();
+  // Q is in TMEM for the MMA warp: the row warps and the MMA warp meet on a
+  // named barrier; the copy warps, which do not read Q, start at once.
+  if (!copy_warp) {
+    tc5::fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(5 * 32) : "memory");
+    tc5::fence_after();
+  }
 
   if (copy_warp) {
     // ================= copies (lane 0 of warp 5: keys, of warp 6: values) =================
