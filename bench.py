@@ -1,8 +1,9 @@
 """Benchmark: decode attention over a paged KV cache on one GB300 (or N replicas).
 
 One step is one layer's decode attention over one batch:
-    pa_append_decode_attention (the append of the new token fused into the
-    split kernel, then the log-sum-exp combine kernel),
+    pa_append_decode_attention (one kernel: the append of the new token
+    fused into the split kernel, whose last split per group merges the
+    partials by their log-sum-exp),
 and once per 32-layer model step pa_plan (host) -> pa_plan_upload, inside the
 timed region: the plan depends only on seq_lens, which every layer shares.  Inputs are synthetic and
 seeded, with the shapes of the five workloads in
@@ -17,7 +18,7 @@ The JSON line reports:
   value         KV-read GB/s of the whole job (K and V bytes of every attended
                 token / device time per step), all ranks together
   ms_per_step   device time per layer step (CUDA events, max over ranks)
-  roofline      the fused call (split + combine kernels) against the
+  roofline      the fused call (one split kernel launch) against the
                 measured HBM copy bandwidth: its mean duration over the timed
                 region; us_per_launch_isolated is one call alone (own graph)
   e2e           the same metric with host buffers: per-step inputs copied
@@ -204,7 +205,7 @@ def read_peaks():
 # kernels, the device helpers, the planner that sets the grid, and the C-ABI
 # that fills the launch parameters.
 DECODE_SOURCES = ("api.cu", "device_common.cuh", "elem.cuh", "quant_common.cuh",
-                  "split_launch.cuh", "pa_internal.h", "launch.h", "plan.cpp")
+                  "split_launch.cuh", "split_merge.cuh", "pa_internal.h", "launch.h", "plan.cpp")
 
 
 def kernel_source_hash():
@@ -428,7 +429,7 @@ def run_ours(args):
     full, rem = divmod(K, LAYERS)
     graphs_full = [capture_model_step(i, LAYERS) for i in range(2)] if full else []
     graphs_rem = [capture_model_step(i, rem) for i in range(2)] if rem else []
-    launches_per_step = 1 + (1 if plan0.c.num_groups > 0 else 0)
+    launches_per_step = 1  # the split kernel; its last split per group merges
 
     def run_steps(nsteps, gfull, grem, m0=0):
         """nsteps layer-steps as model-step graphs; returns the model steps issued."""
@@ -674,8 +675,8 @@ def run_ours(args):
             "kv_read_bytes_per_step": kv_bytes,
             "splits": int(plan0.c.max_splits),
             "work_items": int(plan0.c.num_work_items),
-            "step": "one layer: pa_append_decode_attention (append fused into the split kernel, "
-                    "then the combine kernel); pa_plan + pa_plan_upload once per "
+            "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
+                    "split kernel, whose last split per group merges); pa_plan + pa_plan_upload once per "
                     f"{LAYERS}-layer model step, inside the timing",
             "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
                       "calls back to back, programmatic dependent launch between kernels)",
@@ -687,7 +688,7 @@ def run_ours(args):
         "roofline": {
             "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if q8 else
                        "pa_append_decode_attention = split_decode_kernel") +
-                      " (with the append) + combine_kernel, timed together",
+                      " (with the append and the split merge)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -176,6 +176,10 @@ void pa_plan_free(pa_plan_t* plan);
  * decode calls that use the same plan and workspace.  A plan of the same
  * structure uploaded later (the next decode step's plan, for example) also
  * serves a call or a captured CUDA graph made with the earlier one.
+ * The list ends with one counter per split group, zero in the plan.  A
+ * decode call counts the finished splits of each group there and leaves
+ * every counter at zero again; a call that set PA_DEV_PLAN_MISMATCH or
+ * PA_DEV_TIMEOUT may not, so upload the plan again before the next call.
  * Returns PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
  */
 pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t workspace_bytes,
@@ -185,7 +189,9 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * Decode attention (the operation at the top of this header), computed with
  * an online softmax normaliser (xLLM introduction, SoftMax: online
  * normalizer).  Splits follow the plan; their (output, log-sum-exp) partials
- * are merged by a separate combine kernel (swiftLLM paged attention v2).
+ * go to the workspace, and the last split of each (sequence, KV head) to
+ * finish merges them into out within the same kernel (swiftLLM paged
+ * attention v2).  One kernel launch per call.
  *
  * Device: q, k_pages, v_pages, block_table, seq_lens, out [B][Hq][D] fp16,
  * workspace (holding the uploaded plan), dev_status.

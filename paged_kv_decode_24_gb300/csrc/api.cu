@@ -354,7 +354,9 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.out = out;
   p.ws_header = (const int32_t*)ws;
   p.items = (const int4*)(ws + lay.items_off);
-  p.item_slots = (const int32_t*)(ws + lay.slots_off);
+  p.item_slots = (const int2*)(ws + lay.slots_off);
+  p.groups = (const int4*)(ws + lay.groups_off);
+  p.counters = (int*)(ws + lay.counters_off);
   p.part_lse = (float*)(ws + lay.lse_off);
   p.part_o = (float*)(ws + lay.o_off);
   p.status = dev_status;
@@ -385,21 +387,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
       return PA_ERR_CUDA;
     st = cuda_status(launch_split(p, D, G, shape->dtype, plan->num_ctas, s));
   }
-  if (st != PA_OK || plan->num_groups == 0) return st;
-
-  CombineParams c{};
-  c.ws_header = (const int32_t*)ws;
-  c.groups = (const int4*)(ws + lay.groups_off);
-  c.part_lse = p.part_lse;
-  c.part_o = p.part_o;
-  c.out = out;
-  c.status = dev_status;
-  c.group_size = G;
-  c.num_q_heads = shape->num_q_heads;
-  c.num_items = p.num_items;
-  c.num_groups = p.num_groups;
-  c.num_split_items = p.num_split_items;
-  return cuda_status(launch_combine(c, D, shape->dtype, plan->num_groups * G, s));
+  return st;
 }
 
 }  // namespace

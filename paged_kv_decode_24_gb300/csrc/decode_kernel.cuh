@@ -17,7 +17,7 @@
 // per query head (xLLM introduction, SoftMax with an online normalizer):
 // running max m, running sum l, and an accumulator rescaled whenever m grows.
 // At the end the NW warp states (m, l, acc) meet in shared memory and merge
-// with the same log-sum-exp rule the combine kernel uses.  No atomics touch
+// with the same log-sum-exp rule the split merge uses.  No atomics touch
 // data, and every reduction has a fixed order, so reruns are bit-identical.
 // This follows the from-scratch engine article, section 3.4: shared memory
 // instead of atomicAdd.
@@ -43,9 +43,9 @@
 // task touches that page, so the write races with nothing.
 //
 // A task whose sequence has more than one split writes its normalised output
-// and log2-sum-exp to the workspace.  combine_kernel merges them (swiftLLM,
-// paged attention v2 / Flash-Decoding).  Otherwise the task writes fp16
-// output directly.
+// and log2-sum-exp to the workspace; the group's last task to finish merges
+// them into the output (split_merge.cuh; swiftLLM, paged attention v2 /
+// Flash-Decoding).  Otherwise the task writes its output directly.
 #pragma once
 
 #include <cuda.h>
@@ -55,6 +55,7 @@
 #include "device_common.cuh"
 #include "elem.cuh"
 #include "pa_internal.h"
+#include "split_merge.cuh"
 
 namespace pa {
 
@@ -71,7 +72,9 @@ struct SplitParams {
   void* out;
   const int32_t* ws_header;
   const int4* items;
-  const int32_t* item_slots;  // partial slot of each task, -1 = direct output
+  const int2* item_slots;  // {partial slot (-1 = direct output), group} of each task
+  const int4* groups;      // {sequence, KV head, splits, first slot} of each split group
+  int* counters;           // per group: its split tasks finished so far (split_merge.cuh)
   float* part_lse;
   float* part_o;
   int32_t* status;
@@ -91,6 +94,27 @@ struct SplitParams {
   // prefetch the first pf_pages (<= 32) pages of each warp's share.
   int32_t pf_pages, pf_ctas;
 };
+
+// A split task's slot and group agree with each other and with the task.
+__device__ __forceinline__ bool split_slot_ok(const SplitParams& p, int2 sg, int4 grp, int b,
+                                              int kvh) {
+  return sg.x >= 0 && sg.x < p.num_split_items && sg.y >= 0 && sg.y < p.num_groups &&
+         grp.x == b && grp.y == kvh && grp.z >= 2 && grp.z <= kMaxSplits && grp.w >= 0 &&
+         sg.x >= grp.w && sg.x < grp.w + grp.z && grp.w + grp.z <= p.num_split_items;
+}
+
+// The merge target of split group gi (its record grp) of this launch.
+__device__ __forceinline__ MergeTarget merge_target(const SplitParams& p, int gi, int4 grp, int G) {
+  MergeTarget t;
+  t.lse = p.part_lse;
+  t.o = p.part_o;
+  t.out = p.out;
+  t.counter = p.counters + gi;
+  t.grp = grp;
+  t.G = G;
+  t.num_q_heads = p.num_q_heads;
+  return t;
+}
 
 // Before the wait on the previous kernel, lane k of a warp may prefetch page
 // k of the warp's share of task `it` (page j = warp + k * NW of a shared
@@ -200,7 +224,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   using Geo = Geometry<D, G>;
   using L = WarpLayout<D, G, NSH>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ int cta_failed;
+  __shared__ int cta_failed, cta_last;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -224,11 +248,14 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   const int count = coop ? 1 : min(NW, p.num_items - first);
   const int task = coop ? first : (warp < count ? first + warp : -1);
   int4 it = make_int4(0, 0, 0, 0);
-  int slot = -1;
+  int2 sg = make_int2(-1, -1);  // {partial slot, group}
+  int4 grp = make_int4(-1, -1, 0, 0);
   if (task >= 0 && task < p.num_items) {
     it = p.items[task];
-    slot = p.item_slots[task];
+    sg = p.item_slots[task];
+    if (sg.y >= 0 && sg.y < p.num_groups) grp = p.groups[sg.y];
   }
+  const int slot = sg.x;
 
   if (task >= 0 && task < p.num_items && (int)blockIdx.x < p.pf_ctas) {
     const int phys = prefetch_page_of_lane<NW>(p, it, coop, warp, lane);
@@ -264,7 +291,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   const bool is_last = (hw & kItemLast) != 0;
   const int pg0 = it.z, pg1 = it.w;
   if (b < 0 || b >= p.batch || kvh >= p.num_kv_heads || pg0 < 0 || pg1 < pg0 ||
-      pg1 > p.max_pages || (is_split && (slot < 0 || slot >= p.num_split_items))) {
+      pg1 > p.max_pages || (is_split && !split_slot_ok(p, sg, grp, b, kvh))) {
     if (lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
     return;  // all warps of a shared task see the same task
   }
@@ -602,6 +629,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
         if (lane == 0) p.part_lse[(size_t)slot * G + h] = lh > 0.f ? mh + lg2(lh) : -INFINITY;
       }
     }
+    if (is_split) split_finish_warp<T, D>(merge_target(p, sg.y, grp, G), lane);
     return;
   }
 
@@ -646,6 +674,8 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
+  if (is_split)  // CTA-uniform: one task
+    split_finish_cta<T, D, NW>(merge_target(p, sg.y, grp, G), &cta_last);
 }
 
 }  // namespace pa

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
   unsigned char* nrow = extra + L::NROW;                      // [2][D] codes, then 2 scales
   float* nscale = reinterpret_cast<float*>(nrow + 2 * D);
   int* cta_failed = reinterpret_cast<int*>(base + L::FLAG);
+  int* cta_last = cta_failed + 1;
 
   if ((int)blockIdx.x >= p.num_ctas) return;  // whole CTA
   // Plan data is written only by pa_plan_upload (a copy, which the
@@ -143,11 +144,14 @@ __global__ void __launch_bounds__(NW * 32, 4)
   const int count = coop ? 1 : min(NW, p.num_items - first);
   const int task = coop ? first : (warp < count ? first + warp : -1);
   int4 it = make_int4(0, 0, 0, 0);
-  int slot = -1;
+  int2 sg = make_int2(-1, -1);  // {partial slot, group}
+  int4 grp = make_int4(-1, -1, 0, 0);
   if (task >= 0 && task < p.num_items) {
     it = p.items[task];
-    slot = p.item_slots[task];
+    sg = p.item_slots[task];
+    if (sg.y >= 0 && sg.y < p.num_groups) grp = p.groups[sg.y];
   }
+  const int slot = sg.x;
   if (task >= 0 && task < p.num_items && (int)blockIdx.x < p.pf_ctas) {
     const int phys = prefetch_page_of_lane<NW>(p, it, coop, warp, lane);
     if (phys >= 0) {
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
   const bool is_last = (hw & kItemLast) != 0;
   const int pg0 = it.z, pg1 = it.w;
   if (b < 0 || b >= p.batch || kvh >= p.num_kv_heads || pg0 < 0 || pg1 < pg0 ||
-      pg1 > p.max_pages || (is_split && (slot < 0 || slot >= p.num_split_items))) {
+      pg1 > p.max_pages || (is_split && !split_slot_ok(p, sg, grp, b, kvh))) {
     if (lane == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
     return;  // all warps of a shared task see the same task
   }
@@ -550,6 +554,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
       float* dst = p.part_o + (size_t)slot * G * D;
       for (int i = lane * 4; i < G * D; i += 128)
         *reinterpret_cast<float4*>(dst + i) = *reinterpret_cast<const float4*>(stage + i);
+      split_finish_warp<__half, D>(merge_target(p, sg.y, grp, G), lane);
     }
     return;
   }
@@ -607,6 +612,8 @@ __global__ void __launch_bounds__(NW * 32, 4)
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
+  if (is_split)  // CTA-uniform: one task
+    split_finish_cta<__half, D, NW>(merge_target(p, sg.y, grp, G), cta_last);
 }
 
 }  // namespace pa

@@ -17,7 +17,7 @@ namespace pa {
 
 constexpr int kPageSize = 16;        // tokens per page (the only size built)
 constexpr int kWarpsPerCta = 4;      // warps sharing one task's pages
-constexpr int kMaxSplits = 1024;     // per (sequence, KV head); the combine keeps weights in smem
+constexpr int kMaxSplits = 1024;     // per (sequence, KV head)
 constexpr int kMinChunkPages = 48;   // auto planner never cuts finer than this
 constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per warp
 constexpr int kPlanWaves = 2;        // auto planner: tasks ~ waves x resident CTAs
@@ -87,9 +87,11 @@ inline int resident_ctas_per_sm(int head_dim, int group) {
 }
 
 // Workspace = [plan blob | lse partials | o partials].
-// Blob = header (16 x int32) | tasks (int4 each) | task partial slots (int32
-// each, -1 = direct output) | groups (int4 each: seq, kv head, splits, first
-// slot).
+// Blob = header (16 x int32) | tasks (int4 each) | task slots (int2 each:
+// partial slot, -1 = direct output, and the task's group) | groups (int4
+// each: seq, kv head, splits, first slot) | group counters (int32 each,
+// zero in the plan: split tasks of the group finished so far in a launch;
+// the task that completes the group merges it and sets it back to zero).
 // header: [0] magic [1] tasks [2] groups [3] partial slots [4] plan_id lo
 //         [5] plan_id hi [6] group size [7] head_dim [8] CTAs [9] shared CTAs.
 // Kernels check words 0..3 and 8..9 against their launch.  The partials of a
@@ -97,7 +99,7 @@ inline int resident_ctas_per_sm(int head_dim, int group) {
 // CTAs runs task i with all its warps; the CTAs after it run the remaining
 // (short) tasks four at a time, one per warp, in task order.
 struct Layout {
-  size_t items_off, slots_off, groups_off, blob_bytes, lse_off, o_off, total;
+  size_t items_off, slots_off, groups_off, counters_off, blob_bytes, lse_off, o_off, total;
 };
 
 inline size_t align_sz(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -106,8 +108,9 @@ inline Layout layout(int items, int groups, int nslots, int group, int head_dim)
   Layout l{};
   l.items_off = 64;
   l.slots_off = l.items_off + 16 * (size_t)items;
-  l.groups_off = align_sz(l.slots_off + 4 * (size_t)items, 16);
-  l.blob_bytes = align_sz(l.groups_off + 16 * (size_t)groups, 16);
+  l.groups_off = align_sz(l.slots_off + 8 * (size_t)items, 16);
+  l.counters_off = l.groups_off + 16 * (size_t)groups;
+  l.blob_bytes = align_sz(l.counters_off + 4 * (size_t)groups, 16);
   l.lse_off = align_sz(l.blob_bytes, 256);
   l.o_off = align_sz(l.lse_off + 4 * (size_t)nslots * group, 256);
   l.total = align_sz(l.o_off + 4 * (size_t)nslots * group * head_dim, 256);

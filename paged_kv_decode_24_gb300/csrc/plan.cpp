@@ -1,5 +1,5 @@
 // Host-side split planner: turns host seq_lens into the warp task list that
-// the split-decode kernel walks, plus the combine groups.
+// the split-decode kernel walks, plus the split groups it merges.
 //
 // Flash-Decoding (swiftLLM, feature list: paged attention v2) cuts a long
 // sequence into chunks processed in parallel, each producing a partial
@@ -190,15 +190,16 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
         items[4 * pos + 1] = (int32_t)hw;
         items[4 * pos + 2] = lo;
         items[4 * pos + 3] = hi;
-        slots[pos] = n > 1 ? icount++ : -1;
+        slots[2 * pos + 0] = n > 1 ? icount++ : -1;
+        slots[2 * pos + 1] = n > 1 ? gcount - 1 : -1;
       }
     }
   }
-  // zero the alignment gaps so the blob bytes are fully defined
-  const size_t used = lay.slots_off + 4 * (size_t)W;
+  // zero the alignment gaps and the group counters, so the blob bytes are
+  // fully defined
+  const size_t used = lay.slots_off + 8 * (size_t)W;
   if (lay.groups_off > used) memset(blob + used, 0, lay.groups_off - used);
-  if (lay.blob_bytes > lay.groups_off + 16 * (size_t)C)
-    memset(blob + lay.groups_off + 16 * (size_t)C, 0, lay.blob_bytes - lay.groups_off - 16 * (size_t)C);
+  memset(blob + lay.counters_off, 0, lay.blob_bytes - lay.counters_off);
 
   plan_out->shape = *shape;
   plan_out->num_work_items = W;

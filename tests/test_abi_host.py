@@ -35,14 +35,24 @@ def _shape(w):
 
 
 def _decode_blob(plan):
-    """Header (16 int32) | tasks (4 int32 each) | task slots (1 int32 each,
-    padded to 16 bytes) | groups (4 int32 each)."""
+    """Header (16 int32) | tasks (4 int32 each) | task slots (2 int32 each:
+    partial slot, group; padded to 16 bytes) | groups (4 int32 each) | group
+    counters (1 int32 each, zero in the plan)."""
     blob = plan.blob()
     W, C, nslots = blob[1], blob[2], blob[3]
     items = blob[16:16 + 4 * W].reshape(W, 4)
-    slots = blob[16 + 4 * W:16 + 5 * W]
-    g0 = (16 + 5 * W + 3) // 4 * 4
+    sg = blob[16 + 4 * W:16 + 6 * W].reshape(W, 2)
+    slots, task_group = sg[:, 0], sg[:, 1]
+    g0 = (16 + 6 * W + 3) // 4 * 4
     groups = blob[g0:g0 + 4 * C].reshape(C, 4)
+    counters = blob[g0 + 4 * C:g0 + 5 * C]
+    assert len(counters) == C and np.all(counters == 0)
+    for i in range(W):  # a split task names the group of its own (sequence, head)
+        if slots[i] >= 0:
+            b, h = groups[task_group[i]][:2]
+            assert (b, h) == (items[i][0], int(items[i][1]) & 0xFFFF)
+        else:
+            assert task_group[i] == -1
     NC, n_shared = blob[8], blob[9]
     return blob, items, groups, slots, nslots, (NC, n_shared)
 

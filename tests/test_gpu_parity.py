@@ -321,8 +321,8 @@ def test_device_seq_len_out_of_range_is_flagged():
 
 def test_maximum_split_count():
     """A request for more splits than the limit is clamped to 1024 page-aligned
-    splits (two pages each here). The combine then merges 1024 partials per
-    head, and the result still matches the unsplit oracle."""
+    splits (two pages each here). The split merge then combines 1024 partials
+    per head, and the result still matches the unsplit oracle."""
     w = workloads.make_custom(seq_lens=[32768, 40], num_q_heads=8, num_kv_heads=2, head_dim=64,
                               seed=29)
     dd = DeviceDecode(w)
