@@ -43,8 +43,11 @@ struct MergeTarget {
   int G, num_q_heads;
 };
 
-// Splits whose partials are loaded at once by one thread.
+// Splits whose partials one thread loads at once: 16, or 4 for a group of
+// at most 4 splits (fewer predicated-off loads).  A group always takes the
+// same batch, so its output bits never depend on which task merges.
 constexpr int kMergeBatch = 16;
+constexpr int kMergeBatchSmall = 4;
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   int old;
@@ -53,8 +56,8 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 }
 
 // The merged chunk (head h, dims d0 .. d0+3) of the group: a running
-// (max, sum, accumulator) over batches of kMergeBatch splits.
-template <int D>
+// (max, sum, accumulator) over batches of NB splits.
+template <int D, int NB>
 __device__ __forceinline__ float4 merge_chunk(const MergeTarget& t, int h, int d0) {
   const int ns = t.grp.z, off = t.grp.w;
   const float* lb = t.lse + (size_t)off * t.G + h;
@@ -62,11 +65,11 @@ __device__ __forceinline__ float4 merge_chunk(const MergeTarget& t, int h, int d
   const size_t sstride = (size_t)t.G * D;
   float m = -INFINITY, z = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
-    float l[kMergeBatch];
-    float4 x[kMergeBatch];
+  for (int s0 = 0; s0 < ns; s0 += NB) {
+    float l[NB];
+    float4 x[NB];
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const int s = s0 + u;
       l[u] = -INFINITY;
       x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -77,7 +80,7 @@ __device__ __forceinline__ float4 merge_chunk(const MergeTarget& t, int h, int d
     }
     float mn = m;
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) mn = fmaxf(mn, l[u]);
+    for (int u = 0; u < NB; ++u) mn = fmaxf(mn, l[u]);
     if (mn == -INFINITY) continue;  // every split so far is empty
     const float sc = ex2(m - mn);   // 0 while m is still -inf
     z *= sc;
@@ -86,7 +89,7 @@ __device__ __forceinline__ float4 merge_chunk(const MergeTarget& t, int h, int d
     a.z *= sc;
     a.w *= sc;
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const float e = ex2(l[u] - mn);  // 0 for an empty or absent split
       z += e;
       a.x = fmaf(e, x[u].x, a.x);
@@ -106,7 +109,8 @@ __device__ __forceinline__ void merge_chunks(const MergeTarget& t, int first, in
   constexpr int CPH = D / 4;  // chunks per head
   for (int u = first; u < t.G * CPH; u += stride) {
     const int h = u / CPH, d0 = (u % CPH) * 4;
-    const float4 r = merge_chunk<D>(t, h, d0);
+    const float4 r = t.grp.z <= kMergeBatchSmall ? merge_chunk<D, kMergeBatchSmall>(t, h, d0)
+                                                 : merge_chunk<D, kMergeBatch>(t, h, d0);
     uint2 v;
     v.x = Elem<T>::from_f2(r.x, r.y);
     v.y = Elem<T>::from_f2(r.z, r.w);

@@ -1,0 +1,127 @@
+"""GPU: the split merge, run by the last split task of each group.
+
+A split task adds one to its group's counter after writing its partial; the
+task that completes the group merges the partials into out and sets the
+counter back to zero.  Which task merges depends on timing.  These tests
+check, against the float64 oracle and across repeated calls:
+- a group whose split tasks mix the two task forms (a CTA's warps sharing a
+  task, and a task run by one warp of a bundle) merges to the oracle's
+  result and to the same bits on every call, for each split kernel;
+- every counter is zero again after a call, and many calls on one upload
+  agree bit for bit.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_decode_24_gb300 import workloads
+from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    return lib
+
+
+def blob_parts(plan):
+    """Tasks, their {slot, group} words, the counters' int32 offset and the
+    number of CTA-shared tasks, from the plan's host copy."""
+    blob = plan.blob()
+    W, C = int(blob[1]), int(blob[2])
+    items = blob[16:16 + 4 * W].reshape(W, 4)
+    sg = blob[16 + 4 * W:16 + 6 * W].reshape(W, 2)
+    g0 = (16 + 6 * W + 3) // 4 * 4
+    return items, sg, g0 + 4 * C, C, int(blob[9])
+
+
+def counters(dd):
+    _, _, c0, C, _ = blob_parts(dd.plan_obj)
+    return dd.workspace[:(c0 + C) * 4].view(torch.int32)[c0:c0 + C].cpu().numpy()
+
+
+def mixed_groups(plan):
+    """Groups with both a CTA-shared task and a per-warp task."""
+    items, sg, _, _, n_shared = blob_parts(plan)
+    kinds = {}
+    for i in range(len(items)):
+        if sg[i, 0] >= 0:
+            kinds.setdefault(int(sg[i, 1]), set()).add(i < n_shared)
+    return [g for g, k in kinds.items() if k == {True, False}]
+
+
+def mixed_workload(num_q_heads, kv="fp16", dtype="fp16", seed=71):
+    # 17-page sequences cut in two give 8- and 9-page splits.  Planned for one
+    # SM (four CTA slots) the 32+ tasks are many, so the 8-page ones are
+    # bundled one per warp while the 9-page ones get a CTA each.
+    return workloads.make_custom(seq_lens=[272, 270, 260, 258, 50], num_q_heads=num_q_heads,
+                                 num_kv_heads=4, head_dim=128, seed=seed, forced_splits=2,
+                                 kv=kv, dtype=dtype)
+
+
+@pytest.mark.parametrize("num_q_heads,dtype", [(4, "fp16"), (16, "fp16"), (16, "bf16")])
+def test_mixed_task_forms_merge_to_oracle_and_same_bits(num_q_heads, dtype):
+    w = mixed_workload(num_q_heads, dtype=dtype)
+    dd = DeviceDecode(w, num_sms=1)
+    dd.append()
+    dd.make_plan()
+    assert mixed_groups(dd.plan_obj), "the plan has no group that mixes the task forms"
+    first = dd.decode().clone()
+    assert dd.read_status() == 0
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.seq_lens)
+    want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
+    assert_close(first.float().cpu().numpy(), want, "mixed task forms", dtype=dtype)
+    assert np.all(counters(dd) == 0)
+    for _ in range(20):
+        again = dd.decode()
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+    assert np.all(counters(dd) == 0)
+
+
+def test_mixed_task_forms_int8_cache():
+    w = mixed_workload(16, kv="int8", seed=73)
+    dd = DeviceDecode(w, num_sms=1)
+    dd.append_q8()
+    dd.make_plan()
+    assert mixed_groups(dd.plan_obj)
+    first = dd.decode_q8().clone()
+    assert dd.read_status() == 0
+    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
+                                         w.v_new, w.block_table, w.seq_lens)
+    want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
+    assert_close(first.cpu().numpy(), want, "mixed task forms, INT8 cache")
+    for _ in range(20):
+        assert torch.equal(dd.decode_q8().view(torch.int16), first.view(torch.int16))
+    assert np.all(counters(dd) == 0)
+
+
+def test_many_calls_on_one_upload():
+    """200 calls on one uploaded plan of the default workload's shape (one
+    sequence, 32 heads, 16 splits): identical outputs, counters at zero."""
+    w = workloads.make_custom(seq_lens=[4096], num_q_heads=32, num_kv_heads=32, head_dim=128,
+                              seed=79, forced_splits=16)
+    dd = DeviceDecode(w)
+    dd.append()
+    dd.make_plan()
+    assert dd.plan_obj.c.num_groups == 32
+    first = dd.decode().clone()
+    outs = [dd.decode().clone() for _ in range(200)]
+    torch.cuda.synchronize()
+    assert dd.read_status() == 0
+    assert all(torch.equal(o.view(torch.int16), first.view(torch.int16)) for o in outs)
+    assert np.all(counters(dd) == 0)
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.seq_lens)
+    heads = [(0, h) for h in (0, 7, 31)]
+    want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale, heads=heads)
+    got = first.cpu().numpy()
+    for (b, h) in heads:
+        assert_close(got[b, h], want[b, h], f"head {h}")
