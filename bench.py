@@ -429,7 +429,11 @@ def run_ours(args):
     full, rem = divmod(K, LAYERS)
     graphs_full = [capture_model_step(i, LAYERS) for i in range(2)] if full else []
     graphs_rem = [capture_model_step(i, rem) for i in range(2)] if rem else []
-    launches_per_step = 1  # the split kernel; its last split per group merges
+    # the split kernel, whose last split per group merges; with
+    # PA_COMBINE_KERNEL=1 a separate combine kernel follows when any
+    # sequence is split
+    two_kernel = os.environ.get("PA_COMBINE_KERNEL", "").strip() == "1"
+    launches_per_step = 1 + (1 if two_kernel and plan0.c.num_groups > 0 else 0)
 
     def run_steps(nsteps, gfull, grem, m0=0):
         """nsteps layer-steps as model-step graphs; returns the model steps issued."""
@@ -688,7 +692,8 @@ def run_ours(args):
         "roofline": {
             "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if q8 else
                        "pa_append_decode_attention = split_decode_kernel") +
-                      " (with the append and the split merge)",
+                      (" (with the append) + combine_kernel, timed together"
+                       if two_kernel else " (with the append and the split merge)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

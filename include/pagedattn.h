@@ -191,7 +191,11 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * normalizer).  Splits follow the plan; their (output, log-sum-exp) partials
  * go to the workspace, and the last split of each (sequence, KV head) to
  * finish merges them into out within the same kernel (swiftLLM paged
- * attention v2).  One kernel launch per call.
+ * attention v2).  One kernel launch per call.  With the environment
+ * variable PA_COMBINE_KERNEL=1 (read once per process) the partials are
+ * instead merged by a separate combine kernel launched after the split
+ * kernel on the same stream (two launches when a sequence is split).  The
+ * two forms agree to rounding; each gives the same bits on every call.
  *
  * Device: q, k_pages, v_pages, block_table, seq_lens, out [B][Hq][D] fp16,
  * workspace (holding the uploaded plan), dev_status.

@@ -378,6 +378,11 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   static const int pf_ctas = env_int("PA_L2_PREFETCH_CTAS", -1, 0, INT32_MAX);
   p.pf_pages = pf_pages;
   p.pf_ctas = pf_ctas >= 0 ? pf_ctas : first_wave_ctas(D, G);
+  // Split groups are merged by their last split task inside the split kernel;
+  // PA_COMBINE_KERNEL=1 (read once per process) selects the two-kernel form,
+  // a separate combine kernel launched after the split kernel.
+  static const int combine_kernel = env_int("PA_COMBINE_KERNEL", 0, 0, 1);
+  p.fuse_merge = combine_kernel ? 0 : 1;
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;
@@ -387,7 +392,21 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
       return PA_ERR_CUDA;
     st = cuda_status(launch_split(p, D, G, shape->dtype, plan->num_ctas, s));
   }
-  return st;
+  if (st != PA_OK || p.fuse_merge || plan->num_groups == 0) return st;
+
+  CombineParams c{};
+  c.ws_header = (const int32_t*)ws;
+  c.groups = (const int4*)(ws + lay.groups_off);
+  c.part_lse = p.part_lse;
+  c.part_o = p.part_o;
+  c.out = out;
+  c.status = dev_status;
+  c.group_size = G;
+  c.num_q_heads = shape->num_q_heads;
+  c.num_items = p.num_items;
+  c.num_groups = p.num_groups;
+  c.num_split_items = p.num_split_items;
+  return cuda_status(launch_combine(c, D, shape->dtype, plan->num_groups * G, s));
 }
 
 }  // namespace

@@ -1,5 +1,5 @@
-// KV append (fp16 and INT8 caches), the multi-token append, the block copy
-// and the debug gather-index export.
+// The stand-alone split combine, KV append (fp16 and INT8 caches), the
+// multi-token append, the block copy and the debug gather-index export.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -10,6 +10,115 @@
 #include "quant_common.cuh"
 
 namespace pa {
+
+// ---------------------------------------------------------------------------
+// Combine: one CTA per (sequence, KV head, query head in the group) whose
+// sequence was split.  With partials (o_s, lse_s) in base 2:
+//   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s
+// (swiftLLM, paged attention v2 / Flash-Decoding).  The group's partials sit
+// in consecutive slots.  Warp w takes splits w, w+8, ... in batches of four
+// with their loads in flight together.  It keeps a running (max, sum,
+// rescaled accumulator) like the online softmax.  The 8 warp states then
+// merge in shared memory in warp order.  The order is fixed, so the result
+// is deterministic.  The plan (groups) is read before the wait on the split
+// kernel; after it, one round of loads brings every partial a warp needs.
+constexpr int kCombineWarps = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
+  constexpr int DPL = D / 32;
+  __shared__ float sm_m[kCombineWarps], sm_z[kCombineWarps];
+  __shared__ float sm_acc[kCombineWarps][D];
+
+  const int G = p.group_size;
+  const int gi = blockIdx.x / G;
+  const int j = blockIdx.x % G;
+  const int4 hdr = *reinterpret_cast<const int4*>(p.ws_header);
+  const int4 grp = gi < p.num_groups ? p.groups[gi] : make_int4(0, 0, 0, 0);
+
+  // The next kernel in the stream may become resident now; it waits for this
+  // grid before it touches anything this kernel reads or writes.
+  pdl_launch_dependents();
+  pdl_wait_primary();  // partials of the split kernel are visible after this
+
+  if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
+      hdr.w != p.num_split_items || gi >= p.num_groups) {
+    if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+    return;
+  }
+  const int ns = grp.z, off = grp.w;  // {seq, kv head, splits, first slot}
+  if (ns < 1 || ns > kMaxSplits || off < 0 || off + ns > p.num_split_items) {
+    if (threadIdx.x == 0) set_status(p.status, PA_DEV_PLAN_MISMATCH);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* ob = p.part_o + ((size_t)off * G + j) * D + lane * DPL;
+  const float* lb = p.part_lse + (size_t)off * G + j;
+  const size_t sstride = (size_t)G * D;
+
+  float m = -INFINITY, z = 0.f, acc[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+  for (int s0 = warp; s0 < ns; s0 += 4 * kCombineWarps) {
+    float lse[4], x[4][DPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * kCombineWarps;
+      lse[u] = -INFINITY;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) x[u][d] = 0.f;
+      if (s < ns) {
+        lse[u] = lb[(size_t)s * G];
+        if constexpr (DPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(ob + (size_t)s * sstride);
+          x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(ob + (size_t)s * sstride);
+          x[u][0] = v.x; x[u][1] = v.y;
+        }
+      }
+    }
+    const float mb = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
+    const float mn = fmaxf(m, mb);
+    if (mn == -INFINITY) continue;  // every split so far is empty
+    const float sc = ex2(m - mn);   // 0 while m is still -inf
+    z *= sc;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] *= sc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float e = ex2(lse[u] - mn);  // 0 for an empty or absent split
+      z += e;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[d] = fmaf(e, x[u][d], acc[d]);
+    }
+    m = mn;
+  }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_z[warp] = z;
+  }
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) sm_acc[warp][lane * DPL + d] = acc[d];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, sm_m[w]);
+    float Z = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kCombineWarps; ++w) {
+        const float sc = ex2(sm_m[w] - M);
+        Z = fmaf(sm_z[w], sc, Z);
+        O = fmaf(sm_acc[w][threadIdx.x], sc, O);
+      }
+    }
+    const float r = Z > 0.f ? O / Z : 0.f;
+    static_cast<T*>(p.out)[((size_t)grp.x * p.num_q_heads + (size_t)grp.y * G + j) * D +
+                           threadIdx.x] = Elem<T>::from_f(r);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Append: k_new[b][h] -> k_pages[block_table[b][(L-1)/S]][h][(L-1)%S], same
@@ -200,6 +309,26 @@ static int grid_for(long long work, int threads) {
   if (g < 1) g = 1;
   if (g > 152 * 16) g = 152 * 16;
   return (int)g;
+}
+
+cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,
+                           cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dtype == PA_DTYPE_BF16) {
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, p);
+  }
+  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, combine_kernel<__half, 64>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<__half, 128>, p);
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {

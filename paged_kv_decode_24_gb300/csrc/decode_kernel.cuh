@@ -45,7 +45,8 @@
 // A task whose sequence has more than one split writes its normalised output
 // and log2-sum-exp to the workspace; the group's last task to finish merges
 // them into the output (split_merge.cuh; swiftLLM, paged attention v2 /
-// Flash-Decoding).  Otherwise the task writes its output directly.
+// Flash-Decoding), or, with fuse_merge off, combine_kernel does after this
+// kernel.  Otherwise the task writes its output directly.
 #pragma once
 
 #include <cuda.h>
@@ -93,6 +94,9 @@ struct SplitParams {
   // L2 prefetch before the wait on the previous kernel: CTAs [0, pf_ctas)
   // prefetch the first pf_pages (<= 32) pages of each warp's share.
   int32_t pf_pages, pf_ctas;
+  // 1: the last split task of each group merges it (split_merge.cuh);
+  // 0: split tasks only write partials, and combine_kernel merges them.
+  int32_t fuse_merge;
 };
 
 // A split task's slot and group agree with each other and with the task.
@@ -629,7 +633,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
         if (lane == 0) p.part_lse[(size_t)slot * G + h] = lh > 0.f ? mh + lg2(lh) : -INFINITY;
       }
     }
-    if (is_split) split_finish_warp<T, D>(merge_target(p, sg.y, grp, G), lane);
+    if (is_split && p.fuse_merge) split_finish_warp<T, D>(merge_target(p, sg.y, grp, G), lane);
     return;
   }
 
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
-  if (is_split)  // CTA-uniform: one task
+  if (is_split && p.fuse_merge)  // CTA-uniform: one task
     split_finish_cta<T, D, NW>(merge_target(p, sg.y, grp, G), &cta_last);
 }
 

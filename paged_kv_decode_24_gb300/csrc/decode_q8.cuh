@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
       float* dst = p.part_o + (size_t)slot * G * D;
       for (int i = lane * 4; i < G * D; i += 128)
         *reinterpret_cast<float4*>(dst + i) = *reinterpret_cast<const float4*>(stage + i);
-      split_finish_warp<__half, D>(merge_target(p, sg.y, grp, G), lane);
+      if (p.fuse_merge) split_finish_warp<__half, D>(merge_target(p, sg.y, grp, G), lane);
     }
     return;
   }
@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
       if (d == 0) p.part_lse[(size_t)slot * G + h] = Z > 0.f ? M + lg2(Z) : -INFINITY;
     }
   }
-  if (is_split)  // CTA-uniform: one task
+  if (is_split && p.fuse_merge)  // CTA-uniform: one task
     split_finish_cta<__half, D, NW>(merge_target(p, sg.y, grp, G), cta_last);
 }
 

@@ -1,6 +1,6 @@
 // Kernel parameter blocks and launchers (host <-> device glue, internal).
-// The append kernels work for both 16-bit element types: they copy rows bit
-// for bit.
+// Append and combine work for both 16-bit element types: the append copies
+// rows bit for bit, and the combine's output type is chosen at launch.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -11,6 +11,18 @@
 namespace pa {
 
 struct SplitParams;  // decode_kernel.cuh
+
+struct CombineParams {
+  const int32_t* ws_header;
+  const int4* groups;
+  const float* part_lse;
+  const float* part_o;
+  void* out;  // fp16 or bf16, as the launch's dtype
+  int32_t* status;
+  int32_t group_size;
+  int32_t num_q_heads;
+  int32_t num_items, num_groups, num_split_items;  // must match the workspace header
+};
 
 struct AppendParams {
   const __half* k_new;
@@ -76,6 +88,8 @@ cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtyp
 cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
                             cudaStream_t stream);
 cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const int32_t* block_table, const int32_t* seq_lens, int32_t* out,
                           int32_t* status, int batch, int max_pages, int num_pages,
