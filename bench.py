@@ -92,6 +92,9 @@ def parse():
                     help="element type of q, K, V and out (the INT8 cache takes fp16)")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
                     help="per-layer KV caches; fewer only to shrink profiler captures")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="decode: force this split count per sequence in place of the "
+                         "workload's own (0 = the planner's choice); for experiments")
     args = ap.parse_args()
     return args
 
@@ -355,6 +358,8 @@ def run_ours(args):
         raise SystemExit("the INT8 cache takes fp16 q/out")
     w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank,
                               kv=args.kv, dtype=args.dtype)
+    if args.splits is not None:
+        w.forced_splits = max(0, int(args.splits))
     shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
                                w.max_pages_per_seq, w.num_pages, args.dtype)
     kv_bytes = w.kv_bytes_int8() if q8 else w.kv_bytes()
@@ -678,6 +683,9 @@ def run_ours(args):
             "sum_seq_len": int(w.seq_lens.sum()),
             "kv_read_bytes_per_step": kv_bytes,
             "splits": int(plan0.c.max_splits),
+            "split_merge": ("separate combine_kernel after the split kernel (PA_COMBINE_KERNEL=1)"
+                            if two_kernel else "by the last split task of each group, inside "
+                            "the split kernel"),
             "work_items": int(plan0.c.num_work_items),
             "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
                     "split kernel, whose last split per group merges); pa_plan + pa_plan_upload once per "
