@@ -87,8 +87,9 @@ def test_mixed_task_forms_merge_to_oracle_and_same_bits(num_q_heads, dtype):
     assert np.all(counters(dd) == 0)
 
 
-def test_mixed_task_forms_int8_cache():
-    w = mixed_workload(16, kv="int8", seed=73)
+@pytest.mark.parametrize("num_q_heads", [4, 16])
+def test_mixed_task_forms_int8_cache(num_q_heads):
+    w = mixed_workload(num_q_heads, kv="int8", seed=73)
     dd = DeviceDecode(w, num_sms=1)
     dd.append_q8()
     dd.make_plan()
