@@ -1,0 +1,59 @@
+"""GPU parity at the long end: one 131072-token sequence (four times the
+longest benchmark context) beside a short one, on each split kernel (CUDA
+cores for MHA, tensor cores for GQA, the INT8 cache), with the automatic
+plan.  The planner cuts the long sequence into well over a hundred splits,
+so the split merge combines that many partials per head.  Sampled heads of
+both sequences are compared with the float64 oracle.
+"""
+
+from __future__ import annotations
+
+import pytest
+
+import oracle
+from paged_kv_decode_24_gb300 import workloads
+from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    return lib
+
+
+LONG = 131072
+
+
+@pytest.mark.parametrize("hq,hkv,kv", [(8, 8, "fp16"), (16, 2, "fp16"), (8, 2, "int8")])
+def test_131072_token_context(hq, hkv, kv):
+    w = workloads.make_custom(seq_lens=[LONG, 77], num_q_heads=hq, num_kv_heads=hkv,
+                              head_dim=128, seed=8000 + hq + hkv, kv=kv)
+    dd = DeviceDecode(w)
+    dd.make_plan()
+    assert dd.plan_obj.c.max_splits >= 100
+    if kv == "int8":
+        dd.append_q8()
+        got = dd.decode_q8().cpu().numpy()
+    else:
+        dd.append()
+        got = dd.decode().cpu().numpy()
+    assert dd.read_status() == 0
+    heads = [(0, 0), (0, hq - 1), (0, hq // 2 + 1), (1, 0), (1, hq - 1)]
+    if kv == "int8":
+        kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales,
+                                             w.k_new, w.v_new, w.block_table, w.seq_lens)
+        want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens,
+                                          w.scale, heads=heads)
+    else:
+        kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                  w.seq_lens)
+        want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale,
+                                       heads=heads)
+    for (b, h) in heads:
+        assert_close(got[b, h], want[b, h], f"{kv} Hq={hq} Hkv={hkv} sequence {b} head {h}")
