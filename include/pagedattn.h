@@ -199,6 +199,9 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  *
  * Device: q, k_pages, v_pages, block_table, seq_lens, out [B][Hq][D] fp16,
  * workspace (holding the uploaded plan), dev_status.
+ * A workspace serves one call at a time: the call writes its split partials
+ * and group counters there, so calls in flight at once (on two streams, say)
+ * each need their own workspace.
  * scale: the logit scale, normally 1/sqrt(head_dim).
  * out receives fp16 rounded to nearest even from the fp32 result.  A
  * sequence of length 0 gets zeros.
