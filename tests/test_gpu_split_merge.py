@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import oracle
-from paged_kv_decode_24_gb300 import workloads
+from paged_kv_decode_24_gb300 import binding, workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
 from tests.parity import assert_close
 
@@ -126,3 +126,50 @@ def test_many_calls_on_one_upload():
     got = first.cpu().numpy()
     for (b, h) in heads:
         assert_close(got[b, h], want[b, h], f"head {h}")
+
+
+def test_corrupted_group_words_are_flagged_and_upload_recovers():
+    """Split tasks check their {slot, group} word and the group record
+    against their own task before touching a partial or a counter.  A
+    workspace whose words are corrupted is flagged PA_DEV_PLAN_MISMATCH;
+    uploading the plan again restores the task list and zeroes the counters,
+    and the next call matches the oracle."""
+    w = workloads.make_custom(seq_lens=[600, 300, 900], num_q_heads=8, num_kv_heads=2,
+                              head_dim=128, seed=97, forced_splits=3)
+    dd = DeviceDecode(w)
+    dd.append()
+    dd.make_plan()
+    items, sg, c0, C, _ = blob_parts(dd.plan_obj)
+    W = len(items)
+    g0 = (16 + 6 * W + 3) // 4 * 4
+    split = np.nonzero(sg[:, 0] >= 0)[0]
+    assert len(split) > 3 and C > 1
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.seq_lens)
+    want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
+
+    def corrupt(edit):
+        words = dd.workspace[:(g0 + 4 * C) * 4].view(torch.int32)
+        edit(words)
+        dd.status.zero_()
+        dd.decode()
+        assert dd.read_status() & binding.PA_DEV_PLAN_MISMATCH
+        dd.status.zero_()
+        binding.upload(dd.plan_obj, dd.workspace)
+        got = dd.decode().cpu().numpy()
+        assert dd.read_status() == 0
+        assert np.all(counters(dd) == 0)
+        assert_close(got, want, "after a fresh upload")
+
+    def every_split_task_to_group_0(words):
+        for i in split:
+            words[16 + 4 * W + 2 * int(i) + 1] = 0
+
+    def group_1_split_count_zero(words):
+        words[g0 + 4 * 1 + 2] = 0
+
+    def group_index_out_of_range(words):
+        words[16 + 4 * W + 2 * int(split[0]) + 1] = C + 5
+
+    corrupt(every_split_task_to_group_0)
+    corrupt(group_1_split_count_zero)
+    corrupt(group_index_out_of_range)
