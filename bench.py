@@ -145,6 +145,7 @@ def oracle_worker(args):
 def run_oracle_subprocess(cfg, seconds, kv="fp16", dtype="fp16"):
     """The oracle in a fresh single-threaded process (started by exec, so no
     CUDA state is shared)."""
+    from paged_kv_decode_24_gb300 import workloads
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
@@ -158,7 +159,7 @@ def run_oracle_subprocess(cfg, seconds, kv="fp16", dtype="fp16"):
     res = json.loads(r.stdout.strip().splitlines()[-1])
     gbs = res["kv_bytes"] / res["seconds"] / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"config {cfg} ({kv} cache, {dtype}): {res['sample']}, "
+            "sample": f"{workloads.CONFIG_NAMES[cfg]} ({kv} cache, {dtype}): {res['sample']}, "
                       f"{res['seconds']:.1f} s of float64 numpy"}
 
 
@@ -167,6 +168,7 @@ def run_oracle_all_cores(cfg, seconds, kv="fp16", dtype="fp16"):
     process per core (started by exec, no CUDA state), each on its own share
     of the sequences (offset i, stride n), all for about ``seconds``.  GB/s =
     the KV bytes of all of them / the longest one's time."""
+    from paged_kv_decode_24_gb300 import workloads
     n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -187,7 +189,7 @@ def run_oracle_all_cores(cfg, seconds, kv="fp16", dtype="fp16"):
     kvb = sum(r["kv_bytes"] for r in res)
     dt = max(r["seconds"] for r in res)
     return {"value": kvb / dt / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
-            "sample": f"config {cfg} ({kv} cache, {dtype}): {n} single-threaded processes, "
+            "sample": f"{workloads.CONFIG_NAMES[cfg]} ({kv} cache, {dtype}): {n} single-threaded processes, "
                       f"sequences dealt round-robin, {dt:.1f} s of float64 numpy each"}
 
 
