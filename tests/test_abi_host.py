@@ -198,11 +198,26 @@ def test_plan_in_caller_buffer(lib):
     with pytest.raises(binding.PagedAttnError) as e:
         binding.Plan(s, w.seq_lens, 152, host_buffer=small)
     assert e.value.code == 3
-    buf = np.zeros(ref.c.blob_bytes + 64, np.uint8)
+    # a dirty buffer: every byte of the plan, gaps and group counters
+    # included, is written (the kernels need the counters at zero)
+    buf = np.full(ref.c.blob_bytes + 64, 0xFF, np.uint8)
     p = binding.Plan(s, w.seq_lens, 152, host_buffer=buf)
     assert p.c.owns_blob == 0 and p.c.host_blob == buf.ctypes.data
     got = buf[:ref.c.blob_bytes].view(np.int32)
     assert np.array_equal(np.delete(got, [4, 5]), np.delete(ref.blob(), [4, 5]))
+    # the same with split groups, whose counters must come out zero
+    w2 = workloads.make_custom(seq_lens=[3000, 50, 700], num_q_heads=8, num_kv_heads=2,
+                               head_dim=128, seed=5)
+    s2 = _shape(w2)
+    ref2 = binding.Plan(s2, w2.seq_lens, 152, 4)
+    buf2 = np.full(ref2.c.blob_bytes, 0xFF, np.uint8)
+    binding.Plan(s2, w2.seq_lens, 152, 4, host_buffer=buf2)
+    got2 = buf2.view(np.int32)
+    assert np.array_equal(np.delete(got2, [4, 5]), np.delete(ref2.blob(), [4, 5]))
+    W, C = int(got2[1]), int(got2[2])
+    c0 = (16 + 6 * W + 3) // 4 * 4 + 4 * C
+    assert C == 6  # every sequence is split (at most 4 ways), two KV heads each
+    assert np.all(got2[c0:c0 + C] == 0) and c0 + C <= len(got2)
     p.free()   # must not free the caller's buffer
     assert buf[:4].view(np.int32)[0] == 0x564B4150
 
