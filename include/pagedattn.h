@@ -78,7 +78,7 @@ typedef enum {
 #define PA_DEV_BAD_PAGE 0x1       /* block-table entry outside [0, num_pages): page skipped */
 #define PA_DEV_BAD_SEQ_LEN 0x2    /* seq_len < 0 or > max_pages_per_seq * page_size: clamped */
 #define PA_DEV_PLAN_MISMATCH 0x4  /* workspace does not hold this plan, or seq_lens differ from it */
-#define PA_DEV_TIMEOUT 0x8        /* a bounded wait on a page copy gave up: output not written */
+#define PA_DEV_TIMEOUT 0x8        /* a bounded wait gave up: the outputs it feeds are not written */
 
 typedef struct {
   int32_t batch;             /* B, >= 0 */
@@ -119,7 +119,45 @@ typedef struct {
   size_t blob_bytes;         /* bytes pa_plan_upload copies into the workspace */
   size_t workspace_bytes;    /* minimum workspace for pa_decode_attention */
   void* host_blob;           /* task list in host memory, owned by the plan */
+  /* How the decode calls made with this plan run (copied from the options
+   * of pa_plan_ex; pa_plan and pa_plan_in leave them 0).  Every 0 is the
+   * default. */
+  int32_t merge;             /* PA_MERGE_IN_SPLIT_KERNEL or PA_MERGE_COMBINE_KERNEL */
+  int32_t l2_prefetch_pages; /* see pa_plan_options_t */
+  int32_t l2_prefetch_ctas;  /* see pa_plan_options_t */
+  int32_t reserved;          /* 0 */
+  uint64_t wait_limit_ns;    /* see pa_plan_options_t */
 } pa_plan_t;
+
+/* How the split partials of a sequence are merged (paged attention v2's
+ * log-sum-exp reduce). */
+#define PA_MERGE_IN_SPLIT_KERNEL 0 /* the last split task of each (sequence, KV head) to
+                                      finish merges them inside the split kernel: one launch */
+#define PA_MERGE_COMBINE_KERNEL 1  /* split tasks only write partials; a separate combine
+                                      kernel launched after the split kernel merges them */
+
+/*
+ * Options of a decode plan.  A zeroed struct, or a NULL pointer, gives the
+ * defaults: every field's 0 is its default.  The planner fields change the
+ * task list; the others are copied into the plan and read by each decode
+ * call made with it.
+ */
+typedef struct {
+  int32_t min_chunk_pages;   /* automatic plan: no split shorter than this many pages (0: 48) */
+  int32_t waves;             /* automatic plan: about waves x resident CTAs tasks (0: 2) */
+  int32_t bundle_max_pages;  /* when the GPU runs several waves of tasks, tasks of at most
+                                this many pages run one per warp, four to a CTA
+                                (0: 8; negative: never) */
+  int32_t merge;             /* PA_MERGE_IN_SPLIT_KERNEL (0) or PA_MERGE_COMBINE_KERNEL */
+  int32_t l2_prefetch_pages; /* pages per warp that the split kernel's first CTAs ask L2 for
+                                while the previous kernel still runs (0: 2; negative:
+                                none; at most 32) */
+  int32_t l2_prefetch_ctas;  /* CTAs that prefetch (0: the first wave, the CTAs the GPU
+                                holds at once; negative: none) */
+  uint64_t wait_limit_ns;    /* how long a warp waits for one page copy before it gives up,
+                                sets PA_DEV_TIMEOUT and writes nothing (0: 1 s).  A copy
+                                that was issued always lands before the kernel exits. */
+} pa_plan_options_t;
 
 /*
  * Append the new token's K and V (decode-phase cache update; from-scratch
@@ -164,6 +202,17 @@ pa_status_t pa_plan_in(const pa_shape_t* shape, const int32_t* seq_lens_host, in
                        int32_t forced_splits, void* host_buffer, size_t host_buffer_bytes,
                        pa_plan_t* plan_out);
 
+/*
+ * pa_plan and pa_plan_in with options (NULL: the defaults).  host_buffer
+ * NULL: the plan allocates and owns its task list (as pa_plan); otherwise
+ * the list goes into host_buffer (as pa_plan_in).  A field out of range
+ * (merge not a PA_MERGE_* value, l2_prefetch_pages > 32) returns
+ * PA_ERR_INVALID_ARG.
+ */
+pa_status_t pa_plan_ex(const pa_shape_t* shape, const int32_t* seq_lens_host, int32_t num_sms,
+                       int32_t forced_splits, const pa_plan_options_t* options,
+                       void* host_buffer, size_t host_buffer_bytes, pa_plan_t* plan_out);
+
 /* Release the plan's host memory (safe on a zeroed or already freed plan). */
 void pa_plan_free(pa_plan_t* plan);
 
@@ -191,11 +240,11 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * normalizer).  Splits follow the plan; their (output, log-sum-exp) partials
  * go to the workspace, and the last split of each (sequence, KV head) to
  * finish merges them into out within the same kernel (swiftLLM paged
- * attention v2).  One kernel launch per call.  With the environment
- * variable PA_COMBINE_KERNEL=1 (read once per process) the partials are
- * instead merged by a separate combine kernel launched after the split
- * kernel on the same stream (two launches when a sequence is split).  The
- * two forms agree to rounding; each gives the same bits on every call.
+ * attention v2).  One kernel launch per call.  With a plan made with
+ * merge = PA_MERGE_COMBINE_KERNEL (pa_plan_ex) the partials are instead
+ * merged by a separate combine kernel launched after the split kernel on the
+ * same stream (two launches when a sequence is split).  The two forms agree
+ * to rounding; each gives the same bits on every call.
  *
  * Device: q, k_pages, v_pages, block_table, seq_lens, out [B][Hq][D] fp16,
  * workspace (holding the uploaded plan), dev_status.
@@ -205,8 +254,9 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * scale: the logit scale, normally 1/sqrt(head_dim).
  * out receives fp16 rounded to nearest even from the fp32 result.  A
  * sequence of length 0 gets zeros.
- * Returns PA_ERR_PLAN if plan->shape differs from *shape, and
- * PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
+ * Returns PA_ERR_PLAN if plan->shape differs from *shape in batch, heads,
+ * head_dim, page_size or max_pages_per_seq (the fields the task list depends
+ * on), and PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
  */
 pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
                                 const void* k_pages, const void* v_pages,
@@ -295,21 +345,25 @@ pa_status_t pa_append_decode_attention_q8(const pa_shape_t* shape, const pa_plan
  * accounting), and latency-critical loops where a cudaMalloc could stall on
  * device synchronisation.
  *
- * Same arguments and result as pa_decode_attention, minus the workspace.
- * The task list and the split partials live in one file-scope __device__
- * array of PA_STATIC_WORKSPACE_BYTES (16 MiB).  Every GPU that loads the
- * library holds the array until the process exits.  Each call uploads the
- * plan's task list into it (host_blob must still be valid), then launches
- * the same kernels.  No cudaMalloc, cudaFree or allocating library routine
- * is called.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current.  Make that first call
- *    before any stream capture.
- *  - A plan whose workspace_bytes exceeds PA_STATIC_WORKSPACE_BYTES is
- *    rejected with PA_ERR_WORKSPACE before anything is launched.
+ * Same arguments, checks and result as pa_decode_attention, minus the
+ * workspace.  The task list and the split partials live in one file-scope
+ * __device__ array of PA_STATIC_WORKSPACE_BYTES (16 MiB).  Every GPU that
+ * loads the library holds the array until the process exits.  Each call
+ * uploads the plan's task list into it (host_blob must still be valid), then
+ * launches the same kernels.  No cudaMalloc, cudaFree or allocating library
+ * routine is called.
+ *  - Each call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so a context rebuilt after cudaDeviceReset is
+ *    found anew.  The first call on a device may load the library's device
+ *    code there: make that first call before any stream capture.
+ *  - Every argument check of pa_decode_attention runs before anything is
+ *    queued; a rejected call (a plan whose workspace_bytes exceeds
+ *    PA_STATIC_WORKSPACE_BYTES gives PA_ERR_WORKSPACE) leaves the array as
+ *    it was.
  *  - All calls on a device share the array, which keeps the previous call's
- *    contents.  Nothing in it needs to start at zero.  Calls that overlap on
- *    the GPU (other streams, other host threads) race on it: serialise them.
+ *    contents.  What must start at zero (the split groups' counters) comes
+ *    zeroed in each call's upload.  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on it: serialise them.
  */
 pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t* plan,
                                        const void* q, const void* k_pages, const void* v_pages,
@@ -334,21 +388,39 @@ pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const pa_plan_t*
  */
 typedef struct {
   pa_shape_t shape;     /* the shape the plan was made for */
-  int32_t num_tiles;    /* CTAs: 128 query rows (tokens x heads of one KV head) each
-                           on tcgen05; 64 for the mma.sync form (PA_PREFILL_ROWS=64) */
+  int32_t num_tiles;    /* CTAs: rows_per_tile query rows (tokens x heads of one KV head) each */
   int32_t total_q;      /* T */
   int32_t owns_blob;    /* 1: host_blob is released by pa_prefill_plan_free */
-  int32_t reserved;
+  int32_t rows_per_tile; /* 128: the tcgen05 kernel; 64: the mma.sync kernel */
   uint64_t plan_id;
   size_t blob_bytes;    /* bytes pa_prefill_plan_upload copies */
   size_t workspace_bytes;
   void* host_blob;
+  uint64_t wait_limit_ns; /* bound of each wait in the kernel (see pa_prefill_options_t) */
 } pa_prefill_plan_t;
+
+/* Options of a multi-token plan; a zeroed struct or NULL gives the
+ * defaults. */
+typedef struct {
+  int32_t rows_per_tile;  /* 0 or 128: the tcgen05 kernel (TMEM accumulators, 128 rows per
+                             CTA); 64: the mma.sync kernel (64 rows per CTA) */
+  int32_t reserved;       /* 0 */
+  uint64_t wait_limit_ns; /* how long a warp waits on one barrier (a copy, an MMA, another
+                             warp) before it gives up, sets PA_DEV_TIMEOUT and leaves its
+                             rows unwritten (0: 1 s).  Copies and MMAs that were issued
+                             finish before the kernel exits. */
+} pa_prefill_options_t;
 
 /* Host: the tile list (longest work first) and the row offsets cu.
  * q_lens_host[b] must satisfy 0 <= q_lens[b] <= seq_lens[b]. */
 pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* seq_lens_host,
                             const int32_t* q_lens_host, pa_prefill_plan_t* plan_out);
+
+/* pa_prefill_plan with options (NULL: the defaults).  rows_per_tile other
+ * than 0, 64 or 128 returns PA_ERR_INVALID_ARG. */
+pa_status_t pa_prefill_plan_ex(const pa_shape_t* shape, const int32_t* seq_lens_host,
+                               const int32_t* q_lens_host, const pa_prefill_options_t* options,
+                               pa_prefill_plan_t* plan_out);
 void pa_prefill_plan_free(pa_prefill_plan_t* plan);
 pa_status_t pa_prefill_plan_upload(const pa_prefill_plan_t* plan, void* workspace,
                                    size_t workspace_bytes, void* stream);

@@ -48,14 +48,47 @@ class PaPlan(ctypes.Structure):
                 ("warps_per_cta", ctypes.c_int32),
                 ("owns_blob", ctypes.c_int32), ("plan_id", ctypes.c_uint64),
                 ("blob_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
-                ("host_blob", ctypes.c_void_p)]
+                ("host_blob", ctypes.c_void_p), ("merge", ctypes.c_int32),
+                ("l2_prefetch_pages", ctypes.c_int32), ("l2_prefetch_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64)]
+
+
+PA_MERGE_IN_SPLIT_KERNEL = 0
+PA_MERGE_COMBINE_KERNEL = 1
+MERGES = {"split": PA_MERGE_IN_SPLIT_KERNEL, "combine": PA_MERGE_COMBINE_KERNEL}
+
+
+class PaPlanOptions(ctypes.Structure):
+    _fields_ = [("min_chunk_pages", ctypes.c_int32), ("waves", ctypes.c_int32),
+                ("bundle_max_pages", ctypes.c_int32), ("merge", ctypes.c_int32),
+                ("l2_prefetch_pages", ctypes.c_int32), ("l2_prefetch_ctas", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_uint64)]
 
 
 class PaPrefillPlan(ctypes.Structure):
     _fields_ = [("shape", PaShape), ("num_tiles", ctypes.c_int32), ("total_q", ctypes.c_int32),
-                ("owns_blob", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("owns_blob", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32),
                 ("plan_id", ctypes.c_uint64), ("blob_bytes", ctypes.c_size_t),
-                ("workspace_bytes", ctypes.c_size_t), ("host_blob", ctypes.c_void_p)]
+                ("workspace_bytes", ctypes.c_size_t), ("host_blob", ctypes.c_void_p),
+                ("wait_limit_ns", ctypes.c_uint64)]
+
+
+class PaPrefillOptions(ctypes.Structure):
+    _fields_ = [("rows_per_tile", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_uint64)]
+
+
+def plan_options(**kw) -> PaPlanOptions:
+    """pa_plan_options_t from keyword fields (merge may be "split" or "combine");
+    unnamed fields stay 0, their default."""
+    o = PaPlanOptions()
+    for k, v in kw.items():
+        if k == "merge" and isinstance(v, str):
+            v = MERGES[v]
+        if not hasattr(o, k):
+            raise TypeError(f"unknown plan option {k}")
+        setattr(o, k, int(v))
+    return o
 
 
 class PagedAttnError(RuntimeError):
@@ -74,6 +107,9 @@ _SIGS = {
                                ctypes.POINTER(PaPlan)]),
     "pa_plan_in": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, ctypes.c_int32, ctypes.c_int32, _P,
                                   ctypes.c_size_t, ctypes.POINTER(PaPlan)]),
+    "pa_plan_ex": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.POINTER(PaPlanOptions), _P, ctypes.c_size_t,
+                                  ctypes.POINTER(PaPlan)]),
     "pa_plan_free": (None, [ctypes.POINTER(PaPlan)]),
     "pa_plan_upload": (ctypes.c_int, [ctypes.POINTER(PaPlan), _P, ctypes.c_size_t, _P]),
     "pa_decode_attention": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan), _P, _P,
@@ -106,6 +142,9 @@ _SIGS = {
                                       ctypes.c_int32, _P, _P]),
     "pa_prefill_plan": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P,
                                        ctypes.POINTER(PaPrefillPlan)]),
+    "pa_prefill_plan_ex": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P,
+                                          ctypes.POINTER(PaPrefillOptions),
+                                          ctypes.POINTER(PaPrefillPlan)]),
     "pa_prefill_plan_free": (None, [ctypes.POINTER(PaPrefillPlan)]),
     "pa_prefill_plan_upload": (ctypes.c_int, [ctypes.POINTER(PaPrefillPlan), _P, ctypes.c_size_t,
                                               _P]),
@@ -161,22 +200,30 @@ class Plan:
 
     With ``host_buffer`` (a host tensor or numpy array, e.g. pinned memory)
     the task list is written there by pa_plan_in instead of a malloc'ed block.
+    With ``options`` (a PaPlanOptions, see plan_options) the plan is made by
+    pa_plan_ex.
     """
 
     def __init__(self, shape: PaShape, seq_lens_host, num_sms: int, forced_splits: int = 0,
-                 host_buffer=None):
+                 host_buffer=None, options: PaPlanOptions | None = None):
         lib = load()
         self.shape = shape
         self.c = PaPlan()
         lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
         self._lens = lens
         lp = lens.ctypes.data if lens.size else None
-        if host_buffer is None:
+        ptr, nbytes = None, 0
+        if host_buffer is not None:
+            self._buf = host_buffer
+            ptr, nbytes = _host_ptr(host_buffer)
+        if options is not None:
+            self.options = options
+            code = lib.pa_plan_ex(ctypes.byref(shape), lp, int(num_sms), int(forced_splits),
+                                  ctypes.byref(options), ptr, nbytes, ctypes.byref(self.c))
+        elif host_buffer is None:
             code = lib.pa_plan(ctypes.byref(shape), lp, int(num_sms), int(forced_splits),
                                ctypes.byref(self.c))
         else:
-            self._buf = host_buffer
-            ptr, nbytes = _host_ptr(host_buffer)
             code = lib.pa_plan_in(ctypes.byref(shape), lp, int(num_sms), int(forced_splits), ptr,
                                   nbytes, ctypes.byref(self.c))
         _check("pa_plan", code)
@@ -390,7 +437,8 @@ def gather_indices(shape, block_table, seq_lens, out_slots, status, stream=None)
 class PrefillPlan:
     """Owner of a pa_prefill_plan_t (tile list and row offsets, host side)."""
 
-    def __init__(self, shape: PaShape, seq_lens_host, q_lens_host):
+    def __init__(self, shape: PaShape, seq_lens_host, q_lens_host, rows_per_tile: int = 0,
+                 wait_limit_ns: int = 0):
         lib = load()
         self.shape = shape
         self.c = PaPrefillPlan()
@@ -398,8 +446,13 @@ class PrefillPlan:
         self._qlens = np.ascontiguousarray(np.asarray(q_lens_host, dtype=np.int32))
         lp = self._lens.ctypes.data if self._lens.size else None
         qp = self._qlens.ctypes.data if self._qlens.size else None
-        _check("pa_prefill_plan", lib.pa_prefill_plan(ctypes.byref(shape), lp, qp,
-                                                      ctypes.byref(self.c)))
+        if rows_per_tile or wait_limit_ns:
+            self.options = PaPrefillOptions(int(rows_per_tile), 0, int(wait_limit_ns))
+            code = lib.pa_prefill_plan_ex(ctypes.byref(shape), lp, qp,
+                                          ctypes.byref(self.options), ctypes.byref(self.c))
+        else:
+            code = lib.pa_prefill_plan(ctypes.byref(shape), lp, qp, ctypes.byref(self.c))
+        _check("pa_prefill_plan", code)
 
     @property
     def workspace_bytes(self) -> int:

@@ -255,6 +255,35 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
 }  // namespace
 }  // namespace pa
 
+namespace pa {
+
+pa_status_t check_decode_call(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens, float scale,
+                              const void* out, const void* workspace, size_t workspace_bytes,
+                              const int32_t* dev_status, bool* launches) {
+  *launches = false;
+  pa_status_t st = check_shape(shape);
+  if (st != PA_OK) return st;
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
+  if (shape->batch == 0) return PA_OK;
+  if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
+      plan->num_shared_ctas > plan->num_ctas || plan->l2_prefetch_pages > 32 ||
+      (plan->merge != PA_MERGE_IN_SPLIT_KERNEL && plan->merge != PA_MERGE_COMBINE_KERNEL))
+    return PA_ERR_PLAN;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
+      !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  *launches = true;
+  return PA_OK;
+}
+
+}  // namespace pa
+
 extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan,
                                            const void* q, const void* k_pages, const void* v_pages,
                                            const int32_t* block_table, const int32_t* seq_lens,
@@ -314,20 +343,10 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
                         const int32_t* block_table, const int32_t* seq_lens, float scale,
                         void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         void* stream) {
-  pa_status_t st = check_shape(shape);
-  if (st != PA_OK) return st;
-  if (!plan) return PA_ERR_INVALID_ARG;
-  if (!same_plan_shape(plan->shape, *shape)) return PA_ERR_PLAN;
-  if (shape->batch == 0) return PA_OK;
-  if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
-      plan->num_shared_ctas > plan->num_ctas)
-    return PA_ERR_PLAN;
-  if (!aligned(q, 16) || !aligned(kv.k, 16) || !aligned(kv.v, 16) || !aligned(out, 16) ||
-      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
-      !aligned(workspace, 256))
-    return PA_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < plan->workspace_bytes) return PA_ERR_WORKSPACE;
+  bool launches = false;
+  pa_status_t st = check_decode_call(shape, plan, q, kv.k, kv.v, block_table, seq_lens, scale, out,
+                                     workspace, workspace_bytes, dev_status, &launches);
+  if (st != PA_OK || !launches) return st;
   if (kv.int8() && shape->dtype != PA_DTYPE_F16) return PA_ERR_UNSUPPORTED;
 
   const int G = shape->num_q_heads / shape->num_kv_heads;
@@ -372,17 +391,16 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   p.num_ctas = plan->num_ctas;
   p.num_shared = plan->num_shared_ctas;
   // Only the first wave's CTAs can start before the previous kernel ends, so
-  // only they prefetch.  PA_L2_PREFETCH_PAGES (0..32) and PA_L2_PREFETCH_CTAS
-  // override both for experiments; read once per process.
-  static const int pf_pages = env_int("PA_L2_PREFETCH_PAGES", kL2PrefetchPages, 0, 32);
-  static const int pf_ctas = env_int("PA_L2_PREFETCH_CTAS", -1, 0, INT32_MAX);
-  p.pf_pages = pf_pages;
-  p.pf_ctas = pf_ctas >= 0 ? pf_ctas : first_wave_ctas(D, G);
-  // Split groups are merged by their last split task inside the split kernel;
-  // PA_COMBINE_KERNEL=1 (read once per process) selects the two-kernel form,
-  // a separate combine kernel launched after the split kernel.
-  static const int combine_kernel = env_int("PA_COMBINE_KERNEL", 0, 0, 1);
-  p.fuse_merge = combine_kernel ? 0 : 1;
+  // by default only they prefetch; the plan's options may say otherwise.
+  p.pf_pages = plan->l2_prefetch_pages == 0 ? kL2PrefetchPages
+                                            : (plan->l2_prefetch_pages < 0 ? 0 : plan->l2_prefetch_pages);
+  p.pf_ctas = plan->l2_prefetch_ctas == 0 ? first_wave_ctas(D, G)
+                                          : (plan->l2_prefetch_ctas < 0 ? 0 : plan->l2_prefetch_ctas);
+  // Split groups are merged by their last split task inside the split kernel,
+  // or, for a plan made with PA_MERGE_COMBINE_KERNEL, by a separate combine
+  // kernel launched after the split kernel.
+  p.fuse_merge = plan->merge == PA_MERGE_COMBINE_KERNEL ? 0 : 1;
+  p.wait_ns = wait_limit_or_default(plan->wait_limit_ns);
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;
@@ -505,6 +523,7 @@ extern "C" pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_pr
   p.num_pages = shape->num_pages;
   p.num_tiles = plan->num_tiles;
   p.total_q = plan->total_q;
+  p.wait_ns = wait_limit_or_default(plan->wait_limit_ns);
   if (!encode_pool_map(&p.tmap_k, k_pages, *shape) || !encode_pool_map(&p.tmap_v, v_pages, *shape))
     return PA_ERR_CUDA;
   const int G = shape->num_q_heads / shape->num_kv_heads;

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   constexpr int DPL = D / 32;
   __shared__ float sm_m[kCombineWarps], sm_z[kCombineWarps];
   __shared__ float sm_acc[kCombineWarps][D];
+  __shared__ int sm_missing;
 
   const int G = p.group_size;
   const int gi = blockIdx.x / G;
@@ -56,7 +57,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const float* lb = p.part_lse + (size_t)off * G + j;
   const size_t sstride = (size_t)G * D;
 
+  if (threadIdx.x == 0) sm_missing = 0;
+  __syncthreads();
   float m = -INFINITY, z = 0.f, acc[DPL];
+  bool missing = false;  // a split task that gave up marked its slot NaN
 #pragma unroll
   for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
   for (int s0 = warp; s0 < ns; s0 += 4 * kCombineWarps) {
@@ -78,6 +82,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
         }
       }
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) missing |= isnan(lse[u]);
     const float mb = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
     const float mn = fmaxf(m, mb);
     if (mn == -INFINITY) continue;  // every split so far is empty
@@ -98,9 +104,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     sm_m[warp] = m;
     sm_z[warp] = z;
   }
+  if (missing) sm_missing = 1;
 #pragma unroll
   for (int d = 0; d < DPL; ++d) sm_acc[warp][lane * DPL + d] = acc[d];
   __syncthreads();
+  if (sm_missing) return;  // a split gave up: the group's output stays unwritten
   if (threadIdx.x < D) {
     float M = -INFINITY;
 #pragma unroll

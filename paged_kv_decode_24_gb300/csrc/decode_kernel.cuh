@@ -97,6 +97,7 @@ struct SplitParams {
   // 1: the last split task of each group merges it (split_merge.cuh);
   // 0: split tasks only write partials, and combine_kernel merges them.
   int32_t fuse_merge;
+  uint64_t wait_ns;  // bound of each wait on a page copy (the plan's wait_limit_ns)
 };
 
 // A split task's slot and group agree with each other and with the task.
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   for (int k = 0; k < npk; ++k) {
     const int hk = 2 * k;
     const int sk = hk % NSH;
-    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sk, (hk / NSH) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sk, (hk / NSH) & 1, p.wait_ns))) {
       failed = true;
       hfail = hk;
       break;
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 
     const int hv = hk + 1;
     const int sv = hv % NSH;
-    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sv, (hv / NSH) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(ws_u32 + L::BAR + 8 * sv, (hv / NSH) & 1, p.wait_ns))) {
       failed = true;
       hfail = hv;
       break;
@@ -577,7 +578,7 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
       set_status(p.status, PA_DEV_TIMEOUT);
       const int last = min(nhalf, hfail + NSH);
       for (int h = hfail; h < last; ++h)
-        mbar_wait_bounded(ws_u32 + L::BAR + 8 * (h % NSH), (h / NSH) & 1, 10000000ull);
+        mbar_wait_bounded(ws_u32 + L::BAR + 8 * (h % NSH), (h / NSH) & 1, kDrainWaitNs);
       cta_failed = 1;
     }
     __syncwarp();
@@ -604,7 +605,10 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 
   if (!coop) {
     // ---- a task of its own: normalise and write from registers
-    if (failed) return;
+    if (failed) {
+      if (is_split) mark_split_missing(p.part_lse, slot, G, lane);
+      return;
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const int rep = h * Geo::HEAD_LANES;  // lane (rg 0, c = h*HEAD_LANES) holds head h's state
@@ -639,7 +643,10 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
 
   // ---- shared task: merge the NW warp states in shared memory (rings are free)
   __syncthreads();
-  if (cta_failed) return;
+  if (cta_failed) {
+    if (is_split && warp == 0) mark_split_missing(p.part_lse, slot, G, lane);
+    return;
+  }
   float* st = reinterpret_cast<float*>(smem_raw);  // [NW][2G + G*D]
   constexpr int SLOT = 2 * G + G * D;
   float* mine = st + warp * SLOT;

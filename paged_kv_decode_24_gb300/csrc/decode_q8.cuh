@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
   int kfail = 0;
   for (int k = 0; k < npk; ++k) {
     const int s = k % NS;
-    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * s, (k / NS) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * s, (k / NS) & 1, p.wait_ns))) {
       failed = true;
       kfail = k;
       break;
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
       set_status(p.status, PA_DEV_TIMEOUT);
       const int last = min(npk, kfail + NS);
       for (int k = kfail; k < last; ++k)
-        mbar_wait_bounded(bars + 8 * (k % NS), (k / NS) & 1, 10000000ull);
+        mbar_wait_bounded(bars + 8 * (k % NS), (k / NS) & 1, kDrainWaitNs);
       *cta_failed = 1;
     }
     __syncwarp();
@@ -524,7 +524,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
   if (!coop) {
     // ---- a task of its own: normalise into this warp's (now free) ring,
     // then write coalesced
-    if (failed) return;
+    if (failed) {
+      if (is_split) mark_split_missing(p.part_lse, slot, G, lane);
+      return;
+    }
     float* stage = reinterpret_cast<float*>(base + warp * L::RING);  // [G][D]
     const float inv0 = l_part[0] > 0.f ? 1.f / l_part[0] : 0.f;
     const float inv1 = l_part[1] > 0.f ? 1.f / l_part[1] : 0.f;
@@ -561,7 +564,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
   // ---- shared task: merge the NW warp states in shared memory (rings are free)
   __syncthreads();
-  if (*cta_failed) return;
+  if (*cta_failed) {
+    if (is_split && warp == 0) mark_split_missing(p.part_lse, slot, G, lane);
+    return;
+  }
   float* st = reinterpret_cast<float*>(base);  // [NW][2G + G*D]
   constexpr int SLOT = 2 * G + G * D;
   float* mine = st + warp * SLOT;

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
   for (int k = 0; k < npk; ++k) {
     const int hk = 2 * k;
     const int sk = hk % NSH;
-    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * sk, (hk / NSH) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * sk, (hk / NSH) & 1, p.wait_ns))) {
       failed = true;
       hfail = hk;
       break;
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
     const int hv = hk + 1;
     const int sv = hv % NSH;
-    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * sv, (hv / NSH) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(bars + 8 * sv, (hv / NSH) & 1, p.wait_ns))) {
       failed = true;
       hfail = hv;
       break;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(NW * 32, 4)
       set_status(p.status, PA_DEV_TIMEOUT);
       const int last = min(nhalf, hfail + NSH);
       for (int h = hfail; h < last; ++h)
-        mbar_wait_bounded(bars + 8 * (h % NSH), (h / NSH) & 1, 10000000ull);
+        mbar_wait_bounded(bars + 8 * (h % NSH), (h / NSH) & 1, kDrainWaitNs);
       *cta_failed = 1;
     }
     __syncwarp();
@@ -468,7 +468,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
   if (!coop) {
     // ---- a task of its own: normalise into this warp's (now free) ring,
     // then write coalesced
-    if (failed) return;
+    if (failed) {
+      if (is_split) mark_split_missing(p.part_lse, slot, G, lane);
+      return;
+    }
     float* stage = reinterpret_cast<float*>(base + warp * L::RING);  // [G][D]
     const float inv0 = l_part[0] > 0.f ? 1.f / l_part[0] : 0.f;
     const float inv1 = l_part[1] > 0.f ? 1.f / l_part[1] : 0.f;
@@ -507,7 +510,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
   // ---- shared task: merge the NW warp states in shared memory (rings are free)
   __syncthreads();
-  if (*cta_failed) return;
+  if (*cta_failed) {
+    if (is_split && warp == 0) mark_split_missing(p.part_lse, slot, G, lane);
+    return;
+  }
   float* st = reinterpret_cast<float*>(base);  // [NW][2G + G*D]
   constexpr int SLOT = 2 * G + G * D;
   float* mine = st + warp * SLOT;

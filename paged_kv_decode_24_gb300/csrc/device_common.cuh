@@ -8,7 +8,8 @@
 namespace pa {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
+constexpr uint64_t kDrainWaitNs = 10000000ull;   // waits for copies already issued, after a failure
+constexpr uint64_t kShortWaitNs = 100000ull;     // limits below this are checked on every try
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,10 +62,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for a barrier phase, giving up after kWaitLimitNs.  Returns false on
-// timeout; the caller reports it and stops.
+// Non-blocking test of a barrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for a barrier phase, giving up after limit_ns.  Returns false on
+// timeout; the caller reports it and stops.  A try_wait may suspend the
+// thread for a while, so long limits read the clock every 64 tries; a limit
+// below kShortWaitNs polls with the non-blocking test and reads the clock
+// every time, so that it is kept even when it is shorter than one copy.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = kWaitLimitNs) {
+                                                  uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_test_wait(bar, parity))
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {

@@ -39,6 +39,18 @@ struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
 
+// A pair of fp32 weights as hi + lo parts in the element type: hi is each
+// value rounded to nearest even, lo the remainder (exact in fp32) rounded
+// the same way.  hi + lo keeps about twice the element type's significant
+// bits, so products with 16-bit operands see p to ~22 bits (fp16) or ~16
+// bits (bf16) instead of 11 or 8.
+template <typename T>
+__device__ __forceinline__ void split_hi_lo(float2 a, uint32_t& hi, uint32_t& lo) {
+  hi = Elem<T>::from_f2(a.x, a.y);
+  const float2 h = Elem<T>::to_f2(hi);
+  lo = Elem<T>::from_f2(a.x - h.x, a.y - h.y);
+}
+
 // Eight packed elements (one 16-byte load) -> four fp32 pairs.
 template <typename T>
 __device__ __forceinline__ void elem8_to_float2x4(const uint4& raw, float2* f) {

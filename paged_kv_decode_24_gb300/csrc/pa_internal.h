@@ -27,16 +27,10 @@ constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
 
-// Integer tuning knob from the environment, for experiments: `fallback`
-// unless the variable holds an integer in [lo, hi].
-inline int env_int(const char* name, int fallback, int lo, int hi) {
-  const char* v = getenv(name);
-  if (!v || !*v) return fallback;
-  char* end = nullptr;
-  const long x = strtol(v, &end, 10);
-  if (end == v || x < lo || x > hi) return fallback;
-  return (int)x;
-}
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // a plan's wait limit of 0 means ~1 s
+
+// The wait limit a kernel uses for a plan's wait_limit_ns (0: the default).
+inline uint64_t wait_limit_or_default(uint64_t ns) { return ns ? ns : kDefaultWaitNs; }
 
 // Item flags live in the top bits of the kv_head word.
 constexpr uint32_t kItemSplit = 0x80000000u;  // writes a partial (o, lse) instead of out
@@ -140,5 +134,15 @@ inline PrefillLayout prefill_layout(int tiles, int batch) {
 
 // Validation shared by every entry point.
 pa_status_t check_shape(const pa_shape_t* s);
+
+// Every host-side check of pa_decode_attention (shape, plan against shape,
+// pointers, scale, workspace size), in the order that call makes them.
+// Returns PA_OK for a call that would launch, and also for batch == 0, which
+// launches nothing (*launches is then false).
+pa_status_t check_decode_call(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens, float scale,
+                              const void* out, const void* workspace, size_t workspace_bytes,
+                              const int32_t* dev_status, bool* launches);
 
 }  // namespace pa

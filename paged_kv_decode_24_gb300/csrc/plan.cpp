@@ -51,15 +51,20 @@ namespace {
 
 // Fill *plan_out and, when dst is non-null, write the task list into dst
 // (dst_bytes long).  With dst == nullptr and alloc set, the list goes into a
-// fresh malloc'ed block owned by the plan.
+// fresh malloc'ed block owned by the plan.  opt may be null (defaults).
 pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int32_t num_sms,
-                      int32_t forced_splits, void* dst, size_t dst_bytes, bool alloc,
-                      pa_plan_t* plan_out) {
+                      int32_t forced_splits, const pa_plan_options_t* opt, void* dst,
+                      size_t dst_bytes, bool alloc, pa_plan_t* plan_out) {
   if (!plan_out) return PA_ERR_INVALID_ARG;
   memset(plan_out, 0, sizeof(*plan_out));
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
   if (num_sms <= 0 || forced_splits < 0) return PA_ERR_INVALID_ARG;
+  const pa_plan_options_t o = opt ? *opt : pa_plan_options_t{};
+  if (o.min_chunk_pages < 0 || o.waves < 0 || o.waves > 64 ||
+      (o.merge != PA_MERGE_IN_SPLIT_KERNEL && o.merge != PA_MERGE_COMBINE_KERNEL) ||
+      o.l2_prefetch_pages > 32)
+    return PA_ERR_INVALID_ARG;
   const int B = shape->batch, Hkv = shape->num_kv_heads, D = shape->head_dim;
   const int G = shape->num_q_heads / Hkv, S = shape->page_size;
   if (B > 0 && !seq_lens_host) return PA_ERR_INVALID_ARG;
@@ -74,12 +79,12 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   }
 
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
-  // that the task count is about three times the CTAs the GPU holds at once
-  // (one CTA per task), never finer than kMinChunkPages.
-  // Overridable for experiments: PA_PLAN_MIN_CHUNK, PA_PLAN_BUNDLE_MAX (pages), PA_PLAN_WAVES.
-  const int min_chunk = env_int("PA_PLAN_MIN_CHUNK", kMinChunkPages, 1, 1 << 20);
-  const int bundle_max = env_int("PA_PLAN_BUNDLE_MAX", kBundleMaxPages, 0, 1 << 20);
-  const int waves = env_int("PA_PLAN_WAVES", kPlanWaves, 1, 64);
+  // that the task count is about `waves` times the CTAs the GPU holds at
+  // once (one CTA per task), never finer than min_chunk pages.
+  const int min_chunk = o.min_chunk_pages > 0 ? o.min_chunk_pages : kMinChunkPages;
+  const int bundle_max = o.bundle_max_pages > 0 ? o.bundle_max_pages
+                                                : (o.bundle_max_pages < 0 ? 0 : kBundleMaxPages);
+  const int waves = o.waves > 0 ? o.waves : kPlanWaves;
   int32_t chunk = 0;
   if (forced_splits == 0) {
     const int64_t slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
@@ -215,6 +220,10 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->blob_bytes = lay.blob_bytes;
   plan_out->workspace_bytes = lay.total;
   plan_out->host_blob = blob;
+  plan_out->merge = o.merge;
+  plan_out->l2_prefetch_pages = o.l2_prefetch_pages;
+  plan_out->l2_prefetch_ctas = o.l2_prefetch_ctas;
+  plan_out->wait_limit_ns = o.wait_limit_ns;
   return PA_OK;
 }
 
@@ -223,15 +232,24 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
 
 extern "C" pa_status_t pa_plan(const pa_shape_t* shape, const int32_t* seq_lens_host,
                                int32_t num_sms, int32_t forced_splits, pa_plan_t* plan_out) {
-  return pa::plan_impl(shape, seq_lens_host, num_sms, forced_splits, nullptr, 0, true, plan_out);
+  return pa::plan_impl(shape, seq_lens_host, num_sms, forced_splits, nullptr, nullptr, 0, true,
+                       plan_out);
 }
 
 extern "C" pa_status_t pa_plan_in(const pa_shape_t* shape, const int32_t* seq_lens_host,
                                   int32_t num_sms, int32_t forced_splits, void* host_buffer,
                                   size_t host_buffer_bytes, pa_plan_t* plan_out) {
   if (!host_buffer) return PA_ERR_INVALID_ARG;
-  return pa::plan_impl(shape, seq_lens_host, num_sms, forced_splits, host_buffer,
+  return pa::plan_impl(shape, seq_lens_host, num_sms, forced_splits, nullptr, host_buffer,
                        host_buffer_bytes, false, plan_out);
+}
+
+extern "C" pa_status_t pa_plan_ex(const pa_shape_t* shape, const int32_t* seq_lens_host,
+                                  int32_t num_sms, int32_t forced_splits,
+                                  const pa_plan_options_t* options, void* host_buffer,
+                                  size_t host_buffer_bytes, pa_plan_t* plan_out) {
+  return pa::plan_impl(shape, seq_lens_host, num_sms, forced_splits, options, host_buffer,
+                       host_buffer_bytes, host_buffer == nullptr, plan_out);
 }
 
 extern "C" void pa_plan_free(pa_plan_t* plan) {

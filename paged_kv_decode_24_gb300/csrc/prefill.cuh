@@ -23,9 +23,10 @@
 //   online softmax per row in base 2, with lazy rescaling: the running max
 //       moves only when a stage beats it by more than 2^8;
 //   O[16 x D] += P[16 x 32] . V                P repacked from the S
-//       fragments into A fragments in the element type (one rounding of p,
-//       as FlashAttention does); V by ldmatrix.trans, D/8 n-tiles x 2
-//       k-steps.
+//       fragments into A fragments in the element type, as hi + lo parts
+//       (split_hi_lo: about twice the type's bits of p, as in the decode
+//       kernels), each multiplied into O; V by ldmatrix.trans, D/8 n-tiles
+//       x 2 k-steps.
 // The output is O / l, rounded to the element type.
 #pragma once
 
@@ -50,6 +51,7 @@ struct PrefillParams {
   int32_t* status;
   float qscale;       // scale * log2(e)
   int32_t batch, num_q_heads, num_kv_heads, max_pages, num_pages, num_tiles, total_q;
+  uint64_t wait_ns;   // bound of each barrier wait (the plan's wait_limit_ns)
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
 };
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
   for (int kt = 0; kt < nkt; ++kt) {
     const int s = kt % NS;
     const uint32_t parity = (uint32_t)((kt / NS) & 1);
-    if (!__all_sync(kFull, mbar_wait_bounded(full + 8 * s, parity))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(full + 8 * s, parity, p.wait_ns))) {
       failed = true;
       break;
     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     }
     const bool dead0 = m_run[0] == -INFINITY, dead1 = m_run[1] == -INFINITY;
     float ps0 = 0.f, ps1 = 0.f;
-    uint32_t pa[L::PAGES][4];
+    uint32_t pa[L::PAGES][4], pl[L::PAGES][4];  // P hi and lo parts
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const float p0 = dead0 ? 0.f : ex2(sc[nt][0] - m_run[0]);
@@ -292,8 +294,8 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
       ps0 += p0 + p1;
       ps1 += p2 + p3;
       // n-tile 2u is tokens 0-7 (a0, a1) of page u's k-step, 2u+1 tokens 8-15 (a2, a3)
-      pa[nt >> 1][(nt & 1) * 2 + 0] = Elem<T>::from_f2(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = Elem<T>::from_f2(p2, p3);
+      split_hi_lo<T>(make_float2(p0, p1), pa[nt >> 1][(nt & 1) * 2 + 0], pl[nt >> 1][(nt & 1) * 2 + 0]);
+      split_hi_lo<T>(make_float2(p2, p3), pa[nt >> 1][(nt & 1) * 2 + 1], pl[nt >> 1][(nt & 1) * 2 + 1]);
     }
     l_part[0] = l_part[0] * al0 + ps0;
     l_part[1] = l_part[1] * al1 + ps1;
@@ -320,6 +322,8 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         }
         mma_16816<T>(o[2 * nd], pa[u][0], pa[u][1], pa[u][2], pa[u][3], r[0], r[1]);
         mma_16816<T>(o[2 * nd + 1], pa[u][0], pa[u][1], pa[u][2], pa[u][3], r[2], r[3]);
+        mma_16816<T>(o[2 * nd], pl[u][0], pl[u][1], pl[u][2], pl[u][3], r[0], r[1]);
+        mma_16816<T>(o[2 * nd + 1], pl[u][0], pl[u][1], pl[u][2], pl[u][3], r[2], r[3]);
       }
     }
     __syncwarp();
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     if (warp == 0) {
       bool ok = true;
       if (lane == 0 && issued < nkt && issued == kt + NS) {
-        ok = mbar_wait_bounded(empty + 8 * s, parity);
+        ok = mbar_wait_bounded(empty + 8 * s, parity, p.wait_ns);
         if (ok) issue(issued++);
       }
       if (!__all_sync(kFull, ok)) {
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     // the last NS stages issued may still be in flight after a failure
     for (int kt = issued - NS < 0 ? 0 : issued - NS; kt < issued; ++kt)
-      mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1), 10000000ull);
+      mbar_wait_bounded(full + 8 * (kt % NS), (uint32_t)((kt / NS) & 1), kDrainWaitNs);
   }
   if (*cta_flag) return;
 

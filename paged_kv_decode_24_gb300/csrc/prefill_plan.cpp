@@ -21,13 +21,6 @@ namespace {
 
 std::atomic<uint64_t> g_prefill_ids{1};
 
-// Rows per tile: the tcgen05 kernel's 128 unless PA_PREFILL_ROWS=64 asks
-// for the mma.sync kernel.
-int prefill_rows() {
-  const char* v = getenv("PA_PREFILL_ROWS");
-  return (v && atoi(v) == kPrefillRows) ? kPrefillRows : kPrefillRowsTc5;
-}
-
 struct Tile {
   int32_t b, g, tok0, ntok;
   int64_t work;
@@ -36,16 +29,22 @@ struct Tile {
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* seq_lens_host,
-                                       const int32_t* q_lens_host, pa_prefill_plan_t* plan_out) {
+extern "C" pa_status_t pa_prefill_plan_ex(const pa_shape_t* shape, const int32_t* seq_lens_host,
+                                          const int32_t* q_lens_host,
+                                          const pa_prefill_options_t* options,
+                                          pa_prefill_plan_t* plan_out) {
   using namespace pa;
   if (!plan_out) return PA_ERR_INVALID_ARG;
   memset(plan_out, 0, sizeof(*plan_out));
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
+  const pa_prefill_options_t o = options ? *options : pa_prefill_options_t{};
+  // rows per tile: the tcgen05 kernel's 128 by default, 64 for the mma.sync kernel
+  if (o.rows_per_tile != 0 && o.rows_per_tile != kPrefillRowsTc5 && o.rows_per_tile != kPrefillRows)
+    return PA_ERR_INVALID_ARG;
   const int B = shape->batch, Hkv = shape->num_kv_heads, D = shape->head_dim;
   const int G = shape->num_q_heads / Hkv;
-  const int rows = prefill_rows();
+  const int rows = o.rows_per_tile == 0 ? kPrefillRowsTc5 : o.rows_per_tile;
   const int tok_per_tile = rows / G;
   if (B > 0 && (!seq_lens_host || !q_lens_host)) return PA_ERR_INVALID_ARG;
 
@@ -97,7 +96,14 @@ extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* s
   plan_out->blob_bytes = lay.blob_bytes;
   plan_out->workspace_bytes = lay.blob_bytes;
   plan_out->host_blob = blob;
+  plan_out->rows_per_tile = rows;
+  plan_out->wait_limit_ns = o.wait_limit_ns;
   return PA_OK;
+}
+
+extern "C" pa_status_t pa_prefill_plan(const pa_shape_t* shape, const int32_t* seq_lens_host,
+                                       const int32_t* q_lens_host, pa_prefill_plan_t* plan_out) {
+  return pa_prefill_plan_ex(shape, seq_lens_host, q_lens_host, nullptr, plan_out);
 }
 
 extern "C" void pa_prefill_plan_free(pa_prefill_plan_t* plan) {

@@ -15,17 +15,21 @@
 //     K [D/64 boxes][64 tokens][128 B]        B operand of S, K-major
 //   a ring of NV value stages of 64 tokens, each
 //     V [D/64 boxes][64 tokens][128 B]        B operand of P.V, MN-major
-//   P   NP x [128 rows][128 B]                A operand of P.V, K-major
+//   P   NP x hi, lo [128 rows][128 B]         A operands of P.V, K-major
 // TMEM: S of 64 columns, O of D columns, Q of D/2 columns (two 16-bit
 // elements per 32-bit column).
+// The weights p are kept as two 16-bit parts, hi = p rounded to the element
+// type and lo = the remainder rounded, and O accumulates P_hi V + P_lo V:
+// about twice the element type's bits of p, as in the decode kernels, so
+// the result stays within the decode path's tolerance.
 //
 // Per stage kt:
 //   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 64)       committed to s_done
 //   the row threads load S(kt) into registers and release its columns;
 //   S(kt+1) is issued at once and runs while they compute
 //   row softmax of S(kt) in registers, lazy rescaling
-//   P(kt) to shared memory, once P.V(kt-NP) has finished reading its buffer
-//   O += P V       (4 MMAs, M = 128, N = D, K = 64)    committed to pv_done
+//   P(kt) hi and lo to shared memory, once P.V(kt-NP) has finished reading
+//   O += P_hi V + P_lo V   (8 MMAs, M = 128, N = D, K = 64 each)   committed to pv_done
 // Keys and values have rings of their own: a key stage is refilled as soon
 // as S has read it, a value stage once P.V has.  Sixty-four keys per stage
 // spread each stage's fixed costs (waits, fences, TMEM loads) over twice the
@@ -176,9 +180,9 @@ constexpr int kTc5Threads = 224;  // row warps 0-3, MMA warp 4, key copies 5, va
 template <int D>
 struct Tc5Layout {
   static constexpr int BOXES = D / 64;
-  static constexpr int NK = D == 128 ? 4 : 6;                   // key stages
+  static constexpr int NK = D == 128 ? 3 : 6;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
-  static constexpr int NP = D == 128 ? 1 : 2;                   // P buffers
+  static constexpr int NP = 1;                                  // P buffers (each hi and lo)
   // An idle row warp waits for the last stage's value copies without having
   // waited for P.V of the stage before.  With one value slot that stage's
   // copy may still be in flight, and the parity wait would then read the
@@ -190,9 +194,9 @@ struct Tc5Layout {
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
   static constexpr int K0 = 0;
   static constexpr int V0 = K0 + NK * STAGE;
-  static constexpr int P = V0 + NV * STAGE;                     // NP x 16 KB
-  static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P buffer
-  static constexpr int BUFS = P + NP * PBUF;                    // the 1024-aligned buffers
+  static constexpr int P = V0 + NV * STAGE;                     // NP x (hi, lo) x 16 KB
+  static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P part (hi or lo)
+  static constexpr int BUFS = P + NP * 2 * PBUF;                // the 1024-aligned buffers
   // SMALL bytes hold the mbarriers (k_full[NK], k_free[NK], v_full[NV],
   // v_free[NV], s_done, s_free, pv_done[2], p_ready[2], drain), the TMEM
   // address and a flag.  The buffers start at the first 1024-byte boundary
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         for (int u = 0; u < kTc5Pages; ++u) phys[u] = nxt[u];
         if (kt + 1 < nkt) load_entries(kt + 1);
         const int slot = kt % NR;
-        good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1));
+        good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1), p.wait_ns);
         if (!good) break;
         int nvalid = 0;
         bool zeroed = false;
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       // copies in flight land before the CTA exits: the last stage issued
       // into each slot (on success all of them have been consumed already)
       for (int k = n - NR < 0 ? 0 : n - NR; k < n; ++k)
-        mbar_wait_bounded(full_bar + 8 * (k % NR), (uint32_t)((k / NR) & 1), 10000000ull);
+        mbar_wait_bounded(full_bar + 8 * (k % NR), (uint32_t)((k / NR) & 1), kDrainWaitNs);
     }
     __syncwarp();
   } else if (mma_warp) {
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       const uint32_t idesc_o = tc5::instr_desc<T>(128, D, true);
       auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T
         const int sk = kt % NK;
-        if (!mbar_wait_bounded(k_full + 8 * sk, (uint32_t)((kt / NK) & 1))) return false;
+        if (!mbar_wait_bounded(k_full + 8 * sk, (uint32_t)((kt / NK) & 1), p.wait_ns)) return false;
         tc5::fence_after();
         const uint32_t kst = sbase + L::K0 + sk * L::STAGE;
 #pragma unroll
@@ -449,21 +453,23 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       for (int kt = 0; kt < nkt && good; ++kt) {
         if (kt + 1 < nkt) {
           // the S columns are free once the row warps have loaded S(kt)
-          good = mbar_wait_bounded(s_free, (uint32_t)(kt & 1)) && issue_s(kt + 1);
+          good = mbar_wait_bounded(s_free, (uint32_t)(kt & 1), p.wait_ns) && issue_s(kt + 1);
           if (!good) break;
         }
         const int sv = kt % NV;
-        good = mbar_wait_bounded(p_ready + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1)) &&
-               mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1));
+        good = mbar_wait_bounded(p_ready + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1), p.wait_ns) &&
+               mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1), p.wait_ns);
         if (!good) break;
         tc5::fence_after();
         const uint32_t vst = sbase + L::V0 + sv * L::STAGE;
-        const uint32_t pst = sbase + L::P + (kt % L::NP) * L::PBUF;
+        const uint32_t pst = sbase + L::P + (kt % L::NP) * 2 * L::PBUF;  // hi, then lo
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = tc5::smem_desc(pst + k * 32, 16, 1024);
+          const uint64_t a_hi = tc5::smem_desc(pst + k * 32, 16, 1024);
+          const uint64_t a_lo = tc5::smem_desc(pst + L::PBUF + k * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
-          tc5::mma(t_o, a, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
+          tc5::mma(t_o, a_hi, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
+          tc5::mma(t_o, a_lo, bd, idesc_o, 1u);
         }
         tc5::commit(v_free + 8 * sv);
         tc5::commit(pv_done + 8 * (kt & 1));
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       // every MMA issued finishes before TMEM is freed: one more commit
       // covers them all
       tc5::commit(drain);
-      mbar_wait_bounded(drain, 0u, 10000000ull);
+      mbar_wait_bounded(drain, 0u, kDrainWaitNs);
     }
     __syncwarp();
   } else {
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // Each of the 128 row threads takes its share.
     auto zero_value_tail = [&](int kt) -> bool {
       const int sv_slot = kt % NV;
-      if (!__all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1))))
+      if (!__all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1), p.wait_ns)))
         return false;
       const int first_bad = span - BN * kt;  // tokens [first_bad, BN) of this stage
       unsigned char* vsm = base + L::V0 + sv_slot * L::STAGE;
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // rows that are never written.
     const bool idle = !__any_sync(kFull, ok);
     for (int kt = 0; idle && kt < nkt; ++kt) {
-      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1)));
+      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1), p.wait_ns));
       if (!good) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
             asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(nph[u]) : "l"(bt_row + j));
         }
       }
-      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1)));
+      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1), p.wait_ns));
       if (!good) break;
       tc5::fence_after();
       float sv[BN];
@@ -583,8 +589,9 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         m_run = mx;
       }
       // p = 2^(s * scale - m): one ex2 per key, the arguments and the row
-      // sum on packed pairs (fma.rn.f32x2, add.rn.f32x2)
-      uint32_t pk[BN / 2];
+      // sum on packed pairs (fma.rn.f32x2, add.rn.f32x2); p is kept as hi
+      // (pk) + lo (pl)
+      uint32_t pk[BN / 2], pl[BN / 2];
       float ps;
       {
         float2 t[BN / 4];
@@ -598,8 +605,8 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
           const float2 a0 = make_float2(ex2(x0.x), ex2(x0.y));
           const float2 a1 = make_float2(ex2(x1.x), ex2(x1.y));
           t[c / 4] = fadd2(a0, a1);
-          pk[c / 2] = Elem<T>::from_f2(a0.x, a0.y);
-          pk[c / 2 + 1] = Elem<T>::from_f2(a1.x, a1.y);
+          split_hi_lo<T>(a0, pk[c / 2], pl[c / 2]);
+          split_hi_lo<T>(a1, pk[c / 2 + 1], pl[c / 2 + 1]);
         }
 #pragma unroll
         for (int w = BN / 8; w >= 1; w >>= 1)
@@ -614,15 +621,27 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       const bool any_resc = __any_sync(kFull, resc);
       if (kt >= L::NP) {
         const int k2 = kt - L::NP;
-        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1)));
+        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1), p.wait_ns));
         if (!good) break;
       }
       if (any_resc && kt >= 1) {
         good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((kt - 1) & 1),
-                                                   (uint32_t)(((kt - 1) >> 1) & 1)));
+                                                   (uint32_t)(((kt - 1) >> 1) & 1), p.wait_ns));
         if (!good) break;
       }
       tc5::fence_after();
+      // ---- P(kt) row, hi and lo, into its buffers (K-major, 128-byte
+      // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), before the
+      // rescale so that their registers are free for it
+      unsigned char* prow = base + L::P + (kt % L::NP) * 2 * L::PBUF + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        const int off = (ch ^ (row & 7)) << 4;
+        *reinterpret_cast<uint4*>(prow + off) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(prow + L::PBUF + off) =
+            make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
+      }
       if (any_resc && kt >= 1) {  // rare: rescale this warp's O rows in TMEM
         const float f = resc ? al : 1.f;
 #pragma unroll
@@ -636,15 +655,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         }
         tc5::wait_st();
       }
-      // ---- P(kt) row into its buffer (K-major, 128-byte swizzle: 16-byte
-      // chunk c of row r at chunk c ^ (r % 8)); value rows past the span
-      // (which may hold anything) become zeros
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(base + L::P + (kt % L::NP) * L::PBUF + row * 128 +
-                                  ((ch ^ (row & 7)) << 4)) = v;
-      }
+      // value rows past the span (which may hold anything) become zeros
       if (kv0 + BN > span && !zero_value_tail(kt)) {
         good = false;
         break;
@@ -656,7 +667,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     }
     if (!idle && nkt > 0 && good) {
       good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
-                                                 (uint32_t)(((nkt - 1) >> 1) & 1)));
+                                                 (uint32_t)(((nkt - 1) >> 1) & 1), p.wait_ns));
       // a copy or MMA warp that gave up leaves O incomplete: write nothing
       good = good && *reinterpret_cast<volatile int*>(cta_flag) == 0;
       good = __all_sync(kFull, good);

@@ -43,6 +43,16 @@ struct MergeTarget {
   int G, num_q_heads;
 };
 
+// A split task that gave up (a bounded wait ran out) writes no partial.  It
+// marks its slot's log-sum-exps NaN instead, so that a separate combine
+// kernel leaves the group's output unwritten rather than merging what an
+// earlier call left in the slot.  (The merge inside the split kernel never
+// runs for such a group: the task does not count itself finished.)  Lanes
+// 0 .. G-1 of one warp call it.
+__device__ __forceinline__ void mark_split_missing(float* part_lse, int slot, int G, int lane) {
+  if (slot >= 0 && lane < G) part_lse[(size_t)slot * G + lane] = __int_as_float(0x7fc00000);
+}
+
 // Splits whose partials one thread loads at once: 16, or 4 for a group of
 // at most 4 splits (fewer predicated-off loads).  A group always takes the
 // same batch, so its output bits never depend on which task merges.

@@ -13,8 +13,6 @@
 // uploads its own task list, and every partial is written before it is read.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "pa_internal.h"
 
 namespace {
@@ -22,32 +20,20 @@ namespace {
 // PA_STATIC_WORKSPACE_BYTES (include/pagedattn.h) bytes of device scratch.
 static __device__ __align__(256) unsigned char g_static_workspace[PA_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_device_address[kMaxDevices] = {};
-
 // Device address of the array on the current device.  In host code
 // g_static_workspace names a host-side stand-in, not device memory, so the
-// address must come from the runtime, once per device, with that device
-// current.
+// address must come from the runtime, with the device current.  It is looked
+// up on every call, not cached: once the module is loaded the lookup
+// allocates nothing, and a context rebuilt after cudaDeviceReset may place
+// the array elsewhere.
 pa_status_t static_workspace_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+  if (e != cudaSuccess || p == nullptr) {
     (void)cudaGetLastError();
     return PA_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_device_address[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
-    if (e != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();
-      return PA_ERR_CUDA;
-    }
-    g_device_address[dev] = p;
-  }
-  *out = g_device_address[dev];
+  *out = p;
   return PA_OK;
 }
 
@@ -58,17 +44,16 @@ extern "C" pa_status_t pa_decode_attention_static(const pa_shape_t* shape, const
                                                   const void* v_pages, const int32_t* block_table,
                                                   const int32_t* seq_lens, float scale, void* out,
                                                   int32_t* dev_status, void* stream) {
-  pa_status_t st = pa::check_shape(shape);
-  if (st != PA_OK) return st;
-  if (!plan) return PA_ERR_INVALID_ARG;
-  if (shape->batch == 0) return PA_OK;
-  if (plan->workspace_bytes > (size_t)PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
+  // Every check pa_decode_attention makes, in its order, before anything is
+  // queued into the shared array; the array's size stands in for the
+  // workspace size, so a plan too big for it is PA_ERR_WORKSPACE.
+  const void* ws_check = reinterpret_cast<const void*>(uintptr_t(256));  // alignment only
+  bool launches = false;
+  pa_status_t st = pa::check_decode_call(shape, plan, q, k_pages, v_pages, block_table, seq_lens,
+                                         scale, out, ws_check, (size_t)PA_STATIC_WORKSPACE_BYTES,
+                                         dev_status, &launches);
+  if (st != PA_OK || !launches) return st;
   if (!plan->host_blob || plan->blob_bytes == 0) return PA_ERR_INVALID_ARG;
-  if (plan->shape.batch != shape->batch || plan->shape.num_q_heads != shape->num_q_heads ||
-      plan->shape.num_kv_heads != shape->num_kv_heads || plan->shape.head_dim != shape->head_dim ||
-      plan->shape.page_size != shape->page_size ||
-      plan->shape.max_pages_per_seq != shape->max_pages_per_seq)
-    return PA_ERR_PLAN;
   void* ws = nullptr;
   st = static_workspace_address(&ws);
   if (st != PA_OK) return st;

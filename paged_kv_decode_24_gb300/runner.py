@@ -53,10 +53,13 @@ class DeviceDecode:
         self.plan_obj = None
         self.workspace = None
 
-    def make_plan(self, forced_splits=None, seq_lens_host=None):
+    def make_plan(self, forced_splits=None, seq_lens_host=None, **options):
+        """pa_plan (or pa_plan_ex when plan options are named, e.g.
+        merge="combine", wait_limit_ns=...) and its upload."""
         fs = self.w.forced_splits if forced_splits is None else forced_splits
         lens = self.w.seq_lens if seq_lens_host is None else seq_lens_host
-        self.plan_obj = binding.Plan(self.shape, lens, self.num_sms, fs)
+        opts = binding.plan_options(**options) if options else None
+        self.plan_obj = binding.Plan(self.shape, lens, self.num_sms, fs, options=opts)
         need = self.plan_obj.workspace_bytes
         if self.workspace is None or self.workspace.numel() < need:
             self.workspace = binding.alloc_workspace(self.plan_obj, self.device)
@@ -111,9 +114,11 @@ class DeviceDecode:
 
     # ---- several query tokens per sequence (workloads made with q_lens)
 
-    def make_prefill_plan(self, seq_lens_host=None):
+    def make_prefill_plan(self, seq_lens_host=None, rows_per_tile=0, wait_limit_ns=0):
         lens = self.w.seq_lens if seq_lens_host is None else seq_lens_host
-        self.pf_plan = binding.PrefillPlan(self.shape, lens, self.w.q_lens)
+        self.pf_plan = binding.PrefillPlan(self.shape, lens, self.w.q_lens,
+                                           rows_per_tile=rows_per_tile,
+                                           wait_limit_ns=wait_limit_ns)
         self.pf_ws = binding.alloc_workspace(self.pf_plan, self.device)
         binding.prefill_upload(self.pf_plan, self.pf_ws)
         return self.pf_plan

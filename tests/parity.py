@@ -11,12 +11,7 @@ For bf16 q/K/V/out, rounding the output alone costs up to half an ulp, a
 relative 2^-8 (3.9e-3): the absolute bound is 8e-3 (twice that at |out| = 1),
 and the relative bound and its floor are the fp16 ones.
 
-The multi-token kernel rounds the softmax weights p once to the element
-type before P.V, as FlashAttention does (the decode kernels keep p as hi +
-lo).  That error is at most half an ulp of p times the attended |V|, so it
-scales with |V| (about 0.5 in the workloads), not with |out|: for that path
-the relative bound is taken against max(|oracle|, 0.25).  The absolute
-bounds stay.
+Every path, decode and multi-token alike, is held to these bounds.
 """
 
 from __future__ import annotations
@@ -27,7 +22,6 @@ MAX_ABS = 2e-3
 MAX_REL = 1e-2
 REL_FLOOR = 1e-3
 BF16_MAX_ABS = 8e-3
-P_ROUNDED_REL_FLOOR = 0.25
 
 
 def errors(got, want, rel_floor=REL_FLOOR):

@@ -321,3 +321,114 @@ def test_plans_from_many_host_threads_agree(lib):
         t.join()
     assert not errors
     assert len(out) == 160 and all(np.array_equal(b, ref) for b in out)
+
+
+def test_plan_options_zeroed_equal_the_plain_plan(lib):
+    """pa_plan_ex with a zeroed options struct makes pa_plan's task list, and
+    copies the per-call fields (all zero: the defaults) into the plan."""
+    for cfg in (2, 4, 5):
+        w = workloads.make_config(cfg)
+        ref = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits)
+        p = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits,
+                         options=binding.plan_options())
+        assert np.array_equal(np.delete(p.blob(), [4, 5]), np.delete(ref.blob(), [4, 5]))
+        assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns) == (0,) * 4
+        assert p.c.owns_blob == 1
+
+
+def test_plan_options_shape_the_task_list(lib):
+    w = workloads.make_config(4)
+    s = _shape(w)
+    base = binding.Plan(s, w.seq_lens, 152)
+    # finer minimum chunks and more waves: more, shorter splits
+    fine = binding.Plan(s, w.seq_lens, 152, options=binding.plan_options(min_chunk_pages=16, waves=4))
+    assert fine.c.num_work_items > base.c.num_work_items and fine.c.chunk_pages < base.c.chunk_pages
+    check_plan_covers(w, fine)
+    # the skewed mix bundles its short tasks by default; bundle_max_pages < 0 never does
+    w5 = workloads.make_config(5)
+    b5 = binding.Plan(_shape(w5), w5.seq_lens, 152)
+    assert b5.c.num_shared_ctas < b5.c.num_work_items
+    nb = binding.Plan(_shape(w5), w5.seq_lens, 152, options=binding.plan_options(bundle_max_pages=-1))
+    assert nb.c.num_shared_ctas == nb.c.num_work_items == nb.c.num_ctas
+    check_plan_covers(w5, nb)
+    # the per-call fields are carried by the plan, in a caller buffer too
+    buf = np.zeros(base.c.blob_bytes, np.uint8)
+    o = binding.plan_options(merge="combine", l2_prefetch_pages=32, l2_prefetch_ctas=7,
+                             wait_limit_ns=12345)
+    p = binding.Plan(s, w.seq_lens, 152, host_buffer=buf, options=o)
+    assert p.c.owns_blob == 0 and p.c.host_blob == buf.ctypes.data
+    assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns) == \
+        (binding.PA_MERGE_COMBINE_KERNEL, 32, 7, 12345)
+
+
+@pytest.mark.parametrize("bad", [dict(merge=2), dict(merge=-1), dict(l2_prefetch_pages=33),
+                                 dict(waves=-1), dict(waves=65), dict(min_chunk_pages=-1)])
+def test_plan_options_out_of_range_are_refused(lib, bad):
+    w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=6)
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.Plan(_shape(w), w.seq_lens, 152, options=binding.plan_options(**bad))
+    assert e.value.code == 1, bad
+
+
+def test_decode_refuses_a_plan_with_bad_call_fields(lib):
+    """A plan edited after pa_plan_ex into an unknown merge form is refused
+    before any launch."""
+    w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=7)
+    s = _shape(w)
+    plan = binding.Plan(s, w.seq_lens, 152)
+    plan.c.merge = 5
+    fake = ctypes.c_void_p(0x10000)
+    r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), fake, fake, fake, fake, fake,
+                                ctypes.c_float(0.1), fake, fake, plan.c.workspace_bytes, fake, None)
+    assert r == 8
+
+
+def test_prefill_plan_rows_per_tile_option(lib):
+    lens, qls = [300, 40], [200, 40]
+    s = binding.make_shape(2, 8, 2, 128, 16, 32, 64)
+    d = binding.PrefillPlan(s, lens, qls)
+    assert d.c.rows_per_tile == 128 and d.blob()[8] == 128 and d.c.wait_limit_ns == 0
+    p = binding.PrefillPlan(s, lens, qls, rows_per_tile=64, wait_limit_ns=99)
+    assert p.c.rows_per_tile == 64 and p.blob()[8] == 64 and p.c.wait_limit_ns == 99
+    assert p.c.num_tiles > d.c.num_tiles   # half the rows per tile: about twice the tiles
+    with pytest.raises(binding.PagedAttnError) as e:
+        binding.PrefillPlan(s, lens, qls, rows_per_tile=96)
+    assert e.value.code == 1
+
+
+def test_library_reads_no_environment():
+    """Tuning and test knobs come through the plan options, not from
+    process-global environment variables."""
+    import os
+    import re
+    csrc = os.path.join(os.path.dirname(binding.__file__), "csrc")
+    for name in os.listdir(csrc):
+        text = open(os.path.join(csrc, name), errors="replace").read()
+        assert not re.search(r"\b(secure_)?getenv\s*\(", text), name
+
+
+def test_static_entry_checks_before_anything_is_queued(lib):
+    """pa_decode_attention_static makes pa_decode_attention's checks, in its
+    order, and returns before its first CUDA call when one fails (this host
+    has no GPU, so a call that got further would fail differently)."""
+    w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=8)
+    s = _shape(w)
+    plan = binding.Plan(s, w.seq_lens, 152, 2)
+    fake = ctypes.c_void_p(0x10000)
+    call = lambda shape, pl, scale=0.1, q=fake: lib.pa_decode_attention_static(
+        ctypes.byref(shape), ctypes.byref(pl.c), q, fake, fake, fake, fake, ctypes.c_float(scale),
+        fake, fake, None)
+    assert call(s, plan, scale=float("nan")) == 1
+    assert call(s, plan, scale=float("inf")) == 1
+    assert call(s, plan, q=ctypes.c_void_p(0x10008)) == 1
+    other = binding.make_shape(2, 4, 2, 64, 16, w.max_pages_per_seq + 1, w.num_pages)
+    assert call(other, plan) == 8
+    # batch 0 with a plan of another shape: PA_ERR_PLAN, as pa_decode_attention
+    s0 = binding.make_shape(0, 4, 2, 64, 16, 4, 8)
+    assert call(s0, plan) == 8
+    r = lib.pa_decode_attention(ctypes.byref(s0), ctypes.byref(plan.c), fake, fake, fake, fake,
+                                fake, ctypes.c_float(0.1), fake, fake, 1 << 20, fake, None)
+    assert r == 8
+    # batch 0 with its own plan: nothing to do
+    p0 = binding.Plan(s0, np.zeros(0, np.int32), 152)
+    assert call(s0, p0) == 0

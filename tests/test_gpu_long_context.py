@@ -2,8 +2,8 @@
 longest benchmark context) beside a short one, on each split kernel (CUDA
 cores for MHA, tensor cores for GQA, the INT8 cache), with the automatic
 plan.  The planner cuts the long sequence into well over a hundred splits,
-so the split merge combines that many partials per head.  Sampled heads of
-both sequences are compared with the float64 oracle.
+so the split merge combines that many partials per head.  Every head of
+both sequences is compared with the float64 oracle.
 """
 
 from __future__ import annotations
@@ -44,16 +44,13 @@ def test_131072_token_context(hq, hkv, kv):
         dd.append()
         got = dd.decode().cpu().numpy()
     assert dd.read_status() == 0
-    heads = [(0, 0), (0, hq - 1), (0, hq // 2 + 1), (1, 0), (1, hq - 1)]
     if kv == "int8":
         kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales,
                                              w.k_new, w.v_new, w.block_table, w.seq_lens)
         want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens,
-                                          w.scale, heads=heads)
+                                          w.scale)
     else:
         kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
                                   w.seq_lens)
-        want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale,
-                                       heads=heads)
-    for (b, h) in heads:
-        assert_close(got[b, h], want[b, h], f"{kv} Hq={hq} Hkv={hkv} sequence {b} head {h}")
+        want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
+    assert_close(got, want, f"{kv} Hq={hq} Hkv={hkv}, every head")

@@ -1,19 +1,22 @@
 """The L2 prefetch that the split-decode kernels issue before waiting on the
-previous kernel, at its widest setting: every CTA and all 32 lanes of every
-warp prefetch, so every block-table entry a warp owns goes through the
-bounds checks.  The knobs are read once per process, so the cases run in a
-child process with the environment set.  Results must match the oracle as
-with the default setting, and a block-table entry outside the pool must be
-flagged and skipped, not prefetched.
+previous kernel, at its widest setting (plan options): every CTA and all 32
+lanes of every warp prefetch, so every block-table entry a warp owns goes
+through the bounds checks.  Results must match the oracle as with the
+default setting, and a block-table entry outside the pool must be flagged and
+skipped, not prefetched.  The setting with no prefetch at all must match too.
 """
 
 from __future__ import annotations
 
-import os
-import subprocess
-import sys
+import zlib
 
+import numpy as np
 import pytest
+
+import oracle
+from paged_kv_decode_24_gb300 import binding, workloads
+from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -21,63 +24,57 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+WIDEST = dict(l2_prefetch_pages=32, l2_prefetch_ctas=2147483647)
+NONE = dict(l2_prefetch_pages=-1, l2_prefetch_ctas=-1)
 
-CHILD = r"""
-import sys, zlib
-sys.path.insert(0, sys.argv[1])
-import numpy as np
-import oracle
-from paged_kv_decode_24_gb300 import binding, workloads
-from paged_kv_decode_24_gb300.runner import DeviceDecode
-from tests.parity import assert_close
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    return lib
+
 
 def oracle_step(w):
     kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.seq_lens)
     return oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
 
-for case in [([5, 300, 129, 1000], 32, 8, 128, 0), ([96, 97, 1500], 16, 16, 128, 7),
-             ([2000, 3, 640], 4, 4, 64, 0)]:
+
+@pytest.mark.parametrize("opts", [WIDEST, NONE], ids=["widest", "none"])
+@pytest.mark.parametrize("case", [([5, 300, 129, 1000], 32, 8, 128, 0),
+                                  ([96, 97, 1500], 16, 16, 128, 7), ([2000, 3, 640], 4, 4, 64, 0)],
+                         ids=lambda c: f"L{c[0][:2]}_G{c[1] // c[2]}_D{c[3]}")
+def test_prefetch_setting_matches_oracle(case, opts):
     lens, hq, hkv, d, splits = case
     w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                               seed=zlib.crc32(str(case).encode()) ^ 7, forced_splits=splits)
     dd = DeviceDecode(w)
     dd.append()
-    dd.make_plan(forced_splits=splits)
+    dd.make_plan(forced_splits=splits, **opts)
     got = dd.decode().cpu().numpy()
     assert dd.read_status() == 0, dd.read_status()
-    assert_close(got, oracle_step(w), "prefetch " + str(case))
-
-# INT8 cache
-w = workloads.make_custom(seq_lens=[700, 33, 1024], num_q_heads=32, num_kv_heads=8, head_dim=128,
-                          seed=71, kv="int8")
-dd = DeviceDecode(w)
-dd.make_plan()
-dd.append_q8()
-got = dd.decode_q8().cpu().numpy()
-assert dd.read_status() == 0
-kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
-                                     w.v_new, w.block_table, w.seq_lens)
-want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
-assert_close(got, want, "prefetch int8")
-
-# an entry outside the pool: flagged, skipped, never prefetched
-w = workloads.make_custom(seq_lens=[40, 400], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=72)
-w.block_table[1, 3] = w.num_pages + 1000
-dd = DeviceDecode(w)
-dd.make_plan()
-out = dd.decode().cpu().numpy()
-assert dd.read_status() & binding.PA_DEV_BAD_PAGE
-assert np.all(np.isfinite(out.astype(np.float32)))
-print("prefetch ok")
-"""
+    assert_close(got, oracle_step(w), f"prefetch {opts} {case}")
 
 
-def test_widest_prefetch_matches_oracle():
-    env = dict(os.environ)
-    env["PA_L2_PREFETCH_PAGES"] = "32"
-    env["PA_L2_PREFETCH_CTAS"] = "2147483647"
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], cwd=ROOT, env=env,
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stderr[-3000:]
-    assert "prefetch ok" in r.stdout
+def test_widest_prefetch_int8_cache():
+    w = workloads.make_custom(seq_lens=[700, 33, 1024], num_q_heads=32, num_kv_heads=8,
+                              head_dim=128, seed=71, kv="int8")
+    dd = DeviceDecode(w)
+    dd.make_plan(**WIDEST)
+    dd.append_q8()
+    got = dd.decode_q8().cpu().numpy()
+    assert dd.read_status() == 0
+    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
+                                         w.v_new, w.block_table, w.seq_lens)
+    want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
+    assert_close(got, want, "prefetch int8")
+
+
+def test_widest_prefetch_skips_a_bad_entry():
+    """An entry outside the pool: flagged, skipped, never prefetched."""
+    w = workloads.make_custom(seq_lens=[40, 400], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                              seed=72)
+    w.block_table[1, 3] = w.num_pages + 1000
+    dd = DeviceDecode(w)
+    dd.make_plan(**WIDEST)
+    out = dd.decode().cpu().numpy()
+    assert dd.read_status() & binding.PA_DEV_BAD_PAGE
+    assert np.all(np.isfinite(out.astype(np.float32)))

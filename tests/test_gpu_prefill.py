@@ -1,5 +1,8 @@
 """GPU parity of the multi-token path (pa_kv_append_tokens and
-pa_prefill_attention) against the float64 oracle, through the C ABI.
+pa_prefill_attention) against the float64 oracle, through the C ABI, at the
+decode path's tolerance (tests/parity.py), on both kernels: tcgen05 with
+128-row tiles (the default) and mma.sync with 64-row tiles (plan option
+rows_per_tile = 64).  The benchmark workloads compare every output.
 """
 
 from __future__ import annotations
@@ -12,7 +15,8 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import binding, workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
-from tests.parity import P_ROUNDED_REL_FLOOR, assert_close
+from tests import oracle_pool
+from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +31,7 @@ def _lib(lib):
 
 
 def close(got, want, what, dtype="fp16"):
-    return assert_close(got, want, what, dtype=dtype, rel_floor=P_ROUNDED_REL_FLOOR)
+    return assert_close(got, want, what, dtype=dtype)
 
 
 def oracle_step(w, rows=None):
@@ -37,9 +41,9 @@ def oracle_step(w, rows=None):
                                     rows=rows), (kp, vp)
 
 
-def gpu_step(w):
+def gpu_step(w, rows_per_tile=0):
     dd = DeviceDecode(w)
-    dd.make_prefill_plan()
+    dd.make_prefill_plan(rows_per_tile=rows_per_tile)
     dd.append_tokens()
     out = dd.prefill()
     status = dd.read_status()
@@ -63,15 +67,17 @@ def _ids(c):
     return f"L{c[0][:3]}_q{c[1][:3]}_G{c[2] // c[3]}_D{c[4]}"
 
 
+@pytest.mark.parametrize("rows", [128, 64], ids=["tcgen05", "mma_sync"])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("case", CASES, ids=_ids)
-def test_prefill_parity_full(case, dtype):
+def test_prefill_parity_full(case, dtype, rows):
     lens, qls, hq, hkv, d = case
     w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                               seed=zlib.crc32(str(case).encode()) ^ 32, q_lens=qls, dtype=dtype)
-    got, dd = gpu_step(w)
+    got, dd = gpu_step(w, rows_per_tile=rows)
+    assert dd.pf_plan.c.rows_per_tile == rows
     want, (kp, _) = oracle_step(w)
-    close(got, want, f"prefill {case} {dtype}", dtype=dtype)
+    close(got, want, f"prefill {case} {dtype} rows={rows}", dtype=dtype)
     assert np.array_equal(dd.k_pages.float().cpu().numpy(), kp.astype(np.float32))
 
 
@@ -124,29 +130,29 @@ def test_prefill_bad_page_and_short_seq_len_are_flagged():
 
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_prefill_benchmark_workload(cfg):
+    """Both multi-token workloads at full size, every output (the oracle
+    runs over a spawn-started process pool)."""
     w = workloads.make_prefill_config(cfg)
     got, _ = gpu_step(w)
-    rng = np.random.default_rng(96)
-    rows = sorted({(int(r), int(h)) for r, h in zip(rng.integers(0, w.q.shape[0], 64),
-                                                     rng.integers(0, w.num_q_heads, 64))}
-                  | {(0, 0), (w.q.shape[0] - 1, w.num_q_heads - 1)})
-    want, _ = oracle_step(w, rows=rows)
-    idx = tuple(np.array(rows).T)
-    close(got[idx], want[idx], f"prefill workload {cfg} (sampled)")
+    want = oracle_pool.prefill_all(("prefill_config", cfg))
+    close(got, want, f"prefill workload {cfg}, all {got.shape[0] * got.shape[1]} rows x heads")
 
 
-def test_prefill_whole_prompt_sampled():
+def test_prefill_whole_prompt():
     """q_lens = seq_lens: a whole 2048-token prompt attends causally over
-    itself (512 tiles across the diagonal); sampled rows against the oracle,
-    the first and last rows of every head among them."""
-    w = workloads.make_custom(seq_lens=[2048, 300], num_q_heads=32, num_kv_heads=8,
-                              head_dim=128, seed=97, q_lens=[2048, 300])
+    itself (512 tiles across the diagonal), every output against the oracle."""
+    kw = dict(seq_lens=[2048, 300], num_q_heads=32, num_kv_heads=8, head_dim=128, seed=97,
+              q_lens=[2048, 300])
+    w = workloads.make_custom(**kw)
     got, _ = gpu_step(w)
-    rng = np.random.default_rng(98)
-    rows = {(int(r), int(h)) for r, h in zip(rng.integers(0, w.q.shape[0], 96),
-                                             rng.integers(0, w.num_q_heads, 96))}
-    rows |= {(0, h) for h in range(w.num_q_heads)} | {(2047, h) for h in range(w.num_q_heads)}
-    rows = sorted(rows)
-    want, _ = oracle_step(w, rows=rows)
-    idx = tuple(np.array(rows).T)
-    close(got[idx], want[idx], "whole prompt (sampled)")
+    want = oracle_pool.prefill_all(("custom", kw))
+    close(got, want, "whole prompt")
+
+
+def test_prefill_benchmark_workload_mma_sync():
+    """The piggybacked batch on the mma.sync kernel (64-row tiles), every output."""
+    w = workloads.make_prefill_config(2)
+    got, dd = gpu_step(w, rows_per_tile=64)
+    assert dd.pf_plan.c.rows_per_tile == 64
+    want = oracle_pool.prefill_all(("prefill_config", 2))
+    close(got, want, "prefill workload 2 on mma.sync")
