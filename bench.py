@@ -4,15 +4,20 @@ One step is one layer's decode attention over one batch:
     pa_append_decode_attention (one kernel: the append of the new token
     fused into the split kernel, whose last split per group merges the
     partials by their log-sum-exp),
-and once per 32-layer model step pa_plan (host) -> pa_plan_upload, inside the
-timed region: the plan depends only on seq_lens, which every layer shares.  Inputs are synthetic and
-seeded, with the shapes of the five workloads in
-paged_kv_decode_24_gb300/workloads.py.  The default is workload 2 (LLaMA-2-7B
-heads, one 4096-token sequence, 16 splits).
+and once per 32-layer model step pa_plan_upload of that step's plan, inside
+the timed region.  pa_plan makes each model step's plan on the host while
+the GPU runs the model step before it (the plan depends only on seq_lens,
+which every layer shares).  Inputs are synthetic and seeded, with the
+shapes of the five workloads in paged_kv_decode_24_gb300/workloads.py.  The
+headline is workload 4 (LLaMA-3-8B heads, batch 160, GQA-4, the largest);
+workloads 2, 3 and 5 are timed the same way in the same run and reported
+under per_config.
 
 Each model step (32 layer steps) is one CUDA graph: the plan upload, then
 the 32 layers' calls back to back; K layer steps are timed exactly (a shorter
-graph covers K mod 32).
+graph covers K mod 32).  A spin kernel queued before the start event holds
+the stream while the host queues the timed graphs, so the events time the
+device's work and not the host's launch latency.
 
 The JSON line reports:
   value         KV-read GB/s of the whole job (K and V bytes of every attended
@@ -27,6 +32,7 @@ The JSON line reports:
                 cpu_baseline_all_cores runs it on every core at once
   plan_host_us  one pa_plan call on the host (not part of the device timing)
   append_us     pa_kv_append alone, as its own launch (the step fuses it)
+  per_config    the other workloads' µs per step, GB/s and roofline fraction
 
 Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
 in total), so L2 never holds the pages a step reads.
@@ -74,7 +80,19 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5],
+                    help="the headline workload (default 4: LLaMA-3-8B heads, batch 160, the "
+                         "largest)")
+    ap.add_argument("--also", type=lambda v: [int(x) for x in v.split(",") if x.strip()],
+                    default=None,
+                    help="decode: other workloads timed in the same run and reported under "
+                         "per_config (default 2,3,5 with the default headline; '' for none)")
+    ap.add_argument("--merge", choices=["split", "combine"], default="split",
+                    help="decode: merge split partials in the split kernel (one launch) or in "
+                         "a separate combine kernel (plan option merge)")
+    ap.add_argument("--prefill-rows", type=int, choices=[128, 64], default=128,
+                    help="prefill: query rows per tile, 128 for the tcgen05 kernel, 64 for the "
+                         "mma.sync kernel (plan option rows_per_tile)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
@@ -96,6 +114,8 @@ def parse():
                     help="decode: force this split count per sequence in place of the "
                          "workload's own (0 = the planner's choice); for experiments")
     args = ap.parse_args()
+    if args.also is None:
+        args.also = list(EXTRA_CONFIGS) if args.config == 4 and args.op == "decode" else []
     return args
 
 
@@ -206,40 +226,52 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# Sources the split-decode kernels and their launches are built from: the
-# kernels, the device helpers, the planner that sets the grid, and the C-ABI
-# that fills the launch parameters.
-DECODE_SOURCES = ("api.cu", "device_common.cuh", "elem.cuh", "quant_common.cuh",
-                  "split_launch.cuh", "split_merge.cuh", "pa_internal.h", "launch.h", "plan.cpp")
+# Sources a split-decode kernel family and its launch are built from: the
+# family's kernel files, the device helpers, the planner that sets the grid,
+# and the C-ABI that fills the launch parameters.
+DECODE_COMMON = ("api.cu", "device_common.cuh", "elem.cuh", "split_launch.cuh",
+                 "split_merge.cuh", "pa_internal.h", "launch.h", "plan.cpp")
+DECODE_FAMILY = {"cc": ("decode_kernel.cuh", "decode_d64.cu", "decode_d128.cu"),
+                 "tc": ("decode_kernel.cuh", "decode_tc.cuh", "decode_tc_d64.cu",
+                        "decode_tc_d128.cu"),
+                 "q8": ("decode_kernel.cuh", "decode_tc.cuh", "decode_q8.cuh", "quant_common.cuh",
+                        "decode_q8_d64.cu", "decode_q8_d128.cu")}
 
 
-def kernel_source_hash():
-    """Hash of the split-decode sources, stamped on the committed DRAM-traffic
-    capture so that a changed kernel reports no stale traffic."""
+def decode_family(w, kv):
+    """The split kernel a workload runs on: INT8 cache, CUDA cores (MHA) or
+    tensor cores (GQA)."""
+    if kv == "int8":
+        return "q8"
+    return "cc" if w.num_q_heads == w.num_kv_heads else "tc"
+
+
+def kernel_source_hash(family):
+    """Hash of the sources of one split-decode kernel family, stamped on each
+    committed DRAM-traffic capture so that a changed kernel reports no stale
+    traffic."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_24_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if not (name.startswith("decode") or name in DECODE_SOURCES):
-            continue
+    for name in sorted(DECODE_COMMON + DECODE_FAMILY[family]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(cfg, kv="fp16", dtype="fp16"):
+def traffic_for(cfg, kv, dtype, family):
     """DRAM bytes per launch of the split kernel from a committed ncu capture,
-    only while the kernel sources still hash to what was profiled."""
+    only while that kernel family's sources still hash to what was profiled."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash():
-        return None
     key = "-".join([str(cfg)] + [x for x in (kv, dtype) if x != "fp16"])   # "4", "4-int8", "4-bf16"
     ent = d.get("configs", {}).get(key)
-    return None if ent is None else ent.get("dram_bytes_per_launch")
+    if ent is None or ent.get("source_hash") != kernel_source_hash(family):
+        return None
+    return ent.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -331,13 +363,334 @@ def job_value(kv_bytes_per_rank, ms_per_step, world):
 # our arm
 
 MODEL_LAYERS = 32   # LLaMA-2-7B and LLaMA-3-8B both have 32 decoder layers
+HOLD_US = 300       # spin before a timed region: longer than the host needs to queue the region
+EXTRA_CONFIGS = (2, 3, 5)   # timed in the same run as the headline workload, reported per config
+
+
+def hold_stream(torch, stream, us=HOLD_US):
+    """Keep `stream` busy for about `us` microseconds (torch's spin kernel), so
+    that the work queued after it is already on the device when the timed
+    region starts: the events then time the device's work, not the host's
+    launch latency (the blocking-kernel practice of GPU benchmark harnesses).
+    It runs before the start event and is not part of any timing."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2100))   # clock cycles; the SM clock is at most 2.07 GHz
+
+
+class DecodeBench:
+    """One decode workload on the device: its layers' KV caches, the plan and
+    workspace, and the model-step CUDA graphs that the timings replay.
+
+    A layer step is pa_append_decode_attention (or its INT8-cache form) over
+    that layer's cache.  A model step is one CUDA graph: the plan upload
+    (a2), then the layers' calls back to back, as a serving engine issues
+    them.  Each model step's plan is made on the host (pa_plan_in, into a
+    pinned buffer) while the GPU runs the model step before it: the plan
+    depends only on seq_lens, which every layer shares."""
+
+    def __init__(self, args, cfg, rank, dev, stream, num_sms, layers):
+        import torch
+
+        from paged_kv_decode_24_gb300 import accounting, binding, workloads
+        self.torch, self.binding = torch, binding
+        self.args, self.cfg, self.dev, self.stream, self.LAYERS = args, cfg, dev, stream, layers
+        self.num_sms = num_sms
+        self.q8 = args.kv == "int8"
+        if self.q8 and args.dtype != "fp16":
+            raise SystemExit("the INT8 cache takes fp16 q/out")
+        w = workloads.make_config(cfg, seed=workloads.SEED_BASE + cfg + 1000 * rank, kv=args.kv,
+                                  dtype=args.dtype)
+        if args.splits is not None:
+            w.forced_splits = max(0, int(args.splits))
+        self.w = w
+        self.shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                        w.page_size, w.max_pages_per_seq, w.num_pages, args.dtype)
+        self.kv_bytes = w.kv_bytes_int8() if self.q8 else w.kv_bytes()
+        self.dec_bytes = (accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads,
+                                                  w.head_dim, w.page_size, kv=args.kv)
+                          + accounting.append_bytes(w.batch, w.num_kv_heads, w.head_dim,
+                                                    kv=args.kv))
+        self.lens_host = np.ascontiguousarray(w.seq_lens)
+        to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.elem_t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+        # bf16 workloads hold bf16-exact float32 values: the cast is exact
+        to_elem = lambda a: to_dev(a).to(self.elem_t)
+        self.q = to_elem(w.q)
+        self.k_new = to_elem(w.k_new)
+        self.v_new = to_elem(w.v_new)
+        self.bt = to_dev(w.block_table)
+        self.sl = to_dev(w.seq_lens)
+        if self.q8:
+            cache0 = (to_dev(w.k_codes), to_dev(w.v_codes), to_dev(w.k_scales), to_dev(w.v_scales))
+        else:
+            cache0 = (to_elem(w.k_pages), to_elem(w.v_pages))
+        # One KV cache per layer, as in the model: every layer's pages are
+        # distinct memory, so a layer's reads never hit what the previous
+        # layers left in L2.
+        self.pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(layers - 1)]
+        self.cache_bytes = sum(t.numel() * t.element_size() for t in cache0)
+        self.step_call = binding.append_decode_q8 if self.q8 else binding.append_decode
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        # The plan: pa_plan_ex with the merge form asked for, into pinned host
+        # memory, double-buffered so the host never rewrites a buffer whose
+        # upload may still be pending.
+        self.opts = binding.plan_options(merge=args.merge)
+        self.plan0 = binding.Plan(self.shape, self.lens_host, num_sms, w.forced_splits,
+                                  options=self.opts)
+        self.staging = [torch.empty(int(self.plan0.c.blob_bytes), dtype=torch.uint8).pin_memory()
+                        for _ in range(2)]
+        self.staged_evt = [torch.cuda.Event(), torch.cuda.Event()]
+        self.workspace = binding.alloc_workspace(self.plan0, dev)
+        self.struct0 = self.plan0.structure()
+        self.staged_plans = [None, None]
+        self.ready = set()   # model steps whose plan is already in its buffer
+        self.m = 0           # the next model step
+        self.replan(1)       # both buffers hold a plan before the graphs that upload them
+        self.replan(0)       # are captured; model step 0's is the one in use first
+        with torch.cuda.stream(stream):
+            binding.upload(self.staged_plans[0], self.workspace, stream=stream)
+            # a warm-up call (sets kernel attributes) before capture
+            self.layer_call(self.pools[0], self.q, self.k_new, self.v_new, self.out, stream=stream)
+        stream.synchronize()
+        self.launches_per_step = 1 + (1 if args.merge == "combine" and
+                                      self.plan0.c.num_groups > 0 else 0)
+
+    def layer_call(self, pool, qq, kn, vn, o, stream=None):
+        """One layer's fused append + decode over that layer's cache."""
+        self.step_call(self.shape, self.plan0, qq, kn, vn, *pool, self.bt, self.sl, self.w.scale, o,
+                       self.workspace, self.status, stream=stream)
+
+    def replan(self, m):
+        """a2 on the host: model step m's plan into the pinned buffer its graph uploads."""
+        slot = m % 2
+        self.staged_evt[slot].synchronize()   # that buffer's last upload has completed
+        plan = self.binding.Plan(self.shape, self.lens_host, self.num_sms, self.w.forced_splits,
+                                 host_buffer=self.staging[slot], options=self.opts)
+        if plan.structure() != self.struct0:
+            raise RuntimeError("plan structure changed; captured graphs would be stale")
+        self.staged_plans[slot] = plan
+        self.ready.add(m)
+
+    def capture(self, slot, nlayers):
+        """One model step: the plan upload, then nlayers layers' calls."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self.binding.upload(self.staged_plans[slot], self.workspace)
+            for l in range(nlayers):
+                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out)
+        return g
+
+    def graphs(self, K):
+        full, rem = divmod(K, self.LAYERS)
+        gf = [self.capture(i, self.LAYERS) for i in range(2)] if full else []
+        gr = [self.capture(i, rem) for i in range(2)] if rem else []
+        return gf, gr
+
+    def run_steps(self, nsteps, gfull, grem):
+        """nsteps layer steps as model-step graphs.  Each next model step's
+        plan is made on the host right after the current step is queued, so
+        the host plans step n + 1 while the GPU runs step n."""
+        nf, nr = divmod(nsteps, self.LAYERS)
+        sched = [gfull] * nf + ([grem] if nr else [])
+        for i, gs in enumerate(sched):
+            m = self.m
+            if m not in self.ready:
+                self.replan(m)
+            gs[m % 2].replay()
+            self.staged_evt[m % 2].record(self.stream)
+            self.ready.discard(m)
+            self.m = m + 1
+            if i + 1 < len(sched):
+                self.replan(self.m)
+
+    def time_region(self, K, gfull, grem, world):
+        """Device time (ms) of K layer steps between CUDA events on the
+        launching stream.  The first model step's plan is made before the
+        region, as it would be during the step before it."""
+        torch = self.torch
+        if self.m not in self.ready:
+            self.replan(self.m)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        hold_stream(torch, self.stream)
+        with torch.cuda.stream(self.stream):
+            start.record(self.stream)
+            self.run_steps(K, gfull, grem)
+            end.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        self.check_status()
+        return start.elapsed_time(end)
+
+    def warm(self, nsteps, gfull, grem):
+        with self.torch.cuda.stream(self.stream):
+            self.run_steps(nsteps, gfull, grem)
+        self.stream.synchronize()
+        self.check_status()
+
+    def check_status(self):
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"device status {int(self.status.item()):#x}")
+
+    def isolated_us(self):
+        """One call alone (its own graph, events around it), over the layers'
+        caches in turn so L2 holds none of its pages."""
+        torch = self.torch
+        n_iso = min(self.LAYERS, 8)
+        g1 = []
+        for l in range(n_iso):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out)
+            g1.append(g)
+        iso = []
+        with torch.cuda.stream(self.stream):
+            for i in range(24):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(self.stream)
+                g1[i % n_iso].replay()
+                b.record(self.stream)
+                iso.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in iso[8:]])) * 1e3
+
+    def e2e(self, K, world):
+        """The same metric end to end: every layer step's q, k_new and v_new
+        come in from pinned host memory, and every layer step's output goes
+        back to pinned host memory, inside the model-step graphs.  Inputs come
+        in eight layers per transfer (all layers in one when a model step's
+        inputs total at most 1 MiB): the first chunk before the first layer
+        (with seq_lens, the block table and the plan), each further chunk on a
+        side stream while the chunk before it computes.  A side stream reads
+        each layer's output back as soon as that layer is done.  Only the wait
+        for a chunk of inputs joins the kernel chain, once per eight layers,
+        so the other layers keep their programmatic dependent launch; each
+        layer has its own output buffer, and the graph ends by joining the
+        side streams."""
+        torch, binding, LAYERS, stream = self.torch, self.binding, self.LAYERS, self.stream
+        dev, q, k_new, v_new, out = self.dev, self.q, self.k_new, self.v_new, self.out
+        w = self.w
+        nb = lambda t: t.numel() * t.element_size()
+        nq, nk = q.numel(), k_new.numel()
+        per_layer = nq + 2 * nk                    # elements of one layer's inputs
+        h_in = torch.empty(LAYERS * per_layer, dtype=self.elem_t).pin_memory()
+        for l in range(LAYERS):                    # every layer's inputs, as the host holds them
+            base = l * per_layer
+            h_in[base:base + nq].copy_(q.reshape(-1).cpu())
+            h_in[base + nq:base + nq + nk].copy_(k_new.reshape(-1).cpu())
+            h_in[base + nq + nk:base + per_layer].copy_(v_new.reshape(-1).cpu())
+        d_in = torch.empty_like(h_in, device=dev)
+        hbt = torch.from_numpy(np.ascontiguousarray(w.block_table)).pin_memory()
+        hsl = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).pin_memory()
+        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(LAYERS)]
+        ob = [torch.empty_like(out) for _ in range(LAYERS)]
+        side_out = torch.cuda.Stream(device=dev)
+        side_in = torch.cuda.Stream(device=dev)
+
+        def layer_inputs(l):
+            base = l * per_layer
+            return (d_in[base:base + nq].view(q.shape),
+                    d_in[base + nq:base + nq + nk].view(k_new.shape),
+                    d_in[base + nq + nk:base + per_layer].view(v_new.shape))
+
+        # layers whose inputs one transfer brings in: all of them when a model
+        # step's inputs are small (one transfer, no join at all), else eight
+        CHUNK = LAYERS if LAYERS * per_layer * h_in.element_size() <= (1 << 20) else 8
+
+        def copy_in(l0, l1):
+            d_in[l0 * per_layer:l1 * per_layer].copy_(h_in[l0 * per_layer:l1 * per_layer],
+                                                      non_blocking=True)
+
+        def capture_e2e(slot, nlayers):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.bt.copy_(hbt, non_blocking=True)
+                self.sl.copy_(hsl, non_blocking=True)
+                binding.upload(self.staged_plans[slot], self.workspace)
+                copy_in(0, min(CHUNK, nlayers))
+                side_out.wait_stream(stream)
+                ready = {}
+                for l in range(nlayers):
+                    if l % CHUNK == 0:
+                        nxt = l + CHUNK
+                        if nxt < nlayers:  # the next chunk's inputs, while this one computes
+                            side_in.wait_stream(stream)  # (fork: brings side_in into the capture)
+                            with torch.cuda.stream(side_in):
+                                copy_in(nxt, min(nxt + CHUNK, nlayers))
+                            ready[nxt] = torch.cuda.Event()
+                            ready[nxt].record(side_in)
+                        if l in ready:
+                            stream.wait_event(ready[l])
+                    qq, kk, vv = layer_inputs(l)
+                    self.layer_call(self.pools[l], qq, kk, vv, ob[l])
+                    done = torch.cuda.Event()
+                    done.record(stream)
+                    side_out.wait_event(done)
+                    with torch.cuda.stream(side_out):
+                        hout[l].copy_(ob[l], non_blocking=True)
+                if ready:  # side_in took part only if a chunk came in on it
+                    stream.wait_stream(side_in)
+                stream.wait_stream(side_out)
+            return g
+
+        full, rem = divmod(K, LAYERS)
+        e_full = [capture_e2e(i, LAYERS) for i in range(2)] if full else []
+        e_rem = [capture_e2e(i, rem) for i in range(2)] if rem else []
+        self.warm(K, e_full, e_rem)
+        m0 = self.m
+        e2e_ms = max_over_ranks(self.time_region(K, e_full, e_rem, world) / K, world, dev)
+        nmodel = self.m - m0
+        # the last layer's output, read back to the host, equals the device's
+        last = rem - 1 if rem else LAYERS - 1
+        if not torch.equal(hout[last].to(dev), ob[last]):
+            raise RuntimeError("e2e output read back differs from the device output")
+        h2d_bytes = (K * per_layer * h_in.element_size()
+                     + nmodel * (nb(hbt) + nb(hsl) + int(self.plan0.c.blob_bytes)))
+        return {"value": round(job_value(self.kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": int(round(h2d_bytes / K)),
+                "d2h_bytes_per_step": int(nb(hout[0])),
+                "overlap": f"inputs come in {CHUNK} layers per transfer, each chunk while the "
+                           "one before it computes; a side stream reads each layer's output "
+                           "back while the next layers compute"}
+
+    def append_us(self):
+        """a1 alone: pa_kv_append as its own launch (the step fuses it into the
+        split kernel), one launch per layer's cache in one graph."""
+        torch, binding = self.torch, self.binding
+        app_call = binding.append_q8 if self.q8 else binding.append
+        ga = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=self.stream):
+            for l in range(self.LAYERS):
+                app_call(self.shape, self.k_new, self.v_new, *self.pools[l], self.bt, self.sl,
+                         self.status)
+        ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(self.stream):
+            ga.replay()
+            ev_a[0].record(self.stream)
+            for _ in range(4):
+                ga.replay()
+            ev_a[1].record(self.stream)
+        torch.cuda.synchronize()
+        self.check_status()
+        return ev_a[0].elapsed_time(ev_a[1]) * 1e3 / (4 * self.LAYERS)
+
+    def workload_name(self):
+        return (self.w.name + (", INT8 KV cache (per-row scales)" if self.q8 else "") +
+                (", bf16" if self.args.dtype == "bf16" else ""))
 
 
 def run_ours(args):
     LAYERS = args.layers
     import torch
 
-    from paged_kv_decode_24_gb300 import accounting, binding, workloads
+    from paged_kv_decode_24_gb300 import binding
     from paged_kv_decode_24_gb300 import build as _build
 
     world, rank, local = dist_setup(args)
@@ -354,118 +707,15 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     num_sms = props.multi_processor_count
     stream = torch.cuda.Stream(device=dev)
-
-    q8 = args.kv == "int8"
-    if q8 and args.dtype != "fp16":
-        raise SystemExit("the INT8 cache takes fp16 q/out")
-    w = workloads.make_config(args.config, seed=workloads.SEED_BASE + args.config + 1000 * rank,
-                              kv=args.kv, dtype=args.dtype)
-    if args.splits is not None:
-        w.forced_splits = max(0, int(args.splits))
-    shape = binding.make_shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
-                               w.max_pages_per_seq, w.num_pages, args.dtype)
-    kv_bytes = w.kv_bytes_int8() if q8 else w.kv_bytes()
-    dec_bytes = (accounting.decode_bytes(w.seq_lens, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                         w.page_size, kv=args.kv)
-                 + accounting.append_bytes(w.batch, w.num_kv_heads, w.head_dim, kv=args.kv))
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    lens_host = np.ascontiguousarray(w.seq_lens)
-
-    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    elem_t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
-    # bf16 workloads hold bf16-exact float32 values: the cast is exact
-    to_elem = lambda a: to_dev(a).to(elem_t)
-    q = to_elem(w.q)
-    k_new = to_elem(w.k_new)
-    v_new = to_elem(w.v_new)
-    bt = to_dev(w.block_table)
-    sl = to_dev(w.seq_lens)
-    if q8:
-        cache0 = (to_dev(w.k_codes), to_dev(w.v_codes), to_dev(w.k_scales), to_dev(w.v_scales))
-    else:
-        cache0 = (to_elem(w.k_pages), to_elem(w.v_pages))
-    # One KV cache per layer, as in the model: every layer's pages are distinct
-    # memory, so a layer's reads never hit what the previous layers left in L2.
-    pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(LAYERS - 1)]
-    cache_bytes = sum(t.numel() * t.element_size() for t in cache0)
-    step_call = binding.append_decode_q8 if q8 else binding.append_decode
-
-    def layer_call(pool, qq, kn, vn, o, stream=None):
-        """One layer's fused append + decode over that layer's cache."""
-        step_call(shape, plan0, qq, kn, vn, *pool, bt, sl, w.scale, o, workspace, status,
-                  stream=stream)
-    out = torch.empty_like(q)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    # The plan is made once per model decode step (it depends only on seq_lens,
-    # shared by all layers) into pinned host memory, double-buffered so the
-    # host never rewrites a buffer whose upload may still be pending.
-    plan0 = binding.Plan(shape, lens_host, num_sms, w.forced_splits)
-    staging = [torch.empty(int(plan0.c.blob_bytes), dtype=torch.uint8).pin_memory() for _ in range(2)]
-    staged_evt = [torch.cuda.Event(), torch.cuda.Event()]
-    workspace = binding.alloc_workspace(plan0, dev)
-    struct0 = plan0.structure()
-    staged_plans = [binding.Plan(shape, lens_host, num_sms, w.forced_splits, host_buffer=staging[i])
-                    for i in range(2)]
-
-    def replan(slot):
-        """a2 on the host: a fresh plan into the pinned buffer the slot's graph uploads."""
-        staged_evt[slot].synchronize()
-        plan = binding.Plan(shape, lens_host, num_sms, w.forced_splits, host_buffer=staging[slot])
-        if plan.structure() != struct0:
-            raise RuntimeError("plan structure changed; captured graphs would be stale")
-        staged_plans[slot] = plan
-
-    with torch.cuda.stream(stream):
-        binding.upload(staged_plans[0], workspace, stream=stream)
-        # a warm-up call (sets kernel attributes) before capture
-        layer_call(pools[0], q, k_new, v_new, out, stream=stream)
-    stream.synchronize()
-
-    # One graph per model step: the plan upload (a2), then the layers' fused
-    # calls (a1 + a3..a7) back to back, as a serving engine issues them.
-    def capture_model_step(slot, nlayers):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            binding.upload(staged_plans[slot], workspace)
-            for l in range(nlayers):
-                layer_call(pools[l], q, k_new, v_new, out)
-        return g
-
+    peak, peak_src = read_peaks()
     K = args.steps
-    full, rem = divmod(K, LAYERS)
-    graphs_full = [capture_model_step(i, LAYERS) for i in range(2)] if full else []
-    graphs_rem = [capture_model_step(i, rem) for i in range(2)] if rem else []
-    # the split kernel, whose last split per group merges; with
-    # PA_COMBINE_KERNEL=1 a separate combine kernel follows when any
-    # sequence is split
-    two_kernel = os.environ.get("PA_COMBINE_KERNEL", "").strip() == "1"
-    launches_per_step = 1 + (1 if two_kernel and plan0.c.num_groups > 0 else 0)
 
-    def run_steps(nsteps, gfull, grem, m0=0):
-        """nsteps layer-steps as model-step graphs; returns the model steps issued."""
-        nf, nr = divmod(nsteps, LAYERS)
-        m = m0
-        for _ in range(nf):
-            slot = m % 2
-            replan(slot)
-            gfull[slot].replay()
-            staged_evt[slot].record(stream)
-            m += 1
-        if nr:
-            slot = m % 2
-            replan(slot)
-            grem[slot].replay()
-            staged_evt[slot].record(stream)
-            m += 1
-        return m
-
-    warm_full = graphs_full or [capture_model_step(i, LAYERS) for i in range(2)]
-    with torch.cuda.stream(stream):
-        run_steps(max(args.warmup, LAYERS), warm_full, graphs_rem or warm_full)
-    stream.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item()):#x}")
+    db = DecodeBench(args, args.config, rank, dev, stream, num_sms, LAYERS)
+    w = db.w
+    graphs_full, graphs_rem = db.graphs(K)
+    warm_full = graphs_full or [db.capture(i, LAYERS) for i in range(2)]
+    db.warm(max(args.warmup, LAYERS), warm_full, graphs_rem or warm_full)
 
     uuid = None
     try:
@@ -473,191 +723,34 @@ def run_ours(args):
         uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         pass
+
     def sustain(seconds):
         """Untimed model steps of the same workload for about `seconds`, so the
         clock samples see the GPU under this load."""
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            while time.perf_counter() - t0 < seconds:
-                run_steps(4 * LAYERS, warm_full, warm_full)
-                stream.synchronize()
+        while time.perf_counter() - t0 < seconds:
+            db.warm(4 * LAYERS, warm_full, warm_full)
 
     clocks = ClockSampler(uuid)
     clocks.start()
     sustain(0.4)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        run_steps(K, graphs_full, graphs_rem)
-        end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    total_ms = db.time_region(K, graphs_full, graphs_rem, world)
     sustain(0.4)
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = "0.4 s of the same workload before and after the timed region, and the region"
-    total_ms = start.elapsed_time(end)
     ms_per_step = max_over_ranks(total_ms / K, world, dev)
     # the fused call is the only work in a step besides a2's amortised upload,
     # so its mean launch duration over the timed region is the step time
     dec_mean_ms = total_ms / K
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item()):#x}")
+    iso_us = db.isolated_us()
+    e2e = None if args.no_e2e else db.e2e(K, world)
+    append_us = db.append_us()
 
-    # ---- one call alone (its own graph, events around it), over the layers'
-    # caches in turn so L2 holds none of its pages: reported beside
-    iso = []
-    n_iso = min(LAYERS, 8)
-    g1 = []
-    for l in range(n_iso):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            layer_call(pools[l], q, k_new, v_new, out)
-        g1.append(g)
-    with torch.cuda.stream(stream):
-        for i in range(24):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g1[i % n_iso].replay()
-            b.record(stream)
-            iso.append((a, b))
-    torch.cuda.synchronize()
-    iso_us = float(np.median([a.elapsed_time(b) for a, b in iso[8:]])) * 1e3
-
-    # ---- end to end: every layer step's q, k_new and v_new come in from
-    # pinned host memory, and every layer step's output goes back to pinned
-    # host memory, inside the model-step graphs.  Inputs come in eight layers
-    # per transfer (all layers in one when a model step's inputs total at
-    # most 1 MiB): the first chunk before the first layer (with seq_lens, the
-    # block table and the plan), each further chunk on a side stream while
-    # the chunk before it computes.  A side stream reads each layer's
-    # output back as soon as that layer is done.  Only the wait for a chunk
-    # of inputs joins the kernel chain, once per eight layers, so the other
-    # layers keep their programmatic dependent launch; each layer has its own
-    # output buffer, and the graph ends by joining the side streams.
-    e2e = None
-    if not args.no_e2e:
-        nb = lambda t: t.numel() * t.element_size()
-        nq, nk = q.numel(), k_new.numel()
-        per_layer = nq + 2 * nk                    # elements of one layer's inputs
-        h_in = torch.empty(LAYERS * per_layer, dtype=elem_t).pin_memory()
-        for l in range(LAYERS):                    # every layer's inputs, as the host holds them
-            base = l * per_layer
-            h_in[base:base + nq].copy_(q.reshape(-1).cpu())
-            h_in[base + nq:base + nq + nk].copy_(k_new.reshape(-1).cpu())
-            h_in[base + nq + nk:base + per_layer].copy_(v_new.reshape(-1).cpu())
-        d_in = torch.empty_like(h_in, device=dev)
-        hbt = torch.from_numpy(np.ascontiguousarray(w.block_table)).pin_memory()
-        hsl = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).pin_memory()
-        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(LAYERS)]
-        ob = [torch.empty_like(out) for _ in range(LAYERS)]
-        side_out = torch.cuda.Stream(device=dev)
-
-        def layer_inputs(l):
-            base = l * per_layer
-            return (d_in[base:base + nq].view(q.shape),
-                    d_in[base + nq:base + nq + nk].view(k_new.shape),
-                    d_in[base + nq + nk:base + per_layer].view(v_new.shape))
-
-        side_in = torch.cuda.Stream(device=dev)
-        # layers whose inputs one transfer brings in: all of them when a model
-        # step's inputs are small (one transfer, no join at all), else eight
-        CHUNK = LAYERS if LAYERS * per_layer * h_in.element_size() <= (1 << 20) else 8
-
-        def copy_in(l0, l1):
-            d_in[l0 * per_layer:l1 * per_layer].copy_(h_in[l0 * per_layer:l1 * per_layer],
-                                                      non_blocking=True)
-
-        def capture_e2e(slot, nlayers):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                bt.copy_(hbt, non_blocking=True)
-                sl.copy_(hsl, non_blocking=True)
-                binding.upload(staged_plans[slot], workspace)
-                copy_in(0, min(CHUNK, nlayers))
-                side_out.wait_stream(stream)
-                ready = {}
-                for l in range(nlayers):
-                    if l % CHUNK == 0:
-                        nxt = l + CHUNK
-                        if nxt < nlayers:  # the next chunk's inputs, while this one computes
-                            side_in.wait_stream(stream)  # (fork: brings side_in into the capture)
-                            with torch.cuda.stream(side_in):
-                                copy_in(nxt, min(nxt + CHUNK, nlayers))
-                            ready[nxt] = torch.cuda.Event()
-                            ready[nxt].record(side_in)
-                        if l in ready:
-                            stream.wait_event(ready[l])
-                    qq, kk, vv = layer_inputs(l)
-                    layer_call(pools[l], qq, kk, vv, ob[l])
-                    done = torch.cuda.Event()
-                    done.record(stream)
-                    side_out.wait_event(done)
-                    with torch.cuda.stream(side_out):
-                        hout[l].copy_(ob[l], non_blocking=True)
-                if ready:  # side_in took part only if a chunk came in on it
-                    stream.wait_stream(side_in)
-                stream.wait_stream(side_out)
-            return g
-
-        e_full = [capture_e2e(i, LAYERS) for i in range(2)] if full else []
-        e_rem = [capture_e2e(i, rem) for i in range(2)] if rem else []
-        with torch.cuda.stream(stream):
-            run_steps(K, e_full, e_rem)
-        stream.synchronize()
-        s2 = torch.cuda.Event(enable_timing=True)
-        e2 = torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            s2.record(stream)
-            nmodel = run_steps(K, e_full, e_rem)
-            e2.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        if int(status.item()) != 0:
-            raise RuntimeError(f"device status {int(status.item()):#x}")
-        # the last layer's output, read back to the host, equals the device's
-        last = rem - 1 if rem else LAYERS - 1
-        if not torch.equal(hout[last].to(dev), ob[last]):
-            raise RuntimeError("e2e output read back differs from the device output")
-        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / K, world, dev)
-        h2d_bytes = (K * per_layer * h_in.element_size()
-                     + nmodel * (nb(hbt) + nb(hsl) + int(plan0.c.blob_bytes)))
-        e2e = {"value": round(job_value(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 5),
-               "h2d_bytes_per_step": int(round(h2d_bytes / K)),
-               "d2h_bytes_per_step": int(nb(hout[0])),
-               "overlap": f"inputs come in {CHUNK} layers per transfer, each chunk while the "
-                          "one before it computes; a side stream reads each layer's output "
-                          "back while the next layers compute"}
-
-    # ---- a1 alone: pa_kv_append as its own launch (the step above fuses it
-    # into the split kernel), 32 launches in one graph over the layers' caches
-    app_call = binding.append_q8 if q8 else binding.append
-    ga = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(ga, stream=stream):
-        for l in range(LAYERS):
-            app_call(shape, k_new, v_new, *pools[l], bt, sl, status)
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    with torch.cuda.stream(stream):
-        ga.replay()
-        ev_a[0].record(stream)
-        for _ in range(4):
-            ga.replay()
-        ev_a[1].record(stream)
-    torch.cuda.synchronize()
-    append_us = ev_a[0].elapsed_time(ev_a[1]) * 1e3 / (4 * LAYERS)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item()):#x}")
-
-    peak, peak_src = read_peaks()
-    achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
-    value = job_value(kv_bytes, ms_per_step, world)
+    achieved = db.dec_bytes / (dec_mean_ms * 1e-3) / 1e9
+    value = job_value(db.kv_bytes, ms_per_step, world)
+    plan0 = db.plan0
+    two_kernel = args.merge == "combine"
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -671,36 +764,14 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if args.dtype == "bf16" else "f16",
-        "kv_cache": "int8 codes + fp32 row scales" if q8 else args.dtype,
+        "kv_cache": "int8 codes + fp32 row scales" if db.q8 else args.dtype,
         "accumulate": "f32",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
-        "config": {
-            "workload": w.name + (", INT8 KV cache (per-row scales)" if q8 else "") +
-                        (", bf16" if args.dtype == "bf16" else ""),
-            "config_id": args.config,
-            "batch": w.batch,
-            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}",
-            "head_dim": w.head_dim,
-            "page_size": w.page_size,
-            "sum_seq_len": int(w.seq_lens.sum()),
-            "kv_read_bytes_per_step": kv_bytes,
-            "splits": int(plan0.c.max_splits),
-            "split_merge": ("separate combine_kernel after the split kernel (PA_COMBINE_KERNEL=1)"
-                            if two_kernel else "by the last split task of each group, inside "
-                            "the split kernel"),
-            "work_items": int(plan0.c.num_work_items),
-            "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
-                    "split kernel, whose last split per group merges); pa_plan + pa_plan_upload once per "
-                    f"{LAYERS}-layer model step, inside the timing",
-            "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
-                      "calls back to back, programmatic dependent launch between kernels)",
-            "l2": f"{LAYERS} per-layer KV caches ({LAYERS * cache_bytes / 2**30:.1f} GiB) "
-                  f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": workload_config(args, w, world),
+        "run": run_dict(args, db, LAYERS, l2),
         "hbm_frac_step": round(value / world / peak, 4),
         "roofline": {
-            "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if q8 else
+            "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if db.q8 else
                        "pa_append_decode_attention = split_decode_kernel") +
                       (" (with the append) + combine_kernel, timed together"
                        if two_kernel else " (with the append and the split merge)"),
@@ -711,8 +782,8 @@ def run_ours(args):
                            else "fallback 6800 GB/s (of fallback)",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_for(args.config, args.kv, args.dtype),
-            "algorithmic_bytes_per_launch": dec_bytes,
+            "traffic": traffic_for(args.config, args.kv, args.dtype, decode_family(w, args.kv)),
+            "algorithmic_bytes_per_launch": db.dec_bytes,
             "us_per_launch": round(dec_mean_ms * 1e3, 3),
             "us_per_launch_isolated": round(iso_us, 3),
         },
@@ -721,19 +792,87 @@ def run_ours(args):
         "cpu_baseline": cpu_base,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": db.launches_per_step * K,
         "clocks": clk,
     }
     # host cost of pa_plan alone (reported, not part of the device timing)
     t0 = time.perf_counter()
     for _ in range(20):
-        binding.Plan(shape, lens_host, num_sms, w.forced_splits)
+        binding.Plan(db.shape, db.lens_host, num_sms, w.forced_splits)
     res["plan_host_us"] = round((time.perf_counter() - t0) / 20 * 1e6, 2)
+
+    # the other workloads, timed the same way in the same run (K layer steps
+    # each, after their own warm-up); reported beside the headline
+    extras = [c for c in (args.also or []) if c != args.config]
+    if extras:
+        del db, graphs_full, graphs_rem, warm_full
+        torch.cuda.empty_cache()
+        res["per_config"] = {}
+        for c in extras:
+            xb = DecodeBench(args, c, rank, dev, stream, num_sms, LAYERS)
+            gf, gr = xb.graphs(K)
+            wf = gf or [xb.capture(i, LAYERS) for i in range(2)]
+            xb.warm(max(args.warmup, LAYERS), wf, gr or wf)
+            t_ms = xb.time_region(K, gf, gr, world)
+            ms = max_over_ranks(t_ms / K, world, dev)
+            ach = xb.dec_bytes / (t_ms / K * 1e-3) / 1e9
+            res["per_config"][str(c)] = {
+                "workload": xb.workload_name(),
+                "us_per_step": round(ms * 1e3, 3),
+                "value": round(job_value(xb.kv_bytes, ms, world), 2), "unit": "GB/s",
+                "roofline_frac": round(ach / peak, 4),
+                "achieved": round(ach, 1),
+                "algorithmic_bytes_per_launch": xb.dec_bytes,
+                "traffic": traffic_for(c, args.kv, args.dtype, decode_family(xb.w, args.kv)),
+                "splits": int(xb.plan0.c.max_splits),
+                "gpu_launches": xb.launches_per_step * K,
+            }
+            del xb, gf, gr, wf
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def workload_config(args, w, world):
+    """The workload the line is about: the same dict on both arms."""
+    q8 = args.kv == "int8"
+    return {
+        "workload": (w.name + (", INT8 KV cache (per-row scales)" if q8 else "") +
+                     (", bf16" if args.dtype == "bf16" else "")),
+        "config_id": args.config,
+        "batch": w.batch,
+        "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}",
+        "head_dim": w.head_dim,
+        "page_size": w.page_size,
+        "sum_seq_len": int(w.seq_lens.sum()),
+        "kv_read_bytes_per_step": w.kv_bytes_int8() if q8 else w.kv_bytes(),
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
+def run_dict(args, db, LAYERS, l2):
+    """How our arm ran the workload."""
+    plan0 = db.plan0
+    return {
+        "splits": int(plan0.c.max_splits),
+        "split_merge": ("separate combine_kernel after the split kernel (plan option "
+                        "merge = PA_MERGE_COMBINE_KERNEL)" if args.merge == "combine" else
+                        "by the last split task of each group, inside the split kernel"),
+        "work_items": int(plan0.c.num_work_items),
+        "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
+                "split kernel, whose last split per group merges); pa_plan_upload once per "
+                f"{LAYERS}-layer model step, inside the timing; pa_plan on the host for each "
+                "model step while the GPU runs the one before it",
+        "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
+                  "calls back to back, programmatic dependent launch between kernels); a spin "
+                  "kernel before the start event keeps host launch latency out of the device "
+                  "timing",
+        "l2": f"{LAYERS} per-layer KV caches ({LAYERS * db.cache_bytes / 2**30:.1f} GiB) "
+              f"vs {l2 / 2**20:.0f} MiB L2: each step reads pages the L2 no longer holds",
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -773,10 +912,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
-        "config": {"workload": w.name + (", INT8 KV cache (per-row scales)"
-                                         if args.kv == "int8" else "") +
-                               (", bf16" if args.dtype == "bf16" else ""),
-                   "config_id": args.config},
+        "config": workload_config(args, w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {desc}, about {per_step:.2f} s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -978,7 +1114,7 @@ def run_prefill(args):
     pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(PREFILL_LAYERS - 1)]
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    plan = binding.PrefillPlan(shape, w.seq_lens, w.q_lens)
+    plan = binding.PrefillPlan(shape, w.seq_lens, w.q_lens, rows_per_tile=args.prefill_rows)
     ws = binding.alloc_workspace(plan, dev)
     with torch.cuda.stream(stream):
         binding.prefill_upload(plan, ws, stream=stream)
@@ -1051,7 +1187,7 @@ def run_prefill(args):
                              f"{PREFILL_LAYERS} per-layer KV caches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": ("prefill_kernel (mma.sync m16n8k16, 64-row tiles)"
-                               if os.environ.get("PA_PREFILL_ROWS") == "64" else
+                               if args.prefill_rows == 64 else
                                "prefill_tc5_kernel (tcgen05, 128-row tiles)"), "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
