@@ -90,6 +90,10 @@ def parse():
     ap.add_argument("--merge", choices=["split", "combine"], default="split",
                     help="decode: merge split partials in the split kernel (one launch) or in "
                          "a separate combine kernel (plan option merge)")
+    ap.add_argument("--plan", default="",
+                    help="decode: plan options as name=value pairs, comma-separated "
+                         "(min_chunk_pages, waves, bundle_max_pages, bundle_waves, "
+                         "l2_prefetch_pages, l2_prefetch_ctas); for experiments")
     ap.add_argument("--prefill-rows", type=int, choices=[128, 64], default=128,
                     help="prefill: query rows per tile, 128 for the tcgen05 kernel, 64 for the "
                          "mma.sync kernel (plan option rows_per_tile)")
@@ -436,7 +440,8 @@ class DecodeBench:
         # The plan: pa_plan_ex with the merge form asked for, into pinned host
         # memory, double-buffered so the host never rewrites a buffer whose
         # upload may still be pending.
-        self.opts = binding.plan_options(merge=args.merge)
+        extra = dict(kv.split("=") for kv in args.plan.split(",") if kv.strip())
+        self.opts = binding.plan_options(merge=args.merge, **{k: int(v) for k, v in extra.items()})
         self.plan0 = binding.Plan(self.shape, self.lens_host, num_sms, w.forced_splits,
                                   options=self.opts)
         self.staging = [torch.empty(int(self.plan0.c.blob_bytes), dtype=torch.uint8).pin_memory()
@@ -862,6 +867,8 @@ def run_dict(args, db, LAYERS, l2):
                         "merge = PA_MERGE_COMBINE_KERNEL)" if args.merge == "combine" else
                         "by the last split task of each group, inside the split kernel"),
         "work_items": int(plan0.c.num_work_items),
+        "ctas": int(plan0.c.num_ctas),
+        "plan_options": args.plan or "defaults",
         "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
                 "split kernel, whose last split per group merges); pa_plan_upload once per "
                 f"{LAYERS}-layer model step, inside the timing; pa_plan on the host for each "

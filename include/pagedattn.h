@@ -148,12 +148,15 @@ typedef struct {
   int32_t bundle_max_pages;  /* when the GPU runs several waves of tasks, tasks of at most
                                 this many pages run one per warp, four to a CTA
                                 (0: 8; negative: never) */
+  int32_t bundle_waves;      /* "several": more tasks than bundle_waves x the CTAs the GPU
+                                holds at once (0: 3; negative: bundle at any task count) */
   int32_t merge;             /* PA_MERGE_IN_SPLIT_KERNEL (0) or PA_MERGE_COMBINE_KERNEL */
   int32_t l2_prefetch_pages; /* pages per warp that the split kernel's first CTAs ask L2 for
                                 while the previous kernel still runs (0: 2; negative:
                                 none; at most 32) */
   int32_t l2_prefetch_ctas;  /* CTAs that prefetch (0: the first wave, the CTAs the GPU
                                 holds at once; negative: none) */
+  int32_t reserved;          /* 0 */
   uint64_t wait_limit_ns;    /* how long a warp waits for one page copy before it gives up,
                                 sets PA_DEV_TIMEOUT and writes nothing (0: 1 s).  A copy
                                 that was issued always lands before the kernel exits. */

@@ -60,8 +60,9 @@ MERGES = {"split": PA_MERGE_IN_SPLIT_KERNEL, "combine": PA_MERGE_COMBINE_KERNEL}
 
 class PaPlanOptions(ctypes.Structure):
     _fields_ = [("min_chunk_pages", ctypes.c_int32), ("waves", ctypes.c_int32),
-                ("bundle_max_pages", ctypes.c_int32), ("merge", ctypes.c_int32),
-                ("l2_prefetch_pages", ctypes.c_int32), ("l2_prefetch_ctas", ctypes.c_int32),
+                ("bundle_max_pages", ctypes.c_int32), ("bundle_waves", ctypes.c_int32),
+                ("merge", ctypes.c_int32), ("l2_prefetch_pages", ctypes.c_int32),
+                ("l2_prefetch_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_uint64)]
 
 

@@ -75,6 +75,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// is suspended until it completes or about hint_ns pass, instead of
+// returning at once (without the hint the system's own limit is short, and
+// a waiting warp re-polls, taking issue slots from the warps that work).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;  // longest sleep of one try (20 us)
+
 // Wait for a barrier phase, giving up after limit_ns.  Returns false on
 // timeout; the caller reports it and stops.  A try_wait may suspend the
 // thread for a while, so long limits read the clock every 64 tries; a limit
@@ -93,6 +112,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// The same wait for warps that mostly wait (the copy and MMA warps of a
+// warp-specialised kernel, and its row warps between stages): each try
+// sleeps until the phase completes or kSuspendHintNs pass, so a waiting
+// warp takes no issue slots from the warps that work on the same
+// scheduler; the clock is read after each try that came back empty.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity,
+                                                        uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) return mbar_wait_bounded(bar, parity, limit_ns);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -48,7 +48,18 @@ template <typename T>
 __device__ __forceinline__ void split_hi_lo(float2 a, uint32_t& hi, uint32_t& lo) {
   hi = Elem<T>::from_f2(a.x, a.y);
   const float2 h = Elem<T>::to_f2(hi);
-  lo = Elem<T>::from_f2(a.x - h.x, a.y - h.y);
+  // r = a - h on both lanes with one packed fma (h * -1 + a); the
+  // difference is exact in fp32
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rh, rm, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rh, {%4, %5};\n\t"
+      "mov.b64 rm, {%6, %6};\n\t"
+      "fma.rn.f32x2 rd, rh, rm, ra;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(h.x), "f"(h.y), "f"(-1.f));
+  lo = Elem<T>::from_f2(r.x, r.y);
 }
 
 // Eight packed elements (one 16-byte load) -> four fp32 pairs.

@@ -61,7 +61,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   if (st != PA_OK) return st;
   if (num_sms <= 0 || forced_splits < 0) return PA_ERR_INVALID_ARG;
   const pa_plan_options_t o = opt ? *opt : pa_plan_options_t{};
-  if (o.min_chunk_pages < 0 || o.waves < 0 || o.waves > 64 ||
+  if (o.min_chunk_pages < 0 || o.waves < 0 || o.waves > 64 || o.bundle_waves > 64 ||
       (o.merge != PA_MERGE_IN_SPLIT_KERNEL && o.merge != PA_MERGE_COMBINE_KERNEL) ||
       o.l2_prefetch_pages > 32)
     return PA_ERR_INVALID_ARG;
@@ -116,7 +116,9 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   // That costs latency (a warp walks a whole task) but saves a CTA start per
   // task, which only pays off when the GPU runs several waves of them.
   const int64_t cta_slots = (int64_t)num_sms * resident_ctas_per_sm(D, G);
-  const int bundle_pages = W64 > kBundleWhenOver * cta_slots ? bundle_max : 0;
+  const bool several = o.bundle_waves < 0 ||
+                       W64 > (o.bundle_waves > 0 ? o.bundle_waves : kBundleWhenOver) * cta_slots;
+  const int bundle_pages = several ? bundle_max : 0;
   int n_small = 0;
   for (int b = 0; b < B; ++b) {
     const int32_t np = pages[b], n = nsplit[b];

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         for (int u = 0; u < kTc5Pages; ++u) phys[u] = nxt[u];
         if (kt + 1 < nkt) load_entries(kt + 1);
         const int slot = kt % NR;
-        good = kt < NR || mbar_wait_bounded(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1), p.wait_ns);
+        good = kt < NR || mbar_wait_bounded_sleep(free_bar + 8 * slot, (uint32_t)((kt / NR - 1) & 1), p.wait_ns);
         if (!good) break;
         int nvalid = 0;
         bool zeroed = false;
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       // copies in flight land before the CTA exits: the last stage issued
       // into each slot (on success all of them have been consumed already)
       for (int k = n - NR < 0 ? 0 : n - NR; k < n; ++k)
-        mbar_wait_bounded(full_bar + 8 * (k % NR), (uint32_t)((k / NR) & 1), kDrainWaitNs);
+        mbar_wait_bounded_sleep(full_bar + 8 * (k % NR), (uint32_t)((k / NR) & 1), kDrainWaitNs);
     }
     __syncwarp();
   } else if (mma_warp) {
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       const uint32_t idesc_o = tc5::instr_desc<T>(128, D, true);
       auto issue_s = [&](int kt) -> bool {  // S(kt) = Q K^T
         const int sk = kt % NK;
-        if (!mbar_wait_bounded(k_full + 8 * sk, (uint32_t)((kt / NK) & 1), p.wait_ns)) return false;
+        if (!mbar_wait_bounded_sleep(k_full + 8 * sk, (uint32_t)((kt / NK) & 1), p.wait_ns)) return false;
         tc5::fence_after();
         const uint32_t kst = sbase + L::K0 + sk * L::STAGE;
 #pragma unroll
@@ -453,12 +453,12 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       for (int kt = 0; kt < nkt && good; ++kt) {
         if (kt + 1 < nkt) {
           // the S columns are free once the row warps have loaded S(kt)
-          good = mbar_wait_bounded(s_free, (uint32_t)(kt & 1), p.wait_ns) && issue_s(kt + 1);
+          good = mbar_wait_bounded_sleep(s_free, (uint32_t)(kt & 1), p.wait_ns) && issue_s(kt + 1);
           if (!good) break;
         }
         const int sv = kt % NV;
-        good = mbar_wait_bounded(p_ready + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1), p.wait_ns) &&
-               mbar_wait_bounded(v_full + 8 * sv, (uint32_t)((kt / NV) & 1), p.wait_ns);
+        good = mbar_wait_bounded_sleep(p_ready + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1), p.wait_ns) &&
+               mbar_wait_bounded_sleep(v_full + 8 * sv, (uint32_t)((kt / NV) & 1), p.wait_ns);
         if (!good) break;
         tc5::fence_after();
         const uint32_t vst = sbase + L::V0 + sv * L::STAGE;
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       // every MMA issued finishes before TMEM is freed: one more commit
       // covers them all
       tc5::commit(drain);
-      mbar_wait_bounded(drain, 0u, kDrainWaitNs);
+      mbar_wait_bounded_sleep(drain, 0u, kDrainWaitNs);
     }
     __syncwarp();
   } else {
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // Each of the 128 row threads takes its share.
     auto zero_value_tail = [&](int kt) -> bool {
       const int sv_slot = kt % NV;
-      if (!__all_sync(kFull, mbar_wait_bounded(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1), p.wait_ns)))
+      if (!__all_sync(kFull, mbar_wait_bounded_sleep(v_full + 8 * sv_slot, (uint32_t)((kt / NV) & 1), p.wait_ns)))
         return false;
       const int first_bad = span - BN * kt;  // tokens [first_bad, BN) of this stage
       unsigned char* vsm = base + L::V0 + sv_slot * L::STAGE;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // rows that are never written.
     const bool idle = !__any_sync(kFull, ok);
     for (int kt = 0; idle && kt < nkt; ++kt) {
-      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1), p.wait_ns));
+      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done, (uint32_t)(kt & 1), p.wait_ns));
       if (!good) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
             asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(nph[u]) : "l"(bt_row + j));
         }
       }
-      good = __all_sync(kFull, mbar_wait_bounded(s_done, (uint32_t)(kt & 1), p.wait_ns));
+      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done, (uint32_t)(kt & 1), p.wait_ns));
       if (!good) break;
       tc5::fence_after();
       float sv[BN];
@@ -621,11 +621,11 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       const bool any_resc = __any_sync(kFull, resc);
       if (kt >= L::NP) {
         const int k2 = kt - L::NP;
-        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1), p.wait_ns));
+        good = __all_sync(kFull, mbar_wait_bounded_sleep(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1), p.wait_ns));
         if (!good) break;
       }
       if (any_resc && kt >= 1) {
-        good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((kt - 1) & 1),
+        good = __all_sync(kFull, mbar_wait_bounded_sleep(pv_done + 8 * ((kt - 1) & 1),
                                                    (uint32_t)(((kt - 1) >> 1) & 1), p.wait_ns));
         if (!good) break;
       }
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       if (lane == 0) mbar_arrive(p_ready + 8 * (kt & 1));
     }
     if (!idle && nkt > 0 && good) {
-      good = __all_sync(kFull, mbar_wait_bounded(pv_done + 8 * ((nkt - 1) & 1),
+      good = __all_sync(kFull, mbar_wait_bounded_sleep(pv_done + 8 * ((nkt - 1) & 1),
                                                  (uint32_t)(((nkt - 1) >> 1) & 1), p.wait_ns));
       // a copy or MMA warp that gave up leaves O incomplete: write nothing
       good = good && *reinterpret_cast<volatile int*>(cta_flag) == 0;

@@ -57,7 +57,7 @@ def _decode_blob(plan):
     return blob, items, groups, slots, nslots, (NC, n_shared)
 
 
-def check_plan_covers(w, plan):
+def check_plan_covers(w, plan, bundle_max=8):
     """Every (sequence, kv head) has its pages [0, ceil(L/S)) covered exactly
     once by page ranges, split tasks appear in their group in page order, and
     tasks are longest first."""
@@ -101,7 +101,7 @@ def check_plan_covers(w, plan):
     assert plan.c.num_ctas == NC and plan.c.num_shared_ctas == n_shared
     assert 0 <= n_shared <= len(items)
     assert NC == n_shared + (len(items) - n_shared + 3) // 4
-    assert np.all(sizes[n_shared:] <= 8)
+    assert np.all(sizes[n_shared:] <= bundle_max)
     assert plan.c.workspace_bytes >= plan.c.blob_bytes
     return items, groups
 
@@ -351,6 +351,15 @@ def test_plan_options_shape_the_task_list(lib):
     nb = binding.Plan(_shape(w5), w5.seq_lens, 152, options=binding.plan_options(bundle_max_pages=-1))
     assert nb.c.num_shared_ctas == nb.c.num_work_items == nb.c.num_ctas
     check_plan_covers(w5, nb)
+    # bundle_waves < 0 bundles short tasks at any task count: workload 3's
+    # 1536 tasks (below 3 waves of CTAs) go four to a CTA, one per warp
+    w3 = workloads.make_config(3)
+    b3 = binding.Plan(_shape(w3), w3.seq_lens, 152)
+    assert b3.c.num_shared_ctas == b3.c.num_work_items == b3.c.num_ctas
+    a3 = binding.Plan(_shape(w3), w3.seq_lens, 152,
+                      options=binding.plan_options(bundle_waves=-1, bundle_max_pages=64))
+    assert a3.c.num_shared_ctas == 0 and a3.c.num_ctas == (a3.c.num_work_items + 3) // 4
+    check_plan_covers(w3, a3, bundle_max=64)
     # the per-call fields are carried by the plan, in a caller buffer too
     buf = np.zeros(base.c.blob_bytes, np.uint8)
     o = binding.plan_options(merge="combine", l2_prefetch_pages=32, l2_prefetch_ctas=7,
@@ -362,7 +371,8 @@ def test_plan_options_shape_the_task_list(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(merge=2), dict(merge=-1), dict(l2_prefetch_pages=33),
-                                 dict(waves=-1), dict(waves=65), dict(min_chunk_pages=-1)])
+                                 dict(waves=-1), dict(waves=65), dict(min_chunk_pages=-1),
+                                 dict(bundle_waves=65)])
 def test_plan_options_out_of_range_are_refused(lib, bad):
     w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=6)
     with pytest.raises(binding.PagedAttnError) as e:
