@@ -94,6 +94,10 @@ def parse():
                     help="decode: plan options as name=value pairs, comma-separated "
                          "(min_chunk_pages, waves, bundle_max_pages, bundle_waves, "
                          "l2_prefetch_pages, l2_prefetch_ctas); for experiments")
+    ap.add_argument("--upload", choices=["ahead", "inline"], default="ahead",
+                    help="decode: each model step's graph uploads the next step's plan into a "
+                         "second workspace while its layers run (ahead), or its own plan before "
+                         "its first layer (inline)")
     ap.add_argument("--prefill-rows", type=int, choices=[128, 64], default=128,
                     help="prefill: query rows per tile, 128 for the tcgen05 kernel, 64 for the "
                          "mma.sync kernel (plan option rows_per_tile)")
@@ -447,28 +451,56 @@ class DecodeBench:
         self.staging = [torch.empty(int(self.plan0.c.blob_bytes), dtype=torch.uint8).pin_memory()
                         for _ in range(2)]
         self.staged_evt = [torch.cuda.Event(), torch.cuda.Event()]
-        self.workspace = binding.alloc_workspace(self.plan0, dev)
+        # upload "ahead": model step m's graph computes with workspace m % 2
+        # and, on a side branch at the same time, uploads step m + 1's plan
+        # into the other workspace.  "inline": one workspace, and each graph
+        # uploads its own plan before its first layer.
+        self.ahead = args.upload == "ahead"
+        self.workspaces = [binding.alloc_workspace(self.plan0, dev)
+                           for _ in range(2 if self.ahead else 1)]
+        self.side_up = torch.cuda.Stream(device=dev)
         self.struct0 = self.plan0.structure()
         self.staged_plans = [None, None]
-        self.ready = set()   # model steps whose plan is already in its buffer
+        self.ready = set()   # model steps whose plan is already in its pinned buffer
         self.m = 0           # the next model step
         self.replan(1)       # both buffers hold a plan before the graphs that upload them
         self.replan(0)       # are captured; model step 0's is the one in use first
         with torch.cuda.stream(stream):
-            binding.upload(self.staged_plans[0], self.workspace, stream=stream)
+            binding.upload(self.staged_plans[0], self.ws_for(0), stream=stream)
             # a warm-up call (sets kernel attributes) before capture
-            self.layer_call(self.pools[0], self.q, self.k_new, self.v_new, self.out, stream=stream)
+            self.layer_call(self.pools[0], self.q, self.k_new, self.v_new, self.out,
+                            self.ws_for(0), stream=stream)
         stream.synchronize()
         self.launches_per_step = 1 + (1 if args.merge == "combine" and
                                       self.plan0.c.num_groups > 0 else 0)
 
-    def layer_call(self, pool, qq, kn, vn, o, stream=None):
+    def ws_for(self, slot):
+        """The workspace model steps of this parity compute with."""
+        return self.workspaces[slot] if self.ahead else self.workspaces[0]
+
+    def layer_call(self, pool, qq, kn, vn, o, ws, stream=None):
         """One layer's fused append + decode over that layer's cache."""
         self.step_call(self.shape, self.plan0, qq, kn, vn, *pool, self.bt, self.sl, self.w.scale, o,
-                       self.workspace, self.status, stream=stream)
+                       ws, self.status, stream=stream)
+
+    def upload_in_graph(self, slot):
+        """Inside a model step's capture: inline, this step's plan into the
+        workspace; ahead, the next step's plan into the other workspace on a
+        side branch (joined by join_upload)."""
+        if not self.ahead:
+            self.binding.upload(self.staged_plans[slot], self.ws_for(0))
+            return
+        self.side_up.wait_stream(self.stream)
+        with self.torch.cuda.stream(self.side_up):
+            self.binding.upload(self.staged_plans[1 - slot], self.ws_for(1 - slot))
+
+    def join_upload(self):
+        if self.ahead:
+            self.stream.wait_stream(self.side_up)
 
     def replan(self, m):
-        """a2 on the host: model step m's plan into the pinned buffer its graph uploads."""
+        """a2 on the host: model step m's plan into pinned buffer m % 2, which
+        graph m (inline) or graph m - 1 (ahead) uploads."""
         slot = m % 2
         self.staged_evt[slot].synchronize()   # that buffer's last upload has completed
         plan = self.binding.Plan(self.shape, self.lens_host, self.num_sms, self.w.forced_splits,
@@ -479,13 +511,15 @@ class DecodeBench:
         self.ready.add(m)
 
     def capture(self, slot, nlayers):
-        """One model step: the plan upload, then nlayers layers' calls."""
+        """One model step: a plan upload and nlayers layers' calls."""
         torch = self.torch
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
-            self.binding.upload(self.staged_plans[slot], self.workspace)
+            self.upload_in_graph(slot)
             for l in range(nlayers):
-                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out)
+                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out,
+                                self.ws_for(slot))
+            self.join_upload()
         return g
 
     def graphs(self, K):
@@ -495,20 +529,21 @@ class DecodeBench:
         return gf, gr
 
     def run_steps(self, nsteps, gfull, grem):
-        """nsteps layer steps as model-step graphs.  Each next model step's
-        plan is made on the host right after the current step is queued, so
-        the host plans step n + 1 while the GPU runs step n."""
+        """nsteps layer steps as model-step graphs.  The host makes model
+        step n + 1's plan while the GPU runs step n: inline, right after
+        step n is queued; ahead, right before (graph n uploads it)."""
         nf, nr = divmod(nsteps, self.LAYERS)
         sched = [gfull] * nf + ([grem] if nr else [])
         for i, gs in enumerate(sched):
             m = self.m
-            if m not in self.ready:
-                self.replan(m)
+            read = m + 1 if self.ahead else m   # the plan graph m uploads
+            if read not in self.ready:
+                self.replan(read)
             gs[m % 2].replay()
-            self.staged_evt[m % 2].record(self.stream)
-            self.ready.discard(m)
+            self.staged_evt[read % 2].record(self.stream)
+            self.ready.discard(read)
             self.m = m + 1
-            if i + 1 < len(sched):
+            if not self.ahead and i + 1 < len(sched):
                 self.replan(self.m)
 
     def time_region(self, K, gfull, grem, world):
@@ -516,7 +551,7 @@ class DecodeBench:
         launching stream.  The first model step's plan is made before the
         region, as it would be during the step before it."""
         torch = self.torch
-        if self.m not in self.ready:
+        if not self.ahead and self.m not in self.ready:
             self.replan(self.m)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -551,7 +586,8 @@ class DecodeBench:
         for l in range(n_iso):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
-                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out)
+                self.layer_call(self.pools[l], self.q, self.k_new, self.v_new, self.out,
+                                self.ws_for(0))
             g1.append(g)
         iso = []
         with torch.cuda.stream(self.stream):
@@ -617,7 +653,7 @@ class DecodeBench:
             with torch.cuda.graph(g, stream=stream):
                 self.bt.copy_(hbt, non_blocking=True)
                 self.sl.copy_(hsl, non_blocking=True)
-                binding.upload(self.staged_plans[slot], self.workspace)
+                self.upload_in_graph(slot)
                 copy_in(0, min(CHUNK, nlayers))
                 side_out.wait_stream(stream)
                 ready = {}
@@ -633,7 +669,7 @@ class DecodeBench:
                         if l in ready:
                             stream.wait_event(ready[l])
                     qq, kk, vv = layer_inputs(l)
-                    self.layer_call(self.pools[l], qq, kk, vv, ob[l])
+                    self.layer_call(self.pools[l], qq, kk, vv, ob[l], self.ws_for(slot))
                     done = torch.cuda.Event()
                     done.record(stream)
                     side_out.wait_event(done)
@@ -642,6 +678,7 @@ class DecodeBench:
                 if ready:  # side_in took part only if a chunk came in on it
                     stream.wait_stream(side_in)
                 stream.wait_stream(side_out)
+                self.join_upload()
             return g
 
         full, rem = divmod(K, LAYERS)
@@ -689,6 +726,19 @@ class DecodeBench:
     def workload_name(self):
         return (self.w.name + (", INT8 KV cache (per-row scales)" if self.q8 else "") +
                 (", bf16" if self.args.dtype == "bf16" else ""))
+
+
+REPEATS = 5   # further K-step regions, for the spread of the per-step time
+
+
+def repeat_regions(db, K, gfull, grem, world, dev):
+    """µs per layer step of REPEATS more K-step regions, timed exactly as
+    the first (which alone gives `value`): their p10, median and p90."""
+    us = sorted(max_over_ranks(db.time_region(K, gfull, grem, world) / K, world, dev) * 1e3
+                for _ in range(REPEATS))
+    pick = lambda q: float(np.percentile(us, q))
+    return {"regions": REPEATS, "steps_each": K, "us_per_step_p10": round(pick(10), 3),
+            "us_per_step_median": round(pick(50), 3), "us_per_step_p90": round(pick(90), 3)}
 
 
 def run_ours(args):
@@ -748,6 +798,7 @@ def run_ours(args):
     # the fused call is the only work in a step besides a2's amortised upload,
     # so its mean launch duration over the timed region is the step time
     dec_mean_ms = total_ms / K
+    dist = repeat_regions(db, K, graphs_full, graphs_rem, world, dev)
     iso_us = db.isolated_us()
     e2e = None if args.no_e2e else db.e2e(K, world)
     append_us = db.append_us()
@@ -792,6 +843,7 @@ def run_ours(args):
             "us_per_launch": round(dec_mean_ms * 1e3, 3),
             "us_per_launch_isolated": round(iso_us, 3),
         },
+        "distribution": dist,
         "plan_host_us": None,
         "append_us": round(append_us, 3),
         "cpu_baseline": cpu_base,
@@ -820,6 +872,7 @@ def run_ours(args):
             xb.warm(max(args.warmup, LAYERS), wf, gr or wf)
             t_ms = xb.time_region(K, gf, gr, world)
             ms = max_over_ranks(t_ms / K, world, dev)
+            xdist = repeat_regions(xb, K, gf, gr, world, dev)
             ach = xb.dec_bytes / (t_ms / K * 1e-3) / 1e9
             res["per_config"][str(c)] = {
                 "workload": xb.workload_name(),
@@ -831,6 +884,7 @@ def run_ours(args):
                 "traffic": traffic_for(c, args.kv, args.dtype, decode_family(xb.w, args.kv)),
                 "splits": int(xb.plan0.c.max_splits),
                 "gpu_launches": xb.launches_per_step * K,
+                "distribution": xdist,
             }
             del xb, gf, gr, wf
             torch.cuda.empty_cache()
@@ -871,8 +925,11 @@ def run_dict(args, db, LAYERS, l2):
         "plan_options": args.plan or "defaults",
         "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
                 "split kernel, whose last split per group merges); pa_plan_upload once per "
-                f"{LAYERS}-layer model step, inside the timing; pa_plan on the host for each "
-                "model step while the GPU runs the one before it",
+                f"{LAYERS}-layer model step, inside the timing" +
+                (" (each model step's graph uploads the next step's plan into a second "
+                 "workspace while its layers run)" if args.upload == "ahead" else
+                 " (before the step's first layer)") +
+                "; pa_plan on the host for each model step while the GPU runs the one before it",
         "launch": f"one CUDA graph per {LAYERS}-layer model step (plan upload + the layers' "
                   "calls back to back, programmatic dependent launch between kernels); a spin "
                   "kernel before the start event keeps host launch latency out of the device "
