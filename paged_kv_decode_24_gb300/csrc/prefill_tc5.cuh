@@ -1,39 +1,42 @@
 // Multi-token attention on the fifth-generation tensor cores (tcgen05):
 // the same operation as prefill.cuh, on 128-row tiles, with MMAs issued by
-// one thread from shared-memory descriptors into tensor memory (TMEM).
+// one thread from shared-memory descriptors and tensor memory (TMEM) into
+// TMEM.
 //
 // A CTA owns 128 query rows of one (sequence, KV head): 128 / G query tokens
 // times the G heads of the KV head.  Thread r of warps 0-3 owns row r, which
 // is TMEM lane r, so a row's softmax needs no shuffles.  Warp 4 issues the
 // MMAs, warp 5 the key copies and warp 6 the value copies; the warps meet
 // only on mbarriers.
-// Q sits in TMEM (row r in lane r), where the S MMAs read it as their A
-// operand, so the 128 x D tile is not re-read from shared memory per stage.
 // Shared memory (1024-aligned, 128-byte swizzle everywhere, the layout the
-// TMA copies write and the MMA descriptors read):
+// TMA copies and the row threads write and the MMA descriptors read):
 //   a ring of NK key stages of 64 tokens (four pages), each
 //     K [D/64 boxes][64 tokens][128 B]        B operand of S, K-major
 //   a ring of NV value stages of 64 tokens, each
 //     V [D/64 boxes][64 tokens][128 B]        B operand of P.V, MN-major
-//   P   NP x hi, lo [128 rows][128 B]         A operands of P.V, K-major
-// TMEM: S of 64 columns, O of D columns, Q of D/2 columns (two 16-bit
-// elements per 32-bit column).
+//   Q   [D/64 boxes][128 rows][128 B]         A operand of S, K-major
+// TMEM: S of 64 columns, O of D columns, and P of 64 columns: P_hi then
+// P_lo, keys 2j and 2j+1 in column j, the A operand of P.V (row m in lane m).
 // The weights p are kept as two 16-bit parts, hi = p rounded to the element
 // type and lo = the remainder rounded, and O accumulates P_hi V + P_lo V:
 // about twice the element type's bits of p, as in the decode kernels, so
-// the result stays within the decode path's tolerance.
+// the result stays within the decode path's tolerance.  Keeping P in TMEM
+// spares the shared-memory traffic of storing and reading it (twice the
+// bytes with the lo part) for that of reading Q.
 //
 // Per stage kt:
 //   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 64)       committed to s_done
 //   the row threads load S(kt) into registers and release its columns;
 //   S(kt+1) is issued at once and runs while they compute
 //   row softmax of S(kt) in registers, lazy rescaling
-//   P(kt) hi and lo to shared memory, once P.V(kt-NP) has finished reading
-//   O += P_hi V + P_lo V   (8 MMAs, M = 128, N = D, K = 64 each)   committed to pv_done
+//   P(kt) hi and lo into TMEM, once P.V(kt-1) has finished reading them
+//   O += P_hi V + P_lo V   (8 MMAs, M = 128, N = D, K = 16 each)   committed to pv_done
 // Keys and values have rings of their own: a key stage is refilled as soon
 // as S has read it, a value stage once P.V has.  Sixty-four keys per stage
 // spread each stage's fixed costs (waits, fences, TMEM loads) over twice the
-// keys of a two-page stage.
+// keys of a two-page stage.  Waiting warps sleep on their barriers
+// (mbar_wait_bounded_sleep) so that they take no issue slots from the row
+// warps.
 // Every wait is bounded; on failure the CTA waits (bounded) for its copies
 // and MMAs, frees its TMEM and writes nothing.
 #pragma once
@@ -182,7 +185,7 @@ struct Tc5Layout {
   static constexpr int BOXES = D / 64;
   static constexpr int NK = D == 128 ? 3 : 6;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
-  static constexpr int NP = 1;                                  // P buffers (each hi and lo)
+  static constexpr int NP = 1;                                  // P buffers in TMEM (each hi and lo)
   // An idle row warp waits for the last stage's value copies without having
   // waited for P.V of the stage before.  With one value slot that stage's
   // copy may still be in flight, and the parity wait would then read the
@@ -194,9 +197,9 @@ struct Tc5Layout {
   static constexpr int STAGE = BOXES * KVBOX;                   // one K or V stage
   static constexpr int K0 = 0;
   static constexpr int V0 = K0 + NK * STAGE;
-  static constexpr int P = V0 + NV * STAGE;                     // NP x (hi, lo) x 16 KB
-  static constexpr int PBUF = kTc5Rows * kTc5Tokens * 2;        // one P part (hi or lo)
-  static constexpr int BUFS = P + NP * 2 * PBUF;                // the 1024-aligned buffers
+  static constexpr int QBOX = kTc5Rows * 128;                   // 16 KB: 64 dims of 128 rows
+  static constexpr int Q = V0 + NV * STAGE;                     // Q [D/64 boxes][128 rows][128 B]
+  static constexpr int BUFS = Q + BOXES * QBOX;                 // the 1024-aligned buffers
   // SMALL bytes hold the mbarriers (k_full[NK], k_free[NK], v_full[NV],
   // v_free[NV], s_done, s_free, pv_done[2], p_ready[2], drain), the TMEM
   // address and a flag.  The buffers start at the first 1024-byte boundary
@@ -209,7 +212,7 @@ struct Tc5Layout {
   static constexpr int FLAG = TMEM_SLOT + 16;
   static_assert(FLAG + 16 <= SMALL, "barriers overflow their area");
   static constexpr int BYTES = BUFS + 1024;
-  static constexpr uint32_t TMEM_COLS = 256;                    // S (64), O (D), Q (D/2)
+  static constexpr uint32_t TMEM_COLS = 256;                    // S (64), O (D), P hi + lo (64)
 };
 
 template <typename T, int D, int G>
@@ -281,7 +284,8 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(small + L::TMEM_SLOT);
-  const uint32_t t_s = tmem, t_o = tmem + BN, t_q = t_o + D;  // columns: S, O, Q
+  // columns: S, O, then P: hi (keys 2j, 2j+1 in column j) and lo, 32 each
+  const uint32_t t_s = tmem, t_o = tmem + BN, t_p = t_o + D;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
 
   pdl_launch_dependents();
@@ -310,7 +314,9 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   const int nkt = bad ? 0 : (span + BN - 1) / BN;
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
 
-  // ---- Q tile into TMEM (row = thread of warps 0-3), zero past ntok
+  // ---- Q tile into shared memory (row = thread of warps 0-3), zero past
+  // ntok: K-major with the 128-byte swizzle, [D/64 boxes][128 rows][128 B],
+  // 16-byte chunk c of a row's box at chunk c ^ (row % 8)
   const int row = tid & 127;
   const int tt = row / G;                 // query token of this row within the tile
   const bool ok = !bad && row_warp && tt < ntok;
@@ -319,22 +325,15 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   if (row_warp) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow);
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {  // 16 columns = 32 elements per store
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = ok ? __ldg(src + 4 * c + i) : make_uint4(0u, 0u, 0u, 0u);
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-      }
-      tc5::st16u(t_q + (uint32_t)(16 * c) + lane_off, w);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(base + L::Q + (c >> 3) * L::QBOX + row * 128 +
+                                (((c & 7) ^ (row & 7)) << 4)) = v;
     }
-    tc5::wait_st();
+    fence_proxy_async_smem();  // the tensor core reads it (async proxy)
   }
-  // Q is in TMEM for the MMA warp: the row warps and the MMA warp meet on a
-  // named barrier; the copy warps, which do not read Q, start at once.
+  // Q is in shared memory for the MMA warp: the row warps and the MMA warp
+  // meet on a named barrier; the copy warps, which do not read Q, start at once.
   if (!copy_warp) {
     tc5::fence_before();
     asm volatile("bar.sync 1, %0;" ::"n"(5 * 32) : "memory");
@@ -442,8 +441,9 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         const uint32_t kst = sbase + L::K0 + sk * L::STAGE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
+          const uint64_t ad = tc5::smem_desc(sbase + L::Q + (k >> 2) * L::QBOX + (k & 3) * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
-          tc5::mma_tmem_a(t_s, t_q + (uint32_t)(8 * k), bd, idesc_s, k > 0 ? 1u : 0u);
+          tc5::mma(t_s, ad, bd, idesc_s, k > 0 ? 1u : 0u);
         }
         tc5::commit(k_free + 8 * sk);
         tc5::commit(s_done);
@@ -462,14 +462,11 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         if (!good) break;
         tc5::fence_after();
         const uint32_t vst = sbase + L::V0 + sv * L::STAGE;
-        const uint32_t pst = sbase + L::P + (kt % L::NP) * 2 * L::PBUF;  // hi, then lo
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a_hi = tc5::smem_desc(pst + k * 32, 16, 1024);
-          const uint64_t a_lo = tc5::smem_desc(pst + L::PBUF + k * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
-          tc5::mma(t_o, a_hi, bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
-          tc5::mma(t_o, a_lo, bd, idesc_o, 1u);
+          tc5::mma_tmem_a(t_o, t_p + (uint32_t)(8 * k), bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
+          tc5::mma_tmem_a(t_o, t_p + 32u + (uint32_t)(8 * k), bd, idesc_o, 1u);
         }
         tc5::commit(v_free + 8 * sv);
         tc5::commit(pv_done + 8 * (kt & 1));
@@ -630,18 +627,13 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         if (!good) break;
       }
       tc5::fence_after();
-      // ---- P(kt) row, hi and lo, into its buffers (K-major, 128-byte
-      // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), before the
-      // rescale so that their registers are free for it
-      unsigned char* prow = base + L::P + (kt % L::NP) * 2 * L::PBUF + row * 128;
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const int off = (ch ^ (row & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow + off) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(prow + L::PBUF + off) =
-            make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
-      }
+      // ---- P(kt) row, hi and lo, into TMEM (lane = row, column j = keys
+      // 2j, 2j+1), before the rescale so that their registers are free for it
+      tc5::st16u(t_p + lane_off, pk);
+      tc5::st16u(t_p + 16u + lane_off, pk + 16);
+      tc5::st16u(t_p + 32u + lane_off, pl);
+      tc5::st16u(t_p + 48u + lane_off, pl + 16);
+      tc5::wait_st();
       if (any_resc && kt >= 1) {  // rare: rescale this warp's O rows in TMEM
         const float f = resc ? al : 1.f;
 #pragma unroll
