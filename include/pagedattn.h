@@ -144,7 +144,7 @@ typedef struct {
  */
 typedef struct {
   int32_t min_chunk_pages;   /* automatic plan: no split shorter than this many pages (0: 48) */
-  int32_t waves;             /* automatic plan: about waves x resident CTAs tasks (0: 2) */
+  int32_t waves;             /* automatic plan: about waves x resident CTAs tasks (0: 1) */
   int32_t bundle_max_pages;  /* when the GPU runs several waves of tasks, tasks of at most
                                 this many pages run one per warp, four to a CTA
                                 (0: 8; negative: never) */

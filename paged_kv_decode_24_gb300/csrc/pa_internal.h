@@ -20,7 +20,7 @@ constexpr int kWarpsPerCta = 4;      // warps sharing one task's pages
 constexpr int kMaxSplits = 1024;     // per (sequence, KV head)
 constexpr int kMinChunkPages = 48;   // auto planner never cuts finer than this
 constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per warp
-constexpr int kPlanWaves = 2;        // auto planner: tasks ~ waves x resident CTAs
+constexpr int kPlanWaves = 1;        // auto planner: tasks ~ waves x resident CTAs
 constexpr int kL2PrefetchPages = 2;  // pages per warp asked of L2 before the wait on the previous kernel
 constexpr int kBundleWhenOver = 3;   // bundle short tasks only past this many tasks per CTA slot
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"

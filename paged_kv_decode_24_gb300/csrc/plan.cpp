@@ -4,9 +4,12 @@
 // Flash-Decoding (swiftLLM, feature list: paged attention v2) cuts a long
 // sequence into chunks processed in parallel, each producing a partial
 // output and log-sum-exp, merged afterwards.  The planner decides where to
-// cut: each sequence is split into near-equal page ranges so that the task
-// count fills the GPU about twice over, and tasks are issued longest first so
-// the tail of the grid holds the short ones.
+// cut: each sequence is split into near-equal page ranges no longer than
+// the average load of one resident CTA, so that no task outlasts the rest of
+// the grid, and tasks are issued longest first so the tail of the grid holds
+// the short ones.  A batch whose sequences are already shorter than that is
+// not split: a split costs a partial write, a merge and a CTA start, and
+// balances nothing there.
 #include <stdlib.h>
 #include <string.h>
 
@@ -80,7 +83,8 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
 
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
   // that the task count is about `waves` times the CTAs the GPU holds at
-  // once (one CTA per task), never finer than min_chunk pages.
+  // once (one CTA per task), never finer than min_chunk pages.  The default
+  // of one wave caps a task at the average page load of a CTA slot.
   const int min_chunk = o.min_chunk_pages > 0 ? o.min_chunk_pages : kMinChunkPages;
   const int bundle_max = o.bundle_max_pages > 0 ? o.bundle_max_pages
                                                 : (o.bundle_max_pages < 0 ? 0 : kBundleMaxPages);
