@@ -1,9 +1,10 @@
 """GPU parity at the long end: one 131072-token sequence (four times the
 longest benchmark context) beside a short one, on each split kernel (CUDA
 cores for MHA, tensor cores for GQA, the INT8 cache), with the automatic
-plan.  The planner cuts the long sequence into well over a hundred splits,
-so the split merge combines that many partials per head.  Every head of
-both sequences is compared with the float64 oracle.
+plan aimed at two waves of resident CTAs (plan option waves = 2).  The
+planner cuts the long sequence into well over a hundred splits, so the split
+merge combines that many partials per head.  Every head of both sequences is
+compared with the float64 oracle.
 """
 
 from __future__ import annotations
@@ -35,7 +36,7 @@ def test_131072_token_context(hq, hkv, kv):
     w = workloads.make_custom(seq_lens=[LONG, 77], num_q_heads=hq, num_kv_heads=hkv,
                               head_dim=128, seed=8000 + hq + hkv, kv=kv)
     dd = DeviceDecode(w)
-    dd.make_plan()
+    dd.make_plan(waves=2)
     assert dd.plan_obj.c.max_splits >= 100
     if kv == "int8":
         dd.append_q8()
