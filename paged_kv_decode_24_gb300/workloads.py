@@ -36,6 +36,13 @@ Conventions (the plainest readings of the workload descriptions):
     to integers and clipped to [-127, 127], scales uniform in [0.004, 0.012)
     (about what N(0, 0.5) rows quantise to).  Nothing here quantises; poison
     sets the scales of unowned rows to NaN.
+  * With ``kv="fp8"`` the cache comes as E4M3 bytes with one fp32 scale per
+    row, also drawn directly: sign uniform, exponent field e with probability
+    proportional to 2^e (0 <= e <= 15, so most codes sit in the top binades,
+    as rows scaled to their largest element do), mantissa uniform in 0..7,
+    and the NaN pattern S.1111.111 replaced by S.1111.110; scales uniform in
+    [0.001, 0.004) (about max|x| / 448 for N(0, 0.5) rows).  Poison sets the
+    codes of unowned rows to the NaN pattern and their scales to NaN.
 """
 
 from __future__ import annotations
@@ -82,7 +89,9 @@ class Workload:
     dtype: str = "fp16"                  # element type of q/K/V/out ("fp16" or "bf16")
     q_lens: np.ndarray | None = None     # int32 [B]: query tokens per sequence (multi-token);
                                          # q, k_new, v_new then have sum(q_lens) rows
-    k_codes: np.ndarray | None = None    # int8 [P][Hkv][S][D] (kv="int8")
+    kv: str = "fp16"                     # cache format: "fp16", "int8" or "fp8"
+    k_codes: np.ndarray | None = None    # [P][Hkv][S][D]: int8 codes (kv="int8") or
+                                         # uint8 E4M3 bytes (kv="fp8")
     v_codes: np.ndarray | None = None
     k_scales: np.ndarray | None = None   # float32 [P][Hkv][S]
     v_scales: np.ndarray | None = None
@@ -96,7 +105,8 @@ class Workload:
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 4
 
     def kv_bytes_int8(self) -> int:
-        """The same for the INT8 cache: sum(L) * Hkv * 2 tensors * (D codes + a 4 B scale)."""
+        """The same for an 8-bit cache (INT8 or FP8): sum(L) * Hkv * 2 tensors * (D codes +
+        a 4 B scale)."""
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * 2 * (self.head_dim + 4)
 
 
@@ -215,6 +225,27 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
         if poison:
             q8["k_scales"][pg, :, slot] = np.float32(np.nan)
             q8["v_scales"][pg, :, slot] = np.float32(np.nan)
+    elif kv == "fp8":
+        pe = np.exp2(np.arange(16, dtype=np.float64))
+        pe /= pe.sum()
+
+        def codes():
+            sign = rng.integers(0, 2, size=pool_shape, dtype=np.uint8) << 7
+            e = rng.choice(16, size=pool_shape, p=pe).astype(np.uint8)
+            m = rng.integers(0, 8, size=pool_shape, dtype=np.uint8)
+            c = sign | (e << 3) | m
+            return np.where((c & 0x7F) == 0x7F, c - 1, c).astype(np.uint8)
+
+        def scales():
+            return (np.float32(0.001) + rng.random(pool_shape[:3], dtype=np.float32)
+                    * np.float32(0.003)).astype(np.float32)
+
+        q8 = dict(k_codes=codes(), v_codes=codes(), k_scales=scales(), v_scales=scales())
+        if poison:
+            for key in ("k_codes", "v_codes"):
+                q8[key][pg, :, slot, :] = np.uint8(0x7F)
+            q8["k_scales"][pg, :, slot] = np.float32(np.nan)
+            q8["v_scales"][pg, :, slot] = np.float32(np.nan)
     elif kv != "fp16":
         raise ValueError(kv)
     return Workload(name=name, config=config, batch=B, num_q_heads=num_q_heads,
@@ -222,7 +253,7 @@ def make_custom(*, seq_lens, num_q_heads, num_kv_heads, head_dim, page_size=PAGE
                     num_pages=num_pages, max_pages_per_seq=bt.shape[1],
                     forced_splits=forced_splits, scale=float(scale), seq_lens=seq_lens,
                     block_table=bt, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages,
-                    v_pages=v_pages, dtype=dtype, q_lens=q_lens, **q8)
+                    v_pages=v_pages, dtype=dtype, q_lens=q_lens, kv=kv, **q8)
 
 
 def make_config(cfg: int, seed: int | None = None, poison: bool = False,
