@@ -38,8 +38,9 @@ Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
 in total), so L2 never holds the pages a step reads.
 
 --kv int8 runs the same steps over the INT8 cache (codes with one fp32 scale
-per row) through pa_append_decode_attention_q8; value and roofline then
-count the INT8 rows' bytes (D + 4 per row and tensor).
+per row) through pa_append_decode_attention_q8, --kv fp8 over the FP8 (E4M3)
+cache through pa_append_decode_attention_fp8; value and roofline then count
+the 8-bit rows' bytes (D + 4 per row and tensor).
 
 --impl reference times the float64 CPU oracle (the only reference this
 method has) on the same workload, metric and unit.
@@ -107,8 +108,9 @@ def parse():
     ap.add_argument("--oracle-offset", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-stride", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--kv", choices=["fp16", "int8"], default="fp16",
-                    help="KV-cache type: 16-bit elements, or INT8 codes with per-row fp32 scales")
+    ap.add_argument("--kv", choices=["fp16", "int8", "fp8"], default="fp16",
+                    help="KV-cache type: 16-bit elements, or INT8 codes or FP8 (E4M3) bytes with "
+                         "per-row fp32 scales")
     ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                     help="decode: the decode step; swap: KV block swap-out + swap-in "
                          "(pa_copy_blocks) of a quarter of the workload's sequences; prefill: "
@@ -150,7 +152,10 @@ def oracle_sample(w, budget_s, offset=0, stride=1):
         i += stride
         sub_bt = w.block_table[b:b + 1]
         sub_l = w.seq_lens[b:b + 1]
-        if q8:
+        if q8 and w.kv == "fp8":
+            oracle.decode_attention_fp8(w.q[b:b + 1], w.k_codes, w.v_codes, w.k_scales,
+                                        w.v_scales, sub_bt, sub_l, w.scale)
+        elif q8:
             oracle.decode_attention_q8(w.q[b:b + 1], w.k_codes, w.v_codes, w.k_scales,
                                        w.v_scales, sub_bt, sub_l, w.scale)
         else:
@@ -243,14 +248,18 @@ DECODE_FAMILY = {"cc": ("decode_kernel.cuh", "decode_d64.cu", "decode_d128.cu"),
                  "tc": ("decode_kernel.cuh", "decode_tc.cuh", "decode_tc_d64.cu",
                         "decode_tc_d128.cu"),
                  "q8": ("decode_kernel.cuh", "decode_tc.cuh", "decode_q8.cuh", "quant_common.cuh",
-                        "decode_q8_d64.cu", "decode_q8_d128.cu")}
+                        "decode_q8_d64.cu", "decode_q8_d128.cu"),
+                 "f8": ("decode_kernel.cuh", "decode_tc.cuh", "decode_q8.cuh", "quant_common.cuh",
+                        "decode_f8_d64.cu", "decode_f8_d128.cu")}
 
 
 def decode_family(w, kv):
-    """The split kernel a workload runs on: INT8 cache, CUDA cores (MHA) or
-    tensor cores (GQA)."""
+    """The split kernel a workload runs on: INT8 or FP8 cache, CUDA cores
+    (MHA) or tensor cores (GQA)."""
     if kv == "int8":
         return "q8"
+    if kv == "fp8":
+        return "f8"
     return "cc" if w.num_q_heads == w.num_kv_heads else "tc"
 
 
@@ -403,9 +412,9 @@ class DecodeBench:
         self.torch, self.binding = torch, binding
         self.args, self.cfg, self.dev, self.stream, self.LAYERS = args, cfg, dev, stream, layers
         self.num_sms = num_sms
-        self.q8 = args.kv == "int8"
+        self.q8 = args.kv in ("int8", "fp8")   # an 8-bit cache
         if self.q8 and args.dtype != "fp16":
-            raise SystemExit("the INT8 cache takes fp16 q/out")
+            raise SystemExit("the 8-bit caches take fp16 q/out")
         w = workloads.make_config(cfg, seed=workloads.SEED_BASE + cfg + 1000 * rank, kv=args.kv,
                                   dtype=args.dtype)
         if args.splits is not None:
@@ -437,7 +446,8 @@ class DecodeBench:
         # layers left in L2.
         self.pools = [cache0] + [tuple(t.clone() for t in cache0) for _ in range(layers - 1)]
         self.cache_bytes = sum(t.numel() * t.element_size() for t in cache0)
-        self.step_call = binding.append_decode_q8 if self.q8 else binding.append_decode
+        self.step_call = {"int8": binding.append_decode_q8, "fp8": binding.append_decode_fp8}.get(
+            args.kv, binding.append_decode)
         self.out = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -706,7 +716,8 @@ class DecodeBench:
         """a1 alone: pa_kv_append as its own launch (the step fuses it into the
         split kernel), one launch per layer's cache in one graph."""
         torch, binding = self.torch, self.binding
-        app_call = binding.append_q8 if self.q8 else binding.append
+        app_call = {"int8": binding.append_q8, "fp8": binding.append_fp8}.get(self.args.kv,
+                                                                              binding.append)
         ga = torch.cuda.CUDAGraph()
         with torch.cuda.graph(ga, stream=self.stream):
             for l in range(self.LAYERS):
@@ -724,11 +735,15 @@ class DecodeBench:
         return ev_a[0].elapsed_time(ev_a[1]) * 1e3 / (4 * self.LAYERS)
 
     def workload_name(self):
-        return (self.w.name + (", INT8 KV cache (per-row scales)" if self.q8 else "") +
+        return (self.w.name + KV_NAMES.get(self.args.kv, "") +
                 (", bf16" if self.args.dtype == "bf16" else ""))
 
 
 REPEATS = 5   # further K-step regions, for the spread of the per-step time
+
+# how a workload's name says which 8-bit cache it reads
+KV_NAMES = {"int8": ", INT8 KV cache (per-row scales)",
+            "fp8": ", FP8 (E4M3) KV cache (per-row scales)"}
 
 
 def repeat_regions(db, K, gfull, grem, world, dev):
@@ -820,15 +835,17 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if args.dtype == "bf16" else "f16",
-        "kv_cache": "int8 codes + fp32 row scales" if db.q8 else args.dtype,
+        "kv_cache": {"int8": "int8 codes + fp32 row scales",
+                     "fp8": "e4m3 codes + fp32 row scales"}.get(args.kv, args.dtype),
         "accumulate": "f32",
         "data": "synthetic (seeded; shapes and value laws of the workload)",
         "config": workload_config(args, w, world),
         "run": run_dict(args, db, LAYERS, l2),
         "hbm_frac_step": round(value / world / peak, 4),
         "roofline": {
-            "kernel": ("pa_append_decode_attention_q8 = split_decode_q8_kernel" if db.q8 else
-                       "pa_append_decode_attention = split_decode_kernel") +
+            "kernel": {"int8": "pa_append_decode_attention_q8 = split_decode_q8_kernel (INT8)",
+                       "fp8": "pa_append_decode_attention_fp8 = split_decode_q8_kernel (E4M3)"}.get(
+                           args.kv, "pa_append_decode_attention = split_decode_kernel") +
                       (" (with the append) + combine_kernel, timed together"
                        if two_kernel else " (with the append and the split merge)"),
             "bound": "hbm",
@@ -897,9 +914,9 @@ def run_ours(args):
 
 def workload_config(args, w, world):
     """The workload the line is about: the same dict on both arms."""
-    q8 = args.kv == "int8"
+    q8 = args.kv in ("int8", "fp8")
     return {
-        "workload": (w.name + (", INT8 KV cache (per-row scales)" if q8 else "") +
+        "workload": (w.name + KV_NAMES.get(args.kv, "") +
                      (", bf16" if args.dtype == "bf16" else "")),
         "config_id": args.config,
         "batch": w.batch,

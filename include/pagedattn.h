@@ -336,6 +336,57 @@ pa_status_t pa_append_decode_attention_q8(const pa_shape_t* shape, const pa_plan
                                           void* workspace, size_t workspace_bytes,
                                           int32_t* dev_status, void* stream);
 
+/* ---- FP8 (E4M3) KV cache ---------------------------------------------
+ *
+ * The same paged cache held as FP8 bytes with one fp32 scale per row
+ * ("Eine LLM-Inferenz-Engine von Grund auf mit C++ und CUDA bauen", section 4:
+ * FP8 quantisation of the cache; MonadKai/xLLM, introduction: KV-cache
+ * quantisation).  The byte format is E4M3 of the OCP 8-bit floating-point
+ * specification: sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * subnormals m/8 * 2^-6, no infinities, S.1111.111 NaN, largest finite 448.
+ * A row's value is value(code) * scale.
+ *
+ * Layout (device): as the INT8 cache, with k_codes, v_codes holding E4M3
+ * bytes: [num_pages][Hkv][16][D] uint8 and [num_pages][Hkv][16] fp32 scales
+ * (16-byte aligned).  The plan, workspace and the other buffers are those of
+ * the fp16 calls.
+ *
+ * Quantisation of a new row (append): scale = max|x| / 448 and code = the
+ * E4M3 value nearest x / scale, ties to the even mantissa, magnitudes above
+ * 448 saturated, the sign of a zero kept; both divisions in IEEE fp32
+ * round-to-nearest; an all-zero row gets scale 0 and zero codes.  Non-finite
+ * inputs give unspecified codes.  A decode never uses the bytes of rows past
+ * a sequence's end, so those may hold anything (NaN patterns too).
+ *
+ * Errors are those of the INT8 calls.
+ */
+
+/* pa_kv_append into the FP8 cache: quantise k_new/v_new ([B][Hkv][D] fp16)
+ * and write codes and scales at position seq_lens[b] - 1. */
+pa_status_t pa_kv_append_fp8(const pa_shape_t* shape, const void* k_new, const void* v_new,
+                             void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             int32_t* dev_status, void* stream);
+
+/* pa_decode_attention over the FP8 cache: attention over the dequantised
+ * rows, fp32 accumulation, fp16 output. */
+pa_status_t pa_decode_attention_fp8(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                                    const void* k_codes, const void* v_codes,
+                                    const float* k_scales, const float* v_scales,
+                                    const int32_t* block_table, const int32_t* seq_lens,
+                                    float scale, void* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* pa_kv_append_fp8 and pa_decode_attention_fp8 in one launch, with the same
+ * results as the two calls in sequence. */
+pa_status_t pa_append_decode_attention_fp8(const pa_shape_t* shape, const pa_plan_t* plan,
+                                           const void* q, const void* k_new, const void* v_new,
+                                           void* k_codes, void* v_codes, float* k_scales,
+                                           float* v_scales, const int32_t* block_table,
+                                           const int32_t* seq_lens, float scale, void* out,
+                                           void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_status, void* stream);
+
 /* Size of the library-owned scratch array used by pa_decode_attention_static. */
 #define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 
@@ -459,11 +510,12 @@ pa_status_t pa_prefill_attention(const pa_shape_t* shape, const pa_prefill_plan_
 
 #define PA_KV_16BIT 0 /* fp16 or bf16 pools */
 #define PA_KV_INT8 1  /* INT8 code pools plus fp32 row scales */
+#define PA_KV_FP8 2   /* E4M3 code pools plus fp32 row scales */
 
-/* Pages of num_layers layers' K and V pools (kv_kind: PA_KV_16BIT or
- * PA_KV_INT8) that fit in free_bytes - reserve_bytes:
+/* Pages of num_layers layers' K and V pools (kv_kind: PA_KV_16BIT,
+ * PA_KV_INT8 or PA_KV_FP8) that fit in free_bytes - reserve_bytes:
  *   floor((free - reserve) / (2 * Hkv * page_size * row_bytes * num_layers)),
- * row_bytes = 2 * head_dim (16-bit) or head_dim + 4 (INT8 codes + scale).
+ * row_bytes = 2 * head_dim (16-bit) or head_dim + 4 (8-bit codes + scale).
  * Host only.  Returns 0 when free <= reserve and -1 on a bad argument. */
 int64_t pa_profile_num_blocks(const pa_shape_t* shape, int32_t num_layers, int32_t kv_kind,
                               size_t free_bytes, size_t reserve_bytes);

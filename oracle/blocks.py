@@ -17,8 +17,8 @@ Readings of what the pages leave open:
 * A block is one page: page_size tokens of every KV head of one layer's K
   (or V) pool.  Pages needed for num_layers layers' K and V:
   2 x Hkv x page_size x row_bytes x num_layers bytes each, row_bytes =
-  2 x head_dim for 16-bit elements, head_dim + 4 for INT8 codes plus an fp32
-  scale.  The page count is floor((free - reserve) / that).
+  2 x head_dim for 16-bit elements, head_dim + 4 for 8-bit codes (INT8 or
+  FP8) plus an fp32 scale.  The page count is floor((free - reserve) / that).
 * The free list hands pages out last-freed first; a fresh list hands out
   0, 1, 2, ...  Allocation is all or nothing; freeing a page that is not
   out, out of range, or listed twice is refused and frees nothing.

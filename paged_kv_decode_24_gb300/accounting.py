@@ -27,10 +27,10 @@ def kv_cache_bytes(seq_lens, kv_width: int, bytes_per_element: int, layers: int 
 
 def kv_row_bytes(head_dim: int, kv: str = "fp16") -> int:
     """Bytes of one cached row (one token, one KV head, K or V): D fp16 values,
-    or D int8 codes and one fp32 scale (per-row INT8 cache)."""
+    or D 8-bit codes and one fp32 scale (per-row INT8 or FP8 cache)."""
     if kv == "fp16":
         return 2 * head_dim
-    if kv == "int8":
+    if kv in ("int8", "fp8"):
         return head_dim + 4
     raise ValueError(kv)
 
@@ -39,7 +39,7 @@ def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  page_size: int, kv: str = "fp16") -> int:
     """Algorithmic HBM bytes of one decode-attention call (fp16 q/out).
 
-    K and V of every attended token (fp16 or INT8 rows), q and out, the
+    K and V of every attended token (fp16, INT8 or FP8 rows), q and out, the
     block-table entries that are read (one int32 per used page) and seq_lens.
     """
     lens = np.asarray(seq_lens, np.int64)

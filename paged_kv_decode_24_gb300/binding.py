@@ -130,6 +130,15 @@ _SIGS = {
                                                      ctypes.POINTER(PaPlan), _P, _P, _P, _P, _P,
                                                      _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                                      ctypes.c_size_t, _P, _P]),
+    "pa_kv_append_fp8": (ctypes.c_int, [ctypes.POINTER(PaShape), _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P]),
+    "pa_decode_attention_fp8": (ctypes.c_int, [ctypes.POINTER(PaShape), ctypes.POINTER(PaPlan),
+                                               _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                               ctypes.c_size_t, _P, _P]),
+    "pa_append_decode_attention_fp8": (ctypes.c_int, [ctypes.POINTER(PaShape),
+                                                      ctypes.POINTER(PaPlan), _P, _P, _P, _P, _P,
+                                                      _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                                      ctypes.c_size_t, _P, _P]),
     "pa_profile_num_blocks": (ctypes.c_int64, [ctypes.POINTER(PaShape), ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_size_t, ctypes.c_size_t]),
     "pa_block_allocator_create": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(_P)]),
@@ -358,9 +367,10 @@ def append_decode(shape, plan: Plan, q, k_new, v_new, k_pages, v_pages, block_ta
         _dev_ptr(status, torch.int32, "status"), _stream(stream)))
 
 
-def _q8_pools(k_codes, v_codes, k_scales, v_scales):
+def _q8_pools(k_codes, v_codes, k_scales, v_scales, code_dtype=None):
     torch = _torch()
-    return (_dev_ptr(k_codes, torch.int8, "k_codes"), _dev_ptr(v_codes, torch.int8, "v_codes"),
+    cd = torch.int8 if code_dtype is None else code_dtype
+    return (_dev_ptr(k_codes, cd, "k_codes"), _dev_ptr(v_codes, cd, "v_codes"),
             _dev_ptr(k_scales, torch.float32, "k_scales"),
             _dev_ptr(v_scales, torch.float32, "v_scales"))
 
@@ -400,6 +410,48 @@ def append_decode_q8(shape, plan: Plan, q, k_new, v_new, k_codes, v_codes, k_sca
         ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
         _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
         *_q8_pools(k_codes, v_codes, k_scales, v_scales),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def append_fp8(shape, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens,
+               status, stream=None):
+    """pa_kv_append_fp8: quantise the new rows into the FP8 (E4M3) cache."""
+    torch = _torch()
+    lib = load()
+    _check("pa_kv_append_fp8", lib.pa_kv_append_fp8(
+        ctypes.byref(shape), _dev_ptr(k_new, torch.float16, "k_new"),
+        _dev_ptr(v_new, torch.float16, "v_new"),
+        *_q8_pools(k_codes, v_codes, k_scales, v_scales, torch.uint8),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def decode_fp8(shape, plan: Plan, q, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens,
+               scale, out, workspace, status, stream=None):
+    """pa_decode_attention_fp8: decode over the FP8 (E4M3) cache."""
+    torch = _torch()
+    lib = load()
+    _check("pa_decode_attention_fp8", lib.pa_decode_attention_fp8(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        *_q8_pools(k_codes, v_codes, k_scales, v_scales, torch.uint8),
+        _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+        ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def append_decode_fp8(shape, plan: Plan, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales,
+                      block_table, seq_lens, scale, out, workspace, status, stream=None):
+    """pa_append_decode_attention_fp8: append the new token and attend, one launch."""
+    torch = _torch()
+    lib = load()
+    _check("pa_append_decode_attention_fp8", lib.pa_append_decode_attention_fp8(
+        ctypes.byref(shape), ctypes.byref(plan.c), _dev_ptr(q, torch.float16, "q"),
+        _dev_ptr(k_new, torch.float16, "k_new"), _dev_ptr(v_new, torch.float16, "v_new"),
+        *_q8_pools(k_codes, v_codes, k_scales, v_scales, torch.uint8),
         _dev_ptr(block_table, torch.int32, "block_table"), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
         ctypes.c_float(scale), _dev_ptr(out, torch.float16, "out"),
         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
@@ -513,6 +565,7 @@ def prefill(shape, plan: PrefillPlan, q, k_pages, v_pages, block_table, seq_lens
 
 PA_KV_16BIT = 0
 PA_KV_INT8 = 1
+PA_KV_FP8 = 2
 
 
 def profile_num_blocks(shape, num_layers, kv_kind, free_bytes, reserve_bytes=0) -> int:

@@ -24,6 +24,7 @@ LIB = os.path.join(LIBDIR, "libpagedattn.so")
 
 SOURCES = ["api.cu", "plan.cpp", "aux_kernels.cu", "decode_d64.cu", "decode_d128.cu",
            "decode_tc_d64.cu", "decode_tc_d128.cu", "decode_q8_d64.cu", "decode_q8_d128.cu",
+           "decode_f8_d64.cu", "decode_f8_d128.cu",
            "static_workspace.cu", "blocks.cpp", "prefill_plan.cpp", "prefill_d64.cu",
            "prefill_d128.cu", "prefill_tc5_d64.cu", "prefill_tc5_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -28,6 +28,8 @@ cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int dtype, int
                                  cudaStream_t stream);
 cudaError_t launch_split_q8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
 cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_f8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_f8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
 
 // MHA (G = 1) does one multiply-add per K or V element: the CUDA-core kernel
 // keeps up with HBM.  With G >= 2 query heads per KV head the CUDA-core kernel
@@ -45,12 +47,18 @@ cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtyp
   return cudaErrorInvalidValue;
 }
 
-// The INT8 cache has one kernel for every group size: its products run on
-// tensor cores, which the padding of G = 1 to 8 heads does not slow down.
-cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
+// The 8-bit caches (INT8 codes or E4M3 bytes) have one kernel for every group
+// size: its products run on tensor cores, which the padding of G = 1 to 8
+// heads does not slow down.
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int grid,
                             cudaStream_t stream) {
-  if (head_dim == 64) return launch_split_q8_d64(p, group, grid, stream);
-  if (head_dim == 128) return launch_split_q8_d128(p, group, grid, stream);
+  if (fmt == kCodeE4m3) {
+    if (head_dim == 64) return launch_split_f8_d64(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_f8_d128(p, group, grid, stream);
+  } else {
+    if (head_dim == 64) return launch_split_q8_d64(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_q8_d128(p, group, grid, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -192,12 +200,15 @@ extern "C" pa_status_t pa_kv_append(const pa_shape_t* shape, const void* k_new, 
   return cuda_status(launch_append(p, (cudaStream_t)stream));
 }
 
-extern "C" pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_new,
-                                       const void* v_new, void* k_codes, void* v_codes,
-                                       float* k_scales, float* v_scales,
-                                       const int32_t* block_table, const int32_t* seq_lens,
-                                       int32_t* dev_status, void* stream) {
-  using namespace pa;
+namespace pa {
+namespace {
+
+// pa_kv_append_q8 and pa_kv_append_fp8: the same checks and launch, codes of
+// format fmt.
+pa_status_t append8_impl(const pa_shape_t* shape, const void* k_new, const void* v_new,
+                         void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                         const int32_t* block_table, const int32_t* seq_lens,
+                         int32_t* dev_status, void* stream, int fmt) {
   pa_status_t st = check_shape(shape);
   if (st != PA_OK) return st;
   if (shape->dtype != PA_DTYPE_F16) return PA_ERR_UNSUPPORTED;
@@ -221,7 +232,29 @@ extern "C" pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_ne
   p.head_dim = shape->head_dim;
   p.max_pages = shape->max_pages_per_seq;
   p.num_pages = shape->num_pages;
+  p.fmt = fmt;
   return cuda_status(launch_append_q8(p, (cudaStream_t)stream));
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status_t pa_kv_append_q8(const pa_shape_t* shape, const void* k_new,
+                                       const void* v_new, void* k_codes, void* v_codes,
+                                       float* k_scales, float* v_scales,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t* dev_status, void* stream) {
+  return pa::append8_impl(shape, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                          seq_lens, dev_status, stream, pa::kCodeInt8);
+}
+
+extern "C" pa_status_t pa_kv_append_fp8(const pa_shape_t* shape, const void* k_new,
+                                        const void* v_new, void* k_codes, void* v_codes,
+                                        float* k_scales, float* v_scales,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int32_t* dev_status, void* stream) {
+  return pa::append8_impl(shape, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                          seq_lens, dev_status, stream, pa::kCodeE4m3);
 }
 
 extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
@@ -236,13 +269,14 @@ extern "C" pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace,
 namespace pa {
 namespace {
 
-// The cache a decode reads: fp16 pools, or INT8 code pools with their row
-// scales (scales non-null).
+// The cache a decode reads: 16-bit pools, or 8-bit code pools (INT8 codes or
+// E4M3 bytes, fmt) with their row scales (scales non-null).
 struct KvCache {
   const void* k;
   const void* v;
   const float* k_scales;
   const float* v_scales;
+  int fmt;
   bool int8() const { return k_scales != nullptr; }
 };
 
@@ -290,9 +324,9 @@ extern "C" pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_pla
                                            float scale, void* out, void* workspace,
                                            size_t workspace_bytes, int32_t* dev_status,
                                            void* stream) {
-  return pa::decode_impl(shape, plan, q, nullptr, nullptr, {k_pages, v_pages, nullptr, nullptr},
-                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
-                         stream);
+  const pa::KvCache kv{k_pages, v_pages, nullptr, nullptr, -1};
+  return pa::decode_impl(shape, plan, q, nullptr, nullptr, kv, block_table, seq_lens, scale, out,
+                         workspace, workspace_bytes, dev_status, stream);
 }
 
 extern "C" pa_status_t pa_append_decode_attention(
@@ -302,10 +336,32 @@ extern "C" pa_status_t pa_append_decode_attention(
     int32_t* dev_status, void* stream) {
   if (shape && shape->batch > 0 && (!pa::aligned(k_new, 16) || !pa::aligned(v_new, 16)))
     return PA_ERR_INVALID_ARG;
-  return pa::decode_impl(shape, plan, q, k_new, v_new, {k_pages, v_pages, nullptr, nullptr},
-                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
-                         stream);
+  const pa::KvCache kv{k_pages, v_pages, nullptr, nullptr, -1};
+  return pa::decode_impl(shape, plan, q, k_new, v_new, kv, block_table, seq_lens, scale, out,
+                         workspace, workspace_bytes, dev_status, stream);
 }
+
+namespace pa {
+namespace {
+
+// The decode calls of the 8-bit caches: scales must be 16-byte aligned.
+pa_status_t decode8(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
+                    const void* k_new, const void* v_new, const void* k_codes,
+                    const void* v_codes, const float* k_scales, const float* v_scales,
+                    const int32_t* block_table, const int32_t* seq_lens, float scale, void* out,
+                    void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                    int fmt) {
+  if (shape && shape->batch > 0 &&
+      (!aligned(k_scales, 16) || !aligned(v_scales, 16) ||
+       (k_new != nullptr && (!aligned(k_new, 16) || !aligned(v_new, 16)))))
+    return PA_ERR_INVALID_ARG;
+  const KvCache kv{k_codes, v_codes, k_scales, v_scales, fmt};
+  return decode_impl(shape, plan, q, k_new, v_new, kv, block_table, seq_lens, scale, out,
+                     workspace, workspace_bytes, dev_status, stream);
+}
+
+}  // namespace
+}  // namespace pa
 
 extern "C" pa_status_t pa_decode_attention_q8(const pa_shape_t* shape, const pa_plan_t* plan,
                                               const void* q, const void* k_codes,
@@ -314,11 +370,9 @@ extern "C" pa_status_t pa_decode_attention_q8(const pa_shape_t* shape, const pa_
                                               const int32_t* seq_lens, float scale, void* out,
                                               void* workspace, size_t workspace_bytes,
                                               int32_t* dev_status, void* stream) {
-  if (shape && shape->batch > 0 && (!pa::aligned(k_scales, 16) || !pa::aligned(v_scales, 16)))
-    return PA_ERR_INVALID_ARG;
-  return pa::decode_impl(shape, plan, q, nullptr, nullptr, {k_codes, v_codes, k_scales, v_scales},
-                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
-                         stream);
+  return pa::decode8(shape, plan, q, nullptr, nullptr, k_codes, v_codes, k_scales, v_scales,
+                     block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                     stream, pa::kCodeInt8);
 }
 
 extern "C" pa_status_t pa_append_decode_attention_q8(
@@ -326,13 +380,35 @@ extern "C" pa_status_t pa_append_decode_attention_q8(
     const void* v_new, void* k_codes, void* v_codes, float* k_scales, float* v_scales,
     const int32_t* block_table, const int32_t* seq_lens, float scale, void* out, void* workspace,
     size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  if (shape && shape->batch > 0 &&
-      (!pa::aligned(k_new, 16) || !pa::aligned(v_new, 16) || !pa::aligned(k_scales, 16) ||
-       !pa::aligned(v_scales, 16)))
+  if (shape && shape->batch > 0 && (k_new == nullptr || v_new == nullptr))
     return PA_ERR_INVALID_ARG;
-  return pa::decode_impl(shape, plan, q, k_new, v_new, {k_codes, v_codes, k_scales, v_scales},
-                         block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
-                         stream);
+  return pa::decode8(shape, plan, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales,
+                     block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                     stream, pa::kCodeInt8);
+}
+
+extern "C" pa_status_t pa_decode_attention_fp8(const pa_shape_t* shape, const pa_plan_t* plan,
+                                               const void* q, const void* k_codes,
+                                               const void* v_codes, const float* k_scales,
+                                               const float* v_scales, const int32_t* block_table,
+                                               const int32_t* seq_lens, float scale, void* out,
+                                               void* workspace, size_t workspace_bytes,
+                                               int32_t* dev_status, void* stream) {
+  return pa::decode8(shape, plan, q, nullptr, nullptr, k_codes, v_codes, k_scales, v_scales,
+                     block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                     stream, pa::kCodeE4m3);
+}
+
+extern "C" pa_status_t pa_append_decode_attention_fp8(
+    const pa_shape_t* shape, const pa_plan_t* plan, const void* q, const void* k_new,
+    const void* v_new, void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+    const int32_t* block_table, const int32_t* seq_lens, float scale, void* out, void* workspace,
+    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (shape && shape->batch > 0 && (k_new == nullptr || v_new == nullptr))
+    return PA_ERR_INVALID_ARG;
+  return pa::decode8(shape, plan, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales,
+                     block_table, seq_lens, scale, out, workspace, workspace_bytes, dev_status,
+                     stream, pa::kCodeE4m3);
 }
 
 namespace pa {
@@ -404,7 +480,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;
-    st = cuda_status(launch_split_q8(p, D, G, plan->num_ctas, s));
+    st = cuda_status(launch_split_q8(p, D, G, kv.fmt, plan->num_ctas, s));
   } else {
     if (!encode_pool_map(&p.tmap_k, kv.k, *shape) || !encode_pool_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;

@@ -161,12 +161,12 @@ __global__ void append_kernel(const AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Append into the INT8 cache: one warp per (sequence, KV head) quantises the
-// new K and V rows (per-row INT8, quant_common.cuh) and writes their codes
-// and scales at position L-1.
+// Append into an 8-bit cache: one warp per (sequence, KV head) quantises the
+// new K and V rows (per-row INT8 or E4M3, quant_common.cuh) and writes their
+// codes and scales at position L-1.
 constexpr int kAppendWarps = 8;
 
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_q8_kernel(const AppendQ8Params p) {
   constexpr int PER = D / 32;
   const int lane = threadIdx.x & 31;
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_q8_kernel(const Appe
     const size_t row = ((size_t)page * p.num_kv_heads + h) * kPageSize + pos % kPageSize;
     const size_t src = ((size_t)b * p.num_kv_heads + h) * D;
     float sk, sv;
-    const uint32_t ck = quantize_row_warp<D>(p.k_new + src, lane, sk);
-    const uint32_t cv = quantize_row_warp<D>(p.v_new + src, lane, sv);
+    const uint32_t ck = quantize_row_warp<D, FMT>(p.k_new + src, lane, sk);
+    const uint32_t cv = quantize_row_warp<D, FMT>(p.v_new + src, lane, sv);
     if constexpr (PER == 4) {
       reinterpret_cast<uint32_t*>(p.k_codes + row * D)[lane] = ck;
       reinterpret_cast<uint32_t*>(p.v_codes + row * D)[lane] = cv;
@@ -349,10 +349,17 @@ cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream) {
   const long long rows = (long long)p.batch * p.num_kv_heads;
   long long g = (rows + kAppendWarps - 1) / kAppendWarps;
   const int grid = (int)(g < 1 ? 1 : g > 152 * 16 ? 152 * 16 : g);
-  if (p.head_dim == 64)
-    append_q8_kernel<64><<<grid, kAppendWarps * 32, 0, stream>>>(p);
-  else
-    append_q8_kernel<128><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  if (p.fmt == kCodeE4m3) {
+    if (p.head_dim == 64)
+      append_q8_kernel<64, kCodeE4m3><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+    else
+      append_q8_kernel<128, kCodeE4m3><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  } else {
+    if (p.head_dim == 64)
+      append_q8_kernel<64, kCodeInt8><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+    else
+      append_q8_kernel<128, kCodeInt8><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -29,11 +29,11 @@ struct pa_block_allocator {
 namespace {
 
 // Bytes of one page in every layer's K and V pools (16-bit elements), or in
-// the INT8 cache (codes plus one fp32 scale per row).
+// an 8-bit cache (INT8 or E4M3 codes plus one fp32 scale per row).
 int64_t page_bytes(const pa_shape_t* s, int32_t num_layers, int32_t kv_kind) {
   const int64_t rows = (int64_t)s->num_kv_heads * s->page_size;
   const int64_t d = s->head_dim;
-  const int64_t per_row = kv_kind == PA_KV_INT8 ? d + 4 : 2 * d;
+  const int64_t per_row = kv_kind == PA_KV_16BIT ? 2 * d : d + 4;
   return 2 * rows * per_row * num_layers;
 }
 
@@ -43,7 +43,8 @@ extern "C" int64_t pa_profile_num_blocks(const pa_shape_t* shape, int32_t num_la
                                          int32_t kv_kind, size_t free_bytes,
                                          size_t reserve_bytes) {
   if (!shape || shape->num_kv_heads <= 0 || shape->head_dim <= 0 || shape->page_size <= 0 ||
-      num_layers <= 0 || (kv_kind != PA_KV_16BIT && kv_kind != PA_KV_INT8))
+      num_layers <= 0 ||
+      (kv_kind != PA_KV_16BIT && kv_kind != PA_KV_INT8 && kv_kind != PA_KV_FP8))
     return -1;
   if (free_bytes <= reserve_bytes) return 0;
   const size_t per_page = (size_t)page_bytes(shape, num_layers, kv_kind);

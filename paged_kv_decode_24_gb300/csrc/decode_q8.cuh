@@ -1,5 +1,8 @@
-// Split decode attention over an INT8 paged KV cache with per-row fp32
-// scales (MonadKai/xLLM, introduction: KV-cache quantisation, per-row INT8).
+// Split decode attention over an 8-bit paged KV cache with per-row fp32
+// scales: INT8 codes (MonadKai/xLLM, introduction: KV-cache quantisation,
+// per-row INT8) or E4M3 bytes ("Eine LLM-Inferenz-Engine von Grund auf mit
+// C++ und CUDA bauen", section 4: FP8 quantisation of the cache), the FMT
+// template parameter (kCodeInt8, kCodeE4m3).
 //
 // Tasks, CTA shapes, the per-warp copy ring, the fused append, the in-CTA
 // merge and the split partials are those of decode_tc.cuh; what differs is
@@ -13,7 +16,9 @@
 //
 // The int8 codes become fp16 in registers: with its sign bit flipped a byte
 // is b + 128, and placed under the fp16 exponent of 1024 it reads
-// 1152 + b, exactly.  One byte permute makes two such halves.
+// 1152 + b, exactly.  One byte permute makes two such halves.  E4M3 bytes
+// become fp16 by the hardware conversion of a byte pair (exact: every E4M3
+// value is an fp16 value); they carry no bias.
 //
 // Products, for the 16 tokens of a page and the G <= 8 query heads of the KV
 // head (padded to 8), g = lane / 4 and t = lane % 4:
@@ -24,15 +29,17 @@
 //       g+8) per 16-dim step, so the reduction order is permuted to logical
 //       k (2t, 2t+1) = dims 4t, 4t+1 and (2t+8, 2t+9) = dims 4t+2, 4t+3, and
 //       q is loaded the same way.  The bias 1152 * sum_d q_d of each head is
-//       one product of the same shape, made once per task and subtracted;
-//       then row t of S^T is multiplied by its K scale.
+//       one product of the same shape, made once per task and subtracted
+//       (INT8 only); then row t of S^T is multiplied by its K scale.
 //
 //   O^T[D x 8] += V_codes^T[D x 16 tok] . P'^T[16 tok x 8]
 //       D/16 m-tiles x 2 mma.m16n8k16.  ldmatrix.trans on 2-byte elements
 //       of the row-major V tile gives a thread tokens 2t, 2t+1 of dims 2g,
 //       2g+1; one byte permute per dim pairs the two tokens, so m-tile row
 //       g is dim 2g and row g+8 is dim 2g+1 of its 16 dims.  The V codes
-//       are exact fp16 integers after subtracting 1152.
+//       are exact fp16 integers after subtracting 1152 (INT8).  An E4M3 byte
+//       may be NaN, so on a page the sequence ends in, the E4M3 V codes of
+//       rows past the end are zeroed before the conversion.
 //
 // P' = p * s_v / R carries each token's V scale: R is the largest V scale
 // the warp has met so far, so P' <= 1 stays in the normal fp16 range, and
@@ -45,6 +52,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "decode_tc.cuh"
 #include "quant_common.cuh"
@@ -109,7 +118,7 @@ struct Q8Layout {
 // R is replaced only when a page's largest V scale exceeds 2 R.
 constexpr float kLazyLog2 = 8.f;
 
-template <int D, int G, int NW, int NS>
+template <int D, int G, int NW, int NS, int FMT>
 __global__ void __launch_bounds__(NW * 32, 4)
     split_decode_q8_kernel(const __grid_constant__ SplitParams p) {
   static_assert(G <= 8, "the mma tile holds at most 8 query heads");
@@ -218,8 +227,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
       k_app = (j_app - pstart) / pstride;
       const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
       float sk, sv;
-      const uint32_t ck = quantize_row_warp<D>(static_cast<const __half*>(p.k_new) + src, lane, sk);
-      const uint32_t cv = quantize_row_warp<D>(static_cast<const __half*>(p.v_new) + src, lane, sv);
+      const uint32_t ck =
+          quantize_row_warp<D, FMT>(static_cast<const __half*>(p.k_new) + src, lane, sk);
+      const uint32_t cv =
+          quantize_row_warp<D, FMT>(static_cast<const __half*>(p.v_new) + src, lane, sv);
       if constexpr (D == 128) {
         reinterpret_cast<uint32_t*>(nrow)[lane] = ck;
         reinterpret_cast<uint32_t*>(nrow + D)[lane] = cv;
@@ -254,10 +265,12 @@ __global__ void __launch_bounds__(NW * 32, 4)
       }
     }
     float cb[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t k1152 = 0x64806480u;
+    if constexpr (FMT == kCodeInt8) {
+      const uint32_t k1152 = 0x64806480u;
 #pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk)
-      mma_16816(cb, k1152, k1152, k1152, k1152, qb[kk][0], qb[kk][1]);
+      for (int kk = 0; kk < KSTEPS; ++kk)
+        mma_16816(cb, k1152, k1152, k1152, k1152, qb[kk][0], qb[kk][1]);
+    }
     cb0 = cb[0];
     cb1 = cb[1];
   }
@@ -393,10 +406,19 @@ __global__ void __launch_bounds__(NW * 32, 4)
         // r[0], r[1]: tokens g, g+8 of step kk; r[2], r[3]: of step kk+1
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t u0 = r[2 * h] ^ 0x80808080u, u1 = r[2 * h + 1] ^ 0x80808080u;
-          mma_16816(c[h], biased_pair<0x4140u>(u0), biased_pair<0x4140u>(u1),
-                    biased_pair<0x4342u>(u0), biased_pair<0x4342u>(u1), qb[kk + h][0],
-                    qb[kk + h][1]);
+          if constexpr (FMT == kCodeE4m3) {
+            // bytes 0, 1: dims 4t, 4t+1 (logical k 2t, 2t+1); bytes 2, 3: dims
+            // 4t+2, 4t+3 (logical k 2t+8, 2t+9)
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_half2x2(r[2 * h], a0, a2);
+            e4m3x4_to_half2x2(r[2 * h + 1], a1, a3);
+            mma_16816(c[h], a0, a1, a2, a3, qb[kk + h][0], qb[kk + h][1]);
+          } else {
+            const uint32_t u0 = r[2 * h] ^ 0x80808080u, u1 = r[2 * h + 1] ^ 0x80808080u;
+            mma_16816(c[h], biased_pair<0x4140u>(u0), biased_pair<0x4140u>(u1),
+                      biased_pair<0x4342u>(u0), biased_pair<0x4342u>(u1), qb[kk + h][0],
+                      qb[kk + h][1]);
+          }
         }
       }
       const float ks0 = lds_f32(ksc + 4 * g) * qs, ks8 = lds_f32(ksc + 4 * (g + 8)) * qs;
@@ -468,22 +490,51 @@ __global__ void __launch_bounds__(NW * 32, 4)
           __byte_perm(__shfl_sync(kFull, l23, src1), __shfl_sync(kFull, l23, src2), perm);
       // ---- O^T += V_codes^T . P'^T (hi and lo); rows past nvalid have P' = 0
       const uint32_t vaddr = vtile + lm_off;
-#pragma unroll
-      for (int mt = 0; mt < KSTEPS; mt += 2) {
-        uint32_t r[4];
-        ldsm_x4_t_addr(vaddr ^ (uint32_t)(mt << 4), r);
-        // r[0], r[1]: tokens 0-7, 8-15 of m-tile mt; r[2], r[3]: of mt+1.
-        // Each holds tokens 2t, 2t+1 (byte pairs 0,1 and 2,3) of dims 2g, 2g+1.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t u0 = r[2 * h] ^ 0x80808080u, u1 = r[2 * h + 1] ^ 0x80808080u;
-          const uint32_t a0 = sub1152(biased_pair<0x4240u>(u0));  // dim 2g, tokens 2t, 2t+1
-          const uint32_t a1 = sub1152(biased_pair<0x4341u>(u0));  // dim 2g+1
-          const uint32_t a2 = sub1152(biased_pair<0x4240u>(u1));  // dim 2g, tokens 2t+8, 2t+9
-          const uint32_t a3 = sub1152(biased_pair<0x4341u>(u1));
-          mma_16816(o[mt + h], a0, a1, a2, a3, pb_hi0, pb_hi1);
-          mma_16816(o[mt + h], a0, a1, a2, a3, pb_lo0, pb_lo1);
+      // r[0], r[1] of an m-tile: tokens 0-7, 8-15; each holds tokens 2t, 2t+1
+      // (byte pairs 0,1 and 2,3) of dims 2g, 2g+1.  tail: E4M3 bytes of rows
+      // past nvalid (which may be NaN) are zeroed first.
+      auto pv = [&](auto tail) {
+        uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+        if constexpr (decltype(tail)::value) {
+          vm0 = (2 * t < nvalid ? 0x0000ffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+          vm1 = (2 * t + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
         }
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; mt += 2) {
+          uint32_t r[4];
+          ldsm_x4_t_addr(vaddr ^ (uint32_t)(mt << 4), r);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (FMT == kCodeE4m3) {
+              uint32_t w0 = r[2 * h], w1 = r[2 * h + 1];
+              if constexpr (decltype(tail)::value) {
+                w0 &= vm0;
+                w1 &= vm1;
+              }
+              // bytes (0, 2) are dim 2g of tokens 2t, 2t+1; bytes (1, 3) dim 2g+1
+              // a0: dim 2g, tokens 2t, 2t+1; a1: dim 2g+1; a2, a3: tokens 2t+8, 2t+9
+              e4m3x4_to_half2x2(__byte_perm(w0, 0u, 0x3120u), a0, a1);
+              e4m3x4_to_half2x2(__byte_perm(w1, 0u, 0x3120u), a2, a3);
+            } else {
+              const uint32_t u0 = r[2 * h] ^ 0x80808080u, u1 = r[2 * h + 1] ^ 0x80808080u;
+              a0 = sub1152(biased_pair<0x4240u>(u0));  // dim 2g, tokens 2t, 2t+1
+              a1 = sub1152(biased_pair<0x4341u>(u0));  // dim 2g+1
+              a2 = sub1152(biased_pair<0x4240u>(u1));  // dim 2g, tokens 2t+8, 2t+9
+              a3 = sub1152(biased_pair<0x4341u>(u1));
+            }
+            mma_16816(o[mt + h], a0, a1, a2, a3, pb_hi0, pb_hi1);
+            mma_16816(o[mt + h], a0, a1, a2, a3, pb_lo0, pb_lo1);
+          }
+        }
+      };
+      if constexpr (FMT == kCodeE4m3) {
+        if (nvalid < kPageSize)
+          pv(std::true_type{});
+        else
+          pv(std::false_type{});
+      } else {
+        pv(std::false_type{});
       }
     }
     // the stage is free: refill it

@@ -14,7 +14,7 @@ cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = Q8Layout<D, kWarpsPerCta, NS>::BYTES;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
   static std::atomic<unsigned long long> configured{0};
-  auto kern = split_decode_q8_kernel<D, G, kWarpsPerCta, NS>;
+  auto kern = split_decode_q8_kernel<D, G, kWarpsPerCta, NS, kCodeInt8>;
   return launch_split_kernel(kern, smem, configured, p, grid, stream);
 }
 

@@ -35,6 +35,8 @@ struct AppendParams {
   int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
 };
 
+// Append into an 8-bit cache: INT8 codes or E4M3 bytes (fmt: kCodeInt8 or
+// kCodeE4m3, quant_common.cuh), with their per-row fp32 scales.
 struct AppendQ8Params {
   const __half* k_new;
   const __half* v_new;
@@ -46,6 +48,7 @@ struct AppendQ8Params {
   const int32_t* seq_lens;
   int32_t* status;
   int32_t batch, num_kv_heads, head_dim, max_pages, num_pages;
+  int32_t fmt;
 };
 
 struct CopyBlocksParams {
@@ -85,7 +88,7 @@ cudaError_t launch_prefill_tc5_d128(const PrefillParams& p, int group, int dtype
                                     cudaStream_t stream);
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
-cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int grid,
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int grid,
                             cudaStream_t stream);
 cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,

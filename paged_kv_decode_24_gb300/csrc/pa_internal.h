@@ -32,6 +32,10 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // a plan's wait limit of 0 
 // The wait limit a kernel uses for a plan's wait_limit_ns (0: the default).
 inline uint64_t wait_limit_or_default(uint64_t ns) { return ns ? ns : kDefaultWaitNs; }
 
+// Code formats of the 8-bit caches (per-row fp32 scales in both).
+constexpr int kCodeInt8 = 0;  // two's-complement int8 codes
+constexpr int kCodeE4m3 = 1;  // OCP E4M3 bytes
+
 // Item flags live in the top bits of the kv_head word.
 constexpr uint32_t kItemSplit = 0x80000000u;  // writes a partial (o, lse) instead of out
 constexpr uint32_t kItemLast = 0x40000000u;   // last page range of its sequence

@@ -37,7 +37,8 @@ class DeviceDecode:
         self.v_pages = te(w.v_pages)
         self.block_table = t(w.block_table)
         self.seq_lens = t(w.seq_lens)
-        self.q8 = w.k_codes is not None   # the workload also carries an INT8 cache
+        self.q8 = w.k_codes is not None   # the workload also carries an 8-bit cache
+        self.kv = w.kv                    # its format: "int8" or "fp8"
         if self.q8:
             self.k_codes = t(w.k_codes)
             self.v_codes = t(w.v_codes)
@@ -111,6 +112,40 @@ class DeviceDecode:
                                  self.block_table, self.seq_lens, self.w.scale, dst,
                                  self.workspace, self.status)
         return dst
+
+    def append_fp8(self):
+        binding.append_fp8(self.shape, self.k_new, self.v_new, self.k_codes, self.v_codes,
+                           self.k_scales, self.v_scales, self.block_table, self.seq_lens,
+                           self.status)
+
+    def decode_fp8(self, out=None):
+        if self.plan_obj is None:
+            self.make_plan()
+        dst = self.out if out is None else out
+        binding.decode_fp8(self.shape, self.plan_obj, self.q, self.k_codes, self.v_codes,
+                           self.k_scales, self.v_scales, self.block_table, self.seq_lens,
+                           self.w.scale, dst, self.workspace, self.status)
+        return dst
+
+    def append_decode_fp8(self, out=None):
+        if self.plan_obj is None:
+            self.make_plan()
+        dst = self.out if out is None else out
+        binding.append_decode_fp8(self.shape, self.plan_obj, self.q, self.k_new, self.v_new,
+                                  self.k_codes, self.v_codes, self.k_scales, self.v_scales,
+                                  self.block_table, self.seq_lens, self.w.scale, dst,
+                                  self.workspace, self.status)
+        return dst
+
+    # the 8-bit cache the workload carries (INT8 or FP8)
+    def append8(self):
+        return self.append_fp8() if self.kv == "fp8" else self.append_q8()
+
+    def decode8(self, out=None):
+        return self.decode_fp8(out) if self.kv == "fp8" else self.decode_q8(out)
+
+    def append_decode8(self, out=None):
+        return self.append_decode_fp8(out) if self.kv == "fp8" else self.append_decode_q8(out)
 
     # ---- several query tokens per sequence (workloads made with q_lens)
 

@@ -137,7 +137,8 @@ def test_library_grow_and_page_count(lib):
     with pytest.raises(binding.PagedAttnError) as e:
         binding.BlockAllocator(1).grow(np.full(4, -1, np.int32), 16, 0, 40)   # pool short
     assert e.value.code == 7
-    for kv, kind, d in ((binding.PA_KV_16BIT, "16bit", 128), (binding.PA_KV_INT8, "int8", 64)):
+    for kv, kind, d in ((binding.PA_KV_16BIT, "16bit", 128), (binding.PA_KV_INT8, "int8", 64),
+                        (binding.PA_KV_FP8, "fp8", 128)):
         s = binding.make_shape(4, 32, 8, d, 16, 64, 100)
         for free, reserve in ((80 * 2**30, 2**30), (12345678, 0), (10, 20)):
             assert binding.profile_num_blocks(s, 32, kv, free, reserve) == \
