@@ -18,6 +18,7 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.cache8 import oracle_append_decode
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -73,15 +74,14 @@ def test_two_kernel_form_matches_oracle(case):
         outs[merge] = first
 
 
-def test_two_kernel_form_int8_cache():
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_two_kernel_form_8bit_cache(kv):
     w = workloads.make_custom(seq_lens=[700, 33, 1024], num_q_heads=32, num_kv_heads=8,
-                              head_dim=128, seed=83, kv="int8", forced_splits=4)
+                              head_dim=128, seed=83, kv=kv, forced_splits=4)
     dd = DeviceDecode(w)
     dd.make_plan(merge="combine")
-    dd.append_q8()
-    got = dd.decode_q8().cpu().numpy()
+    dd.append8()
+    got = dd.decode8().cpu().numpy()
     assert dd.read_status() == 0
-    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
-                                         w.v_new, w.block_table, w.seq_lens)
-    want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
-    assert_close(got, want, "combine kernel, INT8 cache")
+    want, _ = oracle_append_decode(w)
+    assert_close(got, want, f"combine kernel, {kv} cache")

@@ -14,6 +14,7 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.cache8 import oracle_append_decode
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -31,25 +32,23 @@ def _lib(lib):
 LONG = 131072
 
 
-@pytest.mark.parametrize("hq,hkv,kv", [(8, 8, "fp16"), (16, 2, "fp16"), (8, 2, "int8")])
+@pytest.mark.parametrize("hq,hkv,kv", [(8, 8, "fp16"), (16, 2, "fp16"), (8, 2, "int8"),
+                                       (8, 8, "fp8")])
 def test_131072_token_context(hq, hkv, kv):
     w = workloads.make_custom(seq_lens=[LONG, 77], num_q_heads=hq, num_kv_heads=hkv,
                               head_dim=128, seed=8000 + hq + hkv, kv=kv)
     dd = DeviceDecode(w)
     dd.make_plan(waves=2)
     assert dd.plan_obj.c.max_splits >= 100
-    if kv == "int8":
-        dd.append_q8()
-        got = dd.decode_q8().cpu().numpy()
+    if kv in ("int8", "fp8"):
+        dd.append8()
+        got = dd.decode8().cpu().numpy()
     else:
         dd.append()
         got = dd.decode().cpu().numpy()
     assert dd.read_status() == 0
-    if kv == "int8":
-        kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales,
-                                             w.k_new, w.v_new, w.block_table, w.seq_lens)
-        want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens,
-                                          w.scale)
+    if kv in ("int8", "fp8"):
+        want, _ = oracle_append_decode(w)
     else:
         kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
                                   w.seq_lens)

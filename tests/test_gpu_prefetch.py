@@ -16,6 +16,7 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import binding, workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.cache8 import oracle_append_decode
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -54,18 +55,17 @@ def test_prefetch_setting_matches_oracle(case, opts):
     assert_close(got, oracle_step(w), f"prefetch {opts} {case}")
 
 
-def test_widest_prefetch_int8_cache():
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_widest_prefetch_8bit_cache(kv):
     w = workloads.make_custom(seq_lens=[700, 33, 1024], num_q_heads=32, num_kv_heads=8,
-                              head_dim=128, seed=71, kv="int8")
+                              head_dim=128, seed=71, kv=kv)
     dd = DeviceDecode(w)
     dd.make_plan(**WIDEST)
-    dd.append_q8()
-    got = dd.decode_q8().cpu().numpy()
+    dd.append8()
+    got = dd.decode8().cpu().numpy()
     assert dd.read_status() == 0
-    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
-                                         w.v_new, w.block_table, w.seq_lens)
-    want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
-    assert_close(got, want, "prefetch int8")
+    want, _ = oracle_append_decode(w)
+    assert_close(got, want, f"prefetch {kv}")
 
 
 def test_widest_prefetch_skips_a_bad_entry():

@@ -19,6 +19,7 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import binding, workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.cache8 import oracle_append_decode
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -87,21 +88,20 @@ def test_mixed_task_forms_merge_to_oracle_and_same_bits(num_q_heads, dtype):
     assert np.all(counters(dd) == 0)
 
 
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
 @pytest.mark.parametrize("num_q_heads", [4, 16])
-def test_mixed_task_forms_int8_cache(num_q_heads):
-    w = mixed_workload(num_q_heads, kv="int8", seed=73)
+def test_mixed_task_forms_8bit_cache(num_q_heads, kv):
+    w = mixed_workload(num_q_heads, kv=kv, seed=73)
     dd = DeviceDecode(w, num_sms=1)
-    dd.append_q8()
+    dd.append8()
     dd.make_plan()
     assert mixed_groups(dd.plan_obj)
-    first = dd.decode_q8().clone()
+    first = dd.decode8().clone()
     assert dd.read_status() == 0
-    kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales, w.k_new,
-                                         w.v_new, w.block_table, w.seq_lens)
-    want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.scale)
-    assert_close(first.cpu().numpy(), want, "mixed task forms, INT8 cache")
+    want, _ = oracle_append_decode(w)
+    assert_close(first.cpu().numpy(), want, f"mixed task forms, {kv} cache")
     for _ in range(20):
-        assert torch.equal(dd.decode_q8().view(torch.int16), first.view(torch.int16))
+        assert torch.equal(dd.decode8().view(torch.int16), first.view(torch.int16))
     assert np.all(counters(dd) == 0)
 
 

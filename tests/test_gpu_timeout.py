@@ -26,6 +26,7 @@ import pytest
 import oracle
 from paged_kv_decode_24_gb300 import binding, workloads
 from paged_kv_decode_24_gb300.runner import DeviceDecode
+from tests.cache8 import oracle_append_decode
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -65,6 +66,7 @@ DECODE = [
     ("gqa4_tensor_cores", 16, 4, "fp16", "split"),
     ("gqa4_combine_kernel", 16, 4, "fp16", "combine"),
     ("int8_cache", 16, 4, "int8", "split"),
+    ("fp8_cache", 16, 4, "fp8", "split"),
 ]
 
 
@@ -75,13 +77,10 @@ def test_decode_wait_limit_runs_out(case):
     w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
                               seed=zlib.crc32(name.encode()) ^ 5, kv=kv, forced_splits=0)
     dd = DeviceDecode(w)
-    if kv == "int8":
-        dd.append_q8()
-        kc, vc, ks, vs = oracle.kv_append_q8(w.k_codes, w.v_codes, w.k_scales, w.v_scales,
-                                             w.k_new, w.v_new, w.block_table, w.seq_lens)
-        want = oracle.decode_attention_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens,
-                                          w.scale)
-        call = dd.decode_q8
+    if kv in ("int8", "fp8"):
+        dd.append8()
+        want, _ = oracle_append_decode(w)
+        call = dd.decode8
     else:
         dd.append()
         kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
