@@ -117,7 +117,7 @@ def parse():
                          "several query tokens per sequence (--config 1 or 2 picks the "
                          "multi-token workload)")
     ap.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16",
-                    help="element type of q, K, V and out (the INT8 cache takes fp16)")
+                    help="element type of q, K, V and out (the 8-bit caches take fp16)")
     ap.add_argument("--layers", type=int, default=MODEL_LAYERS,
                     help="per-layer KV caches; fewer only to shrink profiler captures")
     ap.add_argument("--splits", type=int, default=None,

@@ -90,7 +90,7 @@ typedef struct {
   int32_t num_pages;         /* P: pages in each pool */
   int32_t dtype;             /* element type of q, k_new, v_new, the pools and out:
                                 PA_DTYPE_F16 (0, the default of a zeroed struct) or
-                                PA_DTYPE_BF16 (1); the INT8-cache calls take F16 only */
+                                PA_DTYPE_BF16 (1); the INT8- and FP8-cache calls take F16 only */
 } pa_shape_t;
 
 #define PA_DTYPE_F16 0
@@ -552,8 +552,8 @@ pa_status_t pa_block_table_grow(pa_block_allocator_t* allocator, int32_t* row, i
  *
  * pairs: device (or mapped) int32 [n][2] = (src block, dst block), 8-byte
  * aligned.  Pools 16-byte aligned; block_bytes a positive multiple of 16
- * (a 16-bit pool's block is Hkv * 16 * D * 2 bytes; an INT8 code pool's
- * Hkv * 16 * D; a scale pool's Hkv * 16 * 4).  No block may be both read
+ * (a 16-bit pool's block is Hkv * 16 * D * 2 bytes; an INT8 or E4M3 code
+ * pool's Hkv * 16 * D; a scale pool's Hkv * 16 * 4).  No block may be both read
  * and written by one call, and destinations must be distinct.  A pair with
  * an index outside [0, src_blocks) or [0, dst_blocks) is skipped and sets
  * PA_DEV_BAD_PAGE in *dev_status.  n = 0 launches nothing. */

@@ -97,7 +97,7 @@ static bool encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// An INT8 code pool [P][Hkv][16][D] as a 4-D tensor with one box per
+// An 8-bit code pool (INT8 or E4M3) [P][Hkv][16][D] as a 4-D tensor with one box per
 // (page, head) tile: D bytes x 16 rows, 128-byte swizzle for D = 128 and
 // 64-byte swizzle for D = 64 (a row is never wider than its swizzle span).
 static bool encode_code_map(CUtensorMap* map, const void* pool, const pa_shape_t& s) {
@@ -160,7 +160,7 @@ extern "C" const char* pa_status_string(pa_status_t status) {
     case PA_ERR_INVALID_ARG: return "invalid argument";
     case PA_ERR_UNSUPPORTED:
       return "unsupported shape (head_dim 64/128, page_size 16, Hq/Hkv in 1,2,4,8, "
-             "dtype f16/bf16; INT8 cache f16 only)";
+             "dtype f16/bf16; 8-bit caches f16 only)";
     case PA_ERR_WORKSPACE: return "workspace smaller than the plan requires";
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_DEVICE_OOB: return "device detected an out-of-range index";

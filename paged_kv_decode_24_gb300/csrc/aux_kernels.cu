@@ -1,4 +1,4 @@
-// The stand-alone split combine, KV append (fp16 and INT8 caches), the
+// The stand-alone split combine, KV append (fp16, INT8 and FP8 caches), the
 // multi-token append, the block copy and the debug gather-index export.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

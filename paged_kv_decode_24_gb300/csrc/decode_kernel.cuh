@@ -61,7 +61,7 @@
 namespace pa {
 
 // Element pointers (q, pools, new rows, out) hold the kernel's element type
-// (fp16 or bf16; fp16 for the INT8-cache kernel's q, new rows and out).
+// (fp16 or bf16; fp16 for the 8-bit-cache kernel's q, new rows and out).
 struct SplitParams {
   const void* q;
   const void* k_pages;
@@ -85,8 +85,9 @@ struct SplitParams {
   int32_t num_shared;  // CTAs [0, num_shared) share a task; the rest run up to NW short tasks
   CUtensorMap tmap_k;  // pools as 4-D tensors [P][Hkv][16][D] for the TMA tensor copies
   CUtensorMap tmap_v;
-  // INT8 cache (split_decode_q8_kernel only): codes [P][Hkv][16][D] and
-  // per-row scales [P][Hkv][16]; the fused append writes them.
+  // 8-bit cache (split_decode_q8_kernel only): INT8 codes or E4M3 bytes
+  // [P][Hkv][16][D] and per-row scales [P][Hkv][16]; the fused append
+  // writes them.
   const int8_t* k_codes;
   const int8_t* v_codes;
   const float* k_scales;

@@ -93,7 +93,7 @@ __device__ __forceinline__ uint32_t q8_swz(int row, int x) {
     return (uint32_t)(row * 64 + (((x >> 4) ^ ((row >> 1) & 3)) << 4) + (x & 15));
 }
 
-// Shared memory of the INT8 kernel, per CTA: NW rings of NS page stages
+// Shared memory of the 8-bit kernel, per CTA: NW rings of NS page stages
 // (K code tile, then V code tile; 1024-aligned for the swizzle), then per
 // warp NS mbarriers, NS page ids, NS scale blocks (16 K then 16 V row
 // scales) and the new row's codes and scales (fused append).

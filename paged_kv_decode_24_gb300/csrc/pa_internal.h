@@ -43,7 +43,7 @@ constexpr uint32_t kItemHeadMask = 0x0000ffffu;
 
 // Per-warp ring depth in half-stages (one K or V tile of one page each).
 PA_HD constexpr int half_stages_for(int head_dim) { return head_dim == 64 ? 6 : 3; }
-// The INT8 cache's ring holds whole pages (K and V code tiles and their
+// The 8-bit caches' ring holds whole pages (K and V code tiles and their
 // row scales on one barrier): 3 pages of D = 128 or 6 of D = 64 keep about
 // 12 KB per warp in flight, as the fp16 ring does.
 PA_HD constexpr int q8_page_stages_for(int head_dim) { return head_dim == 64 ? 6 : 3; }

@@ -2,7 +2,7 @@
 
 Moves a host workload into torch CUDA tensors once, then issues
 pa_kv_append / pa_plan / pa_plan_upload / pa_decode_attention (and their
-INT8-cache forms when the workload carries one) through ``binding``.  It
+8-bit-cache forms, INT8 or FP8, when the workload carries one) through ``binding``.  It
 holds no arithmetic of its own.
 """
 
