@@ -8,6 +8,7 @@ Argument errors are rejected before any CUDA call.
 from __future__ import annotations
 
 import ctypes
+import types
 
 import numpy as np
 import pytest
@@ -442,3 +443,41 @@ def test_static_entry_checks_before_anything_is_queued(lib):
     # batch 0 with its own plan: nothing to do
     p0 = binding.Plan(s0, np.zeros(0, np.int32), 152)
     assert call(s0, p0) == 0
+
+
+def test_one_wave_split_rule(lib):
+    """The automatic split size is the average page load of a resident CTA,
+    never under 48 pages: chunk = max(48, ceil(units / (SMs * r))) with r
+    resident CTAs per SM, the same r that option waves = 2 halves.  Every
+    sequence is cut into ceil(pages / chunk) ranges of at most chunk pages."""
+    # workload 4: every (sequence, KV head) is shorter than that load, so no split
+    w4 = workloads.make_config(4)
+    p4 = binding.Plan(_shape(w4), w4.seq_lens, 152)
+    assert p4.c.num_groups == 0 and p4.c.num_work_items == w4.batch * w4.num_kv_heads
+    rng = np.random.default_rng(5)
+    for trial in range(16):
+        B = int(rng.integers(1, 48))
+        lens = rng.integers(1, 24000, size=B).astype(np.int32)
+        hkv = int(rng.choice([1, 2, 8, 32]))
+        hq = hkv * int(rng.choice([1, 2, 4, 8]))
+        d = int(rng.choice([64, 128]))
+        max_pages = int(lens.max() + 15) // 16
+        shape = binding.make_shape(B, hq, hkv, d, 16, max_pages, max_pages * B)
+        # only the plan is made: the shape and lengths, no pools
+        w = types.SimpleNamespace(page_size=16, batch=B, num_kv_heads=hkv, seq_lens=lens)
+        sms = int(rng.choice([8, 40, 152]))
+        p1 = binding.Plan(shape, lens, sms)
+        p2 = binding.Plan(shape, lens, sms, options=binding.plan_options(waves=2))
+        units = int(sum(max(1, (int(L) + 15) // 16) for L in lens)) * hkv
+        fits = [r for r in range(1, 17)
+                if p1.c.chunk_pages == max(48, -(-units // (sms * r)))
+                and p2.c.chunk_pages == max(48, -(-units // (2 * sms * r)))]
+        assert fits, (trial, p1.c.chunk_pages, p2.c.chunk_pages, units, sms)
+        items, _ = check_plan_covers(w, p1)
+        assert np.all(items[:, 3] - items[:, 2] <= p1.c.chunk_pages)
+        per_seq = {}
+        for b, hw, lo, hi in items:
+            per_seq[(int(b), int(hw) & 0xFFFF)] = per_seq.get((int(b), int(hw) & 0xFFFF), 0) + 1
+        for (b, h), n in per_seq.items():
+            pages = max(1, (int(lens[b]) + 15) // 16)
+            assert n == min(1024, -(-pages // p1.c.chunk_pages)) or (int(lens[b]) == 0 and n == 1)
