@@ -1,9 +1,13 @@
 /* The decode path driven from plain C through the C ABI, on a GPU: device
  * buffers from the CUDA runtime, pa_kv_append, pa_plan, pa_plan_upload and
- * pa_decode_attention on one stream.  Every sequence holds one token (the
- * one appended), so each query head's softmax is a single weight 1 and its
- * output must be exactly the new V row of its KV head (a closed form; the
- * values are exact in fp16).  Exit status 0 on success. */
+ * pa_decode_attention on one stream, then pa_append_decode_attention_fp8
+ * over an FP8 (E4M3) cache with the same plan.  Every sequence holds one
+ * token (the one appended), so each query head's softmax is a single weight
+ * 1 and its output must be exactly the new V row of its KV head (a closed
+ * form; the values are exact in fp16, and for the FP8 cache the V rows are
+ * E4M3 values times 2^-7 with largest magnitude 448 * 2^-7, so the row's
+ * scale is 2^-7 and its codes dequantise exactly).  Exit status 0 on
+ * success. */
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -103,6 +107,51 @@ int main(void) {
     for (int h = 0; h < HQ; ++h)
       for (int d = 0; d < D; ++d)
         if (out[b][h][d] != vn[b][h / (HQ / HKV)][d]) ++bad;
+
+  /* FP8 cache: V rows (256 + 32 * (d % 7)) / 128, i.e. E4M3 values 256..448
+   * times 2^-7, so max|v| / 448 = 2^-7 exactly and every code is exact */
+  static uint16_t vn8[B][HKV][D];
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < HKV; ++h)
+      for (int d = 0; d < D; ++d) vn8[b][h][d] = half_bits((float)(256 + 32 * (d % 7)) / 128.0f);
+  void *dvn8, *dkc, *dvc, *dks, *dvs;
+  const size_t codes = (size_t)P * HKV * S * D, scales = (size_t)P * HKV * S * 4;
+  CUDA_OK(cudaMalloc(&dvn8, sizeof(vn8)));
+  CUDA_OK(cudaMalloc(&dkc, codes));
+  CUDA_OK(cudaMalloc(&dvc, codes));
+  CUDA_OK(cudaMalloc(&dks, scales));
+  CUDA_OK(cudaMalloc(&dvs, scales));
+  CUDA_OK(cudaMemset(dkc, 0, codes));
+  CUDA_OK(cudaMemset(dvc, 0, codes));
+  CUDA_OK(cudaMemset(dks, 0, scales));
+  CUDA_OK(cudaMemset(dvs, 0, scales));
+  CUDA_OK(cudaMemcpy(dvn8, vn8, sizeof(vn8), cudaMemcpyHostToDevice));
+  CUDA_OK(cudaMemset(dout, 0, sizeof(out)));
+  if (pa_append_decode_attention_fp8(&s, &plan, dq, dkn, dvn8, dkc, dvc, (float*)dks, (float*)dvs,
+                                     dbt, dsl, 0.125f, dout, ws, plan.workspace_bytes, dst,
+                                     st) != PA_OK) {
+    fprintf(stderr, "the FP8 call returned an error\n");
+    return 4;
+  }
+  CUDA_OK(cudaStreamSynchronize(st));
+  int32_t status8 = -1;
+  CUDA_OK(cudaMemcpy(&status8, dst, 4, cudaMemcpyDeviceToHost));
+  CUDA_OK(cudaMemcpy(out, dout, sizeof(out), cudaMemcpyDeviceToHost));
+  int bad8 = status8 != 0;
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < HQ; ++h)
+      for (int d = 0; d < D; ++d)
+        if (out[b][h][d] != vn8[b][h / (HQ / HKV)][d]) ++bad8;
+  cudaFree(dvn8);
+  cudaFree(dkc);
+  cudaFree(dvc);
+  cudaFree(dks);
+  cudaFree(dvs);
+  if (bad8) {
+    fprintf(stderr, "FP8 cache: status %d, %d outputs differ from their V rows\n", (int)status8,
+            bad8);
+    return 1;
+  }
   pa_plan_free(&plan);
   cudaFree(ws);
   cudaFree(dq);
@@ -119,6 +168,6 @@ int main(void) {
     fprintf(stderr, "status %d, %d outputs differ from their V rows\n", (int)status, bad);
     return 1;
   }
-  printf("decode from C ok\n");
+  printf("decode from C ok (fp16 and FP8 caches)\n");
   return 0;
 }

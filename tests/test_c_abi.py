@@ -35,9 +35,9 @@ def test_header_and_host_calls_from_c(lib, tmp_path):
 
 @pytest.mark.gpu
 def test_decode_from_c_on_gpu(lib, tmp_path):
-    """pa_kv_append -> pa_plan -> pa_plan_upload -> pa_decode_attention from a
-    C program: one token per sequence, so each head's output is exactly the
-    new V row of its KV head."""
+    """pa_kv_append -> pa_plan -> pa_plan_upload -> pa_decode_attention, then
+    pa_append_decode_attention_fp8, from a C program: one token per sequence,
+    so each head's output is exactly the new V row of its KV head."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
