@@ -99,6 +99,11 @@ def parse():
                     help="decode: each model step's graph uploads the next step's plan into a "
                          "second workspace while its layers run (ahead), or its own plan before "
                          "its first layer (inline)")
+    ap.add_argument("--decode-rows", choices=["tiles", "decode-call"], default="tiles",
+                    help="prefill: sequences with one query token go through the multi-token "
+                         "kernel's tiles like the others (tiles), or through "
+                         "pa_append_decode_attention on a second stream while the rest run "
+                         "(decode-call)")
     ap.add_argument("--prefill-rows", type=int, choices=[128, 64], default=128,
                     help="prefill: query rows per tile, 128 for the tcgen05 kernel, 64 for the "
                          "mma.sync kernel (plan option rows_per_tile)")
@@ -1197,18 +1202,34 @@ def run_prefill(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = binding.PrefillPlan(shape, w.seq_lens, w.q_lens, rows_per_tile=args.prefill_rows)
     ws = binding.alloc_workspace(plan, dev)
+    mixed = None
+    if args.decode_rows == "decode-call":
+        from paged_kv_decode_24_gb300.runner import MixedStep
+        mixed = MixedStep(w, dev, rows_per_tile=args.prefill_rows)
+        torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         binding.prefill_upload(plan, ws, stream=stream)
-        binding.append_tokens(shape, plan, kn, vn, *pools[0], bt, sl, ws, status, stream=stream)
-        binding.prefill(shape, plan, q, *pools[0], bt, sl, w.scale, out, ws, status, stream=stream)
+        if mixed is None:
+            binding.append_tokens(shape, plan, kn, vn, *pools[0], bt, sl, ws, status,
+                                  stream=stream)
+            binding.prefill(shape, plan, q, *pools[0], bt, sl, w.scale, out, ws, status,
+                            stream=stream)
+        else:
+            mixed.run(*pools[0], stream=stream)
     stream.synchronize()
+
+    def layer(l):
+        if mixed is None:
+            binding.append_tokens(shape, plan, kn, vn, *pools[l], bt, sl, ws, status)
+            binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status)
+        else:
+            mixed.run(*pools[l], stream=stream)
 
     def capture(nl):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for l in range(nl):
-                binding.append_tokens(shape, plan, kn, vn, *pools[l], bt, sl, ws, status)
-                binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status)
+                layer(l)
         return g
 
     K = args.steps
@@ -1219,13 +1240,17 @@ def run_prefill(args):
         for _ in range(max(1, args.warmup // PREFILL_LAYERS)):
             g_full.replay()
     stream.synchronize()
-    # the split of a step: attention alone, in its own events
+    # the split of a step: attention alone, in its own events (with the
+    # decode call, the whole two-stream step, appends included)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
         for l in range(PREFILL_LAYERS):
-            binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status,
-                            stream=stream)
+            if mixed is None:
+                binding.prefill(shape, plan, q, *pools[l], bt, sl, w.scale, out, ws, status,
+                                stream=stream)
+            else:
+                mixed.run(*pools[l], stream=stream)
         ev[1].record(stream)
     torch.cuda.synchronize()
     attn_ms = ev[0].elapsed_time(ev[1]) / PREFILL_LAYERS
@@ -1244,8 +1269,9 @@ def run_prefill(args):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item()):#x}")
+    st = int(status.item()) | (mixed.read_status() if mixed is not None else 0)
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x}")
     ms = max_over_ranks(start.elapsed_time(end) / K, world, dev)
     value = world * flops / (ms * 1e-3) / 1e12
     try:
@@ -1263,13 +1289,22 @@ def run_prefill(args):
         "data": "synthetic (seeded; shapes and value laws of the workload)",
         "config": {"workload": w.name, "config_id": args.config, "query_rows": rows,
                    "flops_per_step": flops, "tiles": int(plan.c.num_tiles),
-                   "step": "one layer: pa_kv_append_tokens + pa_prefill_attention",
+                   "step": ("one layer: pa_kv_append_tokens + pa_prefill_attention"
+                            if mixed is None else
+                            f"one layer: the {len(mixed.dec)} single-token sequences through "
+                            "pa_append_decode_attention on a second stream, forked from and "
+                            f"joined back into the step's stream, while the other "
+                            f"{len(mixed.pre)} go through pa_kv_append_tokens + "
+                            "pa_prefill_attention"),
                    "launch": f"CUDA graph of {PREFILL_LAYERS} layers' calls over "
                              f"{PREFILL_LAYERS} per-layer KV caches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": ("prefill_kernel (mma.sync m16n8k16, 64-row tiles)"
                                if args.prefill_rows == 64 else
-                               "prefill_tc5_kernel (tcgen05, 128-row tiles)"), "bound": "tensor",
+                               "prefill_tc5_kernel (tcgen05, 128-row tiles)") +
+                              ("" if mixed is None else
+                               " beside split_decode_tc_kernel on a second stream: the whole "
+                               "step, appends included"), "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops (of measured; fp16 has "
@@ -1278,7 +1313,7 @@ def run_prefill(args):
                      "traffic": None, "us_per_launch": round(attn_ms * 1e3, 3)},
         "cpu_baseline": cpu_base,
         "e2e": None,
-        "gpu_launches": 2 * K,
+        "gpu_launches": (2 if mixed is None else 3) * K,
         "clocks": clk,
     }
     if rank == 0:

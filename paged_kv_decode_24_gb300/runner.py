@@ -180,3 +180,103 @@ class DeviceDecode:
     def read_status(self) -> int:
         self.torch.cuda.synchronize(self.device)
         return int(self.status.item())
+
+
+class MixedStep:
+    """A multi-token step whose batch mixes prefill chunks with single-token
+    decodes (swiftLLM's piggybacked prefill and decode), served on two
+    streams as an engine would serve it: the sequences with one query token
+    through pa_append_decode_attention, the others through
+    pa_kv_append_tokens + pa_prefill_attention.  Both parts read and write
+    the same pools through their own rows of the block table (their pages
+    are distinct).  The second stream forks from the caller's stream and
+    joins back into it, so the step is ordered like one call.  This class
+    only selects rows on the host and issues the calls."""
+
+    def __init__(self, w, device="cuda", num_sms=None, rows_per_tile=0):
+        import torch
+        self.torch = torch
+        self.w = w
+        self.device = torch.device(device)
+        elem = torch.bfloat16 if getattr(w, "dtype", "fp16") == "bf16" else torch.float16
+        ql = np.asarray(w.q_lens, np.int64)
+        cu = np.concatenate([[0], np.cumsum(ql)])
+        self.dec = np.nonzero(ql == 1)[0]
+        self.pre = np.nonzero(ql != 1)[0]
+        self.rows_dec = cu[self.dec]
+        self.rows_pre = (np.concatenate([np.arange(cu[b], cu[b + 1]) for b in self.pre])
+                         if len(self.pre) else np.zeros(0, np.int64)).astype(np.int64)
+
+        def t(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
+
+        def te(a):
+            return t(a).to(elem)
+
+        dtype = getattr(w, "dtype", "fp16")
+        if num_sms is None:
+            num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        S, mp = w.page_size, w.max_pages_per_seq
+        # decode part
+        self.shape_d = binding.make_shape(len(self.dec), w.num_q_heads, w.num_kv_heads,
+                                          w.head_dim, S, mp, w.num_pages, dtype)
+        self.q_d = te(w.q[self.rows_dec])
+        self.kn_d, self.vn_d = te(w.k_new[self.rows_dec]), te(w.v_new[self.rows_dec])
+        self.bt_d, self.sl_d = t(w.block_table[self.dec]), t(w.seq_lens[self.dec])
+        self.out_d = torch.empty_like(self.q_d)
+        self.status_d = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.plan_d = binding.Plan(self.shape_d, np.ascontiguousarray(w.seq_lens[self.dec]),
+                                   int(num_sms))
+        self.ws_d = binding.alloc_workspace(self.plan_d, self.device)
+        binding.upload(self.plan_d, self.ws_d)
+        # prefill part
+        self.shape_p = binding.make_shape(len(self.pre), w.num_q_heads, w.num_kv_heads,
+                                          w.head_dim, S, mp, w.num_pages, dtype)
+        self.q_p = te(w.q[self.rows_pre])
+        self.kn_p, self.vn_p = te(w.k_new[self.rows_pre]), te(w.v_new[self.rows_pre])
+        self.bt_p, self.sl_p = t(w.block_table[self.pre]), t(w.seq_lens[self.pre])
+        self.out_p = torch.empty_like(self.q_p)
+        self.status_p = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.plan_p = binding.PrefillPlan(self.shape_p,
+                                          np.ascontiguousarray(w.seq_lens[self.pre]),
+                                          np.ascontiguousarray(w.q_lens[self.pre]),
+                                          rows_per_tile=rows_per_tile)
+        self.ws_p = binding.alloc_workspace(self.plan_p, self.device)
+        binding.prefill_upload(self.plan_p, self.ws_p)
+        self.side = torch.cuda.Stream(device=self.device)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_join = torch.cuda.Event()
+
+    def run(self, k_pages, v_pages, stream=None):
+        """The step over pools (k_pages, v_pages) on `stream` (default: the
+        current stream), the decode part on a second stream in between."""
+        torch = self.torch
+        s0 = torch.cuda.current_stream(self.device) if stream is None else stream
+        self.ev_fork.record(s0)
+        self.side.wait_event(self.ev_fork)
+        if len(self.dec):
+            binding.append_decode(self.shape_d, self.plan_d, self.q_d, self.kn_d, self.vn_d,
+                                  k_pages, v_pages, self.bt_d, self.sl_d, self.w.scale,
+                                  self.out_d, self.ws_d, self.status_d, stream=self.side)
+        if len(self.pre):
+            binding.append_tokens(self.shape_p, self.plan_p, self.kn_p, self.vn_p, k_pages,
+                                  v_pages, self.bt_p, self.sl_p, self.ws_p, self.status_p,
+                                  stream=s0)
+            binding.prefill(self.shape_p, self.plan_p, self.q_p, k_pages, v_pages, self.bt_p,
+                            self.sl_p, self.w.scale, self.out_p, self.ws_p, self.status_p,
+                            stream=s0)
+        self.ev_join.record(self.side)
+        s0.wait_event(self.ev_join)
+
+    def output(self):
+        """Every query row's output, in the batch's row order."""
+        torch = self.torch
+        out = torch.empty((self.w.q.shape[0], self.w.num_q_heads, self.w.head_dim),
+                          dtype=self.q_d.dtype, device=self.device)
+        out[torch.from_numpy(self.rows_dec).to(self.device)] = self.out_d
+        out[torch.from_numpy(self.rows_pre).to(self.device)] = self.out_p
+        return out
+
+    def read_status(self) -> int:
+        self.torch.cuda.synchronize(self.device)
+        return int(self.status_d.item()) | int(self.status_p.item())

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from paged_kv_decode_24_gb300 import binding, workloads
-from paged_kv_decode_24_gb300.runner import DeviceDecode
+from paged_kv_decode_24_gb300.runner import DeviceDecode, MixedStep
 from tests import oracle_pool
 from tests.parity import assert_close
 
@@ -156,3 +156,45 @@ def test_prefill_benchmark_workload_mma_sync():
     assert dd.pf_plan.c.rows_per_tile == 64
     want = oracle_pool.prefill_all(("prefill_config", 2))
     close(got, want, "prefill workload 2 on mma.sync")
+
+
+def _pools_match(dd, w):
+    kp, vp = oracle.kv_append_tokens(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                     w.seq_lens, w.q_lens)
+    ek = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    assert torch.equal(dd.k_pages, torch.from_numpy(kp).to(dd.k_pages.device).to(ek))
+    assert torch.equal(dd.v_pages, torch.from_numpy(vp).to(dd.v_pages.device).to(ek))
+
+
+def test_piggybacked_batch_on_two_streams():
+    """The piggybacked workload served as an engine would: its single-token
+    sequences through pa_append_decode_attention on a second stream, its
+    prefill chunks through pa_kv_append_tokens + pa_prefill_attention.
+    Every output row and every pool row match the oracle of the whole step."""
+    w = workloads.make_prefill_config(2)
+    assert np.sum(w.q_lens == 1) == 56
+    dd = DeviceDecode(w)   # the pools
+    ms = MixedStep(w)
+    ms.run(dd.k_pages, dd.v_pages)
+    assert ms.read_status() == 0
+    got = ms.output().float().cpu().numpy()
+    want = oracle_pool.prefill_all(("prefill_config", 2))
+    close(got, want, "piggybacked batch on two streams, every output")
+    _pools_match(dd, w)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("rows", [128, 64], ids=["tcgen05", "mma_sync"])
+def test_mixed_batch_on_two_streams_small(dtype, rows):
+    """Single-token and multi-token sequences interleaved in one batch (and a
+    sequence with no query), on both multi-token kernels and element types."""
+    w = workloads.make_custom(seq_lens=[700, 33, 260, 1, 1500, 96], q_lens=[1, 33, 1, 1, 200, 0],
+                              num_q_heads=16, num_kv_heads=4, head_dim=128, seed=91, dtype=dtype)
+    dd = DeviceDecode(w)
+    ms = MixedStep(w, rows_per_tile=rows)
+    ms.run(dd.k_pages, dd.v_pages)
+    assert ms.read_status() == 0
+    got = ms.output().float().cpu().numpy()
+    want, _ = oracle_step(w)
+    close(got, want, f"mixed batch on two streams, {dtype}, rows={rows}", dtype=dtype)
+    _pools_match(dd, w)
