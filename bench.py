@@ -10,8 +10,9 @@ the GPU runs the model step before it (the plan depends only on seq_lens,
 which every layer shares).  Inputs are synthetic and seeded, with the
 shapes of the five workloads in paged_kv_decode_24_gb300/workloads.py.  The
 headline is workload 4 (LLaMA-3-8B heads, batch 160, GQA-4, the largest);
-workloads 2, 3 and 5 are timed the same way in the same run and reported
-under per_config.
+workloads 2, 3 and 5, and workload 4 over the INT8 and FP8 caches, are timed
+the same way in the same run and reported under per_config (8-bit lines count
+8-bit bytes).
 
 Each model step (32 layer steps) is one CUDA graph: the plan upload, then
 the 32 layers' calls back to back; K layer steps are timed exactly (a shorter
@@ -32,7 +33,8 @@ The JSON line reports:
                 cpu_baseline_all_cores runs it on every core at once
   plan_host_us  one pa_plan call on the host (not part of the device timing)
   append_us     pa_kv_append alone, as its own launch (the step fuses it)
-  per_config    the other workloads' µs per step, GB/s and roofline fraction
+  per_config    the other workloads' (and the 8-bit caches') µs per step,
+                GB/s and roofline fraction
 
 Each of the 32 layers has its own KV cache (distinct device memory, 2-29 GiB
 in total), so L2 never holds the pages a step reads.
@@ -57,6 +59,7 @@ if "--impl" in _sys.argv and "reference" in _sys.argv:
         _os.environ[_k] = "1"
 
 import argparse
+import copy
 import hashlib
 import json
 import math
@@ -84,10 +87,10 @@ def parse():
     ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5],
                     help="the headline workload (default 4: LLaMA-3-8B heads, batch 160, the "
                          "largest)")
-    ap.add_argument("--also", type=lambda v: [int(x) for x in v.split(",") if x.strip()],
-                    default=None,
+    ap.add_argument("--also", type=parse_also, default=None,
                     help="decode: other workloads timed in the same run and reported under "
-                         "per_config (default 2,3,5 with the default headline; '' for none)")
+                         "per_config, each a workload id or id-kv for an 8-bit cache (default "
+                         "2,3,5,4-int8,4-fp8 with the default headline; '' for none)")
     ap.add_argument("--merge", choices=["split", "combine"], default="split",
                     help="decode: merge split partials in the split kernel (one launch) or in "
                          "a separate combine kernel (plan option merge)")
@@ -130,7 +133,8 @@ def parse():
                          "workload's own (0 = the planner's choice); for experiments")
     args = ap.parse_args()
     if args.also is None:
-        args.also = list(EXTRA_CONFIGS) if args.config == 4 and args.op == "decode" else []
+        args.also = (list(EXTRA_CONFIGS) if args.config == 4 and args.op == "decode" and
+                     args.kv == "fp16" and args.dtype == "fp16" else [])
     return args
 
 
@@ -386,7 +390,23 @@ def job_value(kv_bytes_per_rank, ms_per_step, world):
 
 MODEL_LAYERS = 32   # LLaMA-2-7B and LLaMA-3-8B both have 32 decoder layers
 HOLD_US = 300       # spin before a timed region: longer than the host needs to queue the region
-EXTRA_CONFIGS = (2, 3, 5)   # timed in the same run as the headline workload, reported per config
+# timed in the same run as the headline workload, reported per config: other
+# workloads, and the headline workload over the 8-bit caches
+EXTRA_CONFIGS = ((2, None), (3, None), (5, None), (4, "int8"), (4, "fp8"))
+
+
+def parse_also(v):
+    """'2,3,4-fp8' -> [(2, None), (3, None), (4, 'fp8')]."""
+    out = []
+    for x in v.split(","):
+        x = x.strip()
+        if not x:
+            continue
+        c, _, kv = x.partition("-")
+        if kv and kv not in ("int8", "fp8"):
+            raise argparse.ArgumentTypeError(f"unknown cache {kv!r} in --also")
+        out.append((int(c), kv or None))
+    return out
 
 
 def hold_stream(torch, stream, us=HOLD_US):
@@ -882,13 +902,17 @@ def run_ours(args):
 
     # the other workloads, timed the same way in the same run (K layer steps
     # each, after their own warm-up); reported beside the headline
-    extras = [c for c in (args.also or []) if c != args.config]
+    extras = [(c, kv) for c, kv in (args.also or [])
+              if (c, kv or args.kv) != (args.config, args.kv)]
     if extras:
         del db, graphs_full, graphs_rem, warm_full
         torch.cuda.empty_cache()
         res["per_config"] = {}
-        for c in extras:
-            xb = DecodeBench(args, c, rank, dev, stream, num_sms, LAYERS)
+        for c, kv in extras:
+            xa = copy.copy(args)
+            if kv is not None:
+                xa.kv, xa.dtype = kv, "fp16"
+            xb = DecodeBench(xa, c, rank, dev, stream, num_sms, LAYERS)
             gf, gr = xb.graphs(K)
             wf = gf or [xb.capture(i, LAYERS) for i in range(2)]
             xb.warm(max(args.warmup, LAYERS), wf, gr or wf)
@@ -896,14 +920,14 @@ def run_ours(args):
             ms = max_over_ranks(t_ms / K, world, dev)
             xdist = repeat_regions(xb, K, gf, gr, world, dev)
             ach = xb.dec_bytes / (t_ms / K * 1e-3) / 1e9
-            res["per_config"][str(c)] = {
+            res["per_config"][str(c) if kv is None else f"{c}-{kv}"] = {
                 "workload": xb.workload_name(),
                 "us_per_step": round(ms * 1e3, 3),
                 "value": round(job_value(xb.kv_bytes, ms, world), 2), "unit": "GB/s",
                 "roofline_frac": round(ach / peak, 4),
                 "achieved": round(ach, 1),
                 "algorithmic_bytes_per_launch": xb.dec_bytes,
-                "traffic": traffic_for(c, args.kv, args.dtype, decode_family(xb.w, args.kv)),
+                "traffic": traffic_for(c, xa.kv, xa.dtype, decode_family(xb.w, xa.kv)),
                 "splits": int(xb.plan0.c.max_splits),
                 "gpu_launches": xb.launches_per_step * K,
                 "distribution": xdist,
