@@ -191,9 +191,14 @@ class MixedStep:
     the same pools through their own rows of the block table (their pages
     are distinct).  The second stream forks from the caller's stream and
     joins back into it, so the step is ordered like one call.  This class
-    only selects rows on the host and issues the calls."""
+    only selects rows on the host and issues the calls.
 
-    def __init__(self, w, device="cuda", num_sms=None, rows_per_tile=0):
+    The decode part is planned as if it had a third of the SMs
+    (decode_sms): its plan then cuts fewer splits, so fewer decode CTAs, and
+    the tile CTAs of the other part find shared memory beside them on every
+    SM, so the two parts run at once instead of in turn."""
+
+    def __init__(self, w, device="cuda", num_sms=None, rows_per_tile=0, decode_sms=None):
         import torch
         self.torch = torch
         self.w = w
@@ -225,8 +230,10 @@ class MixedStep:
         self.bt_d, self.sl_d = t(w.block_table[self.dec]), t(w.seq_lens[self.dec])
         self.out_d = torch.empty_like(self.q_d)
         self.status_d = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if decode_sms is None:
+            decode_sms = max(1, int(num_sms) // 3)
         self.plan_d = binding.Plan(self.shape_d, np.ascontiguousarray(w.seq_lens[self.dec]),
-                                   int(num_sms))
+                                   int(decode_sms))
         self.ws_d = binding.alloc_workspace(self.plan_d, self.device)
         binding.upload(self.plan_d, self.ws_d)
         # prefill part
