@@ -232,10 +232,12 @@ class MixedStep:
         self.status_d = torch.zeros(1, dtype=torch.int32, device=self.device)
         if decode_sms is None:
             decode_sms = max(1, int(num_sms) // 3)
-        self.plan_d = binding.Plan(self.shape_d, np.ascontiguousarray(w.seq_lens[self.dec]),
-                                   int(decode_sms))
-        self.ws_d = binding.alloc_workspace(self.plan_d, self.device)
-        binding.upload(self.plan_d, self.ws_d)
+        self.plan_d = self.ws_d = None
+        if len(self.dec):   # an empty part makes no plan and launches nothing
+            self.plan_d = binding.Plan(self.shape_d, np.ascontiguousarray(w.seq_lens[self.dec]),
+                                       int(decode_sms))
+            self.ws_d = binding.alloc_workspace(self.plan_d, self.device)
+            binding.upload(self.plan_d, self.ws_d)
         # prefill part
         self.shape_p = binding.make_shape(len(self.pre), w.num_q_heads, w.num_kv_heads,
                                           w.head_dim, S, mp, w.num_pages, dtype)
@@ -244,12 +246,14 @@ class MixedStep:
         self.bt_p, self.sl_p = t(w.block_table[self.pre]), t(w.seq_lens[self.pre])
         self.out_p = torch.empty_like(self.q_p)
         self.status_p = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.plan_p = binding.PrefillPlan(self.shape_p,
-                                          np.ascontiguousarray(w.seq_lens[self.pre]),
-                                          np.ascontiguousarray(w.q_lens[self.pre]),
-                                          rows_per_tile=rows_per_tile)
-        self.ws_p = binding.alloc_workspace(self.plan_p, self.device)
-        binding.prefill_upload(self.plan_p, self.ws_p)
+        self.plan_p = self.ws_p = None
+        if len(self.pre):
+            self.plan_p = binding.PrefillPlan(self.shape_p,
+                                              np.ascontiguousarray(w.seq_lens[self.pre]),
+                                              np.ascontiguousarray(w.q_lens[self.pre]),
+                                              rows_per_tile=rows_per_tile)
+            self.ws_p = binding.alloc_workspace(self.plan_p, self.device)
+            binding.prefill_upload(self.plan_p, self.ws_p)
         self.side = torch.cuda.Stream(device=self.device)
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()

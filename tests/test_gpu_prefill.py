@@ -198,3 +198,19 @@ def test_mixed_batch_on_two_streams_small(dtype, rows):
     want, _ = oracle_step(w)
     close(got, want, f"mixed batch on two streams, {dtype}, rows={rows}", dtype=dtype)
     _pools_match(dd, w)
+
+
+@pytest.mark.parametrize("q_lens", [[1, 1, 1], [40, 7, 0]], ids=["decodes_only", "prefills_only"])
+def test_mixed_batch_with_one_part_empty(q_lens):
+    """A batch of only single-token sequences, or with none: the empty part
+    makes no plan and launches nothing; the other part matches the oracle."""
+    w = workloads.make_custom(seq_lens=[300, 45, 90], q_lens=q_lens, num_q_heads=8,
+                              num_kv_heads=2, head_dim=128, seed=92)
+    dd = DeviceDecode(w)
+    ms = MixedStep(w)
+    assert (ms.plan_d is None) == (len(ms.dec) == 0) and (ms.plan_p is None) == (len(ms.pre) == 0)
+    ms.run(dd.k_pages, dd.v_pages)
+    assert ms.read_status() == 0
+    want, _ = oracle_step(w)
+    close(ms.output().float().cpu().numpy(), want, f"mixed batch {q_lens}")
+    _pools_match(dd, w)
