@@ -1,5 +1,6 @@
-"""GPU: the Python usage example (examples/decode_step.py) runs as shipped
-and its output matches the float64 oracle."""
+"""GPU: the Python usage examples (examples/decode_step.py,
+examples/serving_loop.py) run as shipped and their outputs match the float64
+oracle."""
 
 from __future__ import annotations
 
@@ -43,3 +44,27 @@ def test_decode_step_example():
     want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
     assert abs(w.scale - w.head_dim ** -0.5) < 1e-12
     assert_close(out.cpu().numpy(), want, "examples/decode_step.py")
+
+
+def test_serving_loop_example():
+    """examples/serving_loop.py: after steps with page allocation, a swap-out
+    and a new sequence, every layer's last-step output matches the oracle
+    over the final pools, the swapped pages came back bit for bit, and the
+    allocator holds exactly the pages no sequence uses."""
+    spec = importlib.util.spec_from_file_location(
+        "serving_loop", os.path.join(ROOT, "examples", "serving_loop.py"))
+    ex = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(ex)
+    r = ex.serve()
+    table, lens = r["block_table"], r["seq_lens"]
+    used = table[table >= 0]
+    assert len(np.unique(used)) == len(used)               # no page in two rows
+    assert r["free"] == r["k_pages"][0].shape[0] - len(used)
+    assert all((table[b] >= 0).sum() == -(-int(L) // ex.PAGE) for b, L in enumerate(lens))
+    host_k, host_v, pages, (dev_k, dev_v) = r["swapped"]
+    assert torch.equal(host_k, dev_k) and torch.equal(host_v, dev_v)
+    for layer, out in enumerate(r["out"]):
+        want = oracle.decode_attention(r["q"][layer].cpu().numpy(),
+                                       r["k_pages"][layer].cpu().numpy(),
+                                       r["v_pages"][layer].cpu().numpy(), table, lens, r["scale"])
+        assert_close(out.cpu().numpy(), want, f"examples/serving_loop.py layer {layer}")
