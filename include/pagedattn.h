@@ -120,12 +120,13 @@ typedef struct {
   size_t workspace_bytes;    /* minimum workspace for pa_decode_attention */
   void* host_blob;           /* task list in host memory, owned by the plan */
   /* How the decode calls made with this plan run (copied from the options
-   * of pa_plan_ex; pa_plan and pa_plan_in leave them 0).  Every 0 is the
-   * default. */
+   * of pa_plan_ex; pa_plan and pa_plan_in leave them 0, and every 0 is the
+   * default), and the 8-bit kernels' page stages (set by every planner). */
   int32_t merge;             /* PA_MERGE_IN_SPLIT_KERNEL or PA_MERGE_COMBINE_KERNEL */
   int32_t l2_prefetch_pages; /* see pa_plan_options_t */
   int32_t l2_prefetch_ctas;  /* see pa_plan_options_t */
-  int32_t reserved;          /* 0 */
+  int32_t q8_stages;         /* page stages per warp of the 8-bit-cache calls at head_dim 128:
+                                2 or 3, set by every planner (see pa_plan_options_t) */
   uint64_t wait_limit_ns;    /* see pa_plan_options_t */
 } pa_plan_t;
 
@@ -156,7 +157,11 @@ typedef struct {
                                 none; at most 32) */
   int32_t l2_prefetch_ctas;  /* CTAs that prefetch (0: the first wave, the CTAs the GPU
                                 holds at once; negative: none) */
-  int32_t reserved;          /* 0 */
+  int32_t q8_stages;         /* page stages per warp of the INT8 and FP8 split kernel at
+                                head_dim 128: 2 or 3 (0: the planner's choice, 2 when the
+                                tasks average at most 12 pages per warp, else 3; more
+                                pages in flight pay only on long tasks).  Head_dim 64
+                                always takes 6. */
   uint64_t wait_limit_ns;    /* how long a warp waits for one page copy before it gives up,
                                 sets PA_DEV_TIMEOUT and writes nothing (0: 1 s).  A copy
                                 that was issued always lands before the kernel exits. */
@@ -259,7 +264,9 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * sequence of length 0 gets zeros.
  * Returns PA_ERR_PLAN if plan->shape differs from *shape in batch, heads,
  * head_dim, page_size or max_pages_per_seq (the fields the task list depends
- * on), and PA_ERR_WORKSPACE if workspace_bytes < plan->workspace_bytes.
+ * on) or a field a planner sets is out of range (task and CTA counts, merge,
+ * l2_prefetch_pages, q8_stages), and PA_ERR_WORKSPACE if workspace_bytes <
+ * plan->workspace_bytes.
  */
 pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,
                                 const void* k_pages, const void* v_pages,

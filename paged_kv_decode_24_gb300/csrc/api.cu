@@ -27,9 +27,11 @@ cudaError_t launch_split_tc_d64(const SplitParams& p, int group, int dtype, int 
 cudaError_t launch_split_tc_d128(const SplitParams& p, int group, int dtype, int grid,
                                  cudaStream_t stream);
 cudaError_t launch_split_q8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
-cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_q8_d128(const SplitParams& p, int group, int stages, int grid,
+                                 cudaStream_t stream);
 cudaError_t launch_split_f8_d64(const SplitParams& p, int group, int grid, cudaStream_t stream);
-cudaError_t launch_split_f8_d128(const SplitParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_split_f8_d128(const SplitParams& p, int group, int stages, int grid,
+                                 cudaStream_t stream);
 
 // MHA (G = 1) does one multiply-add per K or V element: the CUDA-core kernel
 // keeps up with HBM.  With G >= 2 query heads per KV head the CUDA-core kernel
@@ -49,15 +51,16 @@ cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtyp
 
 // The 8-bit caches (INT8 codes or E4M3 bytes) have one kernel for every group
 // size: its products run on tensor cores, which the padding of G = 1 to 8
-// heads does not slow down.
-cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int grid,
-                            cudaStream_t stream) {
+// heads does not slow down.  At head_dim 128 the plan picks 2 or 3 page
+// stages per warp (pa_plan_t.q8_stages).
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int stages,
+                            int grid, cudaStream_t stream) {
   if (fmt == kCodeE4m3) {
     if (head_dim == 64) return launch_split_f8_d64(p, group, grid, stream);
-    if (head_dim == 128) return launch_split_f8_d128(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_f8_d128(p, group, stages, grid, stream);
   } else {
     if (head_dim == 64) return launch_split_q8_d64(p, group, grid, stream);
-    if (head_dim == 128) return launch_split_q8_d128(p, group, grid, stream);
+    if (head_dim == 128) return launch_split_q8_d128(p, group, stages, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -304,7 +307,8 @@ pa_status_t check_decode_call(const pa_shape_t* shape, const pa_plan_t* plan, co
   if (shape->batch == 0) return PA_OK;
   if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
       plan->num_shared_ctas > plan->num_ctas || plan->l2_prefetch_pages > 32 ||
-      (plan->merge != PA_MERGE_IN_SPLIT_KERNEL && plan->merge != PA_MERGE_COMBINE_KERNEL))
+      (plan->merge != PA_MERGE_IN_SPLIT_KERNEL && plan->merge != PA_MERGE_COMBINE_KERNEL) ||
+      (plan->q8_stages != 2 && plan->q8_stages != 3))
     return PA_ERR_PLAN;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
@@ -480,7 +484,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;
-    st = cuda_status(launch_split_q8(p, D, G, kv.fmt, plan->num_ctas, s));
+    st = cuda_status(launch_split_q8(p, D, G, kv.fmt, plan->q8_stages, plan->num_ctas, s));
   } else {
     if (!encode_pool_map(&p.tmap_k, kv.k, *shape) || !encode_pool_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;

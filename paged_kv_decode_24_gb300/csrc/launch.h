@@ -88,8 +88,8 @@ cudaError_t launch_prefill_tc5_d128(const PrefillParams& p, int group, int dtype
                                     cudaStream_t stream);
 cudaError_t launch_split(const SplitParams& p, int head_dim, int group, int dtype, int grid,
                          cudaStream_t stream);
-cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int grid,
-                            cudaStream_t stream);
+cudaError_t launch_split_q8(const SplitParams& p, int head_dim, int group, int fmt, int stages,
+                            int grid, cudaStream_t stream);
 cudaError_t launch_append_q8(const AppendQ8Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int head_dim, int dtype, int grid,
                            cudaStream_t stream);

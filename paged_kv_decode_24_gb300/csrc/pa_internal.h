@@ -23,6 +23,7 @@ constexpr int kBundleMaxPages = 8;   // tasks this short are bundled one per war
 constexpr int kPlanWaves = 1;        // auto planner: tasks ~ waves x resident CTAs
 constexpr int kL2PrefetchPages = 2;  // pages per warp asked of L2 before the wait on the previous kernel
 constexpr int kBundleWhenOver = 3;   // bundle short tasks only past this many tasks per CTA slot
+constexpr int kQ8ShortPagesPerWarp = 12;  // 8-bit kernel: two page stages up to this mean
 constexpr uint32_t kMagic = 0x564b4150u;  // "PAKV"
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxCtaSmem = 227 * 1024;
@@ -46,6 +47,8 @@ PA_HD constexpr int half_stages_for(int head_dim) { return head_dim == 64 ? 6 : 
 // The 8-bit caches' ring holds whole pages (K and V code tiles and their
 // row scales on one barrier): 3 pages of D = 128 or 6 of D = 64 keep about
 // 12 KB per warp in flight, as the fp16 ring does.
+// At D = 128 a plan may ask for 2 (pa_plan_t.q8_stages) when its tasks are
+// short.
 PA_HD constexpr int q8_page_stages_for(int head_dim) { return head_dim == 64 ? 6 : 3; }
 
 // Shared memory of one warp of the split-decode kernel; the kernel carves

@@ -52,6 +52,16 @@ uint64_t next_plan_id() {
 namespace pa {
 namespace {
 
+// Page stages per warp of the 8-bit-cache kernel at head_dim 128: two when
+// the tasks average at most kQ8ShortPagesPerWarp pages per warp, else three.
+// A warp that streams few pages gains nothing from a third page in flight:
+// two stages measured faster on short tasks (workloads of many short
+// sequences, the short tasks of a skewed mix), three on long ones.
+int q8_stages_for(int n_tasks, int n_shared, int64_t total_pages) {
+  const int64_t warps = (int64_t)n_shared * kWarpsPerCta + (n_tasks - n_shared);
+  return warps > 0 && total_pages <= (int64_t)kQ8ShortPagesPerWarp * warps ? 2 : 3;
+}
+
 // Fill *plan_out and, when dst is non-null, write the task list into dst
 // (dst_bytes long).  With dst == nullptr and alloc set, the list goes into a
 // fresh malloc'ed block owned by the plan.  opt may be null (defaults).
@@ -66,19 +76,20 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   const pa_plan_options_t o = opt ? *opt : pa_plan_options_t{};
   if (o.min_chunk_pages < 0 || o.waves < 0 || o.waves > 64 || o.bundle_waves > 64 ||
       (o.merge != PA_MERGE_IN_SPLIT_KERNEL && o.merge != PA_MERGE_COMBINE_KERNEL) ||
-      o.l2_prefetch_pages > 32)
+      o.l2_prefetch_pages > 32 || (o.q8_stages != 0 && o.q8_stages != 2 && o.q8_stages != 3))
     return PA_ERR_INVALID_ARG;
   const int B = shape->batch, Hkv = shape->num_kv_heads, D = shape->head_dim;
   const int G = shape->num_q_heads / Hkv, S = shape->page_size;
   if (B > 0 && !seq_lens_host) return PA_ERR_INVALID_ARG;
 
   std::vector<int32_t> pages(B), nsplit(B);
-  int64_t total_units = 0;
+  int64_t total_units = 0, total_pages = 0;
   for (int b = 0; b < B; ++b) {
     const int32_t L = seq_lens_host[b];
     if (L < 0 || (int64_t)L > (int64_t)shape->max_pages_per_seq * S) return PA_ERR_INVALID_ARG;
     pages[b] = (L + S - 1) / S;
     total_units += (int64_t)std::max(pages[b], 1) * Hkv;
+    total_pages += (int64_t)pages[b] * Hkv;
   }
 
   // Split counts.  Forced: min(forced, pages).  Auto: pages per split such
@@ -229,6 +240,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->merge = o.merge;
   plan_out->l2_prefetch_pages = o.l2_prefetch_pages;
   plan_out->l2_prefetch_ctas = o.l2_prefetch_ctas;
+  plan_out->q8_stages = o.q8_stages != 0 ? o.q8_stages : q8_stages_for(W, n_shared, total_pages);
   plan_out->wait_limit_ns = o.wait_limit_ns;
   return PA_OK;
 }

@@ -481,3 +481,26 @@ def test_one_wave_split_rule(lib):
         for (b, h), n in per_seq.items():
             pages = max(1, (int(lens[b]) + 15) // 16)
             assert n == min(1024, -(-pages // p1.c.chunk_pages)) or (int(lens[b]) == 0 and n == 1)
+
+
+def test_q8_stage_rule(lib):
+    """The 8-bit kernel's page stages: 2 when the tasks average at most 12
+    pages per warp, else 3; the option forces either; other values are
+    refused."""
+    want = {1: 2, 2: 2, 3: 2, 4: 3, 5: 2}
+    for cfg, ns in want.items():
+        w = workloads.make_config(cfg)
+        p = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits)
+        items, _ = check_plan_covers(w, p)
+        pages = int(np.sum(items[:, 3] - items[:, 2]))
+        n_shared = p.c.num_shared_ctas
+        warps = n_shared * 4 + (p.c.num_work_items - n_shared)
+        assert p.c.q8_stages == ns == (2 if pages <= 12 * warps else 3), (cfg, pages, warps)
+        for forced in (2, 3):
+            f = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits,
+                             options=binding.plan_options(q8_stages=forced))
+            assert f.c.q8_stages == forced
+    w = workloads.make_config(4)
+    for bad in (1, 4, -1):
+        with pytest.raises(binding.PagedAttnError):
+            binding.Plan(_shape(w), w.seq_lens, 152, options=binding.plan_options(q8_stages=bad))

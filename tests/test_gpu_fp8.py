@@ -209,3 +209,22 @@ def test_fp8_and_int8_share_the_plan():
     assert_close(got_i, oracle.decode_attention_q8(wi.q, wi.k_codes, wi.v_codes, wi.k_scales,
                                                    wi.v_scales, wi.block_table, wi.seq_lens,
                                                    wi.scale), "int8")
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[3] == 128], ids=_ids)
+def test_fp8_both_page_stage_counts(case):
+    """Plans forced to 2 and to 3 page stages per warp give the oracle's
+    outputs and the same pools."""
+    lens, hq, hkv, d, splits, dist = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              dist=dist, seed=zlib.crc32(str(case).encode()) ^ 28,
+                              forced_splits=splits, kv="fp8")
+    want, pools = oracle_fp8(w)
+    for ns in (2, 3):
+        dd = DeviceDecode(w)
+        dd.make_plan(q8_stages=ns)
+        assert dd.plan_obj.c.q8_stages == ns
+        got = dd.append_decode_fp8().cpu().numpy()
+        assert dd.read_status() == 0
+        assert_close(got, want, f"fp8 {case} stages={ns}")
+        assert_pools_equal(dd, pools)

@@ -187,3 +187,22 @@ def test_q8_bad_page_is_flagged_and_skipped():
     want1 = oracle.decode_attention_q8(w.q, kc, vc, w.k_scales, w.v_scales, w.block_table,
                                        w.seq_lens, w.scale, heads=[(1, h) for h in range(4)])
     assert_close(out[1], want1[1], "sequence 1")
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[3] == 128], ids=_ids)
+def test_q8_both_page_stage_counts(case):
+    """Plans forced to 2 and to 3 page stages per warp give the oracle's
+    outputs and the same pools."""
+    lens, hq, hkv, d, splits, dist = case
+    w = workloads.make_custom(seq_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              dist=dist, seed=zlib.crc32(str(case).encode()) ^ 28,
+                              forced_splits=splits, kv="int8")
+    want, pools = oracle_q8(w)
+    for ns in (2, 3):
+        dd = DeviceDecode(w)
+        dd.make_plan(q8_stages=ns)
+        assert dd.plan_obj.c.q8_stages == ns
+        got = dd.append_decode_q8().cpu().numpy()
+        assert dd.read_status() == 0
+        assert_close(got, want, f"q8 {case} stages={ns}")
+        assert_pools_equal(dd, pools)
