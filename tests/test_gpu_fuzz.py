@@ -6,8 +6,10 @@ bf16, INT8, FP8), the group size and head dimension, ragged sequence lengths
 (automatic, or forced), the merge form, the SM count the plan is made for
 (small counts make the planner bundle short tasks one per warp), the 8-bit
 kernel's page stages, and the fused or separate append.  The multi-token
-cases draw query counts per sequence and both tile kernels.  Every output is
-compared at the path's tolerance, and the appended pools bit for bit.
+cases draw query counts per sequence and both tile kernels, and the mixed
+cases serve batches of single-token and multi-token sequences on two
+streams.  Every output is compared at the path's tolerance, and the
+appended pools bit for bit.
 """
 
 from __future__ import annotations
@@ -148,3 +150,31 @@ def test_random_multi_token_case(seed):
     assert_close(got.float().cpu().numpy(), want, f"random multi-token case {seed}: {c}",
                  dtype=c["dtype"])
     _pools_bit_exact([(dd.k_pages, kp), (dd.v_pages, vp)], c)
+
+
+MIXED_SEEDS = list(range(7400, 7412))
+
+
+@pytest.mark.parametrize("seed", MIXED_SEEDS)
+def test_random_mixed_batch_on_two_streams(seed):
+    """Random batches of single-token and multi-token sequences served by
+    MixedStep (decode call on a second stream beside the multi-token call)."""
+    from paged_kv_decode_24_gb300.runner import MixedStep
+    rng = np.random.default_rng(seed)
+    lens = [max(1, x) for x in _lengths(rng, int(rng.integers(2, 9)))]
+    qls = [1 if rng.random() < 0.5 else int(rng.integers(0, L + 1)) for L in lens]
+    g, hkv = int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 2, 4]))
+    dtype = str(rng.choice(["fp16", "bf16"]))
+    w = workloads.make_custom(seq_lens=lens, q_lens=qls, num_q_heads=hkv * g, num_kv_heads=hkv,
+                              head_dim=int(rng.choice([64, 128])), seed=seed, dtype=dtype)
+    dd = DeviceDecode(w)
+    ms = MixedStep(w, rows_per_tile=int(rng.choice([128, 64])),
+                   decode_sms=int(rng.choice([1, 16, 50])))
+    ms.run(dd.k_pages, dd.v_pages)
+    assert ms.read_status() == 0, (lens, qls)
+    kp, vp = oracle.kv_append_tokens(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                     w.seq_lens, w.q_lens)
+    want = oracle.prefill_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.q_lens, w.scale)
+    assert_close(ms.output().float().cpu().numpy(), want, f"random mixed batch {seed}",
+                 dtype=dtype)
+    _pools_bit_exact([(dd.k_pages, kp), (dd.v_pages, vp)], (lens, qls))
