@@ -98,6 +98,10 @@ def parse():
                     help="decode: plan options as name=value pairs, comma-separated "
                          "(min_chunk_pages, waves, bundle_max_pages, bundle_waves, "
                          "l2_prefetch_pages, l2_prefetch_ctas); for experiments")
+    ap.add_argument("--early-kv", choices=["on", "off"], default="on",
+                    help="decode: plan option early_kv; each layer's call reads its own "
+                         "layer's cache, which no kernel still running writes, so its first "
+                         "page copies may start before the wait on the layer ahead (on)")
     ap.add_argument("--upload", choices=["ahead", "inline"], default="ahead",
                     help="decode: each model step's graph uploads the next step's plan into a "
                          "second workspace while its layers run (ahead), or its own plan before "
@@ -480,7 +484,9 @@ class DecodeBench:
         # memory, double-buffered so the host never rewrites a buffer whose
         # upload may still be pending.
         extra = dict(kv.split("=") for kv in args.plan.split(",") if kv.strip())
-        self.opts = binding.plan_options(merge=args.merge, **{k: int(v) for k, v in extra.items()})
+        fields = {"merge": args.merge, "early_kv": int(args.early_kv == "on")}
+        fields.update({k: int(v) for k, v in extra.items()})
+        self.opts = binding.plan_options(**fields)
         self.plan0 = binding.Plan(self.shape, self.lens_host, num_sms, w.forced_splits,
                                   options=self.opts)
         self.staging = [torch.empty(int(self.plan0.c.blob_bytes), dtype=torch.uint8).pin_memory()
@@ -969,6 +975,8 @@ def run_dict(args, db, LAYERS, l2):
         "work_items": int(plan0.c.num_work_items),
         "ctas": int(plan0.c.num_ctas),
         "plan_options": args.plan or "defaults",
+        "early_kv": ("on: each layer's first page copies start before the wait on the layer "
+                     "ahead; q and the new rows after it" if args.early_kv == "on" else "off"),
         "step": "one layer: pa_append_decode_attention (one kernel: the append fused into the "
                 "split kernel, whose last split per group merges); pa_plan_upload once per "
                 f"{LAYERS}-layer model step, inside the timing" +

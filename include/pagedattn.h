@@ -128,6 +128,7 @@ typedef struct {
   int32_t q8_stages;         /* page stages per warp of the 8-bit-cache calls at head_dim 128:
                                 2 or 3, set by every planner (see pa_plan_options_t) */
   uint64_t wait_limit_ns;    /* see pa_plan_options_t */
+  int32_t early_kv;          /* see pa_plan_options_t */
 } pa_plan_t;
 
 /* How the split partials of a sequence are merged (paged attention v2's
@@ -165,6 +166,18 @@ typedef struct {
   uint64_t wait_limit_ns;    /* how long a warp waits for one page copy before it gives up,
                                 sets PA_DEV_TIMEOUT and writes nothing (0: 1 s).  A copy
                                 that was issued always lands before the kernel exits. */
+  int32_t early_kv;          /* 1: the split kernel reads seq_lens and the block table and
+                                starts its first page copies (K/V pages, and scales of an
+                                8-bit cache) before it waits for the kernel ahead of it in
+                                the stream, which with programmatic dependent launch may
+                                still be running; q and the new token's rows are read after
+                                the wait.  Set it only when no kernel queued ahead of the
+                                call that may still be running writes the caches, their
+                                scales, the block table, seq_lens or dev_status: a chain of
+                                layer calls, each over its own layer's cache, with seq_lens
+                                and the block table copied in before the chain, qualifies;
+                                pa_kv_append followed by pa_decode_attention on the same
+                                cache does not.  0 (default): everything after the wait. */
 } pa_plan_options_t;
 
 /*
@@ -214,8 +227,8 @@ pa_status_t pa_plan_in(const pa_shape_t* shape, const int32_t* seq_lens_host, in
  * pa_plan and pa_plan_in with options (NULL: the defaults).  host_buffer
  * NULL: the plan allocates and owns its task list (as pa_plan); otherwise
  * the list goes into host_buffer (as pa_plan_in).  A field out of range
- * (merge not a PA_MERGE_* value, l2_prefetch_pages > 32) returns
- * PA_ERR_INVALID_ARG.
+ * (merge not a PA_MERGE_* value, l2_prefetch_pages > 32, early_kv
+ * not 0 or 1) returns PA_ERR_INVALID_ARG.
  */
 pa_status_t pa_plan_ex(const pa_shape_t* shape, const int32_t* seq_lens_host, int32_t num_sms,
                        int32_t forced_splits, const pa_plan_options_t* options,
@@ -265,7 +278,7 @@ pa_status_t pa_plan_upload(const pa_plan_t* plan, void* workspace, size_t worksp
  * Returns PA_ERR_PLAN if plan->shape differs from *shape in batch, heads,
  * head_dim, page_size or max_pages_per_seq (the fields the task list depends
  * on) or a field a planner sets is out of range (task and CTA counts, merge,
- * l2_prefetch_pages, q8_stages), and PA_ERR_WORKSPACE if workspace_bytes <
+ * l2_prefetch_pages, q8_stages, early_kv), and PA_ERR_WORKSPACE if workspace_bytes <
  * plan->workspace_bytes.
  */
 pa_status_t pa_decode_attention(const pa_shape_t* shape, const pa_plan_t* plan, const void* q,

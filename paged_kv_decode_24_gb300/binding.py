@@ -50,7 +50,8 @@ class PaPlan(ctypes.Structure):
                 ("blob_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("host_blob", ctypes.c_void_p), ("merge", ctypes.c_int32),
                 ("l2_prefetch_pages", ctypes.c_int32), ("l2_prefetch_ctas", ctypes.c_int32),
-                ("q8_stages", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64)]
+                ("q8_stages", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64),
+                ("early_kv", ctypes.c_int32)]
 
 
 PA_MERGE_IN_SPLIT_KERNEL = 0
@@ -63,7 +64,7 @@ class PaPlanOptions(ctypes.Structure):
                 ("bundle_max_pages", ctypes.c_int32), ("bundle_waves", ctypes.c_int32),
                 ("merge", ctypes.c_int32), ("l2_prefetch_pages", ctypes.c_int32),
                 ("l2_prefetch_ctas", ctypes.c_int32), ("q8_stages", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_uint64)]
+                ("wait_limit_ns", ctypes.c_uint64), ("early_kv", ctypes.c_int32)]
 
 
 class PaPrefillPlan(ctypes.Structure):

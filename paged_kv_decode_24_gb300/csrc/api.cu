@@ -308,7 +308,7 @@ pa_status_t check_decode_call(const pa_shape_t* shape, const pa_plan_t* plan, co
   if (plan->num_work_items <= 0 || plan->num_ctas <= 0 || plan->num_shared_ctas < 0 ||
       plan->num_shared_ctas > plan->num_ctas || plan->l2_prefetch_pages > 32 ||
       (plan->merge != PA_MERGE_IN_SPLIT_KERNEL && plan->merge != PA_MERGE_COMBINE_KERNEL) ||
-      (plan->q8_stages != 2 && plan->q8_stages != 3))
+      (plan->q8_stages != 2 && plan->q8_stages != 3) || (plan->early_kv != 0 && plan->early_kv != 1))
     return PA_ERR_PLAN;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(dev_status, 4) ||
@@ -481,6 +481,7 @@ pa_status_t decode_impl(const pa_shape_t* shape, const pa_plan_t* plan, const vo
   // kernel launched after the split kernel.
   p.fuse_merge = plan->merge == PA_MERGE_COMBINE_KERNEL ? 0 : 1;
   p.wait_ns = wait_limit_or_default(plan->wait_limit_ns);
+  p.early_kv = plan->early_kv;
   if (kv.int8()) {
     if (!encode_code_map(&p.tmap_k, kv.k, *shape) || !encode_code_map(&p.tmap_v, kv.v, *shape))
       return PA_ERR_CUDA;

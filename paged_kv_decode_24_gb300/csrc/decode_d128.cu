@@ -7,15 +7,23 @@ namespace pa {
 
 namespace {
 
-template <typename T, int G>
-cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
+template <typename T, int G, bool E>
+cudaError_t launch_ge(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int D = 128;
   constexpr int NSH = half_stages_for(D);
   constexpr int smem = kWarpsPerCta * warp_smem(D, G, NSH).bytes;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
   static std::atomic<unsigned long long> configured{0};
-  auto kern = split_decode_kernel<T, D, G, kWarpsPerCta, NSH>;
+  auto kern = split_decode_kernel<T, D, G, kWarpsPerCta, NSH, E>;
   return launch_split_kernel(kern, smem, configured, p, grid, stream);
+}
+
+// The instance of the plan's early_kv: first page copies before (E) or
+// after the wait on the previous kernel.
+template <typename T, int G>
+cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
+  return p.early_kv ? launch_ge<T, G, true>(p, grid, stream)
+                    : launch_ge<T, G, false>(p, grid, stream);
 }
 
 template <typename T>

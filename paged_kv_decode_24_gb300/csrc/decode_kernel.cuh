@@ -99,6 +99,9 @@ struct SplitParams {
   // 0: split tasks only write partials, and combine_kernel merges them.
   int32_t fuse_merge;
   uint64_t wait_ns;  // bound of each wait on a page copy (the plan's wait_limit_ns)
+  // 1: seq_lens, the block table and the first page copies come before the
+  // wait on the previous kernel (the plan's early_kv); 0: after it.
+  int32_t early_kv;
 };
 
 // A split task's slot and group agree with each other and with the task.
@@ -224,7 +227,7 @@ struct MinCtas {
   static constexpr int value = G <= 4 ? 4 : 2;
 };
 
-template <typename T, int D, int G, int NW, int NSH>
+template <typename T, int D, int G, int NW, int NSH, bool EARLY>
 __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
     split_decode_kernel(const SplitParams p) {
   using Geo = Geometry<D, G>;
@@ -281,7 +284,11 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   __syncthreads();
 
   pdl_launch_dependents();
-  pdl_wait_primary();  // everything the previous kernel wrote is visible after this
+  // Everything the previous kernel wrote is visible after the wait.  With
+  // early_kv the task's seq_len, block-table entries and first page copies
+  // come before it (nothing still running writes them); q and the new rows
+  // always come after it.
+  if constexpr (!EARLY) pdl_wait_primary();
 
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
       hdr.w != p.num_split_items || hdr_ctas.x != p.num_ctas || hdr_ctas.y != p.num_shared ||
@@ -315,41 +322,47 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   const int pstride = coop ? NW : 1;
   const int npk = coop ? (warp < npg ? (npg - warp + NW - 1) / NW : 0) : npg;
 
-  // Fused append: k_app is this warp's page index that holds position L-1,
-  // or -1.  The new K and V rows are staged in this warp's shared memory now.
+  // What the previous kernel may write (the new rows, q) is read by
+  // load_inputs: here, after the wait, or with early_kv after the first
+  // page copies and the wait.
   int k_app = -1;
   T* nrow = reinterpret_cast<T*>(ws + L::NROW);  // [2][D]: K row, V row
-  if (p.k_new != nullptr && seq_len > 0) {
-    const int j_app = (seq_len - 1) / kPageSize - pg0;
-    if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
-      k_app = (j_app - pstart) / pstride;
-      const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
-      for (int i = lane; i < D / 8; i += 32) {
-        reinterpret_cast<uint4*>(nrow)[i] =
-            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
-        reinterpret_cast<uint4*>(nrow + D)[i] =
-            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
-      }
-      __syncwarp();
-    }
-  }
-
-  // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
   float2 qf[G][Geo::CH * 4];
-  {
-    const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int ch = 0; ch < Geo::CH; ++ch) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * D + ch * 64 + c * 8));
-        float2 f[4];
-        elem8_to_float2x4<T>(raw, f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          qf[h][ch * 4 + e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
+  auto load_inputs = [&]() {
+    // Fused append: k_app is this warp's page index that holds position L-1,
+    // or -1.  The new K and V rows are staged in this warp's shared memory now.
+    if (p.k_new != nullptr && seq_len > 0) {
+      const int j_app = (seq_len - 1) / kPageSize - pg0;
+      if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
+        k_app = (j_app - pstart) / pstride;
+        const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
+        for (int i = lane; i < D / 8; i += 32) {
+          reinterpret_cast<uint4*>(nrow)[i] =
+              __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
+          reinterpret_cast<uint4*>(nrow + D)[i] =
+              __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
+        }
+        __syncwarp();
       }
-  }
+    }
+
+    // q for the G heads of this KV head, pre-scaled by scale*log2(e), as pairs.
+    {
+      const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int ch = 0; ch < Geo::CH; ++ch) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * D + ch * 64 + c * 8));
+          float2 f[4];
+          elem8_to_float2x4<T>(raw, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            qf[h][ch * 4 + e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
+        }
+    }
+  };
+  if constexpr (!EARLY) load_inputs();
 
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages + pg0;
   const size_t page_stride = (size_t)p.num_kv_heads * kPageSize * D;  // halves
@@ -402,6 +415,11 @@ __global__ void __launch_bounds__(NW * 32, MinCtas<G>::value)
   const int nhalf = 2 * npk;
   const int npre = nhalf < NSH ? nhalf : NSH;
   for (int hi = 0; hi < npre; ++hi) issue(hi);
+
+  if constexpr (EARLY) {
+    pdl_wait_primary();
+    load_inputs();
+  }
 
   // Softmax state of this lane's head: m is shared by the lanes of a head,
   // l_part is this lane's own share of the running sum.

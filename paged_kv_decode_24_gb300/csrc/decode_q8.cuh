@@ -118,7 +118,7 @@ struct Q8Layout {
 // R is replaced only when a page's largest V scale exceeds 2 R.
 constexpr float kLazyLog2 = 8.f;
 
-template <int D, int G, int NW, int NS, int FMT>
+template <int D, int G, int NW, int NS, int FMT, bool EARLY>
 __global__ void __launch_bounds__(NW * 32, 4)
     split_decode_q8_kernel(const __grid_constant__ SplitParams p) {
   static_assert(G <= 8, "the mma tile holds at most 8 query heads");
@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
   __syncthreads();
 
   pdl_launch_dependents();
-  pdl_wait_primary();  // everything the previous kernel wrote is visible after this
+  // Everything the previous kernel wrote is visible after the wait.  With
+  // early_kv the task's seq_len, block-table entries and first page copies
+  // come before it; q and the new rows always come after it.
+  if constexpr (!EARLY) pdl_wait_primary();
 
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
       hdr.w != p.num_split_items || hdr_ctas.x != p.num_ctas || hdr_ctas.y != p.num_shared ||
@@ -218,63 +221,6 @@ __global__ void __launch_bounds__(NW * 32, 4)
   const int pstride = coop ? NW : 1;
   const int npk = coop ? (warp < npg ? (npg - warp + NW - 1) / NW : 0) : npg;
 
-  // Fused append: the warp whose pages hold position L-1 quantises the new
-  // K and V rows into its shared memory now and patches them in later.
-  int k_app = -1;
-  if (p.k_new != nullptr && seq_len > 0) {
-    const int j_app = (seq_len - 1) / kPageSize - pg0;
-    if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
-      k_app = (j_app - pstart) / pstride;
-      const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
-      float sk, sv;
-      const uint32_t ck =
-          quantize_row_warp<D, FMT>(static_cast<const __half*>(p.k_new) + src, lane, sk);
-      const uint32_t cv =
-          quantize_row_warp<D, FMT>(static_cast<const __half*>(p.v_new) + src, lane, sv);
-      if constexpr (D == 128) {
-        reinterpret_cast<uint32_t*>(nrow)[lane] = ck;
-        reinterpret_cast<uint32_t*>(nrow + D)[lane] = cv;
-      } else {
-        reinterpret_cast<uint16_t*>(nrow)[lane] = (uint16_t)ck;
-        reinterpret_cast<uint16_t*>(nrow + D)[lane] = (uint16_t)cv;
-      }
-      if (lane == 0) {
-        nscale[0] = sk;
-        nscale[1] = sv;
-      }
-      __syncwarp();
-    }
-  }
-
-  // Q^T fragments with the permuted reduction order: b0 = dims 4t, 4t+1 and
-  // b1 = dims 4t+2, 4t+3 of each 16-dim step, column n = head g.  Heads past
-  // G are zero.  cb = the same product with every K code at its bias 1152.
-  uint32_t qb[KSTEPS][2];
-  float cb0, cb1;
-  {
-    const __half* qrow =
-        static_cast<const __half*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      if (g < G) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t));
-        qb[kk][0] = v.x;
-        qb[kk][1] = v.y;
-      } else {
-        qb[kk][0] = qb[kk][1] = 0u;
-      }
-    }
-    float cb[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (FMT == kCodeInt8) {
-      const uint32_t k1152 = 0x64806480u;
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk)
-        mma_16816(cb, k1152, k1152, k1152, k1152, qb[kk][0], qb[kk][1]);
-    }
-    cb0 = cb[0];
-    cb1 = cb[1];
-  }
-
   // ldmatrix row addresses of this lane, as an offset inside a tile: lane l
   // addresses row (l & 7) + 8 ((l >> 3) & 1) of 16-byte chunk (l >> 4) (+ the
   // step's chunk pair), swizzled like the TMA copy.  Chunk pairs start at
@@ -288,6 +234,69 @@ __global__ void __launch_bounds__(NW * 32, 4)
     else
       lm_off = (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
   }
+
+  // What the previous kernel may write (the new rows, q) is read by
+  // load_inputs: here, after the wait, or with early_kv after the first
+  // page copies and the wait.
+  int k_app = -1;
+  uint32_t qb[KSTEPS][2];
+  float cb0, cb1;
+  auto load_inputs = [&]() {
+    // Fused append: the warp whose pages hold position L-1 quantises the new
+    // K and V rows into its shared memory now and patches them in later.
+    if (p.k_new != nullptr && seq_len > 0) {
+      const int j_app = (seq_len - 1) / kPageSize - pg0;
+      if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
+        k_app = (j_app - pstart) / pstride;
+        const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
+        float sk, sv;
+        const uint32_t ck =
+            quantize_row_warp<D, FMT>(static_cast<const __half*>(p.k_new) + src, lane, sk);
+        const uint32_t cv =
+            quantize_row_warp<D, FMT>(static_cast<const __half*>(p.v_new) + src, lane, sv);
+        if constexpr (D == 128) {
+          reinterpret_cast<uint32_t*>(nrow)[lane] = ck;
+          reinterpret_cast<uint32_t*>(nrow + D)[lane] = cv;
+        } else {
+          reinterpret_cast<uint16_t*>(nrow)[lane] = (uint16_t)ck;
+          reinterpret_cast<uint16_t*>(nrow + D)[lane] = (uint16_t)cv;
+        }
+        if (lane == 0) {
+          nscale[0] = sk;
+          nscale[1] = sv;
+        }
+        __syncwarp();
+      }
+    }
+
+    // Q^T fragments with the permuted reduction order: b0 = dims 4t, 4t+1 and
+    // b1 = dims 4t+2, 4t+3 of each 16-dim step, column n = head g.  Heads past
+    // G are zero.  cb = the same product with every K code at its bias 1152.
+    {
+      const __half* qrow =
+          static_cast<const __half*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        if (g < G) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t));
+          qb[kk][0] = v.x;
+          qb[kk][1] = v.y;
+        } else {
+          qb[kk][0] = qb[kk][1] = 0u;
+        }
+      }
+      float cb[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (FMT == kCodeInt8) {
+        const uint32_t k1152 = 0x64806480u;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk)
+          mma_16816(cb, k1152, k1152, k1152, k1152, qb[kk][0], qb[kk][1]);
+      }
+      cb0 = cb[0];
+      cb1 = cb[1];
+    }
+  };
+  if constexpr (!EARLY) load_inputs();
 
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages + pg0;
   const uint64_t policy = l2_evict_first_policy();
@@ -334,6 +343,11 @@ __global__ void __launch_bounds__(NW * 32, 4)
 
   const int npre = npk < NS ? npk : NS;
   for (int k = 0; k < npre; ++k) issue(k);
+
+  if constexpr (EARLY) {
+    pdl_wait_primary();
+    load_inputs();
+  }
 
   // Running state.  m_run: per-head reference maximum (log2 units, lazy);
   // l_part: this lane's share of the running sums; R (vref): V-scale

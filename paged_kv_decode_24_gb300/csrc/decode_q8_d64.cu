@@ -7,15 +7,23 @@ namespace pa {
 
 namespace {
 
-template <int G>
-cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
+template <int G, bool E>
+cudaError_t launch_ge(const SplitParams& p, int grid, cudaStream_t stream) {
   constexpr int D = 64;
   constexpr int NS = q8_page_stages_for(D);
   constexpr int smem = Q8Layout<D, kWarpsPerCta, NS>::BYTES;
   static_assert(smem <= kMaxCtaSmem, "split-decode CTA does not fit in shared memory");
   static std::atomic<unsigned long long> configured{0};
-  auto kern = split_decode_q8_kernel<D, G, kWarpsPerCta, NS, kCodeInt8>;
+  auto kern = split_decode_q8_kernel<D, G, kWarpsPerCta, NS, kCodeInt8, E>;
   return launch_split_kernel(kern, smem, configured, p, grid, stream);
+}
+
+// The instance of the plan's early_kv: first page copies before (E) or
+// after the wait on the previous kernel.
+template <int G>
+cudaError_t launch_g(const SplitParams& p, int grid, cudaStream_t stream) {
+  return p.early_kv ? launch_ge<G, true>(p, grid, stream)
+                    : launch_ge<G, false>(p, grid, stream);
 }
 
 }  // namespace

@@ -115,7 +115,7 @@ struct TcLayout {
   static constexpr int BYTES = FLAG + 16 + 1024;      // + slack to align the base to 1024
 };
 
-template <typename T, int D, int G, int NW, int NSH>
+template <typename T, int D, int G, int NW, int NSH, bool EARLY>
 __global__ void __launch_bounds__(NW * 32, 4)
     split_decode_tc_kernel(const __grid_constant__ SplitParams p) {
   static_assert(G <= 8, "the mma tile holds at most 8 query heads");
@@ -179,7 +179,10 @@ __global__ void __launch_bounds__(NW * 32, 4)
   __syncthreads();
 
   pdl_launch_dependents();
-  pdl_wait_primary();  // everything the previous kernel wrote is visible after this
+  // Everything the previous kernel wrote is visible after the wait.  With
+  // early_kv the task's seq_len, block-table entries and first page copies
+  // come before it; q and the new rows always come after it.
+  if constexpr (!EARLY) pdl_wait_primary();
 
   if (hdr.x != (int)kMagic || hdr.y != p.num_items || hdr.z != p.num_groups ||
       hdr.w != p.num_split_items || hdr_ctas.x != p.num_ctas || hdr_ctas.y != p.num_shared ||
@@ -212,40 +215,46 @@ __global__ void __launch_bounds__(NW * 32, 4)
   const int pstride = coop ? NW : 1;
   const int npk = coop ? (warp < npg ? (npg - warp + NW - 1) / NW : 0) : npg;
 
-  // Fused append: k_app is this warp's page index that holds position L-1,
-  // or -1.  The new K and V rows are staged in this warp's shared memory.
+  // What the previous kernel may write (the new rows, q) is read by
+  // load_inputs: here, after the wait, or with early_kv after the first
+  // page copies and the wait.
   int k_app = -1;
-  if (p.k_new != nullptr && seq_len > 0) {
-    const int j_app = (seq_len - 1) / kPageSize - pg0;
-    if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
-      k_app = (j_app - pstart) / pstride;
-      const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
-      for (int i = lane; i < D / 8; i += 32) {
-        reinterpret_cast<uint4*>(nrow)[i] =
-            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
-        reinterpret_cast<uint4*>(nrow + D)[i] =
-            __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
-      }
-      __syncwarp();
-    }
-  }
-
-  // Q^T fragments (B operand of S^T = K Q^T): column n = head g of the group,
-  // rows = dims.  Heads past G are zero.
   uint32_t qb[KSTEPS][2];
-  {
-    const T* qrow =
-        static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      if (g < G) {
-        qb[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 2 * t));
-        qb[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 2 * t + 8));
-      } else {
-        qb[kk][0] = qb[kk][1] = 0u;
+  auto load_inputs = [&]() {
+    // Fused append: k_app is this warp's page index that holds position L-1,
+    // or -1.  The new K and V rows are staged in this warp's shared memory.
+    if (p.k_new != nullptr && seq_len > 0) {
+      const int j_app = (seq_len - 1) / kPageSize - pg0;
+      if (j_app >= pstart && j_app < npg && (j_app - pstart) % pstride == 0) {
+        k_app = (j_app - pstart) / pstride;
+        const size_t src = ((size_t)b * p.num_kv_heads + kvh) * D;
+        for (int i = lane; i < D / 8; i += 32) {
+          reinterpret_cast<uint4*>(nrow)[i] =
+              __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + i);
+          reinterpret_cast<uint4*>(nrow + D)[i] =
+              __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + i);
+        }
+        __syncwarp();
       }
     }
-  }
+
+    // Q^T fragments (B operand of S^T = K Q^T): column n = head g of the group,
+    // rows = dims.  Heads past G are zero.
+    {
+      const T* qrow =
+          static_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)kvh * G + g) * D;
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        if (g < G) {
+          qb[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 2 * t));
+          qb[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 2 * t + 8));
+        } else {
+          qb[kk][0] = qb[kk][1] = 0u;
+        }
+      }
+    }
+  };
+  if constexpr (!EARLY) load_inputs();
 
   const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages + pg0;
   const uint64_t policy = l2_evict_first_policy();
@@ -290,6 +299,11 @@ __global__ void __launch_bounds__(NW * 32, 4)
   const int nhalf = 2 * npk;
   const int npre = nhalf < NSH ? nhalf : NSH;
   for (int hi = 0; hi < npre; ++hi) issue(hi);
+
+  if constexpr (EARLY) {
+    pdl_wait_primary();
+    load_inputs();
+  }
 
   // Online softmax state of heads 2t and 2t+1 (identical across the 8 lanes
   // of a t), and this lane's share of their running sums.

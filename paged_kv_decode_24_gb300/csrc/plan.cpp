@@ -76,7 +76,8 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   const pa_plan_options_t o = opt ? *opt : pa_plan_options_t{};
   if (o.min_chunk_pages < 0 || o.waves < 0 || o.waves > 64 || o.bundle_waves > 64 ||
       (o.merge != PA_MERGE_IN_SPLIT_KERNEL && o.merge != PA_MERGE_COMBINE_KERNEL) ||
-      o.l2_prefetch_pages > 32 || (o.q8_stages != 0 && o.q8_stages != 2 && o.q8_stages != 3))
+      o.l2_prefetch_pages > 32 || (o.q8_stages != 0 && o.q8_stages != 2 && o.q8_stages != 3) ||
+      (o.early_kv != 0 && o.early_kv != 1))
     return PA_ERR_INVALID_ARG;
   const int B = shape->batch, Hkv = shape->num_kv_heads, D = shape->head_dim;
   const int G = shape->num_q_heads / Hkv, S = shape->page_size;
@@ -242,6 +243,7 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->l2_prefetch_ctas = o.l2_prefetch_ctas;
   plan_out->q8_stages = o.q8_stages != 0 ? o.q8_stages : q8_stages_for(W, n_shared, total_pages);
   plan_out->wait_limit_ns = o.wait_limit_ns;
+  plan_out->early_kv = o.early_kv;
   return PA_OK;
 }
 

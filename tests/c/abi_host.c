@@ -1,6 +1,7 @@
 /* A plain C99 program against the C ABI: the header compiles as C, and the
  * host-only entry points (no GPU needed) link and behave.  Exit status 0 on
  * success; each failed check prints its line. */
+#include <stddef.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -67,6 +68,18 @@ int main(void) {
   CHECK(pp.total_q == 42 && pp.num_tiles > 0);
   pa_prefill_plan_free(&pp);
 
+  /* the public structs' layout, for the ctypes binding to compare */
+  printf("layout pa_shape_t %zu\n", sizeof(pa_shape_t));
+  printf("layout pa_plan_t %zu merge %zu q8_stages %zu wait_limit_ns %zu early_kv %zu\n",
+         sizeof(pa_plan_t), offsetof(pa_plan_t, merge), offsetof(pa_plan_t, q8_stages),
+         offsetof(pa_plan_t, wait_limit_ns), offsetof(pa_plan_t, early_kv));
+  printf("layout pa_plan_options_t %zu q8_stages %zu wait_limit_ns %zu early_kv %zu\n",
+         sizeof(pa_plan_options_t), offsetof(pa_plan_options_t, q8_stages),
+         offsetof(pa_plan_options_t, wait_limit_ns), offsetof(pa_plan_options_t, early_kv));
+  printf("layout pa_prefill_plan_t %zu wait_limit_ns %zu\n", sizeof(pa_prefill_plan_t),
+         offsetof(pa_prefill_plan_t, wait_limit_ns));
+  printf("layout pa_prefill_options_t %zu wait_limit_ns %zu\n", sizeof(pa_prefill_options_t),
+         offsetof(pa_prefill_options_t, wait_limit_ns));
   if (failures == 0) printf("abi ok\n");
   return failures == 0 ? 0 : 1;
 }

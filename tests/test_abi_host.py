@@ -333,7 +333,8 @@ def test_plan_options_zeroed_equal_the_plain_plan(lib):
         p = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits,
                          options=binding.plan_options())
         assert np.array_equal(np.delete(p.blob(), [4, 5]), np.delete(ref.blob(), [4, 5]))
-        assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns) == (0,) * 4
+        assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns,
+                p.c.early_kv) == (0,) * 5
         assert p.c.owns_blob == 1
 
 
@@ -364,16 +365,18 @@ def test_plan_options_shape_the_task_list(lib):
     # the per-call fields are carried by the plan, in a caller buffer too
     buf = np.zeros(base.c.blob_bytes, np.uint8)
     o = binding.plan_options(merge="combine", l2_prefetch_pages=32, l2_prefetch_ctas=7,
-                             wait_limit_ns=12345)
+                             wait_limit_ns=12345, early_kv=1)
     p = binding.Plan(s, w.seq_lens, 152, host_buffer=buf, options=o)
     assert p.c.owns_blob == 0 and p.c.host_blob == buf.ctypes.data
-    assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns) == \
-        (binding.PA_MERGE_COMBINE_KERNEL, 32, 7, 12345)
+    assert (p.c.merge, p.c.l2_prefetch_pages, p.c.l2_prefetch_ctas, p.c.wait_limit_ns,
+            p.c.early_kv) == (binding.PA_MERGE_COMBINE_KERNEL, 32, 7, 12345, 1)
+    # early_kv changes when the kernel reads, not the task list
+    assert np.array_equal(np.delete(p.blob(), [4, 5]), np.delete(base.blob(), [4, 5]))
 
 
 @pytest.mark.parametrize("bad", [dict(merge=2), dict(merge=-1), dict(l2_prefetch_pages=33),
                                  dict(waves=-1), dict(waves=65), dict(min_chunk_pages=-1),
-                                 dict(bundle_waves=65)])
+                                 dict(bundle_waves=65), dict(early_kv=2), dict(early_kv=-1)])
 def test_plan_options_out_of_range_are_refused(lib, bad):
     w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=6)
     with pytest.raises(binding.PagedAttnError) as e:
@@ -381,13 +384,14 @@ def test_plan_options_out_of_range_are_refused(lib, bad):
     assert e.value.code == 1, bad
 
 
-def test_decode_refuses_a_plan_with_bad_call_fields(lib):
-    """A plan edited after pa_plan_ex into an unknown merge form is refused
-    before any launch."""
+@pytest.mark.parametrize("field,value", [("merge", 5), ("q8_stages", 4), ("early_kv", 2)])
+def test_decode_refuses_a_plan_with_bad_call_fields(lib, field, value):
+    """A plan edited after pa_plan_ex into an out-of-range call field is
+    refused before any launch."""
     w = workloads.make_custom(seq_lens=[10, 20], num_q_heads=4, num_kv_heads=2, head_dim=64, seed=7)
     s = _shape(w)
     plan = binding.Plan(s, w.seq_lens, 152)
-    plan.c.merge = 5
+    setattr(plan.c, field, value)
     fake = ctypes.c_void_p(0x10000)
     r = lib.pa_decode_attention(ctypes.byref(s), ctypes.byref(plan.c), fake, fake, fake, fake, fake,
                                 ctypes.c_float(0.1), fake, fake, plan.c.workspace_bytes, fake, None)

@@ -1,11 +1,13 @@
 """The C ABI from plain C: include/pagedattn.h compiles as C99 with warnings
 as errors, and a C program linked against libpagedattn.so exercises the
 host-only entry points (plans, the block allocator, the multi-token plan),
-with no GPU and no Python in between.
+with no GPU and no Python in between; it also reports the public structs'
+layout, which the ctypes binding must match.
 """
 
 from __future__ import annotations
 
+import ctypes
 import os
 import shutil
 import subprocess
@@ -31,6 +33,29 @@ def test_header_and_host_calls_from_c(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "abi ok" in r.stdout
+    _check_layouts(r.stdout)
+
+
+def _check_layouts(report):
+    """The ctypes structures of the binding have the C structs' sizes and
+    field offsets, as the C compiler lays them out."""
+    from paged_kv_decode_24_gb300 import binding
+    classes = {"pa_shape_t": binding.PaShape, "pa_plan_t": binding.PaPlan,
+               "pa_plan_options_t": binding.PaPlanOptions,
+               "pa_prefill_plan_t": binding.PaPrefillPlan,
+               "pa_prefill_options_t": binding.PaPrefillOptions}
+    seen = set()
+    for line in report.splitlines():
+        if not line.startswith("layout "):
+            continue
+        words = line.split()
+        name, size, pairs = words[1], int(words[2]), words[3:]
+        cls = classes[name]
+        assert ctypes.sizeof(cls) == size, (name, ctypes.sizeof(cls), size)
+        for field, off in zip(pairs[::2], pairs[1::2]):
+            assert getattr(cls, field).offset == int(off), (name, field)
+        seen.add(name)
+    assert seen == set(classes)
 
 
 @pytest.mark.gpu

@@ -5,10 +5,10 @@ bf16, INT8, FP8), the group size and head dimension, ragged sequence lengths
 (zero, one page, page boundaries, thousands of tokens), the split policy
 (automatic, or forced), the merge form, the SM count the plan is made for
 (small counts make the planner bundle short tasks one per warp), the 8-bit
-kernel's page stages, and the fused or separate append.  The multi-token
-cases draw query counts per sequence and both tile kernels, and the mixed
-cases serve batches of single-token and multi-token sequences on two
-streams.  Every output is compared at the path's tolerance, and the
+kernel's page stages, the fused or separate append, and (fused) the early
+page copies of plan option early_kv.  The multi-token cases draw query
+counts per sequence and both tile kernels, and the mixed cases serve
+batches of single-token and multi-token sequences on two streams.  Every output is compared at the path's tolerance, and the
 appended pools bit for bit.
 """
 
@@ -68,7 +68,8 @@ def _decode_case(seed):
                 sms=int(rng.choice([1, 2, 8, 152])),
                 stages=int(rng.choice([0, 2, 3])),
                 fused=bool(rng.integers(0, 2)),
-                dist=("normal", float(rng.choice([0.5, 1.0]))))
+                dist=("normal", float(rng.choice([0.5, 1.0]))),
+                early=bool(rng.integers(0, 2)))
 
 
 DECODE_SEEDS = list(range(7100, 7260))
@@ -87,6 +88,8 @@ def test_random_decode_case(seed):
     opts = dict(merge=c["merge"])
     if c["stages"]:
         opts["q8_stages"] = c["stages"]
+    if c["fused"] and c["early"]:   # (after a separate append kernel it would not hold)
+        opts["early_kv"] = 1
     dd.make_plan(**opts)
     if cache == "fp16":
         if c["fused"]:
