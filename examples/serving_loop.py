@@ -4,8 +4,9 @@ Several sequences decode together for a number of steps, through a model of
 a few layers (one KV cache per layer):
 - pages come from the block allocator as sequences grow, and the
   sequences' block-table rows grow with them (pa_block_table_grow);
-- each step makes one plan on the host (pa_plan), uploads it once, and every
-  layer uses it: one launch per layer appends the step's token and attends
+- each step makes one plan on the host (pa_plan_ex, with the early page
+  copies of plan option early_kv), uploads it once, and every layer uses it:
+  one launch per layer appends the step's token and attends
   (pa_append_decode_attention);
 - halfway through, one sequence finishes: its pages are swapped out to
   pinned host memory (pa_copy_blocks) and given back to the allocator, and
@@ -92,7 +93,10 @@ def serve(prompt_lens=(90, 15, 300, 47), steps=24, layers=2, num_q_heads=8, num_
             lens[b] += 1
         bt_dev = torch.from_numpy(table).to(dev)
         sl_dev = torch.from_numpy(lens).to(dev)
-        plan = binding.Plan(shape, lens, sms)                 # host only
+        # host only.  early_kv: each layer's call reads its own layer's cache,
+        # and seq_lens and the block table were copied in above, so a layer's
+        # first page copies may start while the layer ahead still runs.
+        plan = binding.Plan(shape, lens, sms, options=binding.plan_options(early_kv=1))
         if ws is None or ws.numel() < plan.workspace_bytes:
             ws = binding.alloc_workspace(plan, dev)
         binding.upload(plan, ws)                              # once per step
