@@ -76,11 +76,13 @@ inline int cta_smem_bytes(int head_dim, int group) {
   return kWarpsPerCta * warp_smem(head_dim, group, half_stages_for(head_dim)).bytes;
 }
 
-// Resident split-decode CTAs per SM, from shared memory and a register
-// estimate per group size (the planner runs on the host without a GPU).
+// Resident split-decode CTAs per SM, from shared memory and the registers
+// per thread the kernels compile to (the planner runs on the host without a
+// GPU): 108 for the CUDA-core kernel (G = 1), 128 for the tensor-core and
+// 8-bit kernels, whose launch bounds ask for four CTAs per SM.
 inline int resident_ctas_per_sm(int head_dim, int group) {
   int by_smem = (int)(kSmemPerSm / (size_t)(cta_smem_bytes(head_dim, group) + 1024));
-  const int regs = group <= 1 ? 72 : group == 2 ? 80 : group == 4 ? 128 : 256;
+  const int regs = group <= 1 ? 108 : 128;
   int by_regs = 65536 / (kWarpsPerCta * 32 * regs);
   int n = by_smem < by_regs ? by_smem : by_regs;
   if (n * kWarpsPerCta > 64) n = 64 / kWarpsPerCta;
