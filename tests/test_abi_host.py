@@ -451,9 +451,11 @@ def test_static_entry_checks_before_anything_is_queued(lib):
 
 def test_one_wave_split_rule(lib):
     """The automatic split size is the average page load of a resident CTA,
-    never under 48 pages: chunk = max(48, ceil(units / (SMs * r))) with r
-    resident CTAs per SM, the same r that option waves = 2 halves.  Every
-    sequence is cut into ceil(pages / chunk) ranges of at most chunk pages."""
+    never under 48 pages: chunk = max(48, ceil(units / (SMs * r))) with r = 4
+    resident CTAs per SM for every group size and head_dim (every split
+    kernel stops at four, by registers and shared memory alike), the same r
+    that option waves = 2 halves.  Every sequence is cut into
+    ceil(pages / chunk) ranges of at most chunk pages."""
     # workload 4: every (sequence, KV head) is shorter than that load, so no split
     w4 = workloads.make_config(4)
     p4 = binding.Plan(_shape(w4), w4.seq_lens, 152)
@@ -476,7 +478,7 @@ def test_one_wave_split_rule(lib):
         fits = [r for r in range(1, 17)
                 if p1.c.chunk_pages == max(48, -(-units // (sms * r)))
                 and p2.c.chunk_pages == max(48, -(-units // (2 * sms * r)))]
-        assert fits, (trial, p1.c.chunk_pages, p2.c.chunk_pages, units, sms)
+        assert 4 in fits, (trial, hq // hkv, d, p1.c.chunk_pages, p2.c.chunk_pages, units, sms)
         items, _ = check_plan_covers(w, p1)
         assert np.all(items[:, 3] - items[:, 2] <= p1.c.chunk_pages)
         per_seq = {}
