@@ -15,8 +15,10 @@
 //   a ring of NV value stages of 64 tokens, each
 //     V [D/64 boxes][64 tokens][128 B]        B operand of P.V, MN-major
 //   Q   [D/64 boxes][128 rows][128 B]         A operand of S, K-major
-// TMEM: S of 64 columns, O of D columns, and P of 64 columns: P_hi then
-// P_lo, keys 2j and 2j+1 in column j, the A operand of P.V (row m in lane m).
+// TMEM: two buffers of 64 columns and O of D columns.  Stage kt uses buffer
+// kt & 1: S(kt) lands there, and once the row threads have read it P(kt)
+// takes its place, P_hi then P_lo, keys 2j and 2j+1 in column j, the A
+// operand of P.V (row m in lane m).
 // The weights p are kept as two 16-bit parts, hi = p rounded to the element
 // type and lo = the remainder rounded, and O accumulates P_hi V + P_lo V:
 // about twice the element type's bits of p, as in the decode kernels, so
@@ -25,11 +27,11 @@
 // bytes with the lo part) for that of reading Q.
 //
 // Per stage kt:
-//   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 64)       committed to s_done
-//   the row threads load S(kt) into registers and release its columns;
-//   S(kt+1) is issued at once and runs while they compute
-//   row softmax of S(kt) in registers, lazy rescaling
-//   P(kt) hi and lo into TMEM, once P.V(kt-1) has finished reading them
+//   S(kt) = Q K^T  (D/16 MMAs, M = 128, N = 64) into buffer kt & 1,
+//     issued once P.V(kt-2) has finished reading that buffer;  committed to s_done[kt & 1]
+//   the row threads load S(kt) into registers; row softmax, lazy rescaling
+//   P(kt) hi and lo into the same columns, with no wait on P.V(kt-1),
+//     which reads the other buffer
 //   O += P_hi V + P_lo V   (8 MMAs, M = 128, N = D, K = 16 each)   committed to pv_done
 // Keys and values have rings of their own: a key stage is refilled as soon
 // as S has read it, a value stage once P.V has.  Sixty-four keys per stage
@@ -185,7 +187,6 @@ struct Tc5Layout {
   static constexpr int BOXES = D / 64;
   static constexpr int NK = D == 128 ? 3 : 6;                   // key stages
   static constexpr int NV = D == 128 ? 2 : 4;                   // value stages
-  static constexpr int NP = 1;                                  // P buffers in TMEM (each hi and lo)
   // An idle row warp waits for the last stage's value copies without having
   // waited for P.V of the stage before.  With one value slot that stage's
   // copy may still be in flight, and the parity wait would then read the
@@ -201,7 +202,7 @@ struct Tc5Layout {
   static constexpr int Q = V0 + NV * STAGE;                     // Q [D/64 boxes][128 rows][128 B]
   static constexpr int BUFS = Q + BOXES * QBOX;                 // the 1024-aligned buffers
   // SMALL bytes hold the mbarriers (k_full[NK], k_free[NK], v_full[NV],
-  // v_free[NV], s_done, s_free, pv_done[2], p_ready[2], drain), the TMEM
+  // v_free[NV], s_done[2], pv_done[2], p_ready[2], drain), the TMEM
   // address and a flag.  The buffers start at the first 1024-byte boundary
   // of the allocation (the 128-byte swizzle needs it); the small area goes
   // before them when the gap is wide enough, else after them, so BUFS + 1024
@@ -212,7 +213,7 @@ struct Tc5Layout {
   static constexpr int FLAG = TMEM_SLOT + 16;
   static_assert(FLAG + 16 <= SMALL, "barriers overflow their area");
   static constexpr int BYTES = BUFS + 1024;
-  static constexpr uint32_t TMEM_COLS = 256;                    // S (64), O (D), P hi + lo (64)
+  static constexpr uint32_t TMEM_COLS = 256;                    // two S/P buffers (64 each), O (D)
 };
 
 template <typename T, int D, int G>
@@ -240,9 +241,8 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   const uint32_t k_free = k_full + 8 * NK;      // NK: S has read a key stage
   const uint32_t v_full = k_free + 8 * NK;      // NV: a value stage's copies landed
   const uint32_t v_free = v_full + 8 * NV;      // NV: P.V has read a value stage
-  const uint32_t s_done = v_free + 8 * NV;      // S(kt) computed
-  const uint32_t s_free = s_done + 8;           // S(kt) loaded by the 4 row warps
-  const uint32_t pv_done = s_free + 8;          // 2: P.V(kt) computed
+  const uint32_t s_done = v_free + 8 * NV;      // 2: S(kt) computed, into buffer kt & 1
+  const uint32_t pv_done = s_done + 16;         // 2: P.V(kt) computed
   // 2: P(kt) written and O rescaled by the 4 row warps.  Two phases of one
   // barrier could complete before the MMA warp looks at the first.
   const uint32_t p_ready = pv_done + 16;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       mbar_init(v_free + 8 * s, 1);
     }
     mbar_init(s_done, 1);
-    mbar_init(s_free, 4);
+    mbar_init(s_done + 8, 1);
     mbar_init(pv_done, 1);
     mbar_init(pv_done + 8, 1);
     mbar_init(p_ready, 4);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
   tc5::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(small + L::TMEM_SLOT);
   // columns: S, O, then P: hi (keys 2j, 2j+1 in column j) and lo, 32 each
-  const uint32_t t_s = tmem, t_o = tmem + BN, t_p = t_o + D;
+  const uint32_t t_x = tmem, t_o = tmem + 2 * BN;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // a row warp's TMEM lanes
 
   pdl_launch_dependents();
@@ -443,17 +443,19 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t ad = tc5::smem_desc(sbase + L::Q + (k >> 2) * L::QBOX + (k & 3) * 32, 16, 1024);
           const uint64_t bd = tc5::smem_desc(kst + (k >> 2) * L::KVBOX + (k & 3) * 32, 16, 1024);
-          tc5::mma(t_s, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          tc5::mma(t_x + (uint32_t)(BN * (kt & 1)), ad, bd, idesc_s, k > 0 ? 1u : 0u);
         }
         tc5::commit(k_free + 8 * sk);
-        tc5::commit(s_done);
+        tc5::commit(s_done + 8 * (kt & 1));
         return true;
       };
       bool good = issue_s(0);
       for (int kt = 0; kt < nkt && good; ++kt) {
         if (kt + 1 < nkt) {
-          // the S columns are free once the row warps have loaded S(kt)
-          good = mbar_wait_bounded_sleep(s_free, (uint32_t)(kt & 1), p.wait_ns) && issue_s(kt + 1);
+          // buffer (kt + 1) & 1 holds P(kt - 1) until P.V(kt - 1) has read it
+          good = (kt < 1 || mbar_wait_bounded_sleep(pv_done + 8 * ((kt - 1) & 1),
+                                                    (uint32_t)(((kt - 1) >> 1) & 1), p.wait_ns)) &&
+                 issue_s(kt + 1);
           if (!good) break;
         }
         const int sv = kt % NV;
@@ -465,6 +467,7 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = tc5::smem_desc(vst + k * 2048, L::KVBOX, 1024);
+          const uint32_t t_p = t_x + (uint32_t)(BN * (kt & 1));
           tc5::mma_tmem_a(t_o, t_p + (uint32_t)(8 * k), bd, idesc_o, (kt > 0 || k > 0) ? 1u : 0u);
           tc5::mma_tmem_a(t_o, t_p + 32u + (uint32_t)(8 * k), bd, idesc_o, 1u);
         }
@@ -508,10 +511,9 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
     // rows that are never written.
     const bool idle = !__any_sync(kFull, ok);
     for (int kt = 0; idle && kt < nkt; ++kt) {
-      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done, (uint32_t)(kt & 1), p.wait_ns));
+      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1), p.wait_ns));
       if (!good) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
       if (BN * kt + BN > span && !zero_value_tail(kt)) {
         good = false;
         break;
@@ -543,16 +545,14 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
             asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(nph[u]) : "l"(bt_row + j));
         }
       }
-      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done, (uint32_t)(kt & 1), p.wait_ns));
+      good = __all_sync(kFull, mbar_wait_bounded_sleep(s_done + 8 * (kt & 1), (uint32_t)((kt >> 1) & 1), p.wait_ns));
       if (!good) break;
       tc5::fence_after();
+      const uint32_t t_sp = t_x + (uint32_t)(BN * (kt & 1));  // S(kt), then P(kt)
       float sv[BN];
 #pragma unroll
-      for (int c = 0; c < BN; c += 16) tc5::ld16(t_s + (uint32_t)c + lane_off, sv + c);
+      for (int c = 0; c < BN; c += 16) tc5::ld16(t_sp + (uint32_t)c + lane_off, sv + c);
       tc5::wait_ld();
-      tc5::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
 
       // ---- mask, row max (lazy), weights
       const int kv0 = BN * kt;
@@ -613,14 +613,10 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       }
       l_run = l_run * al + ps;
 
-      // ---- P buffer kt % NP is free once P.V(kt-NP) is done; O may be
-      // rescaled only once P.V(kt-1) is done
+      // ---- P(kt) goes over S(kt) in its buffer, which P.V(kt - 2) has
+      // finished reading before S(kt) was issued; O may be rescaled only
+      // once P.V(kt-1) is done
       const bool any_resc = __any_sync(kFull, resc);
-      if (kt >= L::NP) {
-        const int k2 = kt - L::NP;
-        good = __all_sync(kFull, mbar_wait_bounded_sleep(pv_done + 8 * (k2 & 1), (uint32_t)((k2 >> 1) & 1), p.wait_ns));
-        if (!good) break;
-      }
       if (any_resc && kt >= 1) {
         good = __all_sync(kFull, mbar_wait_bounded_sleep(pv_done + 8 * ((kt - 1) & 1),
                                                    (uint32_t)(((kt - 1) >> 1) & 1), p.wait_ns));
@@ -629,10 +625,10 @@ __global__ void __launch_bounds__(kTc5Threads, 2)
       tc5::fence_after();
       // ---- P(kt) row, hi and lo, into TMEM (lane = row, column j = keys
       // 2j, 2j+1), before the rescale so that their registers are free for it
-      tc5::st16u(t_p + lane_off, pk);
-      tc5::st16u(t_p + 16u + lane_off, pk + 16);
-      tc5::st16u(t_p + 32u + lane_off, pl);
-      tc5::st16u(t_p + 48u + lane_off, pl + 16);
+      tc5::st16u(t_sp + lane_off, pk);
+      tc5::st16u(t_sp + 16u + lane_off, pk + 16);
+      tc5::st16u(t_sp + 32u + lane_off, pl);
+      tc5::st16u(t_sp + 48u + lane_off, pl + 16);
       tc5::wait_st();
       if (any_resc && kt >= 1) {  // rare: rescale this warp's O rows in TMEM
         const float f = resc ? al : 1.f;
