@@ -9,6 +9,8 @@ starts while the one ahead of it still runs (programmatic dependent launch):
 - when each layer's q is the output of the layer ahead (written by the
   kernel still running when the next starts), the outputs are bit-identical
   to the same chain run without early_kv.
+The same chain captured in a CUDA graph (programmatic edges between the
+kernels) and replayed matches the oracle too.
 All five split kernels take part: fp16 and bf16 CUDA-core (MHA) and tensor-core
 (GQA) kernels and the 8-bit kernel over INT8 and FP8 caches, with the split
 merge inside the split kernel or in the separate combine kernel.
@@ -157,3 +159,43 @@ def test_q_from_the_layer_ahead_is_read_after_the_wait(case):
         want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
     assert_close(results[True][0].float().cpu().numpy(), want, f"early_kv layer 0 {case}",
                  dtype=w.dtype)
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[4]], ids=_ids)
+def test_layer_chain_early_kv_in_a_captured_graph(case):
+    """The chain captured once in a CUDA graph (programmatic edges between
+    the layers' kernels, as the bench runs it) and replayed twice: every
+    layer's output and appended rows match the oracle (the append writes the
+    same rows again on the second replay)."""
+    ws = _layers(case)
+    dds = [DeviceDecode(w) for w in ws]
+    plan, work = _plan(dds, case, early=True)
+    outs = [torch.empty_like(dd.q) for dd in dds]
+    for l, dd in enumerate(dds):   # one eager pass: one-time kernel setup outside capture
+        dd.plan_obj, dd.workspace = plan, work
+        _call(dd, dd.q, outs[l])
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l, dd in enumerate(dds):
+            _call(dd, dd.q, outs[l])
+    for _ in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+    for l, (w, dd) in enumerate(zip(ws, dds)):
+        assert dd.read_status() == 0, (case, l)
+        if w.kv in ("int8", "fp8"):
+            want, (kc, vc, ks, vs) = oracle_append_decode(w)
+            pools = [(dd.k_codes, kc), (dd.v_codes, vc), (dd.k_scales, ks), (dd.v_scales, vs)]
+        else:
+            kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                      w.seq_lens)
+            want = oracle.decode_attention(w.q, kp, vp, w.block_table, w.seq_lens, w.scale)
+            pools = [(dd.k_pages, kp), (dd.v_pages, vp)]
+        assert_close(outs[l].float().cpu().numpy(), want, f"early_kv graph {case} layer {l}",
+                     dtype=w.dtype)
+        for dev, host in pools:
+            assert _same_pool(dev.cpu(), host), (case, l)
