@@ -159,10 +159,10 @@ typedef struct {
   int32_t l2_prefetch_ctas;  /* CTAs that prefetch (0: the first wave, the CTAs the GPU
                                 holds at once; negative: none) */
   int32_t q8_stages;         /* page stages per warp of the INT8 and FP8 split kernel at
-                                head_dim 128: 2 or 3 (0: the planner's choice, 2 when the
-                                tasks average at most 12 pages per warp, else 3; more
-                                pages in flight pay only on long tasks).  Head_dim 64
-                                always takes 6. */
+                                head_dim 128: 2 or 3 (0: the planner's choice, 3 when all
+                                the plan's CTAs are resident at once, else 2 when the
+                                tasks average at most 12 pages per warp, else 3).  Head_dim
+                                64 always takes 6. */
   uint64_t wait_limit_ns;    /* how long a warp waits for one page copy before it gives up,
                                 sets PA_DEV_TIMEOUT and writes nothing (0: 1 s).  A copy
                                 that was issued always lands before the kernel exits. */

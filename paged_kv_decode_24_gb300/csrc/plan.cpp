@@ -52,12 +52,16 @@ uint64_t next_plan_id() {
 namespace pa {
 namespace {
 
-// Page stages per warp of the 8-bit-cache kernel at head_dim 128: two when
-// the tasks average at most kQ8ShortPagesPerWarp pages per warp, else three.
-// A warp that streams few pages gains nothing from a third page in flight:
-// two stages measured faster on short tasks (workloads of many short
-// sequences, the short tasks of a skewed mix), three on long ones.
-int q8_stages_for(int n_tasks, int n_shared, int64_t total_pages) {
+// Page stages per warp of the 8-bit-cache kernel at head_dim 128.  Three
+// when every CTA of the plan is resident at once (one wave); otherwise two
+// when the tasks average at most kQ8ShortPagesPerWarp pages per warp, else
+// three.  Over several waves, a warp that streams few pages gains nothing
+// from a third page in flight: two stages measured faster on short tasks
+// (workloads of many short sequences, the short tasks of a skewed mix),
+// three on long ones; in one wave of short tasks three measured faster.
+int q8_stages_for(int n_tasks, int n_shared, int64_t total_pages, int64_t n_ctas,
+                  int64_t cta_slots) {
+  if (n_ctas <= cta_slots) return 3;
   const int64_t warps = (int64_t)n_shared * kWarpsPerCta + (n_tasks - n_shared);
   return warps > 0 && total_pages <= (int64_t)kQ8ShortPagesPerWarp * warps ? 2 : 3;
 }
@@ -241,7 +245,8 @@ pa_status_t plan_impl(const pa_shape_t* shape, const int32_t* seq_lens_host, int
   plan_out->merge = o.merge;
   plan_out->l2_prefetch_pages = o.l2_prefetch_pages;
   plan_out->l2_prefetch_ctas = o.l2_prefetch_ctas;
-  plan_out->q8_stages = o.q8_stages != 0 ? o.q8_stages : q8_stages_for(W, n_shared, total_pages);
+  plan_out->q8_stages =
+      o.q8_stages != 0 ? o.q8_stages : q8_stages_for(W, n_shared, total_pages, NC, cta_slots);
   plan_out->wait_limit_ns = o.wait_limit_ns;
   plan_out->early_kv = o.early_kv;
   return PA_OK;

@@ -490,10 +490,10 @@ def test_one_wave_split_rule(lib):
 
 
 def test_q8_stage_rule(lib):
-    """The 8-bit kernel's page stages: 2 when the tasks average at most 12
-    pages per warp, else 3; the option forces either; other values are
-    refused."""
-    want = {1: 2, 2: 2, 3: 2, 4: 3, 5: 2}
+    """The 8-bit kernel's page stages: 3 when every CTA is resident at once
+    (152 SMs x 4); otherwise 2 when the tasks average at most 12 pages per
+    warp, else 3; the option forces either; other values are refused."""
+    want = {1: 3, 2: 3, 3: 2, 4: 3, 5: 2}
     for cfg, ns in want.items():
         w = workloads.make_config(cfg)
         p = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits)
@@ -501,7 +501,8 @@ def test_q8_stage_rule(lib):
         pages = int(np.sum(items[:, 3] - items[:, 2]))
         n_shared = p.c.num_shared_ctas
         warps = n_shared * 4 + (p.c.num_work_items - n_shared)
-        assert p.c.q8_stages == ns == (2 if pages <= 12 * warps else 3), (cfg, pages, warps)
+        rule = 3 if p.c.num_ctas <= 152 * 4 else (2 if pages <= 12 * warps else 3)
+        assert p.c.q8_stages == ns == rule, (cfg, pages, warps, p.c.num_ctas)
         for forced in (2, 3):
             f = binding.Plan(_shape(w), w.seq_lens, 152, w.forced_splits,
                              options=binding.plan_options(q8_stages=forced))
